@@ -1,0 +1,275 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Each test checks the oracle against a fixed point that the layer's definition or plain
+mathematics gives: exact rational arithmetic, brute-force dense attention through a
+library routine, closed forms, the merge identity, invariants of the selection and of the
+quantiser, and the IEEE binary16 format as numpy implements it.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int8_kv_top_gb300 import synth
+
+HD, HPG, NG = 256, 12, 2
+
+
+def dequant(codes, scales):
+    """k^ = code * scale of its 64-element block (float64)."""
+    return codes.astype(np.float64) * np.repeat(scales.astype(np.float64), 64, axis=-1)
+
+
+def tiny_inputs(T, n, seed=11):
+    return synth.layer_inputs(T, n, seed=seed)
+
+
+# ------------------------------------------------------------------ binary16 format
+def test_half_decode_matches_numpy_for_every_finite_pattern():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    finite = np.isfinite(ref)
+    got = np.array([oracle.half_to_double(int(b)) for b in bits[finite][::7]])
+    np.testing.assert_array_equal(got, ref[finite][::7])
+
+
+def test_float_to_half_rounds_to_nearest_even_like_numpy():
+    rng = np.random.default_rng(3)
+    xs = np.concatenate([
+        rng.standard_normal(3000).astype(np.float32) * 10.0,
+        (rng.uniform(-1, 1, 2000) * 1e-5).astype(np.float32),       # subnormal range
+        np.array([65504, 65519, 65520, 1e9, -0.0, 2.0 ** -25, 2.0 ** -24 * 1.5, 1 + 2 ** -11, 1 + 3 * 2 ** -11],
+                 dtype=np.float32),
+    ])
+    got = np.array([oracle.float_to_half_bits(float(x)) for x in xs], dtype=np.uint16)
+    with np.errstate(over="ignore"):
+        ref = xs.astype(np.float16).view(np.uint16)
+    np.testing.assert_array_equal(got, ref)
+
+
+# ------------------------------------------------------------------ attention (identity)
+@pytest.mark.parametrize("T,pos0", [(8, 0), (6, 40), (1, 0)])
+def test_identity_attention_matches_library_sdpa(T, pos0):
+    n = pos0 + T
+    inp = tiny_inputs(T, n, seed=T + pos0)
+    out, ids, n_set, _ = oracle.prefill(inp, T, pos0)
+    q = torch.from_numpy(inp["q"].astype(np.float64))                   # [T][24][256]
+    k = torch.from_numpy(dequant(inp["kq"], inp["ksc"]))                # [n][2][256]
+    v = torch.from_numpy(dequant(inp["vq"], inp["vsc"]))
+    # query head h reads group h // 12; causal: token t sees cells 0 .. pos0 + t
+    kk = k[:, torch.arange(24) // 12, :].permute(1, 0, 2)               # [24][n][256]
+    vv = v[:, torch.arange(24) // 12, :].permute(1, 0, 2)
+    mask = torch.arange(n)[None, :] <= (pos0 + torch.arange(T))[:, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(q.permute(1, 0, 2), kk, vv, attn_mask=mask,
+                                                           scale=1 / 16).permute(1, 0, 2)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert (ids == -1).all()
+    assert (n_set == (pos0 + np.arange(T) + 1)[:, None]).all()
+
+
+def test_single_cell_gives_its_value_row():
+    inp = tiny_inputs(1, 1)
+    out, *_ = oracle.prefill(inp, 1, 0)
+    vhat = dequant(inp["vq"], inp["vsc"])[0]                           # [2][256]
+    np.testing.assert_allclose(out[0], vhat[np.arange(24) // 12], rtol=0, atol=1e-15)
+
+
+def test_zero_query_gives_mean_of_values():
+    inp = tiny_inputs(1, 37)
+    inp["q"][:] = 0
+    out, *_ = oracle.prefill(inp, 1, 36)
+    vhat = dequant(inp["vq"], inp["vsc"]).mean(axis=0)                 # [2][256]
+    np.testing.assert_allclose(out[0], vhat[np.arange(24) // 12], rtol=1e-13, atol=1e-15)
+
+
+def test_equal_keys_give_mean_of_values():
+    inp = tiny_inputs(1, 20)
+    inp["kq"][:] = inp["kq"][0]
+    inp["ksc"][:] = inp["ksc"][0]
+    out, *_ = oracle.prefill(inp, 1, 19)
+    vhat = dequant(inp["vq"], inp["vsc"]).mean(axis=0)
+    np.testing.assert_allclose(out[0], vhat[np.arange(24) // 12], rtol=1e-13, atol=1e-15)
+
+
+def test_dominant_logit_selects_its_value_row():
+    inp = tiny_inputs(1, 30)
+    inp["q"][:] = 0
+    inp["q"][0, :, :] = 1.0
+    inp["kq"][:] = 0
+    inp["kq"][17] = 127
+    inp["ksc"][17] = 0.02                                              # logit 256*127*0.02/16 = 40.6
+    out, *_ = oracle.prefill(inp, 1, 29)
+    vhat = dequant(inp["vq"], inp["vsc"])[17]
+    np.testing.assert_allclose(out[0], vhat[np.arange(24) // 12], rtol=0, atol=1e-14)
+
+
+# ------------------------------------------------------------------ selection
+def exact_scores(q_tok, kq, ksc, g, n):
+    """sum over the group's 12 heads of q . k^ as exact rationals (the 1/16 is a positive factor)."""
+    qs = [[Fraction(float(x)) for x in q_tok[g * HPG + h]] for h in range(HPG)]
+    qsum = [sum(qs[h][d] for h in range(HPG)) for d in range(HD)]
+    out = []
+    for c in range(n):
+        s = Fraction(0)
+        for b in range(4):
+            sc = Fraction(float(ksc[c, g, b]))
+            s += sc * sum(qsum[d] * int(kq[c, g, d]) for d in range(64 * b, 64 * b + 64))
+        out.append(s)
+    return out
+
+
+@pytest.mark.parametrize("n_kv,topk,idmax,seed", [(12, 4, 7, 1), (9, 4, 7, 2), (31, 5, 8, 3), (8, 4, 7, 4)])
+def test_selection_matches_brute_force_exact_sort(n_kv, topk, idmax, seed):
+    inp = tiny_inputs(1, n_kv, seed=seed)
+    for g in range(NG):
+        cells, _ = oracle.cell_set(inp["q"][0], inp["kq"], inp["ksc"], n_kv, g, topk=topk, identity_max=idmax)
+        sc = exact_scores(inp["q"][0], inp["kq"], inp["ksc"], g, n_kv)
+        order = sorted(range(n_kv), key=lambda c: (-sc[c], c))
+        np.testing.assert_array_equal(cells, np.sort(order[:topk]))
+
+
+def test_exact_key_equals_rational_score():
+    inp = tiny_inputs(1, 6, seed=9)
+    for g in range(NG):
+        sc = exact_scores(inp["q"][0], inp["kq"], inp["ksc"], g, 6)
+        for c in range(6):
+            key = oracle.exact_key(inp["q"][0], inp["kq"], inp["ksc"], c, g)
+            assert Fraction(key, 2 ** 48) == sc[c]
+
+
+def test_identity_threshold_boundary():
+    inp = tiny_inputs(1, 10, seed=5)
+    cells, _ = oracle.cell_set(inp["q"][0], inp["kq"], inp["ksc"], 7, 0, topk=4, identity_max=7)
+    np.testing.assert_array_equal(cells, np.arange(7))                # n_kv == identity_max: all cells
+    cells, _ = oracle.cell_set(inp["q"][0], inp["kq"], inp["ksc"], 8, 0, topk=4, identity_max=7)
+    assert len(cells) == 4                                            # one more cell: top-k
+
+
+def test_exact_ties_go_to_the_lower_index():
+    inp = tiny_inputs(1, 40, seed=6)
+    inp["kq"][:] = inp["kq"][5]
+    inp["ksc"][:] = inp["ksc"][5]
+    for g in range(NG):
+        cells, _ = oracle.cell_set(inp["q"][0], inp["kq"], inp["ksc"], 40, g, topk=6, identity_max=9)
+        np.testing.assert_array_equal(cells, np.arange(6))
+    # duplicates of a winning cell placed above and below it: all copies tie
+    inp = tiny_inputs(1, 40, seed=7)
+    sc = exact_scores(inp["q"][0], inp["kq"], inp["ksc"], 0, 40)
+    best = max(range(40), key=lambda c: (sc[c], -c))
+    for dup in (2, 30, 39):
+        inp["kq"][dup] = inp["kq"][best]
+        inp["ksc"][dup] = inp["ksc"][best]
+    copies = sorted({best, 2, 30, 39})
+    cells, _ = oracle.cell_set(inp["q"][0], inp["kq"], inp["ksc"], 40, 0, topk=2, identity_max=9)
+    np.testing.assert_array_equal(cells, copies[:2])
+
+
+def test_selection_invariants_at_full_budget():
+    n_kv = 2600
+    inp = tiny_inputs(1, n_kv, seed=8)
+    q = inp["q"][0].astype(np.float64)
+    k = dequant(inp["kq"], inp["ksc"])
+    for g in range(NG):
+        cells, differs = oracle.cell_set(inp["q"][0], inp["kq"], inp["ksc"], n_kv, g, with_f64_check=True)
+        assert len(cells) == 2048 and np.all(np.diff(cells) > 0) and cells[0] >= 0 and cells[-1] < n_kv
+        score = (q[g * 12:(g + 1) * 12] @ k[:, g, :].T).sum(axis=0) / 16   # float64, independent of the C code
+        kept = np.zeros(n_kv, bool)
+        kept[cells] = True
+        assert score[kept].min() >= score[~kept].max() - 1e-9
+        assert not differs
+
+
+# ------------------------------------------------------------------ partials and merge
+def test_single_chunk_partials_match_numpy():
+    inp = tiny_inputs(1, 50, seed=12)
+    cells = np.arange(50, dtype=np.int32)
+    q = inp["q"][0].astype(np.float64)
+    k = dequant(inp["kq"], inp["ksc"])
+    v = dequant(inp["vq"], inp["vsc"])
+    for g in range(NG):
+        part = oracle.partials(inp["q"][0], inp["kq"], inp["vq"], inp["ksc"], inp["vsc"], g, cells)
+        assert part.shape == (1, 12, 258)
+        s = q[g * 12:(g + 1) * 12] @ k[:, g, :].T / 16                    # [12][50]
+        m = s.max(axis=1)
+        e = np.exp(s - m[:, None])
+        np.testing.assert_allclose(part[0, :, 256], m, rtol=1e-14)
+        np.testing.assert_allclose(part[0, :, 257], e.sum(axis=1), rtol=1e-13)
+        np.testing.assert_allclose(part[0, :, :256], e @ v[:, g, :], rtol=1e-12, atol=1e-13)
+
+
+def test_merge_of_any_split_equals_unsplit_attention():
+    rng = np.random.default_rng(4)
+    inp = tiny_inputs(1, 300, seed=13)
+    cells = np.sort(rng.choice(300, size=170, replace=False)).astype(np.int32)
+    for g in range(NG):
+        direct = oracle.attend(inp["q"][0], inp["kq"], inp["vq"], inp["ksc"], inp["vsc"], g, cells)
+        # chunked by 64 (the layer's split) and by random cut points (each piece <= 64 cells)
+        part64 = oracle.partials(inp["q"][0], inp["kq"], inp["vq"], inp["ksc"], inp["vsc"], g, cells)
+        np.testing.assert_allclose(oracle.merge_group(part64), direct, rtol=1e-12, atol=1e-13)
+        cuts = np.sort(rng.choice(np.arange(1, 170), size=5, replace=False))
+        pieces = np.split(cells, cuts)
+        pieces = [p for p in pieces if len(p)]
+        parts = np.concatenate([oracle.partials(inp["q"][0], inp["kq"], inp["vq"], inp["ksc"], inp["vsc"], g, p)
+                                for p in pieces])
+        np.testing.assert_allclose(oracle.merge_group(parts), direct, rtol=1e-12, atol=1e-13)
+
+
+def test_merge_closed_form_two_chunks():
+    part = np.full((1, 2, 24, 258), np.nan, dtype=np.float32)
+    o1 = np.linspace(-1, 1, 256, dtype=np.float32)
+    o2 = np.linspace(2, 3, 256, dtype=np.float32)
+    part[0, 0, :, :256], part[0, 0, :, 256], part[0, 0, :, 257] = o1, 0.0, 1.0
+    part[0, 1, :, :256], part[0, 1, :, 256], part[0, 1, :, 257] = o2, np.float32(np.log(2.0)), 1.0
+    out = oracle.merge_f32(part, [2])
+    m2 = float(np.float32(np.log(2.0)))
+    w1 = np.exp(0.0 - m2)                       # chunk 1 relative to the max m = ln 2
+    expect = (w1 * o1.astype(np.float64) + o2) / (w1 + 1.0)
+    np.testing.assert_allclose(out[0], np.broadcast_to(expect, (24, 256)), rtol=1e-14)
+
+
+def test_merge_ignores_slots_past_the_chunk_count():
+    part = synth.merge_partials([3, 1], chunk_cap=4, seed=2)
+    out = oracle.merge_f32(part, [3, 1])
+    assert np.isfinite(out).all()
+    np.testing.assert_allclose(out[1], part[1, 0, :, :256] / part[1, 0, :, 257:258], rtol=1e-6)
+
+
+def test_decode_driver_is_consistent_with_prefill_driver():
+    P, N = 70, 3
+    inp = tiny_inputs(N, P + N, seed=14)
+    part, n_chunks, merged, direct, ids = oracle.decode(inp, N, P, topk=40, identity_max=71)
+    out, ids_p, n_set, _ = oracle.prefill(inp, N, P, topk=40, identity_max=71)
+    np.testing.assert_allclose(merged, direct, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(direct, out, rtol=0, atol=0)
+    np.testing.assert_array_equal(ids, ids_p)
+    assert list(n_set[:, 0]) == [71, 40, 40]                        # 71 = identity, then top-40
+    assert list(n_chunks) == [2, 1, 1]
+
+
+# ------------------------------------------------------------------ quantiser
+def test_quantize_hand_worked_block():
+    # a = 1.0 -> a/127 = 0.0078740157 -> fp16 0x2008 = 2^-7 * (1 + 8/1024) = 0.00787353515625
+    # codes: 1.0/s = 127.007 -> 127; -0.5/s = -63.50 -> -64; 0.25/s = 31.75 -> 32; 0.75/s = 95.25 -> 95
+    x = np.zeros((1, 256), np.float16)
+    x[0, :4] = [1.0, -0.5, 0.25, 0.75]
+    xq, xsc = oracle.quantize(x)
+    assert xsc.view(np.uint16)[0, 0] == 0x2008
+    assert list(xq[0, :4]) == [127, -64, 32, 95]
+    assert (xq[0, 64:] == 0).all() and (xsc.view(np.uint16)[0, 1:] == 0).all()   # zero blocks: +0 scale
+
+
+def test_quantize_roundtrip_bounds():
+    x = synth.fp16_rows(200, seed=3)
+    xq, xsc = oracle.quantize(x)
+    xs = x.astype(np.float64).reshape(200, 2, 4, 64)
+    s = xsc.astype(np.float64)[..., None]
+    codes = xq.astype(np.float64).reshape(200, 2, 4, 64)
+    assert np.abs(codes).max() <= 127
+    assert (np.abs(codes).max(axis=-1) == 127).all()                  # the absmax element maps to +-127
+    # |x - code * scale| <= scale / 2 up to the fp32 rounding of x / scale
+    assert (np.abs(xs - codes * s) <= s * (0.5 + 2.0 ** -20)).all()
+    # the scale is the fp16 rounding of absmax / 127
+    a = np.abs(xs).max(axis=-1)
+    np.testing.assert_array_equal(xsc.reshape(200, 2, 4), (a.astype(np.float32) / np.float32(127)).astype(np.float16))
