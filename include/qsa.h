@@ -1,0 +1,160 @@
+/*
+ * qsa.h - C ABI of the GB300 QSA layer (quantized sparse attention over an int8 KV cache).
+ *
+ * The layer ("round 6 track b - qsa flash", delivered change; "opus_r9_qsa", what
+ * changed) has 2 KV groups with 12 query heads each (query head h reads group h / 12),
+ * head dim 256, int8 K/V codes with one fp16 scale per 64 elements, and softmax scale
+ * 1/16.  Token t of a call sits at position pos0 + t and attends to the causal cells
+ * 0 .. pos0 + t, i.e. n_kv(t) = pos0 + t + 1 cells: all of them while
+ * n_kv <= identity_max (2051), otherwise the topk (2048) cells selected by qsa_select
+ * ("round 6 track b", delivered change: identity ids per token while n_kv <= 2051).
+ *
+ * Conventions for every call:
+ *  - All array pointers are DEVICE pointers owned by the caller; fp16 values are passed
+ *    as IEEE binary16 bit patterns (uint16_t).  Pointers must be 16-byte aligned.
+ *  - The library allocates no memory.  Its only state is a per-thread last-error string
+ *    and one device status word per device (see qsa_check_device_status).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the
+ *    legacy default stream) and never synchronize, except qsa_check_device_status.
+ *  - Return value: QSA_OK, or a negative QSA_ERR_* code with qsa_last_error() set.
+ *    Argument errors are detected on the host before anything is launched.
+ *
+ * Layouts (row-major):
+ *   q    [T][24][256]      fp16   queries of the call's tokens
+ *   kq   [n_cells][2][256] int8   K codes of cache cell c, group g (cells 0 .. n_cells-1)
+ *   vq   [n_cells][2][256] int8   V codes
+ *   ksc  [n_cells][2][4]   fp16   K scale of elements 64b .. 64b+63
+ *   vsc  [n_cells][2][4]   fp16   V scales
+ *   ids  [T][2][topk]      int32  selected cells of (token, group), ascending
+ *   out  [T][24][256]      fp16   prefill output
+ *   part [N][chunk_cap][24][258] fp32  decode partials: o[0..255], m at 256, l at 257
+ *   xp   [N][24][256]      fp32   merged decode output
+ * Cache contract: the call's own tokens are already in the cache (cells pos0 .. pos0+T-1),
+ * so n_cells >= pos0 + T.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QSA_API __attribute__((visibility("default")))
+#else
+#define QSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QSA_OK 0
+#define QSA_ERR_INVALID_ARG (-1) /* null / misaligned pointer, bad size, too few cells  */
+#define QSA_ERR_UNSUPPORTED (-2) /* parameters outside what the kernels implement       */
+#define QSA_ERR_WORKSPACE (-3)   /* workspace missing or smaller than required          */
+#define QSA_ERR_CUDA (-4)        /* a CUDA runtime call or launch failed                */
+#define QSA_ERR_TIMEOUT (-5)     /* a bounded device-side wait gave up (status word)    */
+#define QSA_ERR_DEVICE (-6)      /* another device-side check failed (status word)      */
+
+#define QSA_N_GROUPS 2
+#define QSA_HEADS_PER_GROUP 12
+#define QSA_N_HEADS 24
+#define QSA_HEAD_DIM 256
+#define QSA_SCALE_BLOCK 64
+#define QSA_CHUNK 64          /* decode split: cells per partial                     */
+#define QSA_PART_STRIDE 258   /* floats per (chunk, head) partial: o[256], m, l      */
+
+/* Selection parameters; a NULL pointer means the defaults {2048, 2051, 0.0625}.
+ * Constraints: 1 <= topk <= identity_max + 1, 1 <= identity_max, sm_scale > 0 and finite. */
+typedef struct qsa_params {
+  int topk;          /* cells kept per (token, group) above the identity threshold */
+  int identity_max;  /* n_kv <= identity_max: every causal cell, in order          */
+  float sm_scale;    /* softmax scale applied to q . k                             */
+} qsa_params;
+
+/* Message of the last failing call on this host thread ("" if none). */
+QSA_API const char* qsa_last_error(void);
+
+/*
+ * qsa_prep_quantize - write fp16 K or V rows into the int8 cache format (the
+ * quantisation half of the pages' fused prep kernel, "round 27 track b - qsa prep and
+ * merge", correctness: qsa_prep writes kq vq ksc vsc).  The pages do not state the
+ * quantiser; this library uses the symmetric absmax rule per 64-element block:
+ *   a = max |x|,  scale = fp16_rn(fp32(a / 127)),
+ *   code = clamp(round_half_away_from_zero(fp32(x / scale)), -127, 127),
+ * with scale = +0 and all codes 0 when the scale is 0.
+ *   x   [n_rows][256] fp16 (e.g. n_rows = n_cells * 2 for one cache slice)
+ *   xq  [n_rows][256] int8 (written)     xsc [n_rows][4] fp16 (written)
+ */
+QSA_API int qsa_prep_quantize(const uint16_t* x, int64_t n_rows, int8_t* xq, uint16_t* xsc, void* stream);
+
+/*
+ * Bytes of device workspace qsa_select needs for a call with T tokens at pos0 over a
+ * cache of n_cells cells (0 when no token of the call is above the identity threshold).
+ */
+QSA_API size_t qsa_select_workspace_bytes(int T, int pos0, int n_cells, const qsa_params* params);
+
+/*
+ * qsa_select - top-k cell selection (the pages' qsa_score + qsa_topk, "round 27 track b",
+ * decision; budget boundary 2051/2052 in "round 6 track b", experiment contract).
+ * For every token with n_kv(t) > identity_max and each group g:
+ *   score(c) = sum over the group's 12 heads h of sm_scale * q[t,h,:] . k^[c,g,:],
+ *   k^ = kq * ksc (per 64-element block), over causal cells c < n_kv(t);
+ * ids[t][g][0..topk) = the topk cells of largest score, equal scores going to the lower
+ * cell index, written in ascending cell order.  The ranking is exact: candidates near the
+ * cut are re-scored in exact integer arithmetic, so ids are bit-identical to a ranking by
+ * the mathematically exact score.  Rows of tokens at or under the threshold are not
+ * written.  ws must hold qsa_select_workspace_bytes(T, pos0, n_cells, params) bytes and
+ * is clobbered.  A device-side capacity overflow sets the status word (QSA_ERR_DEVICE).
+ */
+QSA_API int qsa_select(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_cells, int T, int pos0,
+               int32_t* ids, void* ws, size_t ws_bytes, const qsa_params* params, void* stream);
+
+/*
+ * qsa_flash_prefill - prompt attention of T new tokens (the pages' qsa_flash, "opus_r9_qsa",
+ * what changed; "round 14 track b: qsa metadata hoist", decision):
+ *   out[t,h,:] = sum_{c in set(t,g)} softmax_c(sm_scale * q[t,h,:] . k^[c,g,:]) * v^[c,g,:]
+ * with set(t,g) = all causal cells when n_kv(t) <= identity_max (ids rows not read), else
+ * ids[t][g][0..topk).  ids may be NULL when every token of the call is at or under the
+ * threshold.  fp16 operands, fp32 accumulation and softmax, P rounded to fp16, fp16 out.
+ * Ids outside [0, n_kv(t)) are skipped and flagged in the status word.
+ */
+QSA_API int qsa_flash_prefill(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
+                      const uint16_t* vsc, int n_cells, int T, int pos0, const int32_t* ids, uint16_t* out,
+                      const qsa_params* params, void* stream);
+
+/*
+ * qsa_decode_partial - split-KV partial attention for N decode tokens at positions
+ * pos0 .. pos0+N-1 (the pages' qsa_attn / qsa_attn2, "round 27 track b", decision and
+ * correctness).  Token t's cell set (identity or ids, ascending) is cut into consecutive
+ * chunks of 64; for chunk k and head h:
+ *   m = max s,  l = sum exp(s - m),  o = sum exp(s - m) * v^   (natural exp, unnormalised)
+ * written to part[t][k][h][0..255], part[...][256] = m, part[...][257] = l (fp32, head
+ * stride 258, chunk stride 24*258).  n_chunks[t] receives the chunk count; chunk_cap (the
+ * part buffer's second dimension) must be >= ceil(max(identity_max, topk) / 64).
+ */
+QSA_API int qsa_decode_partial(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
+                       const uint16_t* vsc, int n_cells, int N, int pos0, const int32_t* ids, float* part,
+                       int32_t* n_chunks, int chunk_cap, const qsa_params* params, void* stream);
+
+/*
+ * qsa_merge - log-sum-exp merge of decode partials (the pages' qsa_merge / qsa_merge2,
+ * "round 27 track b", decision: float2 (m,l) loads; correctness: L = sum l_k e_k over
+ * ascending k):
+ *   M = max_k m_k,  L = sum_k l_k exp(m_k - M),  xp = sum_k exp(m_k - M) o_k / L
+ * over k < n_chunks[t] (1 <= n_chunks[t] <= chunk_cap; other values are flagged in the
+ * status word and produce NaN rows).  chunk_cap <= 1024.
+ */
+QSA_API int qsa_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp, void* stream);
+
+/*
+ * qsa_check_device_status - synchronize `stream`, read and clear this device's status
+ * word.  Returns QSA_OK, QSA_ERR_TIMEOUT (a bounded wait inside a kernel gave up) or
+ * QSA_ERR_DEVICE (an id out of range, a capacity overflow, a bad chunk count).
+ */
+QSA_API int qsa_check_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QSA_H */

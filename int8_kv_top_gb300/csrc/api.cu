@@ -1,0 +1,245 @@
+// C ABI of the QSA layer: argument validation, the device status word, the per-thread
+// last-error string, and dispatch to the kernel launchers.  Declarations and the
+// contract of every entry point are in include/qsa.h.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/qsa.h"
+#include "common.cuh"
+
+namespace qsa {
+
+// One status word per device; kernels receive its address.
+__device__ int g_status_word = 0;
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace qsa
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  t_last_error[0] = '\0';
+  return QSA_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(QSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Address of this device's status word (looked up once per device).
+int* status_ptr(int* err) {
+  static int* cache[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    *err = cuda_fail(e == cudaSuccess ? cudaErrorInvalidDevice : e, "cudaGetDevice");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, qsa::g_status_word);
+    if (e != cudaSuccess) {
+      *err = cuda_fail(e, "cudaGetSymbolAddress(status word)");
+      return nullptr;
+    }
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int resolve_params(const qsa_params* in, qsa::Params* out) {
+  qsa::Params p{2048, 2051, 0.0625f};
+  if (in) {
+    p.topk = in->topk;
+    p.identity_max = in->identity_max;
+    p.sm_scale = in->sm_scale;
+  }
+  if (p.identity_max < 1) return fail(QSA_ERR_INVALID_ARG, "identity_max must be >= 1 (got %d)", p.identity_max);
+  if (p.topk < 1 || p.topk > p.identity_max + 1)
+    return fail(QSA_ERR_INVALID_ARG, "topk must be in [1, identity_max + 1] (got %d)", p.topk);
+  if (!(p.sm_scale > 0.f) || !(p.sm_scale < 3.0e38f))
+    return fail(QSA_ERR_INVALID_ARG, "sm_scale must be positive and finite");
+  *out = p;
+  return QSA_OK;
+}
+
+#define CHECK_PTR(p, name)                                                                      \
+  do {                                                                                          \
+    if (!(p)) return fail(QSA_ERR_INVALID_ARG, "%s is NULL", name);                             \
+    if (!aligned16(p)) return fail(QSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);      \
+  } while (0)
+
+int check_layer(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_cells, int T, int pos0) {
+  CHECK_PTR(q, "q");
+  CHECK_PTR(kq, "kq");
+  CHECK_PTR(ksc, "ksc");
+  if (T <= 0) return fail(QSA_ERR_INVALID_ARG, "T must be positive (got %d)", T);
+  if (pos0 < 0) return fail(QSA_ERR_INVALID_ARG, "pos0 must be >= 0 (got %d)", pos0);
+  if ((long long)pos0 + T > (long long)n_cells)
+    return fail(QSA_ERR_INVALID_ARG, "cache too small: pos0 + T = %lld > n_cells = %d", (long long)pos0 + T, n_cells);
+  return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qsa_last_error(void) { return t_last_error; }
+
+int qsa_prep_quantize(const uint16_t* x, int64_t n_rows, int8_t* xq, uint16_t* xsc, void* stream) {
+  if (n_rows < 0) return fail(QSA_ERR_INVALID_ARG, "n_rows must be >= 0");
+  if (n_rows == 0) return ok();
+  CHECK_PTR(x, "x");
+  CHECK_PTR(xq, "xq");
+  CHECK_PTR(xsc, "xsc");
+  cudaError_t e = qsa::launch_quantize(reinterpret_cast<const __half*>(x), n_rows, xq, reinterpret_cast<__half*>(xsc),
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_prep_quantize launch");
+  return ok();
+}
+
+size_t qsa_select_workspace_bytes(int T, int pos0, int n_cells, const qsa_params* params) {
+  qsa::Params p;
+  if (T <= 0 || pos0 < 0 || n_cells <= 0 || resolve_params(params, &p) != QSA_OK) return 0;
+  return qsa::select_workspace_bytes(T, pos0, n_cells, p);
+}
+
+int qsa_select(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_cells, int T, int pos0, int32_t* ids,
+               void* ws, size_t ws_bytes, const qsa_params* params, void* stream) {
+  qsa::Params p;
+  int rc = resolve_params(params, &p);
+  if (rc) return rc;
+  if ((rc = check_layer(q, kq, ksc, n_cells, T, pos0))) return rc;
+  const int t_sel = qsa::first_selected_token(pos0, p.identity_max);
+  if (t_sel >= T) return ok();  // every token at or under the threshold: nothing to select
+  CHECK_PTR(ids, "ids");
+  const size_t need = qsa::select_workspace_bytes(T, pos0, n_cells, p);
+  if (need == 0) return fail(QSA_ERR_UNSUPPORTED, "selection over n_kv up to %lld cells is not supported",
+                             (long long)pos0 + T);
+  if (!ws || ws_bytes < need)
+    return fail(QSA_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", ws ? ws_bytes : (size_t)0, need);
+  if (!aligned16(ws)) return fail(QSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  int* st = status_ptr(&rc);
+  if (!st) return rc;
+  cudaError_t e = qsa::launch_select(reinterpret_cast<const __half*>(q), kq, reinterpret_cast<const __half*>(ksc),
+                                     n_cells, T, pos0, ids, ws, p, st, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_select launch");
+  return ok();
+}
+
+int qsa_flash_prefill(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc, const uint16_t* vsc,
+                      int n_cells, int T, int pos0, const int32_t* ids, uint16_t* out, const qsa_params* params,
+                      void* stream) {
+  qsa::Params p;
+  int rc = resolve_params(params, &p);
+  if (rc) return rc;
+  if ((rc = check_layer(q, kq, ksc, n_cells, T, pos0))) return rc;
+  CHECK_PTR(vq, "vq");
+  CHECK_PTR(vsc, "vsc");
+  CHECK_PTR(out, "out");
+  const int t_sel = qsa::first_selected_token(pos0, p.identity_max);
+  if (t_sel < T) CHECK_PTR(ids, "ids (needed: some tokens are above the identity threshold)");
+  int* st = status_ptr(&rc);
+  if (!st) return rc;
+  qsa::FlashArgs a{reinterpret_cast<const __half*>(q), kq, vq, reinterpret_cast<const __half*>(ksc),
+                   reinterpret_cast<const __half*>(vsc), ids, reinterpret_cast<__half*>(out), n_cells, T, pos0, p, st};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int split = t_sel < T ? t_sel : T;
+  cudaError_t e = qsa::launch_flash_dense(a, 0, split, s);
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_flash_prefill (identity tokens) launch");
+  e = qsa::launch_flash_gather(a, split, T, s);
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_flash_prefill (selected tokens) launch");
+  return ok();
+}
+
+int qsa_decode_partial(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc, const uint16_t* vsc,
+                       int n_cells, int N, int pos0, const int32_t* ids, float* part, int32_t* n_chunks, int chunk_cap,
+                       const qsa_params* params, void* stream) {
+  qsa::Params p;
+  int rc = resolve_params(params, &p);
+  if (rc) return rc;
+  if ((rc = check_layer(q, kq, ksc, n_cells, N, pos0))) return rc;
+  CHECK_PTR(vq, "vq");
+  CHECK_PTR(vsc, "vsc");
+  CHECK_PTR(part, "part");
+  CHECK_PTR(n_chunks, "n_chunks");
+  const int need_cap = ((p.identity_max > p.topk ? p.identity_max : p.topk) + QSA_CHUNK - 1) / QSA_CHUNK;
+  if (chunk_cap < need_cap) return fail(QSA_ERR_INVALID_ARG, "chunk_cap %d < %d", chunk_cap, need_cap);
+  if (chunk_cap > 65535) return fail(QSA_ERR_UNSUPPORTED, "chunk_cap %d > 65535", chunk_cap);
+  const int t_sel = qsa::first_selected_token(pos0, p.identity_max);
+  if (t_sel < N) CHECK_PTR(ids, "ids (needed: some tokens are above the identity threshold)");
+  int* st = status_ptr(&rc);
+  if (!st) return rc;
+  cudaError_t e = qsa::launch_decode_partial(
+      reinterpret_cast<const __half*>(q), kq, vq, reinterpret_cast<const __half*>(ksc),
+      reinterpret_cast<const __half*>(vsc), ids, part, n_chunks, chunk_cap, n_cells, N, pos0, p, st,
+      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_decode_partial launch");
+  return ok();
+}
+
+int qsa_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp, void* stream) {
+  CHECK_PTR(part, "part");
+  CHECK_PTR(n_chunks, "n_chunks");
+  CHECK_PTR(xp, "xp");
+  if (N <= 0) return fail(QSA_ERR_INVALID_ARG, "N must be positive (got %d)", N);
+  if (chunk_cap < 1 || chunk_cap > 1024) return fail(QSA_ERR_UNSUPPORTED, "chunk_cap must be in [1, 1024]");
+  int rc = 0;
+  int* st = status_ptr(&rc);
+  if (!st) return rc;
+  cudaError_t e = qsa::launch_merge(part, n_chunks, N, chunk_cap, xp, st, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_merge launch");
+  return ok();
+}
+
+int qsa_check_device_status(void* stream) {
+  int rc = 0;
+  int* st = status_ptr(&rc);
+  if (!st) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, qsa::g_status_word, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "read status word");
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(qsa::g_status_word, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+    if (v == qsa::QSA_DEV_WAIT_TIMEOUT) return fail(QSA_ERR_TIMEOUT, "a bounded device wait timed out");
+    if (v == qsa::QSA_DEV_BAND_OVERFLOW) return fail(QSA_ERR_DEVICE, "selection refinement capacity exceeded");
+    if (v == qsa::QSA_DEV_BAD_ID) return fail(QSA_ERR_DEVICE, "an id or chunk count was out of range");
+    return fail(QSA_ERR_DEVICE, "device status %d", v);
+  }
+  return ok();
+}
+
+}  // extern "C"

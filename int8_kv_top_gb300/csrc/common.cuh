@@ -1,0 +1,96 @@
+// Shared constants, the int8 -> fp16 dequantisation step and the internal launcher
+// interface between the C ABI (api.cu) and the kernel translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace qsa {
+
+constexpr int kGroups = 2;         // KV heads
+constexpr int kHPG = 12;           // query heads per KV head
+constexpr int kHeads = 24;
+constexpr int kD = 256;            // head dim
+constexpr int kBlk = 64;           // elements per fp16 scale
+constexpr int kNB = kD / kBlk;     // scales per row
+constexpr int kChunk = 64;         // decode split size
+constexpr int kPartStride = 258;   // o[256], m, l
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Params {
+  int topk;
+  int identity_max;
+  float sm_scale;
+};
+
+// First token of a call whose cell count n_kv = pos0 + t + 1 exceeds identity_max.
+__host__ __device__ inline int first_selected_token(int pos0, int identity_max) {
+  const long long t = (long long)identity_max - pos0;
+  return t < 0 ? 0 : (int)t;
+}
+
+// 8 int8 codes (two 32-bit words) times one fp16 scale -> 8 fp16 values, packed as four
+// half2 words with the lower-indexed element in the low half.  The bytes are biased to
+// unsigned, placed under an fp16 exponent of 2^10 (1024 + u is exact), the bias 1152 is
+// subtracted (exact integer result) and one multiply rounds code * scale to nearest.
+__device__ __forceinline__ void dequant8(uint32_t w0, uint32_t w1, __half2 s2, uint32_t (&o)[4]) {
+  const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152.0
+  const uint32_t u0 = w0 ^ 0x80808080u, u1 = w1 ^ 0x80808080u;
+  uint32_t h[4];
+  h[0] = __byte_perm(u0, 0x64646464u, 0x4140);
+  h[1] = __byte_perm(u0, 0x64646464u, 0x4342);
+  h[2] = __byte_perm(u1, 0x64646464u, 0x4140);
+  h[3] = __byte_perm(u1, 0x64646464u, 0x4342);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 v = __hsub2(*reinterpret_cast<__half2*>(&h[i]), bias);
+    v = __hmul2(v, s2);
+    o[i] = *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+// All launchers enqueue on `stream`, return a cudaError_t from the launch, and assume the
+// host has validated every argument.  `status` is the device status word.
+
+struct FlashArgs {
+  const __half* q;
+  const int8_t* kq;
+  const int8_t* vq;
+  const __half* ksc;
+  const __half* vsc;
+  const int32_t* ids;
+  __half* out;
+  int n_cells, T, pos0;
+  Params p;
+  int* status;
+};
+
+cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, cudaStream_t stream);
+cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, cudaStream_t stream);
+
+cudaError_t launch_decode_partial(const __half* q, const int8_t* kq, const int8_t* vq, const __half* ksc,
+                                  const __half* vsc, const int32_t* ids, float* part, int32_t* n_chunks,
+                                  int chunk_cap, int n_cells, int N, int pos0, Params p, int* status,
+                                  cudaStream_t stream);
+
+cudaError_t launch_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp,
+                         int* status, cudaStream_t stream);
+
+cudaError_t launch_quantize(const __half* x, int64_t n_rows, int8_t* xq, __half* xsc, cudaStream_t stream);
+
+size_t select_workspace_bytes(int T, int pos0, int n_cells, Params p);
+cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, int n_cells, int T, int pos0,
+                          int32_t* ids, void* ws, Params p, int* status, cudaStream_t stream);
+
+// Driver entry point for tensor-map encoding (resolved once through the runtime).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+}  // namespace qsa

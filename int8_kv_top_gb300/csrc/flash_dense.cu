@@ -1,0 +1,378 @@
+// qsa_flash_prefill, identity tokens (n_kv <= identity_max): dense causal attention of
+// fp16 queries over the int8 KV cache on the tcgen05 tensor cores.
+//
+// The pages' qsa_flash runs one threadgroup per (KV head, token) over 64-cell chunks:
+// partial S for 12 heads, combine and scale by 1/16, max/exp per head, fp16 P, PV
+// accumulate with per-head rescale ("opus_r9_qsa", what changed; "round 6 track b - qsa
+// flash", delivered change: per-cell half4 K and V scales, identity ids while
+// n_kv <= 2051).  That design serves a GPU without a matrix unit big enough for a 128-row
+// tile.  Here the 12 heads of a group share their K/V rows, so a CTA owns a 128-row tile
+// of (token, head) pairs of one group, 32 tokens x 4 heads, and every 64-cell chunk is a
+// dense M=128 contraction:
+//
+//   warp 0      TMA: int8 K and V chunk tiles [64 cells][256] into a 2-stage ring
+//   warps 8-15  dequantise int8 * fp16 scale -> fp16 into 128B-swizzled K^/V^ buffers
+//   warp 1      TMEM owner + single-thread UMMA issue:
+//                 S  = Q K^T   (A = Q from TMEM, B = K^ K-major)      M=128 N=64  K=256
+//                 O += P V^    (A = P from TMEM, B = V^ MN-major)     M=128 N=256 K=64
+//   warps 4-7   one (token, head) row per thread: Q -> TMEM, online softmax on S in
+//               base-2 units (max, exp2, row sum), fp16 P -> TMEM over S, lazy O rescale
+//               (only when the running max grows by more than 2^8), final 1/l and fp16 out.
+//
+// TMEM columns: O [0,256)  S/P double buffer [256,320) [320,384)  Q [384,512).
+// Shared memory: int8 ring 2 x 32 KB, K^ 2 x 32 KB, V^ 2 x 32 KB (fp16).
+// Every mbarrier wait is bounded; a timeout sets the status word and the CTA drains.
+#include <cstring>
+
+#include "common.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kTok = 32;               // tokens per row tile
+constexpr int kHQ = 4;                 // heads per row tile
+constexpr int kRows = kTok * kHQ;      // 128 = UMMA M
+constexpr int kKV = 64;                // cells per chunk (UMMA N of QK^T)
+constexpr int kThreads = 512;
+constexpr int kI8Bytes = kKV * kD;     // one int8 tile (K or V), 16 KB
+constexpr int kHalfTile = kKV * kD * 2;  // one fp16 tile, 32 KB
+constexpr int kSmemI8 = 0;                         // 2 stages x (K, V)
+constexpr int kSmemKh = kSmemI8 + 2 * 2 * kI8Bytes;  // 64 KB
+constexpr int kSmemVh = kSmemKh + 2 * kHalfTile;     // 128 KB
+constexpr int kSmemTotal = kSmemVh + 2 * kHalfTile;  // 192 KB
+constexpr int kSmemAlloc = kSmemTotal + 1024;        // + alignment slack
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct __align__(8) Bars {
+  uint64_t i8_full[2], i8_empty[2];
+  uint64_t kh_full[2], kh_empty[2];
+  uint64_t vh_full[2], vh_empty[2];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_done[2], q_full, drain;  // o_done[i & 1]: PV(i) complete
+};
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  uint32_t a[16], b[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    a[i] = r[i];
+    b[i] = r[16 + i];
+  }
+  tmem_st16(taddr, a);
+  tmem_st16(taddr + 16, b);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    flash_dense_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                       const __half* __restrict__ q, const __half* __restrict__ ksc,
+                       const __half* __restrict__ vsc, __half* __restrict__ out, int n_cells, int pos0, int t_begin,
+                       int t_end, float scale_log2, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ Bars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_ttiles = (t_end - t_begin + kTok - 1) / kTok;
+  const int item = blockIdx.x;
+  const int ttile = n_ttiles - 1 - item / 6;  // heaviest (latest) token tiles first
+  const int g = (item % 6) / 3, hq = item % 3;
+  const int t0 = t_begin + ttile * kTok;
+  const int t_last = min(t0 + kTok, t_end) - 1;
+  const int n_kv_max = pos0 + t_last + 1;
+  const int J = (n_kv_max + kKV - 1) / kKV;
+
+  if (tid == 0) {
+    s_abort = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.i8_full[i], 1);
+      mbar_init(&bars.i8_empty[i], 8);
+      mbar_init(&bars.kh_full[i], 8);
+      mbar_init(&bars.kh_empty[i], 1);
+      mbar_init(&bars.vh_full[i], 8);
+      mbar_init(&bars.vh_empty[i], 1);
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.p_full[i], 4);
+    }
+    mbar_init(&bars.o_done[0], 1);
+    mbar_init(&bars.o_done[1], 1);
+    mbar_init(&bars.q_full, 4);
+    mbar_init(&bars.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      int issued = 0;
+      for (int j = 0; j < J; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(&bars.i8_empty[s], ((j >> 1) & 1) ^ 1, status, &s_abort)) break;
+        uint8_t* dst = smem + kSmemI8 + s * 2 * kI8Bytes;
+        mbar_arrive_expect_tx(&bars.i8_full[s], 2 * kI8Bytes);
+        tma_load_3d(dst, &map_k, &bars.i8_full[s], 0, g, j * kKV);
+        tma_load_3d(dst + kI8Bytes, &map_v, &bars.i8_full[s], 0, g, j * kKV);
+        issued = j + 1;
+      }
+      // drain: the last load of each stage must have landed before the CTA exits
+      for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(&bars.i8_full[j & 1], (j >> 1) & 1, status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issue
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_f16_f32(kRows, kKV, 0, 0);
+      const uint32_t idesc_pv = idesc_f16_f32(kRows, kD, 0, 1);
+      const uint32_t kh0 = smem_u32(smem + kSmemKh), vh0 = smem_u32(smem + kSmemVh);
+      bool ok = mbar_wait(&bars.q_full, 0, status, &s_abort);  // Q rows are in TMEM
+      tc_fence_after();
+      auto issue_pv = [&](int i) -> bool {
+        const int b = i & 1;
+        if (!mbar_wait(&bars.p_full[b], (i >> 1) & 1, status, &s_abort)) return false;
+        if (!mbar_wait(&bars.vh_full[b], (i >> 1) & 1, status, &s_abort)) return false;
+        tc_fence_after();
+        const uint32_t vb = vh0 + b * kHalfTile;
+#pragma unroll
+        for (int kk = 0; kk < kKV / 16; ++kk) {
+          const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, kKV * 128, 1024);
+          umma_ts(tmem + kColO, tmem + kColS + b * 64 + kk * 8, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars.o_done[b]);
+        umma_commit(&bars.vh_empty[b]);
+        return true;
+      };
+      for (int j = 0; ok && j < J; ++j) {
+        const int b = j & 1;
+        if (!mbar_wait(&bars.kh_full[b], (j >> 1) & 1, status, &s_abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kb = kh0 + b * kHalfTile;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t bdesc = sdesc_sw128(kb + (kk >> 2) * (kKV * 128) + (kk & 3) * 32, 16, 1024);
+          umma_ts(tmem + kColS + b * 64, tmem + kColQ + kk * 8, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars.s_full[b]);
+        umma_commit(&bars.kh_empty[b]);
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok) issue_pv(J - 1);
+      // drain: everything issued must complete before TMEM is released
+      umma_commit(&bars.drain);
+      mbar_wait(&bars.drain, 0, status);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ softmax rows
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // TMEM lane == tile row
+    const int tl = r >> 2, hl = r & 3;
+    const int t = t0 + tl;
+    const bool row_valid = t <= t_last;
+    const int h = g * kHPG + hq * kHQ + hl;
+    const int n_kv_row = row_valid ? pos0 + t + 1 : 0;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+
+    // Q row -> TMEM columns [384, 512): 128 words of two fp16 (even dim in the low half)
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)(row_valid ? t : t0) * kHeads + h) * kD);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 v = row_valid ? src[c * 4 + i] : make_uint4(0, 0, 0, 0);
+          w[i * 4 + 0] = v.x;
+          w[i * 4 + 1] = v.y;
+          w[i * 4 + 2] = v.z;
+          w[i * 4 + 3] = v.w;
+        }
+        tmem_st16(lane_base + kColQ + c * 16, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.q_full);
+    }
+
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < J; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait_warp(&bars.s_full[b], (j >> 1) & 1, status, &s_abort)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[64];
+      {
+        uint32_t a[32], c[32];
+        tmem_ld32(lane_base + kColS + b * 64, a);
+        tmem_ld32(lane_base + kColS + b * 64 + 32, c);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          sr[i] = a[i];
+          sr[32 + i] = c[i];
+        }
+      }
+      float s[64];
+      float m_tile = -INFINITY;
+      const int lim = n_kv_row - j * kKV;  // cells i < lim are causal for this row
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        s[i] = (i < lim) ? __uint_as_float(sr[i]) * scale_log2 : -INFINITY;
+        m_tile = fmaxf(m_tile, s[i]);
+      }
+      const float m_new = fmaxf(m_run, m_tile);
+      if (j == 0) {
+        m_run = m_new;
+      } else {
+        const bool need = m_new > m_run + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          // O must hold every PV issued so far before it is rescaled in place
+          // (alternating barriers: the commit after QK(j) already covered PV(j-2), so the
+          // barrier of PV(j-1) is at most one phase behind)
+          if (!mbar_wait_warp(&bars.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, status, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float f = need ? fast_exp2(m_run - m_new) : 1.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < kD; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + kColO + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            tmem_st32(lane_base + kColO + c0, o);
+          }
+          tmem_wait_st();
+          if (need) {
+            l_run *= f;
+            m_run = m_new;
+          }
+        }
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      uint32_t pw[32];
+      float lsum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = fast_exp2(s[2 * i] - m_use), p1 = fast_exp2(s[2 * i + 1] - m_use);
+        lsum += p0 + p1;
+        pw[i] = pack_half2(p0, p1);
+      }
+      l_run += lsum;
+      tmem_st32(lane_base + kColS + b * 64, pw);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full[b]);
+    }
+    if (ok && mbar_wait_warp(&bars.o_done[(J - 1) & 1], ((J - 1) >> 1) & 1, status, &s_abort)) {
+      tc_fence_after();
+      const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      __half* dst = out + ((size_t)(row_valid ? t : 0) * kHeads + h) * kD;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kD; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + kColO + c0, o);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_half2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (row_valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dequantise
+    const int dw = warp - 8;
+    const int blk = lane >> 3;
+    for (int j = 0; j < J; ++j) {
+      const int s = j & 1, b = j & 1;
+      if (!mbar_wait_warp(&bars.i8_full[s], (j >> 1) & 1, status, &s_abort)) break;
+      const uint8_t* src = smem + kSmemI8 + s * 2 * kI8Bytes;
+      bool ok = true;
+#pragma unroll 1
+      for (int kv = 0; kv < 2; ++kv) {
+        uint64_t* empty = kv ? &bars.vh_empty[b] : &bars.kh_empty[b];
+        uint64_t* full = kv ? &bars.vh_full[b] : &bars.kh_full[b];
+        if (j >= 2 && !mbar_wait_warp(empty, ((j >> 1) & 1) ^ 1, status, &s_abort)) { ok = false; break; }
+        const __half* sc = kv ? vsc : ksc;
+        uint8_t* dstb = smem + (kv ? kSmemVh : kSmemKh) + b * kHalfTile;
+        const uint8_t* srcb = src + kv * kI8Bytes;
+#pragma unroll 2
+        for (int u = 0; u < kKV / 8; ++u) {
+          const int cell = dw + 8 * u;
+          const int gc = j * kKV + cell;
+          const __half scale = (gc < n_cells) ? sc[((size_t)gc * kGroups + g) * kNB + blk] : __ushort_as_half(0);
+          const uint2 w = *reinterpret_cast<const uint2*>(srcb + cell * kD + lane * 8);
+          uint32_t o[4];
+          dequant8(w.x, w.y, __half2half2(scale), o);
+          const uint32_t off = blk * (kKV * 128) + cell * 128 + (((lane & 7) ^ (cell & 7)) << 4);
+          *reinterpret_cast<uint4*>(dstb + off) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.i8_empty[s]);
+      if (!ok) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+bool make_kv_map(CUtensorMap* map, const int8_t* base, int n_cells) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kGroups, (cuuint64_t)n_cells};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD, (cuuint64_t)kD * kGroups};
+  const cuuint32_t box[3] = {(cuuint32_t)kD, 1u, (cuuint32_t)kKV};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<int8_t*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, cudaStream_t stream) {
+  if (t_end <= t_begin) return cudaSuccess;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(flash_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  CUtensorMap mk, mv;
+  if (!make_kv_map(&mk, a.kq, a.n_cells) || !make_kv_map(&mv, a.vq, a.n_cells)) return cudaErrorInvalidValue;
+  const int n_ttiles = (t_end - t_begin + kTok - 1) / kTok;
+  const float scale_log2 = a.p.sm_scale * kLog2e;
+  flash_dense_kernel<<<n_ttiles * 6, kThreads, kSmemAlloc, stream>>>(mk, mv, a.q, a.ksc, a.vsc, a.out, a.n_cells,
+                                                                    a.pos0, t_begin, t_end, scale_log2, a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace qsa

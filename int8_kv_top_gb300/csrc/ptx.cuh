@@ -85,6 +85,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// Warp-uniform bounded wait: every lane waits, and the warp proceeds only if all lanes
+// saw the phase complete (so warp-collective tcgen05 operations never diverge).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status,
+                                               volatile int* abort = nullptr) {
+  const bool ok = mbar_wait(bar, parity, status, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

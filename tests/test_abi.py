@@ -1,0 +1,88 @@
+"""The C-ABI library builds, loads, exports every declared symbol and rejects bad
+arguments on the host before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from int8_kv_top_gb300 import build as qbuild
+from int8_kv_top_gb300 import qsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qsa.load()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"QSA_API\s+[\w\s\*]+?\b(qsa_\w+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert {"qsa_flash_prefill", "qsa_select", "qsa_merge", "qsa_decode_partial", "qsa_prep_quantize"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(qsa.EXPORTS) <= names
+
+
+FAKE = 1 << 20  # aligned, never dereferenced: every call below fails validation first
+
+
+def test_null_and_misaligned_pointers(lib):
+    P = ctypes.c_void_p
+    rc = lib.qsa_flash_prefill(None, P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, 4, 0, None, P(FAKE), None, None)
+    assert rc == qsa.QSA_ERR_INVALID_ARG and b"q is NULL" in lib.qsa_last_error()
+    rc = lib.qsa_flash_prefill(P(FAKE + 8), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, 4, 0, None, P(FAKE), None, None)
+    assert rc == qsa.QSA_ERR_INVALID_ARG and b"aligned" in lib.qsa_last_error()
+    rc = lib.qsa_merge(P(FAKE), None, 1, 33, P(FAKE), None)
+    assert rc == qsa.QSA_ERR_INVALID_ARG
+
+
+def test_bad_sizes(lib):
+    P = ctypes.c_void_p
+    args = (P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE))
+    assert lib.qsa_flash_prefill(*args, 100, 0, 0, None, P(FAKE), None, None) == qsa.QSA_ERR_INVALID_ARG   # T = 0
+    assert lib.qsa_flash_prefill(*args, 100, 4, -1, None, P(FAKE), None, None) == qsa.QSA_ERR_INVALID_ARG  # pos0 < 0
+    assert lib.qsa_flash_prefill(*args, 100, 4, 97, None, P(FAKE), None, None) == qsa.QSA_ERR_INVALID_ARG  # cache small
+    assert b"cache too small" in lib.qsa_last_error()
+    # tokens above the threshold need ids
+    assert lib.qsa_flash_prefill(*args, 3000, 4, 2500, None, P(FAKE), None, None) == qsa.QSA_ERR_INVALID_ARG
+    assert lib.qsa_merge(P(FAKE), P(FAKE), 0, 33, P(FAKE), None) == qsa.QSA_ERR_INVALID_ARG
+    assert lib.qsa_merge(P(FAKE), P(FAKE), 1, 2000, P(FAKE), None) == qsa.QSA_ERR_UNSUPPORTED
+    # decode: chunk_cap too small for the default set size (2051 cells -> 33 chunks)
+    rc = lib.qsa_decode_partial(*args, 600, 1, 512, None, P(FAKE), P(FAKE), 32, None, None)
+    assert rc == qsa.QSA_ERR_INVALID_ARG
+    assert lib.qsa_prep_quantize(P(FAKE), -1, P(FAKE), P(FAKE), None) == qsa.QSA_ERR_INVALID_ARG
+    assert lib.qsa_prep_quantize(None, 0, None, None, None) == qsa.QSA_OK
+
+
+def test_bad_params(lib):
+    P = ctypes.c_void_p
+    args = (P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 100, 4, 0, None, P(FAKE))
+    for bad in [(0, 2051, 0.0625), (2053, 2051, 0.0625), (4, 0, 0.0625), (4, 8, 0.0), (4, 8, -1.0),
+                (4, 8, float("inf"))]:
+        p = qsa.qsa_params(*bad)
+        assert lib.qsa_flash_prefill(*args, ctypes.byref(p), None) == qsa.QSA_ERR_INVALID_ARG, bad
+    assert lib.qsa_select_workspace_bytes(4, 0, 100, None) == 0   # no token above the threshold
+
+
+def test_select_rejects_missing_workspace(lib):
+    P = ctypes.c_void_p
+    need = lib.qsa_select_workspace_bytes(64, 2040, 2104, None)
+    rc = lib.qsa_select(P(FAKE), P(FAKE), P(FAKE), 2104, 64, 2040, P(FAKE), None, 0, None, None)
+    assert rc in (qsa.QSA_ERR_WORKSPACE, qsa.QSA_ERR_UNSUPPORTED)
+    if need:
+        rc = lib.qsa_select(P(FAKE), P(FAKE), P(FAKE), 2104, 64, 2040, P(FAKE), P(FAKE), need - 16, None, None)
+        assert rc == qsa.QSA_ERR_WORKSPACE
+    # under the threshold nothing is needed or launched
+    assert lib.qsa_select(P(FAKE), P(FAKE), P(FAKE), 100, 4, 0, None, None, 0, None, None) == qsa.QSA_OK
