@@ -10,7 +10,7 @@
 // of (token, head) pairs of one group, 32 tokens x 4 heads, and every 64-cell chunk is a
 // dense M=128 contraction:
 //
-//   warp 0      TMA: int8 K and V chunk tiles [64 cells][256] into a 2-stage ring
+//   warp 0      TMA: int8 K and V chunk tiles [64 cells][256] + their scale rows, 2-stage ring
 //   warps 8-15  dequantise int8 * fp16 scale -> fp16 into 128B-swizzled K^/V^ buffers
 //   warp 1      TMEM owner + single-thread UMMA issue:
 //                 S  = Q K^T   (A = Q from TMEM, B = K^ K-major)      M=128 N=64  K=256
@@ -20,7 +20,7 @@
 //               (only when the running max grows by more than 2^8), final 1/l and fp16 out.
 //
 // TMEM columns: O [0,256)  S/P double buffer [256,320) [320,384)  Q [384,512).
-// Shared memory: int8 ring 2 x 32 KB, K^ 2 x 32 KB, V^ 2 x 32 KB (fp16).
+// Shared memory: int8 ring 2 x (32 KB codes + 2 KB scales), K^ 2 x 32 KB, V^ 2 x 32 KB (fp16).
 // Every mbarrier wait is bounded; a timeout sets the status word and the CTA drains.
 #include <cstring>
 
@@ -36,10 +36,12 @@ constexpr int kKV = 64;                // cells per chunk (UMMA N of QK^T)
 constexpr int kThreads = 512;
 constexpr int kI8Bytes = kKV * kD;     // one int8 tile (K or V), 16 KB
 constexpr int kHalfTile = kKV * kD * 2;  // one fp16 tile, 32 KB
-constexpr int kSmemI8 = 0;                         // 2 stages x (K, V)
-constexpr int kSmemKh = kSmemI8 + 2 * 2 * kI8Bytes;  // 64 KB
-constexpr int kSmemVh = kSmemKh + 2 * kHalfTile;     // 128 KB
-constexpr int kSmemTotal = kSmemVh + 2 * kHalfTile;  // 192 KB
+constexpr int kScaleBytes = kKV * kGroups * kNB * 2;     // [64 cells][2 groups][4] fp16, 1 KB
+constexpr int kStageBytes = 2 * kI8Bytes + 2 * kScaleBytes;  // K, V codes + K, V scales: 34 KB
+constexpr int kSmemI8 = 0;                                 // 2 stages
+constexpr int kSmemKh = kSmemI8 + 2 * kStageBytes;         // 68 KB
+constexpr int kSmemVh = kSmemKh + 2 * kHalfTile;           // 132 KB
+constexpr int kSmemTotal = kSmemVh + 2 * kHalfTile;        // 196 KB
 constexpr int kSmemAlloc = kSmemTotal + 1024;        // + alignment slack
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -65,8 +67,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __global__ void __launch_bounds__(kThreads, 1)
     flash_dense_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                       const __half* __restrict__ q, const __half* __restrict__ ksc,
-                       const __half* __restrict__ vsc, __half* __restrict__ out, int n_cells, int pos0, int t_begin,
+                       const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_vs,
+                       const __half* __restrict__ q, __half* __restrict__ out, int pos0, int t_begin,
                        int t_end, float scale_log2, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -116,14 +118,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
+      tma_prefetch_desc(&map_ks);
+      tma_prefetch_desc(&map_vs);
       int issued = 0;
       for (int j = 0; j < J; ++j) {
         const int s = j & 1;
         if (j >= 2 && !mbar_wait(&bars.i8_empty[s], ((j >> 1) & 1) ^ 1, status, &s_abort)) break;
-        uint8_t* dst = smem + kSmemI8 + s * 2 * kI8Bytes;
-        mbar_arrive_expect_tx(&bars.i8_full[s], 2 * kI8Bytes);
+        uint8_t* dst = smem + kSmemI8 + s * kStageBytes;
+        mbar_arrive_expect_tx(&bars.i8_full[s], kStageBytes);
         tma_load_3d(dst, &map_k, &bars.i8_full[s], 0, g, j * kKV);
         tma_load_3d(dst + kI8Bytes, &map_v, &bars.i8_full[s], 0, g, j * kKV);
+        tma_load_2d(dst + 2 * kI8Bytes, &map_ks, &bars.i8_full[s], 0, j * kKV);
+        tma_load_2d(dst + 2 * kI8Bytes + kScaleBytes, &map_vs, &bars.i8_full[s], 0, j * kKV);
         issued = j + 1;
       }
       // drain: the last load of each stage must have landed before the CTA exits
@@ -305,21 +311,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < J; ++j) {
       const int s = j & 1, b = j & 1;
       if (!mbar_wait_warp(&bars.i8_full[s], (j >> 1) & 1, status, &s_abort)) break;
-      const uint8_t* src = smem + kSmemI8 + s * 2 * kI8Bytes;
+      const uint8_t* src = smem + kSmemI8 + s * kStageBytes;
       bool ok = true;
 #pragma unroll 1
       for (int kv = 0; kv < 2; ++kv) {
         uint64_t* empty = kv ? &bars.vh_empty[b] : &bars.kh_empty[b];
         uint64_t* full = kv ? &bars.vh_full[b] : &bars.kh_full[b];
         if (j >= 2 && !mbar_wait_warp(empty, ((j >> 1) & 1) ^ 1, status, &s_abort)) { ok = false; break; }
-        const __half* sc = kv ? vsc : ksc;
+        const __half* sc = reinterpret_cast<const __half*>(src + 2 * kI8Bytes + kv * kScaleBytes) + g * kNB + blk;
         uint8_t* dstb = smem + (kv ? kSmemVh : kSmemKh) + b * kHalfTile;
         const uint8_t* srcb = src + kv * kI8Bytes;
 #pragma unroll 2
         for (int u = 0; u < kKV / 8; ++u) {
           const int cell = dw + 8 * u;
-          const int gc = j * kKV + cell;
-          const __half scale = (gc < n_cells) ? sc[((size_t)gc * kGroups + g) * kNB + blk] : __ushort_as_half(0);
+          const __half scale = sc[cell * kGroups * kNB];  // zero-filled past the cache end
           const uint2 w = *reinterpret_cast<const uint2*>(srcb + cell * kD + lane * 8);
           uint32_t o[4];
           dequant8(w.x, w.y, __half2half2(scale), o);
@@ -340,6 +345,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+bool make_scale_map(CUtensorMap* map, const __half* base, int n_cells) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)(kGroups * kNB), (cuuint64_t)n_cells};
+  const cuuint64_t strides[1] = {(cuuint64_t)(kGroups * kNB * 2)};
+  const cuuint32_t box[2] = {(cuuint32_t)(kGroups * kNB), (cuuint32_t)kKV};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<__half*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_kv_map(CUtensorMap* map, const int8_t* base, int n_cells) {
@@ -366,12 +383,14 @@ cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, cudaS
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, a.kq, a.n_cells) || !make_kv_map(&mv, a.vq, a.n_cells)) return cudaErrorInvalidValue;
+  CUtensorMap mk, mv, mks, mvs;
+  if (!make_kv_map(&mk, a.kq, a.n_cells) || !make_kv_map(&mv, a.vq, a.n_cells) ||
+      !make_scale_map(&mks, a.ksc, a.n_cells) || !make_scale_map(&mvs, a.vsc, a.n_cells))
+    return cudaErrorInvalidValue;
   const int n_ttiles = (t_end - t_begin + kTok - 1) / kTok;
   const float scale_log2 = a.p.sm_scale * kLog2e;
-  flash_dense_kernel<<<n_ttiles * 6, kThreads, kSmemAlloc, stream>>>(mk, mv, a.q, a.ksc, a.vsc, a.out, a.n_cells,
-                                                                    a.pos0, t_begin, t_end, scale_log2, a.status);
+  flash_dense_kernel<<<n_ttiles * 6, kThreads, kSmemAlloc, stream>>>(mk, mv, mks, mvs, a.q, a.out, a.pos0, t_begin,
+                                                                    t_end, scale_log2, a.status);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,116 @@
+"""GPU parity: qsa_select (ids bit-exact against the oracle's exact ranking), the gathered
+prefill path, and the end-to-end decode step (select -> partial -> merge)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int8_kv_top_gb300 import qsa, synth
+from tests.qsa_testutil import assert_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_select_prefill(inp, T, pos0, params=None, poison=True):
+    d = to_dev(inp)
+    n_cells = inp["kq"].shape[0]
+    topk = params[0] if params else 2048
+    ids = torch.full((T, 2, topk), -7 if poison else 0, dtype=torch.int32, device="cuda")
+    nbytes = qsa.qsa_select_workspace_bytes(T, pos0, n_cells, params)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") if nbytes else None
+    qsa.qsa_select(d["q"], d["kq"], d["ksc"], n_cells, T, pos0, ids, ws, params)
+    out = torch.full((T, 24, 256), float("nan"), dtype=torch.float16, device="cuda")
+    qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n_cells, T, pos0, ids, out, params)
+    qsa.qsa_check_device_status()
+    return ids.cpu().numpy(), out.float().cpu().numpy()
+
+
+def check_ids(ids_gpu, ids_ref, T, pos0, idmax):
+    sel = (pos0 + np.arange(T) + 1) > idmax
+    np.testing.assert_array_equal(ids_gpu[sel], ids_ref[sel])
+
+
+@pytest.mark.parametrize("T,pos0,params", [
+    (40, 160, (40, 71, 1 / 16)),       # every token selected, topk not a multiple of 128
+    (30, 50, (40, 71, 1 / 16)),        # mixed window: tokens 0..20 identity, the rest selected
+    (12, 400, (256, 300, 1 / 16)),     # two full gather tiles
+    (8, 2050, None),                   # default budget boundary: n_kv 2051 identity, 2052 selected
+    (96, 1984, None),                  # mixed-budget window at pos0 = 1984
+    (32, 2050, None),
+])
+def test_select_and_prefill_small(T, pos0, params):
+    inp = synth.layer_inputs(T, pos0 + T, seed=T * 7 + pos0)
+    topk, idmax, scale = params if params else (2048, 2051, 1 / 16)
+    ids, out = gpu_select_prefill(inp, T, pos0, params)
+    ref_out, ref_ids, _, _ = oracle.prefill(inp, T, pos0, topk=topk, identity_max=idmax, sm_scale=scale)
+    check_ids(ids, ref_ids, T, pos0, idmax)
+    assert_close(out, ref_out, f"T={T} pos0={pos0}")
+
+
+def test_config3_reduced_all_tokens():
+    T, pos0 = 48, 30000
+    inp = synth.layer_inputs(T, pos0 + T, seed=5)
+    ids, out = gpu_select_prefill(inp, T, pos0)
+    ref_out, ref_ids, _, differs = oracle.prefill(inp, T, pos0, f64_check=True)
+    np.testing.assert_array_equal(ids, ref_ids)
+    assert_close(out, ref_out, "T=48 pos0=30000")
+
+
+def test_config3_full_size_sampled():
+    T, pos0 = 1984, 30000
+    inp = synth.layer_inputs(T, pos0 + T, seed=5)
+    ids, out = gpu_select_prefill(inp, T, pos0)
+    toks = np.array([0, 1, 2, 127, 128, 511, 1000, 1500, 1982, 1983], dtype=np.int32)
+    ref_out, ref_ids, _, _ = oracle.prefill(inp, T, pos0, toks=toks)
+    np.testing.assert_array_equal(ids[toks], ref_ids)
+    assert_close(out[toks], ref_out, "config 3 sampled")
+    # properties at every row: ascending, unique, causal
+    assert (np.diff(ids, axis=-1) > 0).all()
+    assert (ids[..., 0] >= 0).all() and (ids[..., -1] <= pos0 + np.arange(T)[:, None]).all()
+    assert np.isfinite(out).all()
+
+
+def test_exact_ties_resolve_to_lower_index():
+    # every cell identical: all scores tie exactly; the band holds all cells (the large-band path)
+    T, pos0 = 3, 2100
+    inp = synth.layer_inputs(T, pos0 + T, seed=3)
+    inp["kq"][:] = inp["kq"][0]
+    inp["ksc"][:] = inp["ksc"][0]
+    ids, out = gpu_select_prefill(inp, T, pos0)
+    expect = np.broadcast_to(np.arange(2048, dtype=np.int32), ids.shape)
+    np.testing.assert_array_equal(ids, expect)
+
+
+def test_near_ties_from_duplicates():
+    # a few duplicated rows scattered through the cache: equal exact scores straddle the cut
+    T, pos0 = 4, 3000
+    inp = synth.layer_inputs(T, pos0 + T, seed=21)
+    src = np.arange(0, 3000, 7)
+    inp["kq"][src + 3] = inp["kq"][src]
+    inp["ksc"][src + 3] = inp["ksc"][src]
+    ids, out = gpu_select_prefill(inp, T, pos0)
+    ref_out, ref_ids, _, _ = oracle.prefill(inp, T, pos0)
+    np.testing.assert_array_equal(ids, ref_ids)
+    assert_close(out, ref_out, "duplicates")
+
+
+@pytest.mark.parametrize("N,P", [(4, 2048), (1, 8192), (4, 8192), (8, 3000), (2, 2050)])
+def test_decode_end_to_end_with_select(N, P):
+    inp = synth.layer_inputs(N, P + N, seed=200 + N + P)
+    d = to_dev(inp)
+    n_cells = P + N
+    cap = qsa.chunk_cap_for()
+    ids = torch.full((N, 2, 2048), -7, dtype=torch.int32, device="cuda")
+    nbytes = qsa.qsa_select_workspace_bytes(N, P, n_cells)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    part = torch.full((N, cap, 24, 258), float("nan"), device="cuda")
+    nch = torch.zeros(N, dtype=torch.int32, device="cuda")
+    xp = torch.full((N, 24, 256), float("nan"), device="cuda")
+    qsa.qsa_select(d["q"], d["kq"], d["ksc"], n_cells, N, P, ids, ws)
+    qsa.qsa_decode_partial(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n_cells, N, P, ids, part, nch, cap)
+    qsa.qsa_merge(part, nch, N, cap, xp)
+    qsa.qsa_check_device_status()
+    _, ref_nc, ref_out, _, ref_ids = oracle.decode(inp, N, P)
+    check_ids(ids.cpu().numpy(), ref_ids, N, P, 2051)
+    np.testing.assert_array_equal(nch.cpu().numpy(), ref_nc)
+    assert_close(xp.cpu().numpy(), ref_out, f"decode N={N} P={P}")
