@@ -148,6 +148,27 @@ QSA_API int qsa_decode_partial(const uint16_t* q, const int8_t* kq, const int8_t
 QSA_API int qsa_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp, void* stream);
 
 /*
+ * qsa_select_noalloc - qsa_select without a caller workspace.  The paper has no
+ * counterpart: this entry point exists for callers that cannot allocate device memory
+ * when they call the layer, for example a runtime whose device memory is all reserved up
+ * front by its own pool, or a plugin interface that hands the kernel only its input and
+ * output buffers.  It computes exactly what qsa_select computes, using a scratch array of
+ * 24 MiB that the library keeps in device memory on every GPU that loads it, for as long as
+ * the process lives.
+ *  - Calls whose qsa_select_workspace_bytes exceeds 24 MiB (roughly more than 16 selected
+ *    tokens, or more than 16384 cells) are rejected with QSA_ERR_UNSUPPORTED before any
+ *    launch; use qsa_select with a workspace for those.
+ *  - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *  - The first call on a device looks up the scratch array's device address (once per
+ *    device, with that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one scratch array and overwrites it.  Calls that
+ *    overlap on the GPU (different streams, or different host threads without ordering)
+ *    race on it and give wrong ids; order them on one stream or synchronize between them.
+ */
+QSA_API int qsa_select_noalloc(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_cells, int T,
+                               int pos0, int32_t* ids, const qsa_params* params, void* stream);
+
+/*
  * qsa_check_device_status - synchronize `stream`, read and clear this device's status
  * word.  Returns QSA_OK, QSA_ERR_TIMEOUT (a bounded wait inside a kernel gave up) or
  * QSA_ERR_DEVICE (an id out of range, a capacity overflow, a bad chunk count).

@@ -243,3 +243,60 @@ int qsa_check_device_status(void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// qsa_select_noalloc: qsa_select for callers that cannot allocate device memory.
+//
+// The selection kernels need scratch memory (the score matrix and its inputs).  qsa_select
+// takes it from the caller; this entry point instead uses a fixed scratch array that lives
+// in the library's own device memory, so the caller passes only its inputs and outputs.
+// The array is kNoAllocScratchBytes on every device that loads the library and stays
+// allocated until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(24) << 20;  // 24 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array on the current device, looked up once per device.
+// In host code the array's name is only a host-side stand-in, never a device address.
+void* noalloc_scratch_ptr(int* err) {
+  static void* cache[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    *err = cuda_fail(e == cudaSuccess ? cudaErrorInvalidDevice : e, "cudaGetDevice");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      *err = cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+      return nullptr;
+    }
+    cache[dev] = p;
+  }
+  return cache[dev];
+}
+
+}  // namespace
+
+extern "C" int qsa_select_noalloc(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_cells, int T,
+                                  int pos0, int32_t* ids, const qsa_params* params, void* stream) {
+  qsa::Params p;
+  int rc = resolve_params(params, &p);
+  if (rc) return rc;
+  if ((rc = check_layer(q, kq, ksc, n_cells, T, pos0))) return rc;
+  if (qsa::first_selected_token(pos0, p.identity_max) >= T) return ok();  // nothing to select
+  const size_t need = qsa::select_workspace_bytes(T, pos0, n_cells, p);
+  if (need == 0 || need > kNoAllocScratchBytes)
+    return fail(QSA_ERR_UNSUPPORTED,
+                "qsa_select_noalloc: this call needs %zu bytes of scratch but the built-in scratch holds %zu "
+                "(about 16 selected tokens over 16384 cells); use qsa_select with a caller workspace",
+                need, kNoAllocScratchBytes);
+  void* ws = noalloc_scratch_ptr(&rc);
+  if (!ws) return rc;
+  return qsa_select(q, kq, ksc, n_cells, T, pos0, ids, ws, kNoAllocScratchBytes, params, stream);
+}

@@ -28,7 +28,7 @@ N_GROUPS, HEADS_PER_GROUP, N_HEADS, HEAD_DIM, CHUNK, PART_STRIDE = 2, 12, 24, 25
 
 # every symbol include/qsa.h declares
 EXPORTS = ("qsa_last_error", "qsa_prep_quantize", "qsa_select_workspace_bytes", "qsa_select", "qsa_flash_prefill",
-           "qsa_decode_partial", "qsa_merge", "qsa_check_device_status")
+           "qsa_decode_partial", "qsa_merge", "qsa_check_device_status", "qsa_select_noalloc")
 
 
 class QSAError(RuntimeError):
@@ -64,6 +64,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_decode_partial.argtypes = [P, P, P, P, P, I, I, I, P, P, P, I, PP, P]
     lib.qsa_merge.argtypes = [P, P, I, I, P, P]
     lib.qsa_check_device_status.argtypes = [P]
+    lib.qsa_select_noalloc.argtypes = [P, P, P, I, I, I, P, PP, P]
     for name in EXPORTS:
         if name not in ("qsa_last_error", "qsa_select_workspace_bytes"):
             getattr(lib, name).restype = ctypes.c_int
@@ -116,6 +117,12 @@ def qsa_select(q, kq, ksc, n_cells: int, T: int, pos0: int, ids, ws, params=None
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(load().qsa_select(_ptr(q), _ptr(kq), _ptr(ksc), n_cells, T, pos0, _ptr(ids), _ptr(ws), ws_bytes,
                              _params(params), _stream(stream)))
+
+
+def qsa_select_noalloc(q, kq, ksc, n_cells: int, T: int, pos0: int, ids, params=None, stream=None):
+    """qsa_select on the library's built-in scratch (for callers that cannot allocate)."""
+    _check(load().qsa_select_noalloc(_ptr(q), _ptr(kq), _ptr(ksc), n_cells, T, pos0, _ptr(ids), _params(params),
+                                     _stream(stream)))
 
 
 def qsa_flash_prefill(q, kq, vq, ksc, vsc, n_cells: int, T: int, pos0: int, ids, out, params=None, stream=None):
