@@ -9,47 +9,52 @@
 // GB300 design (four launches on the caller's stream):
 //  1. prep_q:  Qsum = sum_h q over the group's 12 heads, exact in fp64; hi = fp16(Qsum);
 //              per 64-dim block E_b = sum |Qsum - hi| and H_b = sum |hi| (error norms).
-//     prep_k:  K^ = fp16(kq * ksc) for every cell that any selected token can see, and
-//              kmax_b = max |ksc| per group and block (for the error bound).
-//  2. score:   tcgen05 GEMM  s~[t][c] = fp16(sm_scale * hi[t] . K^[c])  (128 x 256 tiles,
-//              K = 256, TMA-fed 4-stage ring, double-buffered TMEM accumulators), stored
-//              only for causal cells.
-//  3. topk:    one CTA per (token, group) holds the row's scores in registers, finds the
-//              exact k-th largest s~ with two 8-bit radix passes, and bounds |s~ - s| <= d
-//              rigorously (fp16 roundings of hi, K^ and s~, fp32 accumulation).  Cells with
-//              s~ > tau + 2d are in, cells with s~ < tau - 2d are out; the band between is
-//              re-scored with EXACT integer keys (every fp16 value is an integer multiple of
-//              2^-24, so 2^48 * score / sm_scale = sum_b (ksc_b 2^24) * sum_{d in b}
-//              (Qsum_d 2^24) kq_d in 128-bit integers) and resolved by (key desc, index
-//              asc).  A band larger than the shared-memory capacity is resolved by an exact
-//              radix select over recomputed keys.  Ids are emitted in ascending order.
+//     prep_k:  int8 K codes as fp16 (exact integers) for every cell a selected token can
+//              see, and kmax_b = max |ksc| per group and block.
+//  2. score:   tcgen05 GEMM with one TMEM accumulator per 64-dim scale block:
+//                S_b[t][c] = sum_{d in b} hi[t][d] * kq[c][d]     (products exact in fp32)
+//              epilogue  s~[t][c] = fp16(sm_scale * sum_b ksc[c][b] * S_b[t][c]).
+//              128-row x 64-cell tiles, TMA-fed 4-stage ring, two accumulator sets.
+//  3. topk:    one 512-thread CTA per (token, group) holds the row's scores in registers.
+//              |s~ - s| <= a + b|s~| rigorously (a: fp16 rounding of Qsum and fp32
+//              accumulation, from E_b, H_b, kmax; b: fp16 storage), and U(f) = f + a + b|f|,
+//              L(f) = f - a - b|f| are increasing, so with tau = the k-th largest s~, cells
+//              with L(s~) > U(tau) are surely in, cells with U(s~) < L(tau) surely out.
+//              tau is found from a sampled bracket, one compare pass and an exact radix
+//              select inside the bracket (full radix passes when the bracket misses).  The
+//              band between is re-scored with EXACT integer keys (every fp16 value is an
+//              integer multiple of 2^-24, so 2^48 * score / sm_scale = sum_b (ksc_b 2^24) *
+//              sum_{d in b} (Qsum_d 2^24) kq_d, in 128-bit integers) and resolved by (key
+//              desc, index asc); a band beyond shared-memory capacity takes an exact radix
+//              select over recomputed keys.  Ids are emitted in ascending order.
 #include "common.cuh"
 
 namespace qsa {
 namespace {
 
 // ----------------------------------------------------------------- workspace layout
-constexpr int kGM = 128, kGN = 256, kGK = 64, kGStages = 4;
-constexpr int kBandCap = 2048;
-constexpr int kTopkThreads = 1024;
+constexpr int kGM = 128, kGN = 64, kGK = 64, kGStages = 4;
 constexpr int kMaxCells = 65536;
-constexpr int kTopkSmem = 32 * 256 * 4 + 256 * 8 + kBandCap * 16 + kBandCap * 4 + kMaxCells / 8;
+constexpr int kTkThreads = 512;
+constexpr int kCandCap = 4096;
+constexpr int kBandCap = 1024;
+constexpr int kTopkSmem = 2 * 256 * 4 + 256 * 8 + kCandCap * 2 + kCandCap * 4 + kBandCap * 4 + kBandCap * 16 +
+                          kMaxCells / 8;
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
   int t_sel, T_sel, T_pad, n_max, n_pad;
-  size_t off_kmax, off_eh, off_qhi, off_khat, off_scores, total;
+  size_t off_kmax, off_eh, off_qhi, off_kc, off_scores, total;
 };
 
-WsLayout ws_layout(int T, int pos0, int n_cells, Params p) {
-  (void)n_cells;
+WsLayout ws_layout(int T, int pos0, Params p) {
   WsLayout L{};
   L.t_sel = first_selected_token(pos0, p.identity_max);
   L.T_sel = T > L.t_sel ? T - L.t_sel : 0;
   L.T_pad = (int)align_up((size_t)L.T_sel, kGM);
   L.n_max = pos0 + T;  // largest n_kv of the call
-  L.n_pad = (int)align_up((size_t)L.n_max, kGN);
+  L.n_pad = (int)align_up((size_t)L.n_max, 256);
   size_t o = 0;
   L.off_kmax = o;
   o = align_up(o + 8 * sizeof(float), 1024);
@@ -57,7 +62,7 @@ WsLayout ws_layout(int T, int pos0, int n_cells, Params p) {
   o = align_up(o + (size_t)kGroups * L.T_sel * 8 * sizeof(float), 1024);
   L.off_qhi = o;
   o = align_up(o + (size_t)kGroups * L.T_pad * kD * 2, 1024);
-  L.off_khat = o;
+  L.off_kc = o;
   o = align_up(o + (size_t)kGroups * L.n_pad * kD * 2, 1024);
   L.off_scores = o;
   o = align_up(o + (size_t)kGroups * L.T_sel * L.n_pad * 2, 1024);
@@ -110,29 +115,31 @@ __global__ void __launch_bounds__(256) prep_q_kernel(const __half* __restrict__ 
   }
 }
 
-// grid (n_pad / 8, 2), 256 threads: a warp per cell row, lane = 8 dims.
+// grid (n_pad / 8, 2), 256 threads: a warp per cell row, lane = 8 codes.
 __global__ void __launch_bounds__(256) prep_k_kernel(const int8_t* __restrict__ kq, const __half* __restrict__ ksc,
-                                                     int n_max, int n_pad, __half* __restrict__ khat,
+                                                     int n_max, int n_pad, __half* __restrict__ kc,
                                                      float* __restrict__ kmax) {
   const int g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * 8 + warp;
   const int blk = lane >> 3;
   uint4 outw = make_uint4(0, 0, 0, 0);
   if (c < n_max) {
-    const __half sc = ksc[((size_t)c * kGroups + g) * kNB + blk];
     const uint2 w = *reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8);
     uint32_t o[4];
-    dequant8(w.x, w.y, __half2half2(sc), o);
+    dequant8(w.x, w.y, __half2half2(__ushort_as_half(0x3C00)), o);  // scale 1: exact codes
     outw = make_uint4(o[0], o[1], o[2], o[3]);
-    if ((lane & 7) == 0) atomicMax(reinterpret_cast<int*>(kmax) + g * kNB + blk, __float_as_int(fabsf(__half2float(sc))));
+    if ((lane & 7) == 0) {
+      const float a = fabsf(__half2float(ksc[((size_t)c * kGroups + g) * kNB + blk]));
+      atomicMax(reinterpret_cast<int*>(kmax) + g * kNB + blk, __float_as_int(a));
+    }
   }
-  if (c < n_pad) *reinterpret_cast<uint4*>(khat + ((size_t)g * n_pad + c) * kD + lane * 8) = outw;
+  if (c < n_pad) *reinterpret_cast<uint4*>(kc + ((size_t)g * n_pad + c) * kD + lane * 8) = outw;
 }
 
 // ----------------------------------------------------------------- 2. score GEMM
-constexpr int kNtPerCta = 8;
+constexpr int kNtPerCta = 32;                  // 2048 cells per CTA
 constexpr int kSmemA = kGM * kD * 2;           // 64 KB: 4 k-blocks of [128 rows][64] SW128
-constexpr int kSmemBStage = kGN * kGK * 2;     // 32 KB: [256 cells][64] SW128
+constexpr int kSmemBStage = kGN * kD * 2;      // 32 KB: 4 k-blocks of [64 cells][64] SW128
 constexpr int kScoreSmem = kSmemA + kGStages * kSmemBStage + 1024;
 
 struct __align__(8) ScoreBars {
@@ -141,8 +148,8 @@ struct __align__(8) ScoreBars {
 
 __global__ void __launch_bounds__(256, 1)
     score_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                 __half* __restrict__ scores, int T_sel, int T_pad, int n_pad, int n_base, int m_tiles,
-                 int n_chunks, float sm_scale, int* status) {
+                 const __half* __restrict__ ksc, __half* __restrict__ scores, int T_sel, int T_pad, int n_pad,
+                 int n_base, int m_tiles, int n_chunks, float sm_scale, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ ScoreBars bars;
@@ -193,16 +200,18 @@ __global__ void __launch_bounds__(256, 1)
       for (int kb = 0; kb < kD / kGK; ++kb)
         tma_load_2d(sA + kb * (kGM * 128), &map_a, &bars.a_full, kb * kGK, g * T_pad + r0);
       int issued = 0;
-      for (int u = 0; u < n_tiles * 4; ++u) {
-        const int st = u % kGStages, i = u / 4, kb = u % 4;
-        if (u >= kGStages && !mbar_wait(&bars.b_empty[st], ((u / kGStages) & 1) ^ 1, status, &s_abort)) break;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int st = i % kGStages;
+        if (i >= kGStages && !mbar_wait(&bars.b_empty[st], ((i / kGStages) & 1) ^ 1, status, &s_abort)) break;
         mbar_arrive_expect_tx(&bars.b_full[st], kSmemBStage);
-        tma_load_2d(sB + st * kSmemBStage, &map_b, &bars.b_full[st], kb * kGK, g * n_pad + (nt_begin + i) * kGN);
-        issued = u + 1;
+        for (int kb = 0; kb < kD / kGK; ++kb)
+          tma_load_2d(sB + st * kSmemBStage + kb * (kGN * 128), &map_b, &bars.b_full[st], kb * kGK,
+                      g * n_pad + (nt_begin + i) * kGN);
+        issued = i + 1;
       }
       mbar_wait(&bars.a_full, 0, status);
-      for (int u = max(0, issued - kGStages); u < issued; ++u)
-        mbar_wait(&bars.b_full[u % kGStages], (u / kGStages) & 1, status);
+      for (int i = max(0, issued - kGStages); i < issued; ++i)
+        mbar_wait(&bars.b_full[i % kGStages], (i / kGStages) & 1, status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -211,22 +220,19 @@ __global__ void __launch_bounds__(256, 1)
       bool ok = mbar_wait(&bars.a_full, 0, status, &s_abort);
       tc_fence_after();
       for (int i = 0; ok && i < n_tiles; ++i) {
-        const int a = i & 1;
+        const int a = i & 1, st = i % kGStages;
         if (i >= 2 && !mbar_wait(&bars.acc_empty[a], ((i >> 1) & 1) ^ 1, status, &s_abort)) { ok = false; break; }
+        if (!mbar_wait(&bars.b_full[st], (i / kGStages) & 1, status, &s_abort)) { ok = false; break; }
         tc_fence_after();
-        for (int kb = 0; kb < 4; ++kb) {
-          const int u = i * 4 + kb, st = u % kGStages;
-          if (!mbar_wait(&bars.b_full[st], (u / kGStages) & 1, status, &s_abort)) { ok = false; break; }
-          tc_fence_after();
+#pragma unroll
+        for (int b = 0; b < kNB; ++b)
 #pragma unroll
           for (int kk = 0; kk < kGK / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(a0 + kb * (kGM * 128) + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b0 + st * kSmemBStage + kk * 32, 16, 1024);
-            umma_ss(tmem + a * kGN, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t ad = sdesc_sw128(a0 + b * (kGM * 128) + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + st * kSmemBStage + b * (kGN * 128) + kk * 32, 16, 1024);
+            umma_ss(tmem + a * 256 + b * kGN, ad, bd, idesc, kk > 0 ? 1u : 0u);
           }
-          umma_commit(&bars.b_empty[st]);
-        }
-        if (!ok) break;
+        umma_commit(&bars.b_empty[st]);
         umma_commit(&bars.acc_full[a]);
       }
       umma_commit(&bars.drain);
@@ -247,15 +253,26 @@ __global__ void __launch_bounds__(256, 1)
       const int n0 = (nt_begin + i) * kGN;
 #pragma unroll 1
       for (int c0 = 0; c0 < kGN; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + a * kGN + c0, v);
-        tmem_wait_ld();
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+#pragma unroll 1
+        for (int b = 0; b < kNB; ++b) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + a * 256 + b * kGN + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = n0 + c0 + j;  // cells past the row's causal range are neither read nor stored
+            const float sc = (c < n_kv) ? __half2float(__ldg(ksc + ((size_t)c * kGroups + g) * kNB + b)) : 0.f;
+            acc[j] = fmaf(sc, __uint_as_float(v[j]), acc[j]);
+          }
+        }
         const int cell0 = n0 + c0;
         if (row_valid && cell0 < n_kv) {
           uint32_t w[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            w[j] = pack_half2(__uint_as_float(v[2 * j]) * sm_scale, __uint_as_float(v[2 * j + 1]) * sm_scale);
+          for (int j = 0; j < 16; ++j) w[j] = pack_half2(acc[2 * j] * sm_scale, acc[2 * j + 1] * sm_scale);
           if (cell0 + 32 <= n_kv) {
             uint4* d4 = reinterpret_cast<uint4*>(dst_row + cell0);
 #pragma unroll
@@ -317,7 +334,7 @@ __device__ __forceinline__ float order_key_to_float(uint32_t k) {
   return __half2float(__ushort_as_half(b));
 }
 
-// Block-wide sum of one int per thread (1024 threads).
+// Block-wide sum of one int per thread.
 __device__ __forceinline__ int block_sum(int v, int* s_red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -331,7 +348,7 @@ __device__ __forceinline__ int block_sum(int v, int* s_red) {
   return t;
 }
 
-// Block-wide exclusive prefix sum (1024 threads); returns this thread's offset.
+// Block-wide exclusive prefix sum; returns this thread's offset.
 __device__ __forceinline__ int block_excl_scan(int v, int* s_red, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -403,53 +420,78 @@ __device__ __forceinline__ int find_bin_desc(const unsigned* hist, int need, int
   return b;
 }
 
+// Warp-aggregated append of (this lane's) item to a shared list; returns its slot or -1.
+__device__ __forceinline__ int warp_append(bool pred, int* counter) {
+  const unsigned m = __ballot_sync(0xffffffffu, pred);
+  if (!m) return -1;
+  const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(counter, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return pred ? base + __popc(m & ((1u << lane) - 1u)) : -1;
+}
+
+// Warp-aggregated histogram increment (lanes with equal bins add once).
+__device__ __forceinline__ void warp_hist_add(bool pred, unsigned bin, unsigned* hist) {
+  const unsigned active = __ballot_sync(0xffffffffu, pred);
+  if (!pred) return;
+  const unsigned peers = __match_any_sync(active, bin);
+  if ((threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
+}
+
+// Bounds of the score error: a (absolute) and b (relative to the stored fp16 value).
+struct Bound {
+  float a, b;
+  __device__ float U(float f) const { return f + a + b * fabsf(f); }
+  __device__ float L(float f) const { return f - a - b * fabsf(f); }
+};
+
 template <int V>
-__global__ void __launch_bounds__(kTopkThreads, 1)
+__global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
     topk_kernel(const __half* __restrict__ scores, const __half* __restrict__ q, const int8_t* __restrict__ kq,
                 const __half* __restrict__ ksc, const float* __restrict__ eh, const float* __restrict__ kmax,
                 int32_t* __restrict__ ids, int t_sel, int T_sel, int n_pad, int pos0, int K, float sm_scale,
                 int* status) {
   extern __shared__ __align__(16) uint8_t topk_smem[];
-  auto s_hist = reinterpret_cast<unsigned(*)[256]>(topk_smem);                     // [32][256]
-  long long* s_qsum = reinterpret_cast<long long*>(topk_smem + 32 * 256 * 4);    // [256]
-  Key128* s_band_key = reinterpret_cast<Key128*>(topk_smem + 32 * 256 * 4 + kD * 8);
-  int* s_band_idx = reinterpret_cast<int*>(s_band_key + kBandCap);
-  unsigned* s_bits = reinterpret_cast<unsigned*>(s_band_idx + kBandCap);       // [kMaxCells / 32]
+  unsigned* s_hist = reinterpret_cast<unsigned*>(topk_smem);                         // [2][256]
+  long long* s_qsum = reinterpret_cast<long long*>(topk_smem + 2 * 256 * 4);         // [256]
+  Key128* s_band_key = reinterpret_cast<Key128*>(s_qsum + kD);                       // [kBandCap]
+  int* s_band_idx = reinterpret_cast<int*>(s_band_key + kBandCap);                   // [kBandCap]
+  int* s_cand_idx = s_band_idx + kBandCap;                                           // [kCandCap]
+  uint16_t* s_cand_key = reinterpret_cast<uint16_t*>(s_cand_idx + kCandCap);         // [kCandCap]
+  unsigned* s_bits = reinterpret_cast<unsigned*>(s_cand_key + kCandCap);             // [kMaxCells / 32]
   __shared__ int s_red[64];
   __shared__ int s_tmp[8];
-  __shared__ float s_delta;
-  __shared__ int s_band_n;
+  __shared__ int s_cnt[4];  // 0: candidates, 1: band
+  __shared__ Bound s_bound;
 
   const int r = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = kTkThreads / 32;
   const int t = t_sel + r;
   const int n_kv = pos0 + t + 1;
   const __half* row = scores + ((size_t)g * T_sel + r) * n_pad;
 
-  // exact Qsum in units of 2^-24
-  if (tid < kD) {
-    long long s = 0;
+  if (tid < kD) {  // exact Qsum in units of 2^-24
+    long long sq = 0;
     const __half* qt = q + ((size_t)t * kHeads + g * kHPG) * kD + tid;
 #pragma unroll
-    for (int h = 0; h < kHPG; ++h) s += half_int24(__half_as_ushort(qt[h * kD]));
-    s_qsum[tid] = s;
+    for (int h = 0; h < kHPG; ++h) sq += half_int24(__half_as_ushort(qt[h * kD]));
+    s_qsum[tid] = sq;
   }
-  for (int i = tid; i < kMaxCells / 32; i += kTopkThreads) s_bits[i] = 0u;
+  for (int i = tid; i < (n_kv + 31) / 32; i += kTkThreads) s_bits[i] = 0u;
+  for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
   if (tid == 0) {
-    // |s~ - s| <= d: fp16 rounding of Qsum (E), of K^ (2^-11 relative) and fp32
-    // accumulation (2^-14 of the absolute sum) over |kq| <= 128; fp16 rounding of s~
-    // (2^-11 of its bound); doubled for margin.
+    // |s~ - s| <= a + b |s~|: a covers the fp16 rounding of Qsum (E_b) and the fp32
+    // accumulation of 64 exact products per block (64 * 2^-23 of the absolute sum, with
+    // |kq| <= 128) plus the epilogue's roundings (2^-21); b covers the fp16 rounding of the
+    // stored score.  Both doubled for margin.
     const float* e = eh + ((size_t)g * T_sel + r) * 8;
-    float sum_eh = 0.f, sum_h = 0.f, smax = 0.f;
-    for (int b = 0; b < kNB; ++b) {
-      const float km = kmax[g * kNB + b];
-      sum_eh += km * (e[b] + (0.00048828125f + 0.00006103515625f + 0.0000002384185791f) * e[kNB + b]);
-      sum_h += e[kNB + b];
-      smax += km * (e[b] + e[kNB + b]);
-    }
-    const float bound_s = sm_scale * 128.f * smax * 1.001f;
-    s_delta = 2.f * (sm_scale * (128.f * sum_eh + 2.9802322e-08f * sum_h) + 0.00048828125f * bound_s + 6.0e-8f);
-    s_band_n = 0;
-    if (!(bound_s < 60000.f)) set_dev_status(status, QSA_DEV_BAND_OVERFLOW);  // scores would overflow fp16
+    float acc = 0.f;
+    for (int b = 0; b < kNB; ++b) acc += kmax[g * kNB + b] * (e[b] + e[kNB + b] * (7.6293945e-06f + 4.7683716e-07f));
+    s_bound.a = 2.f * (sm_scale * 128.f * acc + 1.2e-7f);
+    s_bound.b = 2.f * 4.8852e-04f;
+    s_cnt[0] = 0;
+    s_cnt[1] = 0;
   }
 
   // this thread's cells [tid*V, tid*V + V)
@@ -464,74 +506,165 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     hv[4 * i + 2] = w.z;
     hv[4 * i + 3] = w.w;
   }
-  auto hbits = [&](int j) -> uint16_t { return (uint16_t)(hv[j >> 1] >> (16 * (j & 1))); };
   auto valid = [&](int j) -> bool { return c0 + j < n_kv; };
+  auto key = [&](int j) -> uint32_t {  // order key; 0 for cells outside the causal range
+    return valid(j) ? fp16_order_key((uint16_t)(hv[j >> 1] >> (16 * (j & 1)))) : 0u;
+  };
+  auto fval = [&](uint32_t k) -> float { return order_key_to_float(k); };
+  __syncthreads();
 
-  // radix pass 1: high byte of the order key
-  for (int i = tid; i < 32 * 256; i += kTopkThreads) (&s_hist[0][0])[i] = 0u;
-  __syncthreads();
+  // ---- tau: bracket from a 1-in-8 sample, then one compare pass
+  int n_samp = 0;
 #pragma unroll
-  for (int j = 0; j < V; ++j)
-    if (valid(j)) atomicAdd(&s_hist[warp][fp16_order_key(hbits(j)) >> 8], 1u);
-  __syncthreads();
-  if (tid < 256) {
-    unsigned s = 0;
-    for (int w = 0; w < 32; ++w) s += s_hist[w][tid];
-    s_hist[0][tid] = s;
-  }
-  __syncthreads();
-  int above1;
-  const int b1 = find_bin_desc(s_hist[0], K, &above1, s_tmp);
-  // pass 2: low byte among keys whose high byte is b1
-  for (int i = tid; i < 32 * 256; i += kTopkThreads) (&s_hist[0][0])[i] = 0u;
-  __syncthreads();
+  for (int j = 0; j < V; j += 8) n_samp += valid(j);
+  n_samp = block_sum(n_samp, s_red);
+  uint32_t key_hi = 0xFFFFu, key_lo = 1u;
+  bool bracket = n_samp >= 64 && 8 * K < n_kv;
+  if (bracket) {
+    const float ks = (float)K * n_samp / n_kv;
+    const int margin = (int)(3.f * sqrtf(ks) + 16.f);
+    const int r_hi = (int)ks - margin;          // sample ranks (1-based) bracketing the k-th
+    const int r_lo = (int)ceilf(ks) + margin;
 #pragma unroll
-  for (int j = 0; j < V; ++j) {
-    const uint32_t k = fp16_order_key(hbits(j));
-    if (valid(j) && (int)(k >> 8) == b1) atomicAdd(&s_hist[warp][k & 0xFFu], 1u);
+    for (int j = 0; j < V; j += 8) warp_hist_add(valid(j), key(j) >> 8, s_hist);
+    __syncthreads();
+    int ab_hi = 0, ab_lo = 0, b_hi = -1, b_lo = -1;
+    if (r_hi >= 1) b_hi = find_bin_desc(s_hist, r_hi, &ab_hi, s_tmp);
+    if (r_lo <= n_samp) b_lo = find_bin_desc(s_hist, r_lo, &ab_lo, s_tmp);
+    for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < V; j += 8) {
+      const uint32_t k = key(j);
+      warp_hist_add(valid(j) && (int)(k >> 8) == b_hi, k & 0xFFu, s_hist);
+      warp_hist_add(valid(j) && (int)(k >> 8) == b_lo, k & 0xFFu, s_hist + 256);
+    }
+    __syncthreads();
+    int dummy;
+    if (b_hi >= 0) key_hi = ((uint32_t)b_hi << 8) | (uint32_t)find_bin_desc(s_hist, r_hi - ab_hi, &dummy, s_tmp);
+    if (b_lo >= 0) key_lo = ((uint32_t)b_lo << 8) | (uint32_t)find_bin_desc(s_hist + 256, r_lo - ab_lo, &dummy, s_tmp);
+    if (key_lo < 1u) key_lo = 1u;
+  }
+  // one pass: count above the bracket, collect the bracket
+  int above = 0;
+  if (bracket) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const uint32_t k = key(j);
+      above += (k > key_hi);
+      const bool in = valid(j) && k >= key_lo && k <= key_hi;
+      const int slot = warp_append(in, &s_cnt[0]);
+      if (slot >= 0 && slot < kCandCap) {
+        s_cand_key[slot] = (uint16_t)k;
+        s_cand_idx[slot] = c0 + j;
+      }
+    }
+  }
+  const int A0 = block_sum(above, s_red);
+  const int Cn = s_cnt[0];
+  const int need_c = K - A0;
+  bracket = bracket && Cn <= kCandCap && need_c >= 1 && need_c <= Cn;
+  uint32_t tau_key;
+  for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
+  __syncthreads();
+  if (bracket) {  // exact (need_c)-th largest key among the candidates (warp-uniform loop)
+    for (int base = warp * 32; base < Cn; base += kTkThreads) {
+      const int i = base + lane;
+      warp_hist_add(i < Cn, i < Cn ? (unsigned)(s_cand_key[i] >> 8) : 0u, s_hist);
+    }
   }
   __syncthreads();
-  if (tid < 256) {
-    unsigned s = 0;
-    for (int w = 0; w < 32; ++w) s += s_hist[w][tid];
-    s_hist[0][tid] = s;
+  if (bracket) {
+    int ab1;
+    const int b1 = find_bin_desc(s_hist, need_c, &ab1, s_tmp);
+    for (int i = tid; i < Cn; i += kTkThreads)
+      if ((int)(s_cand_key[i] >> 8) == b1) atomicAdd(&s_hist[256 + (s_cand_key[i] & 0xFFu)], 1u);
+    __syncthreads();
+    int ab2;
+    const int b2 = find_bin_desc(s_hist + 256, need_c - ab1, &ab2, s_tmp);
+    tau_key = ((uint32_t)b1 << 8) | (uint32_t)b2;
+  } else {  // full radix over every value
+#pragma unroll
+    for (int j = 0; j < V; ++j) warp_hist_add(valid(j), key(j) >> 8, s_hist);
+    __syncthreads();
+    int ab1;
+    const int b1 = find_bin_desc(s_hist, K, &ab1, s_tmp);
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const uint32_t k = key(j);
+      warp_hist_add(valid(j) && (int)(k >> 8) == b1, k & 0xFFu, s_hist + 256);
+    }
+    __syncthreads();
+    int ab2;
+    const int b2 = find_bin_desc(s_hist + 256, K - ab1, &ab2, s_tmp);
+    tau_key = ((uint32_t)b1 << 8) | (uint32_t)b2;
   }
-  __syncthreads();
-  int above2;
-  const int b2 = find_bin_desc(s_hist[0], K - above1, &above2, s_tmp);
-  if (b1 < 0 || b2 < 0) {  // cannot happen for consistent counts; leave the row unwritten
+  if (tau_key == 0u) {  // cannot happen with K <= n_kv; leave the row unwritten
     if (tid == 0) set_dev_status(status, QSA_DEV_BAND_OVERFLOW);
     return;
   }
-  const float tau = order_key_to_float(((uint32_t)b1 << 8) | (uint32_t)b2);
-  const float delta = s_delta;
-  const float band_hi = tau + 2.f * delta, band_lo = tau - 2.f * delta;
 
-  // classify: definitely in (above the band) and band members
-  int n_in = 0;
+  // ---- band: surely in (L(f) > U(tau)), undecided (U(f) >= L(tau))
+  const Bound bd = s_bound;
+  const float tau = fval(tau_key);
+  const float Ut = bd.U(tau), Lt = bd.L(tau);
+  // every cell above the bracket must be surely in, every cell below it surely out
+  if (bracket) {
+    const bool hi_ok = key_hi == 0xFFFFu || bd.L(fval(key_hi + 1u)) > Ut;
+    const bool lo_ok = key_lo <= 1u || bd.U(fval(key_lo - 1u)) < Lt;
+    bracket = hi_ok && lo_ok;
+  }
+  int n_def = 0;
+  if (bracket) {
+    for (int i = tid; i < Cn; i += kTkThreads) {
+      const float f = fval(s_cand_key[i]);
+      if (bd.L(f) > Ut) {
+        ++n_def;
+      } else if (bd.U(f) >= Lt) {
+        const int slot = atomicAdd(&s_cnt[1], 1);
+        if (slot < kBandCap) s_band_idx[slot] = s_cand_idx[i];
+      }
+    }
+  } else {
 #pragma unroll
-  for (int j = 0; j < V; ++j) {
-    if (!valid(j)) continue;
-    const float f = __half2float(__ushort_as_half(hbits(j)));
-    if (f > band_hi) {
-      ++n_in;
-    } else if (f >= band_lo) {
-      const int slot = atomicAdd(&s_band_n, 1);
-      if (slot < kBandCap) s_band_idx[slot] = c0 + j;
+    for (int j = 0; j < V; ++j) {
+      const float f = fval(key(j));
+      const bool def = valid(j) && bd.L(f) > Ut;
+      n_def += def;
+      const int slot = warp_append(valid(j) && !def && bd.U(f) >= Lt, &s_cnt[1]);
+      if (slot >= 0 && slot < kBandCap) s_band_idx[slot] = c0 + j;
     }
   }
-  const int A = block_sum(n_in, s_red);
-  const int B = s_band_n;
+  const int A = (bracket ? A0 : 0) + block_sum(n_def, s_red);
+  const int B = s_cnt[1];
   const int need = K - A;  // 1 <= need <= B by construction
 
   if (B <= kBandCap) {
-    // exact keys of the band, then rank by (key desc, index asc)
-    for (int i = tid; i < B; i += kTopkThreads) {
+    // exact keys, one warp per band cell: lane = 8 codes of block lane/8
+    for (int i = warp; i < B; i += nwarps) {
       const int c = s_band_idx[i];
-      s_band_key[i] = split128(exact_key(s_qsum, kq + ((size_t)c * kGroups + g) * kD, ksc + ((size_t)c * kGroups + g) * kNB));
+      const uint2 w = *reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8);
+      long long part = 0;
+#pragma unroll
+      for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + by] * (long long)(int8_t)(w.x >> (8 * by));
+#pragma unroll
+      for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + 4 + by] * (long long)(int8_t)(w.y >> (8 * by));
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      part += __shfl_xor_sync(0xffffffffu, part, 4);
+      const long long p1 = __shfl_sync(0xffffffffu, part, 8), p2 = __shfl_sync(0xffffffffu, part, 16),
+                      p3 = __shfl_sync(0xffffffffu, part, 24);
+      if (lane == 0) {
+        const __half* sr = ksc + ((size_t)c * kGroups + g) * kNB;
+        __int128 k128 = (__int128)half_int24(__half_as_ushort(sr[0])) * part;
+        k128 += (__int128)half_int24(__half_as_ushort(sr[1])) * p1;
+        k128 += (__int128)half_int24(__half_as_ushort(sr[2])) * p2;
+        k128 += (__int128)half_int24(__half_as_ushort(sr[3])) * p3;
+        s_band_key[i] = split128(k128);
+      }
     }
     __syncthreads();
-    for (int i = tid; i < B; i += kTopkThreads) {
+    for (int i = tid; i < B; i += kTkThreads) {
       const Key128 ki = s_band_key[i];
       const int ci = s_band_idx[i];
       int rank = 0;
@@ -544,43 +677,37 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   } else {
     // large band (many near-ties): exact radix select over the band, keys recomputed per
     // pass, 16 passes of 8 bits over the biased 128-bit key
-    unsigned long long pre_hi = 0, pre_lo = 0;  // fixed prefix bits of the biased key
+    unsigned long long pre_hi = 0, pre_lo = 0;
     int rem = need;
     for (int pass = 0; pass < 16; ++pass) {
-      for (int i = tid; i < 256; i += kTopkThreads) s_hist[0][i] = 0u;
+      for (int i = tid; i < 256; i += kTkThreads) s_hist[i] = 0u;
       __syncthreads();
-      const int shift = 120 - 8 * pass;  // bit position of this digit
+      const int shift = 120 - 8 * pass;
       for (int j = 0; j < V; ++j) {
-        if (!valid(j)) continue;
-        const float f = __half2float(__ushort_as_half(hbits(j)));
-        if (f > band_hi || f < band_lo) continue;
+        const float f = fval(key(j));
+        if (!valid(j) || bd.L(f) > Ut || bd.U(f) < Lt) continue;
         const int c = c0 + j;
         unsigned __int128 kb = (unsigned __int128)exact_key(s_qsum, kq + ((size_t)c * kGroups + g) * kD,
                                                             ksc + ((size_t)c * kGroups + g) * kNB);
         kb ^= (unsigned __int128)1 << 127;
         const unsigned __int128 pre = ((unsigned __int128)pre_hi << 64) | pre_lo;
-        const bool match = (pass == 0) || ((kb >> (shift + 8)) == (pre >> (shift + 8)));
-        if (match) atomicAdd(&s_hist[0][(unsigned)(kb >> shift) & 0xFFu], 1u);
+        if (pass == 0 || (kb >> (shift + 8)) == (pre >> (shift + 8))) atomicAdd(&s_hist[(unsigned)(kb >> shift) & 0xFFu], 1u);
       }
       __syncthreads();
-      int above;
-      const int bin = find_bin_desc(s_hist[0], rem, &above, s_tmp);
-      rem -= above;
+      int ab;
+      const int bin = find_bin_desc(s_hist, rem, &ab, s_tmp);
+      rem -= ab;
       unsigned __int128 pre = ((unsigned __int128)pre_hi << 64) | pre_lo;
       pre |= (unsigned __int128)(unsigned)bin << shift;
       pre_hi = (unsigned long long)(pre >> 64);
       pre_lo = (unsigned long long)pre;
     }
-    // pre = the need-th largest biased key; take every band key above it and the `rem`
-    // lowest-index cells equal to it
     const unsigned __int128 kstar = ((unsigned __int128)pre_hi << 64) | pre_lo;
     int n_tie = 0;
-    unsigned tie_mask = 0;  // bit j: cell j of this thread ties (V <= 32 keeps it in one word)
-    unsigned long long tie_mask_hi = 0;
+    unsigned long long tie_lo = 0, tie_hi = 0;
     for (int j = 0; j < V; ++j) {
-      if (!valid(j)) continue;
-      const float f = __half2float(__ushort_as_half(hbits(j)));
-      if (f > band_hi || f < band_lo) continue;
+      const float f = fval(key(j));
+      if (!valid(j) || bd.L(f) > Ut || bd.U(f) < Lt) continue;
       const int c = c0 + j;
       unsigned __int128 kb = (unsigned __int128)exact_key(s_qsum, kq + ((size_t)c * kGroups + g) * kD,
                                                           ksc + ((size_t)c * kGroups + g) * kNB);
@@ -588,14 +715,14 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
       if (kb > kstar) atomicOr(&s_bits[c >> 5], 1u << (c & 31));
       if (kb == kstar) {
         ++n_tie;
-        if (j < 32) tie_mask |= 1u << j;
-        else tie_mask_hi |= 1ull << (j - 32);
+        if (j < 64) tie_lo |= 1ull << j;
+        else tie_hi |= 1ull << (j - 64);
       }
     }
     int total_ties;
     int before = block_excl_scan(n_tie, s_red, &total_ties);
     for (int j = 0; j < V; ++j) {
-      const bool tie = (j < 32) ? ((tie_mask >> j) & 1u) : ((tie_mask_hi >> (j - 32)) & 1ull);
+      const bool tie = (j < 64) ? ((tie_lo >> j) & 1ull) : ((tie_hi >> (j - 64)) & 1ull);
       if (tie) {
         if (before < rem) atomicOr(&s_bits[(c0 + j) >> 5], 1u << ((c0 + j) & 31));
         ++before;
@@ -604,32 +731,32 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   }
   __syncthreads();
 
-  // emit ascending ids: above-band cells plus the band cells chosen above
+  // ---- emit ascending ids: surely-in cells plus the band cells chosen above
   int n_keep = 0;
-  uint64_t keep = 0;
+  unsigned long long keep_lo = 0, keep_hi = 0;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
     if (!valid(j)) continue;
     const int c = c0 + j;
-    const float f = __half2float(__ushort_as_half(hbits(j)));
-    const bool k = (f > band_hi) || ((s_bits[c >> 5] >> (c & 31)) & 1u);
+    const bool k = bd.L(fval(key(j))) > Ut || ((s_bits[c >> 5] >> (c & 31)) & 1u);
     if (k) {
-      keep |= 1ull << j;
+      if (j < 64) keep_lo |= 1ull << j;
+      else keep_hi |= 1ull << (j - 64);
       ++n_keep;
     }
   }
   int total;
   int pos = block_excl_scan(n_keep, s_red, &total);
-  if (total != K) {
-    if (tid == 0) set_dev_status(status, QSA_DEV_BAND_OVERFLOW);
-  }
+  if (total != K && tid == 0) set_dev_status(status, QSA_DEV_BAND_OVERFLOW);
   int32_t* dst = ids + ((size_t)t * kGroups + g) * K;
 #pragma unroll
-  for (int j = 0; j < V; ++j)
-    if ((keep >> j) & 1ull) {
+  for (int j = 0; j < V; ++j) {
+    const bool k = (j < 64) ? ((keep_lo >> j) & 1ull) : ((keep_hi >> (j - 64)) & 1ull);
+    if (k) {
       if (pos < K) dst[pos] = c0 + j;
       ++pos;
     }
+  }
 }
 
 bool make_2d_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
@@ -648,7 +775,8 @@ bool make_2d_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ou
 }  // namespace
 
 size_t select_workspace_bytes(int T, int pos0, int n_cells, Params p) {
-  const WsLayout L = ws_layout(T, pos0, n_cells, p);
+  (void)n_cells;
+  const WsLayout L = ws_layout(T, pos0, p);
   if (L.T_sel == 0) return 0;
   if (L.n_max > kMaxCells || p.topk > kMaxCells) return 0;
   return L.total;
@@ -656,19 +784,20 @@ size_t select_workspace_bytes(int T, int pos0, int n_cells, Params p) {
 
 cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, int n_cells, int T, int pos0,
                           int32_t* ids, void* ws, Params p, int* status, cudaStream_t stream) {
-  const WsLayout L = ws_layout(T, pos0, n_cells, p);
+  (void)n_cells;
+  const WsLayout L = ws_layout(T, pos0, p);
   if (L.T_sel == 0) return cudaSuccess;
   uint8_t* base = static_cast<uint8_t*>(ws);
   float* kmax = reinterpret_cast<float*>(base + L.off_kmax);
   float* eh = reinterpret_cast<float*>(base + L.off_eh);
   __half* qhi = reinterpret_cast<__half*>(base + L.off_qhi);
-  __half* khat = reinterpret_cast<__half*>(base + L.off_khat);
+  __half* kc = reinterpret_cast<__half*>(base + L.off_kc);
   __half* sc = reinterpret_cast<__half*>(base + L.off_scores);
 
   cudaError_t e = cudaMemsetAsync(kmax, 0, 8 * sizeof(float), stream);
   if (e != cudaSuccess) return e;
   prep_q_kernel<<<dim3(L.T_pad, kGroups), 256, 0, stream>>>(q, L.t_sel, L.T_sel, L.T_pad, qhi, eh);
-  prep_k_kernel<<<dim3(L.n_pad / 8, kGroups), 256, 0, stream>>>(kq, ksc, L.n_max, L.n_pad, khat, kmax);
+  prep_k_kernel<<<dim3(L.n_pad / 8, kGroups), 256, 0, stream>>>(kq, ksc, L.n_max, L.n_pad, kc, kmax);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   static bool attr_done[64] = {};
@@ -682,27 +811,29 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
   }
   CUtensorMap ma, mb;
   if (!make_2d_map(&ma, qhi, kD, (uint64_t)kGroups * L.T_pad, kGK, kGM) ||
-      !make_2d_map(&mb, khat, kD, (uint64_t)kGroups * L.n_pad, kGK, kGN))
+      !make_2d_map(&mb, kc, kD, (uint64_t)kGroups * L.n_pad, kGK, kGN))
     return cudaErrorInvalidValue;
   const int m_tiles = L.T_pad / kGM;
   const int n_tiles = L.n_pad / kGN;
   const int n_chunks = (n_tiles + kNtPerCta - 1) / kNtPerCta;
   const int n_base = pos0 + L.t_sel;  // n_kv of selected row r is n_base + r + 1
-  score_kernel<<<kGroups * m_tiles * n_chunks, 256, kScoreSmem, stream>>>(ma, mb, sc, L.T_sel, L.T_pad, L.n_pad, n_base,
-                                                                         m_tiles, n_chunks, p.sm_scale, status);
+  score_kernel<<<kGroups * m_tiles * n_chunks, 256, kScoreSmem, stream>>>(ma, mb, ksc, sc, L.T_sel, L.T_pad, L.n_pad,
+                                                                         n_base, m_tiles, n_chunks, p.sm_scale,
+                                                                         status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const dim3 grid(L.T_sel, kGroups);
   auto run = [&](auto kern) -> cudaError_t {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmem);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kTopkThreads, kTopkSmem, stream>>>(sc, q, kq, ksc, eh, kmax, ids, L.t_sel, L.T_sel, L.n_pad, pos0,
-                                                    p.topk, p.sm_scale, status);
+    kern<<<grid, kTkThreads, kTopkSmem, stream>>>(sc, q, kq, ksc, eh, kmax, ids, L.t_sel, L.T_sel, L.n_pad, pos0,
+                                                  p.topk, p.sm_scale, status);
     return cudaGetLastError();
   };
-  if (L.n_max <= 16 * kTopkThreads) return run(topk_kernel<16>);
-  if (L.n_max <= 32 * kTopkThreads) return run(topk_kernel<32>);
-  return run(topk_kernel<64>);
+  if (L.n_max <= 16 * kTkThreads) return run(topk_kernel<16>);
+  if (L.n_max <= 32 * kTkThreads) return run(topk_kernel<32>);
+  if (L.n_max <= 64 * kTkThreads) return run(topk_kernel<64>);
+  return run(topk_kernel<128>);
 }
 
 }  // namespace qsa
