@@ -10,9 +10,12 @@
 //   S^T[c][h]  = K^[c] . q[h]      A = K^ (128 cells, K-major)  B = Q^T (16 rows, 12 used)
 //   O^T[d][h] += V^[c][d] P[h][c]  A = V^ as MN-major (dims x cells)  B = P^T (K-major)
 //
-//   warps 8-15  warp-cooperative gathers: each lane loads 8 code bytes of a cell row
-//               (16 rows in flight per warp), dequantises with the cell's fp16 scale and
-//               stores fp16 into the 128B-swizzled K^ / V^ tiles; also the Q^T tile
+//   warps 1, 2  gather producers: 16-byte cp.async copies of the selected cell rows (256
+//               code bytes; each warp instruction moves two rows) and scale rows into K and
+//               V staging rings of two 64-cell half-tiles; V runs one tile behind K, in the
+//               order the MMAs need them (row-sized TMA bulk copies were issue-bound)
+//   warps 8-11  dequantise staged K rows with their fp16 scales into the 128B-swizzled K^
+//               tile (and load each item's Q^T tile); warps 12-15 do the same for V^
 //   warp 0      TMEM owner and single-thread UMMA issue
 //   warps 4-7   one gathered cell per thread (TMEM lane): column-wise online softmax over
 //               the 128 cells (shuffle + shared-memory max per head, base-2 exponent),
@@ -31,13 +34,18 @@ constexpr int kThreads = 512;
 constexpr int kTileHalf = kCells * kD * 2;   // 64 KB fp16 tile
 constexpr int kQBytes = kNQ * kD * 2;        // 8 KB
 constexpr int kPBytes = kNQ * kCells * 2;    // 4 KB
+constexpr int kHalfCells = 64;                               // cells per staging half-tile
+constexpr int kStageCodes = kHalfCells * kD;                   // 16 KB of int8 codes
+constexpr int kStageBytes = kStageCodes + kHalfCells * 16;     // + one 16-byte scale row per cell
 constexpr int kOffK = 0, kOffV = kTileHalf, kOffQ = 2 * kTileHalf, kOffP = kOffQ + 2 * kQBytes;
-constexpr int kSmemTotal = kOffP + 2 * kPBytes;
+constexpr int kOffKSt = kOffP + 2 * kPBytes, kOffVSt = kOffKSt + 2 * kStageBytes;
+constexpr int kSmemTotal = kOffVSt + 2 * kStageBytes;
 constexpr int kSmemAlloc = kSmemTotal + 1024;
 constexpr uint32_t kColS = 0, kColO = 32;
 constexpr float kRescaleThreshold = 8.0f;
 
 struct __align__(8) GBars {
+  uint64_t kst_full[2], kst_empty[2], vst_full[2], vst_empty[2];
   uint64_t q_full[2], q_empty[2];
   uint64_t kh_full, kh_empty, vh_full, vh_empty;
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
@@ -65,16 +73,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     s_abort = 0;
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.q_full[i], 8);
+      mbar_init(&bars.kst_full[i], 32);
+      mbar_init(&bars.kst_empty[i], 4);
+      mbar_init(&bars.vst_full[i], 32);
+      mbar_init(&bars.vst_empty[i], 4);
+      mbar_init(&bars.q_full[i], 4);
       mbar_init(&bars.q_empty[i], 1);
       mbar_init(&bars.s_full[i], 1);
       mbar_init(&bars.p_full[i], 4);
       mbar_init(&bars.o_done[i], 1);
       mbar_init(&bars.o_free[i], 4);
     }
-    mbar_init(&bars.kh_full, 8);
+    mbar_init(&bars.kh_full, 4);
     mbar_init(&bars.kh_empty, 1);
-    mbar_init(&bars.vh_full, 8);
+    mbar_init(&bars.vh_full, 4);
     mbar_init(&bars.vh_empty, 1);
     mbar_init(&bars.drain, 1);
     fence_mbar_init();
@@ -174,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = idrow[slot];
           valid = c >= 0 && c < n_kv;
         }
-        if (!mbar_wait_warp(&bars.s_full[u & 1], (u >> 1) & 1, status, &s_abort)) { ok = false; break; }
+        const bool w_ok = mbar_wait_warp(&bars.s_full[u & 1], (u >> 1) & 1, status, &s_abort);
+        if (named_bar_any(1, 128, !w_ok)) { ok = false; break; }  // all four warps leave together
         tc_fence_after();
         uint32_t sr[16];
         tmem_ld16(lane_base + kColS + (u & 1) * 16, sr);
@@ -205,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (need_any) {  // uniform: every thread derived it from the same shared maxima
-          if (!mbar_wait_warp(&bars.o_done[(u - 1) & 1], ((u - 1) >> 1) & 1, status, &s_abort)) { ok = false; break; }
+          const bool r_ok = mbar_wait_warp(&bars.o_done[(u - 1) & 1], ((u - 1) >> 1) & 1, status, &s_abort);
+          if (named_bar_any(1, 128, !r_ok)) { ok = false; break; }
           tc_fence_after();
           uint32_t o[16];
 #pragma unroll
@@ -253,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float l = s_l[0][h] + s_l[1][h] + s_l[2][h] + s_l[3][h];
         inv_l[h] = l > 0.f ? 1.f / l : 0.f;
       }
-      if (!mbar_wait_warp(&bars.o_done[last_v & 1], (last_v >> 1) & 1, status, &s_abort)) { ok = false; break; }
+      const bool e_ok = mbar_wait_warp(&bars.o_done[last_v & 1], (last_v >> 1) & 1, status, &s_abort);
+      if (named_bar_any(1, 128, !e_ok)) { ok = false; break; }
       tc_fence_after();
       // epilogue: thread = dim i (half 0) and 128 + i (half 1)
       __half* orow = out + ((size_t)t * kHeads + g * kHPG) * kD;
@@ -269,78 +284,113 @@ __global__ void __launch_bounds__(kThreads, 1)
       softmax_bar();  // s_l may be rewritten by the next item only after everyone read it
       if (lane == 0) mbar_arrive(&bars.o_free[k & 1]);
     }
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ gather producers
+    const bool is_v = warp == 2;
+    const int8_t* codes = is_v ? vq : kq;
+    const __half* scales = is_v ? vsc : ksc;
+    uint64_t* full = is_v ? bars.vst_full : bars.kst_full;
+    uint64_t* empty = is_v ? bars.vst_empty : bars.kst_empty;
+    uint8_t* st0 = smem + (is_v ? kOffVSt : kOffKSt);
+    int h = 0;  // half-tile counter of this ring
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int t = t_begin + (it >> 1), g = it & 1;
+      const int n_kv = pos0 + t + 1;
+      const int32_t* idrow = ids + ((size_t)t * kGroups + g) * K;
+      for (int jl = 0; ok && jl < n_tiles; ++jl) {
+        for (int half = 0; half < 2; ++half, ++h) {
+          const int s = h & 1;
+          if (h >= 2 && !mbar_wait_warp(&empty[s], ((h >> 1) & 1) ^ 1, status, &s_abort)) { ok = false; break; }
+          // ids of the half-tile's 64 cells: lane holds cells lane and lane + 32
+          int id0, id1;
+          {
+            const int s0 = jl * kCells + half * kHalfCells + lane, s1 = s0 + 32;
+            id0 = (s0 < K) ? __ldg(idrow + s0) : -1;
+            id1 = (s1 < K) ? __ldg(idrow + s1) : -1;
+            if (id0 >= n_kv) id0 = -1;  // out-of-range ids are skipped (and flagged by the dequant warps)
+            if (id1 >= n_kv) id1 = -1;
+          }
+          uint8_t* st = st0 + s * kStageBytes;
+          // codes: 64 rows x 16 chunks of 16 bytes, two rows per warp instruction
+#pragma unroll 4
+          for (int i = 0; i < kHalfCells / 2; ++i) {
+            const int r = 2 * i + (lane >> 4), ch = lane & 15;
+            const int a = __shfl_sync(0xffffffffu, id0, r & 31), b = __shfl_sync(0xffffffffu, id1, r & 31);
+            const int c = (r < 32) ? a : b;
+            if (c >= 0) cp_async16(st + r * kD + ch * 16, codes + ((size_t)c * kGroups + g) * kD + ch * 16);
+          }
+          // scale rows (both groups, 16 bytes) of cells lane and lane + 32
+          if (id0 >= 0) cp_async16(st + kStageCodes + lane * 16, scales + (size_t)id0 * kGroups * kNB);
+          if (id1 >= 0) cp_async16(st + kStageCodes + (lane + 32) * 16, scales + (size_t)id1 * kGroups * kNB);
+          cp_async_arrive_noinc(&full[s]);
+        }
+      }
+    }
+    cp_async_wait_all();  // nothing of ours may land after the CTA exits
   } else if (warp >= 8) {
-    // ------------------------------------------------------------ gather + dequantise
-    const int dw = warp - 8;
+    // ------------------------------------------------------------ dequantise staged rows
+    const bool is_v = warp >= 12;
+    const int dw = warp & 3;
     const int blk = lane >> 3;
-    int u = 0;
+    uint64_t* st_full = is_v ? bars.vst_full : bars.kst_full;
+    uint64_t* st_empty = is_v ? bars.vst_empty : bars.kst_empty;
+    uint64_t* t_full = is_v ? &bars.vh_full : &bars.kh_full;
+    uint64_t* t_empty = is_v ? &bars.vh_empty : &bars.kh_empty;
+    uint8_t* tile = smem + (is_v ? kOffV : kOffK);
+    const uint8_t* st0 = smem + (is_v ? kOffVSt : kOffKSt);
+    int u = 0, h = 0;
     bool ok = true;
     for (int it = blockIdx.x, k = 0; ok && it < n_items; it += gridDim.x, ++k) {
       const int t = t_begin + (it >> 1), g = it & 1;
       const int n_kv = pos0 + t + 1;
       const int32_t* idrow = ids + ((size_t)t * kGroups + g) * K;
-      // Q^T tile for this item: rows 0..11 = the group's heads (rows 12..15 stay zero)
-      if (k >= 2 && !mbar_wait_warp(&bars.q_empty[k & 1], ((k >> 1) & 1) ^ 1, status, &s_abort)) break;
-      {
+      if (!is_v) {
+        // Q^T tile for this item: rows 0..11 = the group's heads (rows 12..15 stay zero)
+        if (k >= 2 && !mbar_wait_warp(&bars.q_empty[k & 1], ((k >> 1) & 1) ^ 1, status, &s_abort)) break;
         uint8_t* qb = smem + kOffQ + (k & 1) * kQBytes;
         const __half* qt = q + ((size_t)t * kHeads + g * kHPG) * kD;
-        for (int x = dw * 32 + lane; x < kHPG * 32; x += 256) {
-          const int h = x >> 5, ch = x & 31;  // 16-byte chunk ch of row h
-          const uint4 v = *reinterpret_cast<const uint4*>(qt + h * kD + ch * 8);
-          *reinterpret_cast<uint4*>(qb + (ch >> 3) * (kNQ * 128) + h * 128 + (((ch & 7) ^ (h & 7)) << 4)) = v;
+        for (int x = dw * 32 + lane; x < kHPG * 32; x += 128) {
+          const int hh = x >> 5, ch = x & 31;  // 16-byte chunk ch of row hh
+          const uint4 v = *reinterpret_cast<const uint4*>(qt + hh * kD + ch * 8);
+          *reinterpret_cast<uint4*>(qb + (ch >> 3) * (kNQ * 128) + hh * 128 + (((ch & 7) ^ (hh & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.q_full[k & 1]);
       }
-      for (int jl = 0; jl < n_tiles; ++jl, ++u) {
-        // this warp's 16 cells of the tile
-        int cell[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int slot = jl * kCells + dw * 16 + x;
-          int c = -1;
-          if (slot < K) {
-            c = __ldg(idrow + slot);
-            if (c < 0 || c >= n_kv) {
-              if (lane == 0) set_dev_status(status, QSA_DEV_BAD_ID);
+      for (int jl = 0; ok && jl < n_tiles; ++jl, ++u) {
+        if (u >= 1 && !mbar_wait_warp(t_empty, (u - 1) & 1, status, &s_abort)) { ok = false; break; }
+        for (int half = 0; half < 2; ++half, ++h) {
+          const int s = h & 1;
+          if (!mbar_wait_warp(&st_full[s], (h >> 1) & 1, status, &s_abort)) { ok = false; break; }
+          const uint8_t* st = st0 + s * kStageBytes;
+#pragma unroll 4
+          for (int x = 0; x < 16; ++x) {
+            const int r = dw * 16 + x;            // row within the half-tile
+            const int row = half * kHalfCells + r;  // row within the tile
+            const int slot = jl * kCells + row;
+            int c = (slot < K) ? __ldg(idrow + slot) : -1;
+            if (c >= n_kv || (c < 0 && slot < K)) {
+              if (!is_v && lane == 0) set_dev_status(status, QSA_DEV_BAD_ID);
               c = -1;
             }
-          }
-          cell[x] = c;
-        }
-#pragma unroll 1
-        for (int kv = 0; kv < 2; ++kv) {
-          uint64_t* empty = kv ? &bars.vh_empty : &bars.kh_empty;
-          uint64_t* full = kv ? &bars.vh_full : &bars.kh_full;
-          const int8_t* codes = kv ? vq : kq;
-          const __half* scales = kv ? vsc : ksc;
-          uint2 w[16];
-          __half sc[16];
-#pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            if (cell[x] >= 0) {
-              w[x] = __ldg(reinterpret_cast<const uint2*>(codes + ((size_t)cell[x] * kGroups + g) * kD + lane * 8));
-              sc[x] = scales[((size_t)cell[x] * kGroups + g) * kNB + blk];
-            } else {
-              w[x] = make_uint2(0, 0);
-              sc[x] = __ushort_as_half(0);
+            uint32_t o[4] = {0u, 0u, 0u, 0u};
+            if (c >= 0) {
+              const uint2 w = *reinterpret_cast<const uint2*>(st + r * kD + lane * 8);
+              const __half sc = *reinterpret_cast<const __half*>(st + kStageCodes + r * 16 + (g * kNB + blk) * 2);
+              dequant8(w.x, w.y, __half2half2(sc), o);
             }
-          }
-          if (u >= 1 && !mbar_wait_warp(empty, (u - 1) & 1, status, &s_abort)) { ok = false; break; }
-          uint8_t* dst = smem + (kv ? kOffV : kOffK);
-#pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const int r = dw * 16 + x;
-            uint32_t o[4];
-            dequant8(w[x].x, w[x].y, __half2half2(sc[x]), o);
-            *reinterpret_cast<uint4*>(dst + blk * (kCells * 128) + r * 128 + (((lane & 7) ^ (r & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(tile + blk * (kCells * 128) + row * 128 + (((lane & 7) ^ (row & 7)) << 4)) =
                 make_uint4(o[0], o[1], o[2], o[3]);
           }
-          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(full);
+          if (lane == 0) mbar_arrive(&st_empty[s]);
         }
+        if (!ok) break;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(t_full);
       }
     }
   }

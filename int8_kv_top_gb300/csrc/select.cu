@@ -36,10 +36,11 @@ namespace {
 constexpr int kGM = 128, kGN = 64, kGK = 64, kGStages = 4;
 constexpr int kMaxCells = 65536;
 constexpr int kTkThreads = 512;
-constexpr int kCandCap = 4096;
-constexpr int kBandCap = 1024;
-constexpr int kTopkSmem = 2 * 256 * 4 + 256 * 8 + kCandCap * 2 + kCandCap * 4 + kBandCap * 4 + kBandCap * 16 +
-                          kMaxCells / 8;
+constexpr int kCandCap = 2048;
+constexpr int kBandCap = 512;
+// hist 2 KB | qsum 2 KB | band keys + ids | candidate ids | the row (fp16)
+constexpr int kTopkFixedSmem = 4096 + kBandCap * 20 + kCandCap * 4;
+inline int topk_smem_bytes(int n_max) { return kTopkFixedSmem + ((n_max + 7) & ~7) * 2; }
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -146,7 +147,11 @@ struct __align__(8) ScoreBars {
   uint64_t a_full, b_full[kGStages], b_empty[kGStages], acc_full[2], acc_empty[2], drain;
 };
 
-__global__ void __launch_bounds__(256, 1)
+constexpr int kScoreThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-11 epilogue
+
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kScoreThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                  const __half* __restrict__ ksc, __half* __restrict__ scores, int T_sel, int T_pad, int n_pad,
                  int n_base, int m_tiles, int n_chunks, float sm_scale, int* status) {
@@ -176,7 +181,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.acc_full[i], 1);
-      mbar_init(&bars.acc_empty[i], 4);
+      mbar_init(&bars.acc_empty[i], 8);
     }
     mbar_init(&bars.drain, 1);
     fence_mbar_init();
@@ -240,52 +245,61 @@ __global__ void __launch_bounds__(256, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
-    const int quarter = warp & 3;
+    // epilogue: warps 4-7 take cells 0-31 of each 64-cell tile, warps 8-11 cells 32-63
+    __shared__ float4 s_scale[2][kGN];  // the tile's K scales of group g, per accumulator set
+    const int quarter = warp & 3, c0 = (warp >= 8) ? 32 : 0;
+    const int et = tid - 128;  // 0..255
     const int r = r0 + quarter * 32 + lane;
     const bool row_valid = r < T_sel;
     const int n_kv = row_valid ? n_base + r + 1 : 0;
+    const int n_lim = n_base + T_sel;  // cells that exist for this call
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     __half* dst_row = scores + ((size_t)g * T_sel + (row_valid ? r : 0)) * n_pad;
+    bool dead = false;  // after a failed wait keep meeting the epilogue barrier, skip the work
     for (int i = 0; i < n_tiles; ++i) {
       const int a = i & 1;
-      if (!mbar_wait_warp(&bars.acc_full[a], (i >> 1) & 1, status, &s_abort)) break;
-      tc_fence_after();
       const int n0 = (nt_begin + i) * kGN;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kGN; c0 += 32) {
-        float acc[32];
+      {
+        const int cell = et >> 2, b = et & 3;
+        const float v = (n0 + cell < n_lim) ? __half2float(ksc[((size_t)(n0 + cell) * kGroups + g) * kNB + b]) : 0.f;
+        reinterpret_cast<float*>(&s_scale[a][cell])[b] = v;
+      }
+      epilogue_bar();
+      if (!dead) dead = !mbar_wait_warp(&bars.acc_full[a], (i >> 1) & 1, status, &s_abort);
+      if (dead) continue;
+      tc_fence_after();
+      float acc[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-#pragma unroll 1
-        for (int b = 0; b < kNB; ++b) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + a * 256 + b * kGN + c0, v);
-          tmem_wait_ld();
+      for (int j = 0; j < 32; ++j) acc[j] = 0.f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int c = n0 + c0 + j;  // cells past the row's causal range are neither read nor stored
-            const float sc = (c < n_kv) ? __half2float(__ldg(ksc + ((size_t)c * kGroups + g) * kNB + b)) : 0.f;
-            acc[j] = fmaf(sc, __uint_as_float(v[j]), acc[j]);
-          }
-        }
-        const int cell0 = n0 + c0;
-        if (row_valid && cell0 < n_kv) {
-          uint32_t w[16];
+      for (int b = 0; b < kNB; ++b) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + a * 256 + b * kGN + c0, v);
+        tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) w[j] = pack_half2(acc[2 * j] * sm_scale, acc[2 * j + 1] * sm_scale);
-          if (cell0 + 32 <= n_kv) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst_row + cell0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-          } else {
-            const __half* hw = reinterpret_cast<const __half*>(w);
-            for (int j = 0; j < n_kv - cell0; ++j) dst_row[cell0 + j] = hw[j];
-          }
+        for (int j = 0; j < 32; ++j) {
+          const float4 sc = s_scale[a][c0 + j];
+          const float sb = (b == 0) ? sc.x : (b == 1) ? sc.y : (b == 2) ? sc.z : sc.w;
+          acc[j] = fmaf(sb, __uint_as_float(v[j]), acc[j]);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.acc_empty[a]);
+      const int cell0 = n0 + c0;
+      if (row_valid && cell0 < n_kv) {
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = pack_half2(acc[2 * j] * sm_scale, acc[2 * j + 1] * sm_scale);
+        if (cell0 + 32 <= n_kv) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst_row + cell0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        } else {
+          const __half* hw = reinterpret_cast<const __half*>(w);
+          for (int j = 0; j < n_kv - cell0; ++j) dst_row[cell0 + j] = hw[j];
+        }
+      }
     }
   }
   tc_fence_before();
@@ -446,29 +460,33 @@ struct Bound {
   __device__ float L(float f) const { return f - a - b * fabsf(f); }
 };
 
-template <int V>
-__global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
+constexpr uint16_t kPlusInf = 0x7C00u;  // marks a band cell chosen by the exact ranking (kept)
+
+// Row of scores in shared memory (fp16 bits), cells >= n_kv absent.  All passes below are
+// rolled loops: cell i is visited by thread i % 512 (or by warp ranges for ordered output).
+__global__ void __launch_bounds__(kTkThreads, 2)
     topk_kernel(const __half* __restrict__ scores, const __half* __restrict__ q, const int8_t* __restrict__ kq,
                 const __half* __restrict__ ksc, const float* __restrict__ eh, const float* __restrict__ kmax,
                 int32_t* __restrict__ ids, int t_sel, int T_sel, int n_pad, int pos0, int K, float sm_scale,
                 int* status) {
   extern __shared__ __align__(16) uint8_t topk_smem[];
-  unsigned* s_hist = reinterpret_cast<unsigned*>(topk_smem);                         // [2][256]
-  long long* s_qsum = reinterpret_cast<long long*>(topk_smem + 2 * 256 * 4);         // [256]
-  Key128* s_band_key = reinterpret_cast<Key128*>(s_qsum + kD);                       // [kBandCap]
-  int* s_band_idx = reinterpret_cast<int*>(s_band_key + kBandCap);                   // [kBandCap]
-  int* s_cand_idx = s_band_idx + kBandCap;                                           // [kCandCap]
-  uint16_t* s_cand_key = reinterpret_cast<uint16_t*>(s_cand_idx + kCandCap);         // [kCandCap]
-  unsigned* s_bits = reinterpret_cast<unsigned*>(s_cand_key + kCandCap);             // [kMaxCells / 32]
+  unsigned* s_hist = reinterpret_cast<unsigned*>(topk_smem);                   // [2][256]
+  long long* s_qsum = reinterpret_cast<long long*>(topk_smem + 2048);          // [256]
+  Key128* s_band_key = reinterpret_cast<Key128*>(topk_smem + 4096);            // [kBandCap]
+  int* s_band_idx = reinterpret_cast<int*>(s_band_key + kBandCap);             // [kBandCap]
+  int* s_cand_idx = s_band_idx + kBandCap;                                     // [kCandCap]
+  uint16_t* s_row = reinterpret_cast<uint16_t*>(s_cand_idx + kCandCap);        // [n_kv rounded to 8]
   __shared__ int s_red[64];
   __shared__ int s_tmp[8];
-  __shared__ int s_cnt[4];  // 0: candidates, 1: band
+  __shared__ int s_cnt[2];  // 0: candidates, 1: band
+  __shared__ int s_wsum[kTkThreads / 32];
   __shared__ Bound s_bound;
 
   const int r = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nwarps = kTkThreads / 32;
+  constexpr int nwarps = kTkThreads / 32;
   const int t = t_sel + r;
   const int n_kv = pos0 + t + 1;
+  const int n8 = (n_kv + 7) & ~7;
   const __half* row = scores + ((size_t)g * T_sel + r) * n_pad;
 
   if (tid < kD) {  // exact Qsum in units of 2^-24
@@ -478,7 +496,6 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
     for (int h = 0; h < kHPG; ++h) sq += half_int24(__half_as_ushort(qt[h * kD]));
     s_qsum[tid] = sq;
   }
-  for (int i = tid; i < (n_kv + 31) / 32; i += kTkThreads) s_bits[i] = 0u;
   for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
   if (tid == 0) {
     // |s~ - s| <= a + b |s~|: a covers the fp16 rounding of Qsum (E_b) and the fp32
@@ -493,51 +510,43 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
     s_cnt[0] = 0;
     s_cnt[1] = 0;
   }
-
-  // this thread's cells [tid*V, tid*V + V)
-  uint32_t hv[V / 2];
-  const int c0 = tid * V;
-#pragma unroll
-  for (int i = 0; i < V / 8; ++i) {
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (c0 + 8 * i < n_kv) w = __ldg(reinterpret_cast<const uint4*>(row + c0 + 8 * i));
-    hv[4 * i] = w.x;
-    hv[4 * i + 1] = w.y;
-    hv[4 * i + 2] = w.z;
-    hv[4 * i + 3] = w.w;
+  // row -> shared memory (16-byte chunks); the tail past n_kv is padded with -inf
+  for (int i = tid; i < n8 / 8; i += kTkThreads) {
+    uint4 w = __ldg(reinterpret_cast<const uint4*>(row) + i);
+    if (8 * i + 8 > n_kv) {
+      uint16_t* h = reinterpret_cast<uint16_t*>(&w);
+      for (int j = 0; j < 8; ++j)
+        if (8 * i + j >= n_kv) h[j] = 0xFC00u;
+    }
+    reinterpret_cast<uint4*>(s_row)[i] = w;
   }
-  auto valid = [&](int j) -> bool { return c0 + j < n_kv; };
-  auto key = [&](int j) -> uint32_t {  // order key; 0 for cells outside the causal range
-    return valid(j) ? fp16_order_key((uint16_t)(hv[j >> 1] >> (16 * (j & 1)))) : 0u;
-  };
-  auto fval = [&](uint32_t k) -> float { return order_key_to_float(k); };
   __syncthreads();
+  auto key_at = [&](int i) -> uint32_t { return fp16_order_key(s_row[i]); };
 
-  // ---- tau: bracket from a 1-in-8 sample, then one compare pass
-  int n_samp = 0;
-#pragma unroll
-  for (int j = 0; j < V; j += 8) n_samp += valid(j);
-  n_samp = block_sum(n_samp, s_red);
+  // ---- tau: bracket from a 1-in-8 sample, then one compare pass over the row
+  const int n_samp = (n_kv + 7) / 8;  // cells 0, 8, 16, ...
   uint32_t key_hi = 0xFFFFu, key_lo = 1u;
   bool bracket = n_samp >= 64 && 8 * K < n_kv;
   if (bracket) {
     const float ks = (float)K * n_samp / n_kv;
     const int margin = (int)(3.f * sqrtf(ks) + 16.f);
-    const int r_hi = (int)ks - margin;          // sample ranks (1-based) bracketing the k-th
+    const int r_hi = (int)ks - margin;  // sample ranks (1-based) bracketing the k-th largest
     const int r_lo = (int)ceilf(ks) + margin;
-#pragma unroll
-    for (int j = 0; j < V; j += 8) warp_hist_add(valid(j), key(j) >> 8, s_hist);
+    for (int base = warp * 32; base < n_samp; base += kTkThreads) {
+      const int i = base + lane;
+      warp_hist_add(i < n_samp, i < n_samp ? key_at(8 * i) >> 8 : 0u, s_hist);
+    }
     __syncthreads();
     int ab_hi = 0, ab_lo = 0, b_hi = -1, b_lo = -1;
     if (r_hi >= 1) b_hi = find_bin_desc(s_hist, r_hi, &ab_hi, s_tmp);
     if (r_lo <= n_samp) b_lo = find_bin_desc(s_hist, r_lo, &ab_lo, s_tmp);
     for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
     __syncthreads();
-#pragma unroll
-    for (int j = 0; j < V; j += 8) {
-      const uint32_t k = key(j);
-      warp_hist_add(valid(j) && (int)(k >> 8) == b_hi, k & 0xFFu, s_hist);
-      warp_hist_add(valid(j) && (int)(k >> 8) == b_lo, k & 0xFFu, s_hist + 256);
+    for (int base = warp * 32; base < n_samp; base += kTkThreads) {
+      const int i = base + lane;
+      const uint32_t k = i < n_samp ? key_at(8 * i) : 0u;
+      warp_hist_add(i < n_samp && (int)(k >> 8) == b_hi, k & 0xFFu, s_hist);
+      warp_hist_add(i < n_samp && (int)(k >> 8) == b_lo, k & 0xFFu, s_hist + 256);
     }
     __syncthreads();
     int dummy;
@@ -545,95 +554,67 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
     if (b_lo >= 0) key_lo = ((uint32_t)b_lo << 8) | (uint32_t)find_bin_desc(s_hist + 256, r_lo - ab_lo, &dummy, s_tmp);
     if (key_lo < 1u) key_lo = 1u;
   }
-  // one pass: count above the bracket, collect the bracket
   int above = 0;
   if (bracket) {
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-      const uint32_t k = key(j);
+    for (int base = warp * 32; base < n_kv; base += kTkThreads) {
+      const int i = base + lane;
+      const uint32_t k = i < n_kv ? key_at(i) : 0u;
       above += (k > key_hi);
-      const bool in = valid(j) && k >= key_lo && k <= key_hi;
-      const int slot = warp_append(in, &s_cnt[0]);
-      if (slot >= 0 && slot < kCandCap) {
-        s_cand_key[slot] = (uint16_t)k;
-        s_cand_idx[slot] = c0 + j;
-      }
+      const int slot = warp_append(i < n_kv && k >= key_lo && k <= key_hi, &s_cnt[0]);
+      if (slot >= 0 && slot < kCandCap) s_cand_idx[slot] = i;
     }
   }
   const int A0 = block_sum(above, s_red);
   const int Cn = s_cnt[0];
   const int need_c = K - A0;
   bracket = bracket && Cn <= kCandCap && need_c >= 1 && need_c <= Cn;
-  uint32_t tau_key;
   for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
   __syncthreads();
-  if (bracket) {  // exact (need_c)-th largest key among the candidates (warp-uniform loop)
-    for (int base = warp * 32; base < Cn; base += kTkThreads) {
-      const int i = base + lane;
-      warp_hist_add(i < Cn, i < Cn ? (unsigned)(s_cand_key[i] >> 8) : 0u, s_hist);
-    }
+  // exact key of the k-th largest score: among the candidates, or over the whole row
+  const int n_src = bracket ? Cn : n_kv;
+  const int need1 = bracket ? need_c : K;
+  auto src_key = [&](int i) -> uint32_t { return key_at(bracket ? s_cand_idx[i] : i); };
+  for (int base = warp * 32; base < n_src; base += kTkThreads) {
+    const int i = base + lane;
+    warp_hist_add(i < n_src, i < n_src ? src_key(i) >> 8 : 0u, s_hist);
   }
   __syncthreads();
-  if (bracket) {
-    int ab1;
-    const int b1 = find_bin_desc(s_hist, need_c, &ab1, s_tmp);
-    for (int i = tid; i < Cn; i += kTkThreads)
-      if ((int)(s_cand_key[i] >> 8) == b1) atomicAdd(&s_hist[256 + (s_cand_key[i] & 0xFFu)], 1u);
-    __syncthreads();
-    int ab2;
-    const int b2 = find_bin_desc(s_hist + 256, need_c - ab1, &ab2, s_tmp);
-    tau_key = ((uint32_t)b1 << 8) | (uint32_t)b2;
-  } else {  // full radix over every value
-#pragma unroll
-    for (int j = 0; j < V; ++j) warp_hist_add(valid(j), key(j) >> 8, s_hist);
-    __syncthreads();
-    int ab1;
-    const int b1 = find_bin_desc(s_hist, K, &ab1, s_tmp);
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-      const uint32_t k = key(j);
-      warp_hist_add(valid(j) && (int)(k >> 8) == b1, k & 0xFFu, s_hist + 256);
-    }
-    __syncthreads();
-    int ab2;
-    const int b2 = find_bin_desc(s_hist + 256, K - ab1, &ab2, s_tmp);
-    tau_key = ((uint32_t)b1 << 8) | (uint32_t)b2;
+  int ab1;
+  const int b1 = find_bin_desc(s_hist, need1, &ab1, s_tmp);
+  for (int base = warp * 32; base < n_src; base += kTkThreads) {
+    const int i = base + lane;
+    const uint32_t k = i < n_src ? src_key(i) : 0u;
+    warp_hist_add(i < n_src && (int)(k >> 8) == b1, k & 0xFFu, s_hist + 256);
   }
-  if (tau_key == 0u) {  // cannot happen with K <= n_kv; leave the row unwritten
+  __syncthreads();
+  int ab2;
+  const int b2 = find_bin_desc(s_hist + 256, need1 - ab1, &ab2, s_tmp);
+  if (b1 < 0 || b2 < 0) {  // cannot happen with K <= n_kv; leave the row unwritten
     if (tid == 0) set_dev_status(status, QSA_DEV_BAND_OVERFLOW);
     return;
   }
+  const uint32_t tau_key = ((uint32_t)b1 << 8) | (uint32_t)b2;
 
   // ---- band: surely in (L(f) > U(tau)), undecided (U(f) >= L(tau))
   const Bound bd = s_bound;
-  const float tau = fval(tau_key);
+  const float tau = order_key_to_float(tau_key);
   const float Ut = bd.U(tau), Lt = bd.L(tau);
-  // every cell above the bracket must be surely in, every cell below it surely out
-  if (bracket) {
-    const bool hi_ok = key_hi == 0xFFFFu || bd.L(fval(key_hi + 1u)) > Ut;
-    const bool lo_ok = key_lo <= 1u || bd.U(fval(key_lo - 1u)) < Lt;
+  auto f_at = [&](int i) -> float { return __half2float(__ushort_as_half(s_row[i])); };
+  if (bracket) {  // every cell above the bracket surely in, every cell below it surely out
+    const bool hi_ok = key_hi == 0xFFFFu || bd.L(order_key_to_float(key_hi + 1u)) > Ut;
+    const bool lo_ok = key_lo <= 1u || bd.U(order_key_to_float(key_lo - 1u)) < Lt;
     bracket = hi_ok && lo_ok;
   }
   int n_def = 0;
-  if (bracket) {
-    for (int i = tid; i < Cn; i += kTkThreads) {
-      const float f = fval(s_cand_key[i]);
-      if (bd.L(f) > Ut) {
-        ++n_def;
-      } else if (bd.U(f) >= Lt) {
-        const int slot = atomicAdd(&s_cnt[1], 1);
-        if (slot < kBandCap) s_band_idx[slot] = s_cand_idx[i];
-      }
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-      const float f = fval(key(j));
-      const bool def = valid(j) && bd.L(f) > Ut;
-      n_def += def;
-      const int slot = warp_append(valid(j) && !def && bd.U(f) >= Lt, &s_cnt[1]);
-      if (slot >= 0 && slot < kBandCap) s_band_idx[slot] = c0 + j;
-    }
+  const int n_cls = bracket ? Cn : n_kv;
+  for (int base = warp * 32; base < n_cls; base += kTkThreads) {
+    const int i = base + lane;
+    const int c = i < n_cls ? (bracket ? s_cand_idx[i] : i) : 0;
+    const float f = i < n_cls ? f_at(c) : 0.f;
+    const bool def = i < n_cls && bd.L(f) > Ut;
+    n_def += def;
+    const int slot = warp_append(i < n_cls && !def && bd.U(f) >= Lt, &s_cnt[1]);
+    if (slot >= 0 && slot < kBandCap) s_band_idx[slot] = c;
   }
   const int A = (bracket ? A0 : 0) + block_sum(n_def, s_red);
   const int B = s_cnt[1];
@@ -664,6 +645,8 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
       }
     }
     __syncthreads();
+    int chosen[2] = {-1, -1};  // at most B / 512 + 1 <= 2 per thread
+    int nch = 0;
     for (int i = tid; i < B; i += kTkThreads) {
       const Key128 ki = s_band_key[i];
       const int ci = s_band_idx[i];
@@ -672,90 +655,94 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
         const Key128 kj = s_band_key[jj];
         rank += key_gt(kj, ki) || (key_eq(kj, ki) && s_band_idx[jj] < ci);
       }
-      if (rank < need) atomicOr(&s_bits[ci >> 5], 1u << (ci & 31));
+      if (rank < need && nch < 2) chosen[nch++] = ci;
     }
+    __syncthreads();  // every rank read the scores before any is overwritten
+    for (int x = 0; x < nch; ++x) s_row[chosen[x]] = kPlusInf;
   } else {
     // large band (many near-ties): exact radix select over the band, keys recomputed per
     // pass, 16 passes of 8 bits over the biased 128-bit key
-    unsigned long long pre_hi = 0, pre_lo = 0;
+    auto in_band = [&](int c) -> bool {
+      const float f = f_at(c);
+      return !(bd.L(f) > Ut) && bd.U(f) >= Lt;
+    };
+    auto bkey = [&](int c) -> unsigned __int128 {
+      unsigned __int128 kb = (unsigned __int128)exact_key(s_qsum, kq + ((size_t)c * kGroups + g) * kD,
+                                                          ksc + ((size_t)c * kGroups + g) * kNB);
+      return kb ^ ((unsigned __int128)1 << 127);
+    };
+    unsigned __int128 pre = 0;
     int rem = need;
     for (int pass = 0; pass < 16; ++pass) {
       for (int i = tid; i < 256; i += kTkThreads) s_hist[i] = 0u;
       __syncthreads();
       const int shift = 120 - 8 * pass;
-      for (int j = 0; j < V; ++j) {
-        const float f = fval(key(j));
-        if (!valid(j) || bd.L(f) > Ut || bd.U(f) < Lt) continue;
-        const int c = c0 + j;
-        unsigned __int128 kb = (unsigned __int128)exact_key(s_qsum, kq + ((size_t)c * kGroups + g) * kD,
-                                                            ksc + ((size_t)c * kGroups + g) * kNB);
-        kb ^= (unsigned __int128)1 << 127;
-        const unsigned __int128 pre = ((unsigned __int128)pre_hi << 64) | pre_lo;
+      for (int c = tid; c < n_kv; c += kTkThreads) {
+        if (!in_band(c)) continue;
+        const unsigned __int128 kb = bkey(c);
         if (pass == 0 || (kb >> (shift + 8)) == (pre >> (shift + 8))) atomicAdd(&s_hist[(unsigned)(kb >> shift) & 0xFFu], 1u);
       }
       __syncthreads();
       int ab;
       const int bin = find_bin_desc(s_hist, rem, &ab, s_tmp);
       rem -= ab;
-      unsigned __int128 pre = ((unsigned __int128)pre_hi << 64) | pre_lo;
       pre |= (unsigned __int128)(unsigned)bin << shift;
-      pre_hi = (unsigned long long)(pre >> 64);
-      pre_lo = (unsigned long long)pre;
     }
-    const unsigned __int128 kstar = ((unsigned __int128)pre_hi << 64) | pre_lo;
-    int n_tie = 0;
-    unsigned long long tie_lo = 0, tie_hi = 0;
-    for (int j = 0; j < V; ++j) {
-      const float f = fval(key(j));
-      if (!valid(j) || bd.L(f) > Ut || bd.U(f) < Lt) continue;
-      const int c = c0 + j;
-      unsigned __int128 kb = (unsigned __int128)exact_key(s_qsum, kq + ((size_t)c * kGroups + g) * kD,
-                                                          ksc + ((size_t)c * kGroups + g) * kNB);
-      kb ^= (unsigned __int128)1 << 127;
-      if (kb > kstar) atomicOr(&s_bits[c >> 5], 1u << (c & 31));
-      if (kb == kstar) {
-        ++n_tie;
-        if (j < 64) tie_lo |= 1ull << j;
-        else tie_hi |= 1ull << (j - 64);
-      }
+    // take every band key above pre and the `rem` lowest-index cells equal to it; warp w
+    // scans the contiguous cell range [w * span, (w + 1) * span) so ties are met in order
+    const int span = (n_kv + nwarps - 1) / nwarps;
+    const int c_begin = warp * span, c_end = min(n_kv, c_begin + span);
+    int my_ties = 0;
+    for (int base = c_begin; base < c_end; base += 32) {
+      const int c = base + lane;
+      const bool tie = c < c_end && in_band(c) && bkey(c) == pre;
+      my_ties += __popc(__ballot_sync(0xffffffffu, tie));
     }
-    int total_ties;
-    int before = block_excl_scan(n_tie, s_red, &total_ties);
-    for (int j = 0; j < V; ++j) {
-      const bool tie = (j < 64) ? ((tie_lo >> j) & 1ull) : ((tie_hi >> (j - 64)) & 1ull);
-      if (tie) {
-        if (before < rem) atomicOr(&s_bits[(c0 + j) >> 5], 1u << ((c0 + j) & 31));
-        ++before;
+    if (lane == 0) s_wsum[warp] = my_ties;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += s_wsum[w];
+    __syncthreads();
+    for (int base = c_begin; base < c_end; base += 32) {
+      const int c = base + lane;
+      bool gt = false, tie = false;
+      if (c < c_end && in_band(c)) {
+        const unsigned __int128 kb = bkey(c);
+        gt = kb > pre;
+        tie = kb == pre;
       }
+      const unsigned m = __ballot_sync(0xffffffffu, tie);
+      const int rank = before + __popc(m & ((1u << lane) - 1u));
+      before += __popc(m);
+      if (gt || (tie && rank < rem)) s_row[c] = kPlusInf;  // disjoint cells per thread: safe
     }
   }
   __syncthreads();
 
-  // ---- emit ascending ids: surely-in cells plus the band cells chosen above
-  int n_keep = 0;
-  unsigned long long keep_lo = 0, keep_hi = 0;
-#pragma unroll
-  for (int j = 0; j < V; ++j) {
-    if (!valid(j)) continue;
-    const int c = c0 + j;
-    const bool k = bd.L(fval(key(j))) > Ut || ((s_bits[c >> 5] >> (c & 31)) & 1u);
-    if (k) {
-      if (j < 64) keep_lo |= 1ull << j;
-      else keep_hi |= 1ull << (j - 64);
-      ++n_keep;
-    }
+  // ---- emit ascending ids: warp w owns cells [w * span, (w + 1) * span)
+  const int span = (n_kv + nwarps - 1) / nwarps;
+  const int c_begin = warp * span, c_end = min(n_kv, c_begin + span);
+  int my = 0;
+  for (int base = c_begin; base < c_end; base += 32) {
+    const int c = base + lane;
+    my += __popc(__ballot_sync(0xffffffffu, c < c_end && (s_row[c] == kPlusInf || bd.L(f_at(c)) > Ut)));
   }
-  int total;
-  int pos = block_excl_scan(n_keep, s_red, &total);
+  if (lane == 0) s_wsum[warp] = my;
+  __syncthreads();
+  int pos = 0, total = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    total += s_wsum[w];
+    if (w < warp) pos += s_wsum[w];
+  }
   if (total != K && tid == 0) set_dev_status(status, QSA_DEV_BAND_OVERFLOW);
   int32_t* dst = ids + ((size_t)t * kGroups + g) * K;
-#pragma unroll
-  for (int j = 0; j < V; ++j) {
-    const bool k = (j < 64) ? ((keep_lo >> j) & 1ull) : ((keep_hi >> (j - 64)) & 1ull);
-    if (k) {
-      if (pos < K) dst[pos] = c0 + j;
-      ++pos;
-    }
+  for (int base = c_begin; base < c_end; base += 32) {
+    const int c = base + lane;
+    const bool keep = c < c_end && (s_row[c] == kPlusInf || bd.L(f_at(c)) > Ut);
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    const int p = pos + __popc(m & ((1u << lane) - 1u));
+    if (keep && p < K) dst[p] = c;
+    pos += __popc(m);
   }
 }
 
@@ -778,7 +765,7 @@ size_t select_workspace_bytes(int T, int pos0, int n_cells, Params p) {
   (void)n_cells;
   const WsLayout L = ws_layout(T, pos0, p);
   if (L.T_sel == 0) return 0;
-  if (L.n_max > kMaxCells || p.topk > kMaxCells) return 0;
+  if (L.n_max > kMaxCells || p.topk > kMaxCells) return 0;  // row (fp16) must fit in shared memory
   return L.total;
 }
 
@@ -817,23 +804,18 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
   const int n_tiles = L.n_pad / kGN;
   const int n_chunks = (n_tiles + kNtPerCta - 1) / kNtPerCta;
   const int n_base = pos0 + L.t_sel;  // n_kv of selected row r is n_base + r + 1
-  score_kernel<<<kGroups * m_tiles * n_chunks, 256, kScoreSmem, stream>>>(ma, mb, ksc, sc, L.T_sel, L.T_pad, L.n_pad,
+  score_kernel<<<kGroups * m_tiles * n_chunks, kScoreThreads, kScoreSmem, stream>>>(ma, mb, ksc, sc, L.T_sel, L.T_pad, L.n_pad,
                                                                          n_base, m_tiles, n_chunks, p.sm_scale,
                                                                          status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const dim3 grid(L.T_sel, kGroups);
-  auto run = [&](auto kern) -> cudaError_t {
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmem);
-    if (err != cudaSuccess) return err;
-    kern<<<grid, kTkThreads, kTopkSmem, stream>>>(sc, q, kq, ksc, eh, kmax, ids, L.t_sel, L.T_sel, L.n_pad, pos0,
+  const int smem = topk_smem_bytes(L.n_max);
+  if ((e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    return e;
+  topk_kernel<<<grid, kTkThreads, smem, stream>>>(sc, q, kq, ksc, eh, kmax, ids, L.t_sel, L.T_sel, L.n_pad, pos0,
                                                   p.topk, p.sm_scale, status);
-    return cudaGetLastError();
-  };
-  if (L.n_max <= 16 * kTkThreads) return run(topk_kernel<16>);
-  if (L.n_max <= 32 * kTkThreads) return run(topk_kernel<32>);
-  if (L.n_max <= 64 * kTkThreads) return run(topk_kernel<64>);
-  return run(topk_kernel<128>);
+  return cudaGetLastError();
 }
 
 }  // namespace qsa
