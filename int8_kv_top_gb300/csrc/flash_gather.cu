@@ -36,7 +36,8 @@ constexpr int kQBytes = kNQ * kD * 2;        // 8 KB
 constexpr int kPBytes = kNQ * kCells * 2;    // 4 KB
 constexpr int kHalfCells = 64;                               // cells per staging half-tile
 constexpr int kStageCodes = kHalfCells * kD;                   // 16 KB of int8 codes
-constexpr int kStageBytes = kStageCodes + kHalfCells * 16;     // + one 16-byte scale row per cell
+constexpr int kStageIds = kStageCodes + kHalfCells * 16;       // after one 16-byte scale row per cell
+constexpr int kStageBytes = kStageIds + kHalfCells * 4;        // + the half-tile's cell ids
 constexpr int kOffK = 0, kOffV = kTileHalf, kOffQ = 2 * kTileHalf, kOffP = kOffQ + 2 * kQBytes;
 constexpr int kOffKSt = kOffP + 2 * kPBytes, kOffVSt = kOffKSt + 2 * kStageBytes;
 constexpr int kSmemTotal = kOffVSt + 2 * kStageBytes;
@@ -73,9 +74,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     s_abort = 0;
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.kst_full[i], 32);
+      mbar_init(&bars.kst_full[i], 33);  // 32 cp.async completions + the ids' release
       mbar_init(&bars.kst_empty[i], 4);
-      mbar_init(&bars.vst_full[i], 32);
+      mbar_init(&bars.vst_full[i], 33);
       mbar_init(&bars.vst_empty[i], 4);
       mbar_init(&bars.q_full[i], 4);
       mbar_init(&bars.q_empty[i], 1);
@@ -302,16 +303,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int half = 0; half < 2; ++half, ++h) {
           const int s = h & 1;
           if (h >= 2 && !mbar_wait_warp(&empty[s], ((h >> 1) & 1) ^ 1, status, &s_abort)) { ok = false; break; }
-          // ids of the half-tile's 64 cells: lane holds cells lane and lane + 32
+          // ids of the half-tile's 64 cells: lane holds cells lane and lane + 32; they go to the
+          // stage as well (-1: past the set, -2: out of range, skipped and flagged downstream)
           int id0, id1;
+          uint8_t* st = st0 + s * kStageBytes;
           {
             const int s0 = jl * kCells + half * kHalfCells + lane, s1 = s0 + 32;
             id0 = (s0 < K) ? __ldg(idrow + s0) : -1;
             id1 = (s1 < K) ? __ldg(idrow + s1) : -1;
-            if (id0 >= n_kv) id0 = -1;  // out-of-range ids are skipped (and flagged by the dequant warps)
-            if (id1 >= n_kv) id1 = -1;
+            if (s0 < K && (id0 < 0 || id0 >= n_kv)) id0 = -2;
+            if (s1 < K && (id1 < 0 || id1 >= n_kv)) id1 = -2;
+            reinterpret_cast<int*>(st + kStageIds)[lane] = id0;
+            reinterpret_cast<int*>(st + kStageIds)[lane + 32] = id1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[s]);
           }
-          uint8_t* st = st0 + s * kStageBytes;
           // codes: 64 rows x 16 chunks of 16 bytes, two rows per warp instruction
 #pragma unroll 4
           for (int i = 0; i < kHalfCells / 2; ++i) {
@@ -343,8 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int it = blockIdx.x, k = 0; ok && it < n_items; it += gridDim.x, ++k) {
       const int t = t_begin + (it >> 1), g = it & 1;
-      const int n_kv = pos0 + t + 1;
-      const int32_t* idrow = ids + ((size_t)t * kGroups + g) * K;
       if (!is_v) {
         // Q^T tile for this item: rows 0..11 = the group's heads (rows 12..15 stay zero)
         if (k >= 2 && !mbar_wait_warp(&bars.q_empty[k & 1], ((k >> 1) & 1) ^ 1, status, &s_abort)) break;
@@ -369,9 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int x = 0; x < 16; ++x) {
             const int r = dw * 16 + x;            // row within the half-tile
             const int row = half * kHalfCells + r;  // row within the tile
-            const int slot = jl * kCells + row;
-            int c = (slot < K) ? __ldg(idrow + slot) : -1;
-            if (c >= n_kv || (c < 0 && slot < K)) {
+            int c = reinterpret_cast<const int*>(st + kStageIds)[r];
+            if (c == -2) {
               if (!is_v && lane == 0) set_dev_status(status, QSA_DEV_BAD_ID);
               c = -1;
             }

@@ -7,12 +7,13 @@
 // over the group's 12 heads of sm_scale * q . k^, equal scores going to the lower index.
 //
 // GB300 design (four launches on the caller's stream):
-//  1. prep_q:  Qsum = sum_h q over the group's 12 heads, exact in fp64; hi = fp16(Qsum);
-//              per 64-dim block E_b = sum |Qsum - hi| and H_b = sum |hi| (error norms).
+//  1. prep_q:  Qsum = sum_h q over the group's 12 heads, exact in fp64, split as
+//              hi = fp16(Qsum), lo = fp16(Qsum - hi); per 64-dim block the residual norm
+//              E_b = sum |Qsum - hi - lo| and H_b = sum (|hi| + |lo|).
 //     prep_k:  int8 K codes as fp16 (exact integers) for every cell a selected token can
 //              see, and kmax_b = max |ksc| per group and block.
 //  2. score:   tcgen05 GEMM with one TMEM accumulator per 64-dim scale block:
-//                S_b[t][c] = sum_{d in b} hi[t][d] * kq[c][d]     (products exact in fp32)
+//                S_b[t][c] = sum_{d in b} (hi + lo)[t][d] * kq[c][d]   (products exact in fp32)
 //              epilogue  s~[t][c] = fp16(sm_scale * sum_b ksc[c][b] * S_b[t][c]).
 //              128-row x 64-cell tiles, TMA-fed 4-stage ring, two accumulator sets.
 //  3. topk:    one 512-thread CTA per (token, group) holds the row's scores in registers.
@@ -33,7 +34,7 @@ namespace qsa {
 namespace {
 
 // ----------------------------------------------------------------- workspace layout
-constexpr int kGM = 128, kGN = 64, kGK = 64, kGStages = 4;
+constexpr int kGM = 128, kGN = 64, kGK = 64, kGStages = 2;
 constexpr int kMaxCells = 65536;
 constexpr int kTkThreads = 512;
 constexpr int kCandCap = 2048;
@@ -62,7 +63,7 @@ WsLayout ws_layout(int T, int pos0, Params p) {
   L.off_eh = o;
   o = align_up(o + (size_t)kGroups * L.T_sel * 8 * sizeof(float), 1024);
   L.off_qhi = o;
-  o = align_up(o + (size_t)kGroups * L.T_pad * kD * 2, 1024);
+  o = align_up(o + (size_t)kGroups * L.T_pad * kD * 2 * 2, 1024);  // hi and lo
   L.off_kc = o;
   o = align_up(o + (size_t)kGroups * L.n_pad * kD * 2, 1024);
   L.off_scores = o;
@@ -79,11 +80,12 @@ __device__ __forceinline__ long long half_int24(uint16_t h) {
 }
 
 // ----------------------------------------------------------------- 1. prep
-// grid (T_pad, 2), 256 threads: thread = dim.
+// grid (T_pad, 2), 256 threads: thread = dim.  Row layout of qhl: for each 64-dim block b,
+// [hi_b (64) | lo_b (64)] at columns 128 b .. 128 b + 127, with Qsum = hi + lo + residual.
 __global__ void __launch_bounds__(256) prep_q_kernel(const __half* __restrict__ q, int t_sel, int T_sel, int T_pad,
-                                                     __half* __restrict__ qhi, float* __restrict__ eh) {
+                                                     __half* __restrict__ qhl, float* __restrict__ eh) {
   const int r = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
-  __half hi = __ushort_as_half(0);
+  __half hi = __ushort_as_half(0), lo = __ushort_as_half(0);
   double e = 0.0;
   if (r < T_sel) {
     const __half* qt = q + ((size_t)(t_sel + r) * kHeads + g * kHPG) * kD;
@@ -91,12 +93,16 @@ __global__ void __launch_bounds__(256) prep_q_kernel(const __half* __restrict__ 
 #pragma unroll
     for (int h = 0; h < kHPG; ++h) s += (double)__half2float(qt[h * kD + d]);
     hi = __double2half(s);
-    e = s - (double)__half2float(hi);
+    const double rest = s - (double)__half2float(hi);  // exact
+    lo = __double2half(rest);
+    e = rest - (double)__half2float(lo);  // exact residual
   }
-  qhi[((size_t)g * T_pad + r) * kD + d] = hi;
+  __half* dst = qhl + ((size_t)g * T_pad + r) * (2 * kD) + (d >> 6) * 128 + (d & 63);
+  dst[0] = hi;
+  dst[64] = lo;
   if (r >= T_sel) return;
-  // block norms over 64 dims = two warps
-  double ae = fabs(e), ah = fabs((double)__half2float(hi));
+  // block norms over 64 dims = two warps: E_b = sum |residual|, H_b = sum (|hi| + |lo|)
+  double ae = fabs(e), ah = fabs((double)__half2float(hi)) + fabs((double)__half2float(lo));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     ae += __shfl_xor_sync(0xffffffffu, ae, o);
@@ -110,9 +116,9 @@ __global__ void __launch_bounds__(256) prep_q_kernel(const __half* __restrict__ 
   }
   __syncthreads();
   if (d < kNB) {
-    float* dst = eh + ((size_t)g * T_sel + r) * 8;
-    dst[d] = __double2float_ru(s_e[2 * d] + s_e[2 * d + 1]);
-    dst[kNB + d] = __double2float_ru(s_h[2 * d] + s_h[2 * d + 1]);
+    float* dst2 = eh + ((size_t)g * T_sel + r) * 8;
+    dst2[d] = __double2float_ru(s_e[2 * d] + s_e[2 * d + 1]);
+    dst2[kNB + d] = __double2float_ru(s_h[2 * d] + s_h[2 * d + 1]);
   }
 }
 
@@ -139,7 +145,7 @@ __global__ void __launch_bounds__(256) prep_k_kernel(const int8_t* __restrict__ 
 
 // ----------------------------------------------------------------- 2. score GEMM
 constexpr int kNtPerCta = 32;                  // 2048 cells per CTA
-constexpr int kSmemA = kGM * kD * 2;           // 64 KB: 4 k-blocks of [128 rows][64] SW128
+constexpr int kSmemA = kGM * kD * 2 * 2;       // 128 KB: 8 k-blocks (hi_b, lo_b) of [128 rows][64] SW128
 constexpr int kSmemBStage = kGN * kD * 2;      // 32 KB: 4 k-blocks of [64 cells][64] SW128
 constexpr int kScoreSmem = kSmemA + kGStages * kSmemBStage + 1024;
 
@@ -202,7 +208,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       tma_prefetch_desc(&map_a);
       tma_prefetch_desc(&map_b);
       mbar_arrive_expect_tx(&bars.a_full, kSmemA);
-      for (int kb = 0; kb < kD / kGK; ++kb)
+      for (int kb = 0; kb < 2 * kD / kGK; ++kb)
         tma_load_2d(sA + kb * (kGM * 128), &map_a, &bars.a_full, kb * kGK, g * T_pad + r0);
       int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
@@ -232,11 +238,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
         for (int b = 0; b < kNB; ++b)
 #pragma unroll
-          for (int kk = 0; kk < kGK / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(a0 + b * (kGM * 128) + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b0 + st * kSmemBStage + b * (kGN * 128) + kk * 32, 16, 1024);
-            umma_ss(tmem + a * 256 + b * kGN, ad, bd, idesc, kk > 0 ? 1u : 0u);
-          }
+          for (int part = 0; part < 2; ++part)  // hi_b then lo_b against the same codes
+#pragma unroll
+            for (int kk = 0; kk < kGK / 16; ++kk) {
+              const uint64_t ad = sdesc_sw128(a0 + (2 * b + part) * (kGM * 128) + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(b0 + st * kSmemBStage + b * (kGN * 128) + kk * 32, 16, 1024);
+              umma_ss(tmem + a * 256 + b * kGN, ad, bd, idesc, (part > 0 || kk > 0) ? 1u : 0u);
+            }
         umma_commit(&bars.b_empty[st]);
         umma_commit(&bars.acc_full[a]);
       }
@@ -362,32 +370,6 @@ __device__ __forceinline__ int block_sum(int v, int* s_red) {
   return t;
 }
 
-// Block-wide exclusive prefix sum; returns this thread's offset.
-__device__ __forceinline__ int block_excl_scan(int v, int* s_red, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  __syncthreads();
-  if (lane == 31) s_red[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = (lane < (int)(blockDim.x >> 5)) ? s_red[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    s_red[32 + lane] = w;  // inclusive over warps
-  }
-  __syncthreads();
-  *total = s_red[32 + 31];
-  return x - v + (warp > 0 ? s_red[32 + warp - 1] : 0);
-}
-
 // Find the bin holding the `need`-th largest element given a 256-bin histogram in smem
 // (bins scanned from high to low).  Returns the bin and sets *above = count in higher bins.
 __device__ __forceinline__ int find_bin_desc(const unsigned* hist, int need, int* above, int* s_tmp) {
@@ -498,13 +480,13 @@ __global__ void __launch_bounds__(kTkThreads, 2)
   }
   for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
   if (tid == 0) {
-    // |s~ - s| <= a + b |s~|: a covers the fp16 rounding of Qsum (E_b) and the fp32
-    // accumulation of 64 exact products per block (64 * 2^-23 of the absolute sum, with
-    // |kq| <= 128) plus the epilogue's roundings (2^-21); b covers the fp16 rounding of the
-    // stored score.  Both doubled for margin.
+    // |s~ - s| <= a + b |s~|: a covers the residual of Qsum after its fp16 hi + lo split
+    // (E_b) and the fp32 accumulation of 128 exact products per block (128 * 2^-23 of the
+    // absolute sum, with |kq| <= 128) plus the epilogue's roundings (2^-21); b covers the
+    // fp16 rounding of the stored score.  Both doubled for margin.
     const float* e = eh + ((size_t)g * T_sel + r) * 8;
     float acc = 0.f;
-    for (int b = 0; b < kNB; ++b) acc += kmax[g * kNB + b] * (e[b] + e[kNB + b] * (7.6293945e-06f + 4.7683716e-07f));
+    for (int b = 0; b < kNB; ++b) acc += kmax[g * kNB + b] * (e[b] + e[kNB + b] * (1.5258789e-05f + 4.7683716e-07f));
     s_bound.a = 2.f * (sm_scale * 128.f * acc + 1.2e-7f);
     s_bound.b = 2.f * 4.8852e-04f;
     s_cnt[0] = 0;
@@ -783,7 +765,7 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
 
   cudaError_t e = cudaMemsetAsync(kmax, 0, 8 * sizeof(float), stream);
   if (e != cudaSuccess) return e;
-  prep_q_kernel<<<dim3(L.T_pad, kGroups), 256, 0, stream>>>(q, L.t_sel, L.T_sel, L.T_pad, qhi, eh);
+  prep_q_kernel<<<dim3(L.T_pad, kGroups), 256, 0, stream>>>(q, L.t_sel, L.T_sel, L.T_pad, qhi, eh);  // hi/lo
   prep_k_kernel<<<dim3(L.n_pad / 8, kGroups), 256, 0, stream>>>(kq, ksc, L.n_max, L.n_pad, kc, kmax);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -797,7 +779,7 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
     attr_done[dev] = true;
   }
   CUtensorMap ma, mb;
-  if (!make_2d_map(&ma, qhi, kD, (uint64_t)kGroups * L.T_pad, kGK, kGM) ||
+  if (!make_2d_map(&ma, qhi, 2 * kD, (uint64_t)kGroups * L.T_pad, kGK, kGM) ||
       !make_2d_map(&mb, kc, kD, (uint64_t)kGroups * L.n_pad, kGK, kGN))
     return cudaErrorInvalidValue;
   const int m_tiles = L.T_pad / kGM;
