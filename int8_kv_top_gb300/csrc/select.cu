@@ -39,9 +39,8 @@ constexpr int kMaxCells = 65536;
 constexpr int kTkThreads = 512;
 constexpr int kCandCap = 2048;
 constexpr int kBandCap = 512;
-// hist 2 KB | qsum 2 KB | band keys + ids | candidate ids | the row (fp16)
-constexpr int kTopkFixedSmem = 4096 + kBandCap * 20 + kCandCap * 4;
-inline int topk_smem_bytes(int n_max) { return kTopkFixedSmem + ((n_max + 7) & ~7) * 2; }
+// hist 2 KB | qsum 2 KB | band keys + ids | candidate ids | selection bitmap
+constexpr int kTopkSmem = 4096 + kBandCap * 20 + kCandCap * 4 + kMaxCells / 8;
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -351,6 +350,9 @@ __device__ __forceinline__ __int128 exact_key(const long long* __restrict__ s_qs
 __device__ __forceinline__ uint32_t fp16_order_key(uint16_t b) {
   return (b & 0x8000u) ? (uint32_t)(~b & 0xFFFFu) : (uint32_t)(b | 0x8000u);
 }
+__device__ __forceinline__ uint16_t key_to_bits(uint32_t k) {
+  return (k & 0x8000u) ? (uint16_t)(k & 0x7FFFu) : (uint16_t)(~k & 0xFFFFu);
+}
 __device__ __forceinline__ float order_key_to_float(uint32_t k) {
   const uint16_t b = (k & 0x8000u) ? (uint16_t)(k & 0x7FFFu) : (uint16_t)(~k & 0xFFFFu);
   return __half2float(__ushort_as_half(b));
@@ -442,11 +444,63 @@ struct Bound {
   __device__ float L(float f) const { return f - a - b * fabsf(f); }
 };
 
-constexpr uint16_t kPlusInf = 0x7C00u;  // marks a band cell chosen by the exact ranking (kept)
+// Block-wide exclusive prefix sum; returns this thread's offset and the total.
+__device__ __forceinline__ int block_excl_scan(int v, int* s_red, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) s_red[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < (int)(blockDim.x >> 5)) ? s_red[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_red[32 + lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  *total = s_red[32 + 31];
+  return x - v + (warp > 0 ? s_red[32 + warp - 1] : 0);
+}
 
-// Row of scores in shared memory (fp16 bits), cells >= n_kv absent.  All passes below are
-// rolled loops: cell i is visited by thread i % 512 (or by warp ranges for ordered output).
-__global__ void __launch_bounds__(kTkThreads, 2)
+// 8-bit mask of the halves of w (cell 8m + j -> bit j) that are >= th (cmp = 0) or > th (1).
+__device__ __forceinline__ uint32_t mask8(const uint4& w, __half2 th, int strict) {
+  const uint32_t* u = reinterpret_cast<const uint32_t*>(&w);
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = *reinterpret_cast<const __half2*>(&u[i]);
+    const uint32_t x = strict ? __hgt2_mask(h, th) : __hge2_mask(h, th);
+    m |= ((x & 1u) | ((x >> 15) & 2u)) << (2 * i);
+  }
+  return m;
+}
+
+// Smallest order key k in [1, 0xFBFF+...] with pred(k), pred monotone (false .. true).
+template <class P>
+__device__ uint32_t first_key(P pred) {
+  uint32_t lo = 0x0400u, hi = 0xFBFFu;  // finite fp16 values: -65504 .. 65504
+  if (!pred(hi)) return 0xFC00u;        // none
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi) >> 1;
+    if (pred(mid)) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
+}
+
+// One 512-thread CTA per (token, group).  Thread tid owns cells [tid*V, tid*V + V) of the
+// row in registers (fp16 pairs); every pass over the row is a packed fp16 compare against a
+// threshold, because the error-band tests are monotone in the stored score.
+template <int V>
+__global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
     topk_kernel(const __half* __restrict__ scores, const __half* __restrict__ q, const int8_t* __restrict__ kq,
                 const __half* __restrict__ ksc, const float* __restrict__ eh, const float* __restrict__ kmax,
                 int32_t* __restrict__ ids, int t_sel, int T_sel, int n_pad, int pos0, int K, float sm_scale,
@@ -457,18 +511,17 @@ __global__ void __launch_bounds__(kTkThreads, 2)
   Key128* s_band_key = reinterpret_cast<Key128*>(topk_smem + 4096);            // [kBandCap]
   int* s_band_idx = reinterpret_cast<int*>(s_band_key + kBandCap);             // [kBandCap]
   int* s_cand_idx = s_band_idx + kBandCap;                                     // [kCandCap]
-  uint16_t* s_row = reinterpret_cast<uint16_t*>(s_cand_idx + kCandCap);        // [n_kv rounded to 8]
+  unsigned* s_bits = reinterpret_cast<unsigned*>(s_cand_idx + kCandCap);       // [kMaxCells / 32]
   __shared__ int s_red[64];
   __shared__ int s_tmp[8];
-  __shared__ int s_cnt[2];  // 0: candidates, 1: band
-  __shared__ int s_wsum[kTkThreads / 32];
+  __shared__ int s_cnt[2];          // 0: candidates, 1: band
+  __shared__ uint32_t s_thr[2];     // order keys: surely-in threshold, band threshold
   __shared__ Bound s_bound;
 
   const int r = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int nwarps = kTkThreads / 32;
   const int t = t_sel + r;
   const int n_kv = pos0 + t + 1;
-  const int n8 = (n_kv + 7) & ~7;
   const __half* row = scores + ((size_t)g * T_sel + r) * n_pad;
 
   if (tid < kD) {  // exact Qsum in units of 2^-24
@@ -479,6 +532,7 @@ __global__ void __launch_bounds__(kTkThreads, 2)
     s_qsum[tid] = sq;
   }
   for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
+  for (int i = tid; i < (n_kv + 31) / 32; i += kTkThreads) s_bits[i] = 0u;
   if (tid == 0) {
     // |s~ - s| <= a + b |s~|: a covers the residual of Qsum after its fp16 hi + lo split
     // (E_b) and the fp32 accumulation of 128 exact products per block (128 * 2^-23 of the
@@ -492,58 +546,77 @@ __global__ void __launch_bounds__(kTkThreads, 2)
     s_cnt[0] = 0;
     s_cnt[1] = 0;
   }
-  // row -> shared memory (16-byte chunks); the tail past n_kv is padded with -inf
-  for (int i = tid; i < n8 / 8; i += kTkThreads) {
-    uint4 w = __ldg(reinterpret_cast<const uint4*>(row) + i);
-    if (8 * i + 8 > n_kv) {
-      uint16_t* h = reinterpret_cast<uint16_t*>(&w);
-      for (int j = 0; j < 8; ++j)
-        if (8 * i + j >= n_kv) h[j] = 0xFC00u;
-    }
-    reinterpret_cast<uint4*>(s_row)[i] = w;
-  }
-  __syncthreads();
-  auto key_at = [&](int i) -> uint32_t { return fp16_order_key(s_row[i]); };
 
-  // ---- tau: bracket from a 1-in-8 sample, then one compare pass over the row
-  const int n_samp = (n_kv + 7) / 8;  // cells 0, 8, 16, ...
-  uint32_t key_hi = 0xFFFFu, key_lo = 1u;
-  bool bracket = n_samp >= 64 && 8 * K < n_kv;
+  // this thread's cells in registers; cells past n_kv read as -inf
+  uint4 w[V / 8];
+  const int c0 = tid * V;
+#pragma unroll
+  for (int m = 0; m < V / 8; ++m) {
+    const int c = c0 + 8 * m;
+    uint4 x = make_uint4(0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u);
+    if (c < n_kv) {
+      x = __ldg(reinterpret_cast<const uint4*>(row + c));
+      if (c + 8 > n_kv) {
+        uint16_t* hh = reinterpret_cast<uint16_t*>(&x);
+        for (int j = 0; j < 8; ++j)
+          if (c + j >= n_kv) hh[j] = 0xFC00u;
+      }
+    }
+    w[m] = x;
+  }
+  auto half_bits = [](const uint4& x, int j) -> uint16_t {
+    const uint32_t* u = reinterpret_cast<const uint32_t*>(&x);
+    return (uint16_t)(u[j >> 1] >> (16 * (j & 1)));
+  };
+  __syncthreads();
+
+  // ---- tau: bracket from a 1-in-8 sample (cells 0, 8, 16, ...), then one compare pass
+  const int n_samp = (n_kv + 7) / 8;
+  uint32_t key_hi = 0xFBFFu, key_lo = 0x0400u;  // finite range
+  bool bracket = n_samp >= 64;
   if (bracket) {
     const float ks = (float)K * n_samp / n_kv;
     const int margin = (int)(3.f * sqrtf(ks) + 16.f);
     const int r_hi = (int)ks - margin;  // sample ranks (1-based) bracketing the k-th largest
     const int r_lo = (int)ceilf(ks) + margin;
-    for (int base = warp * 32; base < n_samp; base += kTkThreads) {
-      const int i = base + lane;
-      warp_hist_add(i < n_samp, i < n_samp ? key_at(8 * i) >> 8 : 0u, s_hist);
-    }
+#pragma unroll
+    for (int m = 0; m < V / 8; ++m)
+      warp_hist_add(c0 + 8 * m < n_kv, fp16_order_key(half_bits(w[m], 0)) >> 8, s_hist);
     __syncthreads();
     int ab_hi = 0, ab_lo = 0, b_hi = -1, b_lo = -1;
     if (r_hi >= 1) b_hi = find_bin_desc(s_hist, r_hi, &ab_hi, s_tmp);
     if (r_lo <= n_samp) b_lo = find_bin_desc(s_hist, r_lo, &ab_lo, s_tmp);
     for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
     __syncthreads();
-    for (int base = warp * 32; base < n_samp; base += kTkThreads) {
-      const int i = base + lane;
-      const uint32_t k = i < n_samp ? key_at(8 * i) : 0u;
-      warp_hist_add(i < n_samp && (int)(k >> 8) == b_hi, k & 0xFFu, s_hist);
-      warp_hist_add(i < n_samp && (int)(k >> 8) == b_lo, k & 0xFFu, s_hist + 256);
+#pragma unroll
+    for (int m = 0; m < V / 8; ++m) {
+      const bool v = c0 + 8 * m < n_kv;
+      const uint32_t k = fp16_order_key(half_bits(w[m], 0));
+      warp_hist_add(v && (int)(k >> 8) == b_hi, k & 0xFFu, s_hist);
+      warp_hist_add(v && (int)(k >> 8) == b_lo, k & 0xFFu, s_hist + 256);
     }
     __syncthreads();
     int dummy;
     if (b_hi >= 0) key_hi = ((uint32_t)b_hi << 8) | (uint32_t)find_bin_desc(s_hist, r_hi - ab_hi, &dummy, s_tmp);
     if (b_lo >= 0) key_lo = ((uint32_t)b_lo << 8) | (uint32_t)find_bin_desc(s_hist + 256, r_lo - ab_lo, &dummy, s_tmp);
-    if (key_lo < 1u) key_lo = 1u;
+    key_hi = min(key_hi, 0xFBFFu);
+    key_lo = max(key_lo, 0x0400u);
   }
   int above = 0;
   if (bracket) {
-    for (int base = warp * 32; base < n_kv; base += kTkThreads) {
-      const int i = base + lane;
-      const uint32_t k = i < n_kv ? key_at(i) : 0u;
-      above += (k > key_hi);
-      const int slot = warp_append(i < n_kv && k >= key_lo && k <= key_hi, &s_cnt[0]);
-      if (slot >= 0 && slot < kCandCap) s_cand_idx[slot] = i;
+    const __half2 thi = __half2half2(__ushort_as_half(key_to_bits(key_hi)));
+    const __half2 tlo = __half2half2(__ushort_as_half(key_to_bits(key_lo)));
+#pragma unroll
+    for (int m = 0; m < V / 8; ++m) {
+      const uint32_t gt = mask8(w[m], thi, 1);
+      above += __popc(gt);
+      uint32_t in = mask8(w[m], tlo, 0) & ~gt;  // key_lo <= key <= key_hi (padding is -inf)
+      while (in) {
+        const int j = __ffs(in) - 1;
+        in &= in - 1;
+        const int slot = atomicAdd(&s_cnt[0], 1);
+        if (slot < kCandCap) s_cand_idx[slot] = c0 + 8 * m + j;
+      }
     }
   }
   const int A0 = block_sum(above, s_red);
@@ -552,51 +625,81 @@ __global__ void __launch_bounds__(kTkThreads, 2)
   bracket = bracket && Cn <= kCandCap && need_c >= 1 && need_c <= Cn;
   for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
   __syncthreads();
-  // exact key of the k-th largest score: among the candidates, or over the whole row
-  const int n_src = bracket ? Cn : n_kv;
-  const int need1 = bracket ? need_c : K;
-  auto src_key = [&](int i) -> uint32_t { return key_at(bracket ? s_cand_idx[i] : i); };
-  for (int base = warp * 32; base < n_src; base += kTkThreads) {
-    const int i = base + lane;
-    warp_hist_add(i < n_src, i < n_src ? src_key(i) >> 8 : 0u, s_hist);
+  // exact order key of the k-th largest score: among the candidates, or over the whole row
+  uint32_t tau_key;
+  {
+    int ab1, ab2, b1, b2;
+    if (bracket) {
+      for (int base = warp * 32; base < Cn; base += kTkThreads) {
+        const int i = base + lane;
+        warp_hist_add(i < Cn, i < Cn ? fp16_order_key(__half_as_ushort(row[s_cand_idx[i]])) >> 8 : 0u, s_hist);
+      }
+      __syncthreads();
+      b1 = find_bin_desc(s_hist, need_c, &ab1, s_tmp);
+      for (int base = warp * 32; base < Cn; base += kTkThreads) {
+        const int i = base + lane;
+        const uint32_t k = i < Cn ? fp16_order_key(__half_as_ushort(row[s_cand_idx[i]])) : 0u;
+        warp_hist_add(i < Cn && (int)(k >> 8) == b1, k & 0xFFu, s_hist + 256);
+      }
+      __syncthreads();
+      b2 = find_bin_desc(s_hist + 256, need_c - ab1, &ab2, s_tmp);
+    } else {
+      for (int c = tid; c < n_kv; c += kTkThreads) atomicAdd(&s_hist[fp16_order_key(__half_as_ushort(row[c])) >> 8], 1u);
+      __syncthreads();
+      b1 = find_bin_desc(s_hist, K, &ab1, s_tmp);
+      for (int c = tid; c < n_kv; c += kTkThreads) {
+        const uint32_t k = fp16_order_key(__half_as_ushort(row[c]));
+        if ((int)(k >> 8) == b1) atomicAdd(&s_hist[256 + (k & 0xFFu)], 1u);
+      }
+      __syncthreads();
+      b2 = find_bin_desc(s_hist + 256, K - ab1, &ab2, s_tmp);
+    }
+    if (b1 < 0 || b2 < 0) {  // cannot happen with K <= n_kv; leave the row unwritten
+      if (tid == 0) set_dev_status(status, QSA_DEV_BAND_OVERFLOW);
+      return;
+    }
+    tau_key = ((uint32_t)b1 << 8) | (uint32_t)b2;
   }
-  __syncthreads();
-  int ab1;
-  const int b1 = find_bin_desc(s_hist, need1, &ab1, s_tmp);
-  for (int base = warp * 32; base < n_src; base += kTkThreads) {
-    const int i = base + lane;
-    const uint32_t k = i < n_src ? src_key(i) : 0u;
-    warp_hist_add(i < n_src && (int)(k >> 8) == b1, k & 0xFFu, s_hist + 256);
-  }
-  __syncthreads();
-  int ab2;
-  const int b2 = find_bin_desc(s_hist + 256, need1 - ab1, &ab2, s_tmp);
-  if (b1 < 0 || b2 < 0) {  // cannot happen with K <= n_kv; leave the row unwritten
-    if (tid == 0) set_dev_status(status, QSA_DEV_BAND_OVERFLOW);
-    return;
-  }
-  const uint32_t tau_key = ((uint32_t)b1 << 8) | (uint32_t)b2;
 
-  // ---- band: surely in (L(f) > U(tau)), undecided (U(f) >= L(tau))
-  const Bound bd = s_bound;
-  const float tau = order_key_to_float(tau_key);
-  const float Ut = bd.U(tau), Lt = bd.L(tau);
-  auto f_at = [&](int i) -> float { return __half2float(__ushort_as_half(s_row[i])); };
-  if (bracket) {  // every cell above the bracket surely in, every cell below it surely out
-    const bool hi_ok = key_hi == 0xFFFFu || bd.L(order_key_to_float(key_hi + 1u)) > Ut;
-    const bool lo_ok = key_lo <= 1u || bd.U(order_key_to_float(key_lo - 1u)) < Lt;
-    bracket = hi_ok && lo_ok;
+  // ---- thresholds: surely in <=> key >= k_def, undecided <=> k_band <= key < k_def
+  if (tid == 0) {
+    const Bound bd = s_bound;
+    const float tau = order_key_to_float(tau_key);
+    const float Ut = bd.U(tau), Lt = bd.L(tau);
+    s_thr[0] = first_key([&](uint32_t k) { return bd.L(order_key_to_float(k)) > Ut; });
+    s_thr[1] = first_key([&](uint32_t k) { return bd.U(order_key_to_float(k)) >= Lt; });
   }
+  __syncthreads();
+  const uint32_t k_def = s_thr[0], k_band = s_thr[1];
+  // the bracket is usable only if everything above it is surely in and below it surely out
+  bracket = bracket && k_def <= key_hi + 1u && k_band >= key_lo;
   int n_def = 0;
-  const int n_cls = bracket ? Cn : n_kv;
-  for (int base = warp * 32; base < n_cls; base += kTkThreads) {
-    const int i = base + lane;
-    const int c = i < n_cls ? (bracket ? s_cand_idx[i] : i) : 0;
-    const float f = i < n_cls ? f_at(c) : 0.f;
-    const bool def = i < n_cls && bd.L(f) > Ut;
-    n_def += def;
-    const int slot = warp_append(i < n_cls && !def && bd.U(f) >= Lt, &s_cnt[1]);
-    if (slot >= 0 && slot < kBandCap) s_band_idx[slot] = c;
+  if (bracket) {
+    for (int i = tid; i < Cn; i += kTkThreads) {
+      const int c = s_cand_idx[i];
+      const uint32_t k = fp16_order_key(__half_as_ushort(row[c]));
+      if (k >= k_def) {
+        ++n_def;
+      } else if (k >= k_band) {
+        const int slot = atomicAdd(&s_cnt[1], 1);
+        if (slot < kBandCap) s_band_idx[slot] = c;
+      }
+    }
+  } else {
+    const __half2 tdef = __half2half2(__ushort_as_half(key_to_bits(min(k_def, 0xFBFFu))));
+    const __half2 tband = __half2half2(__ushort_as_half(key_to_bits(k_band)));
+#pragma unroll
+    for (int m = 0; m < V / 8; ++m) {
+      const uint32_t def = (k_def <= 0xFBFFu) ? mask8(w[m], tdef, 0) : 0u;
+      n_def += __popc(def);
+      uint32_t bnd = mask8(w[m], tband, 0) & ~def;
+      while (bnd) {
+        const int j = __ffs(bnd) - 1;
+        bnd &= bnd - 1;
+        const int slot = atomicAdd(&s_cnt[1], 1);
+        if (slot < kBandCap) s_band_idx[slot] = c0 + 8 * m + j;
+      }
+    }
   }
   const int A = (bracket ? A0 : 0) + block_sum(n_def, s_red);
   const int B = s_cnt[1];
@@ -606,12 +709,12 @@ __global__ void __launch_bounds__(kTkThreads, 2)
     // exact keys, one warp per band cell: lane = 8 codes of block lane/8
     for (int i = warp; i < B; i += nwarps) {
       const int c = s_band_idx[i];
-      const uint2 w = *reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8);
+      const uint2 x = *reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8);
       long long part = 0;
 #pragma unroll
-      for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + by] * (long long)(int8_t)(w.x >> (8 * by));
+      for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + by] * (long long)(int8_t)(x.x >> (8 * by));
 #pragma unroll
-      for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + 4 + by] * (long long)(int8_t)(w.y >> (8 * by));
+      for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + 4 + by] * (long long)(int8_t)(x.y >> (8 * by));
       part += __shfl_xor_sync(0xffffffffu, part, 1);
       part += __shfl_xor_sync(0xffffffffu, part, 2);
       part += __shfl_xor_sync(0xffffffffu, part, 4);
@@ -627,8 +730,6 @@ __global__ void __launch_bounds__(kTkThreads, 2)
       }
     }
     __syncthreads();
-    int chosen[2] = {-1, -1};  // at most B / 512 + 1 <= 2 per thread
-    int nch = 0;
     for (int i = tid; i < B; i += kTkThreads) {
       const Key128 ki = s_band_key[i];
       const int ci = s_band_idx[i];
@@ -637,16 +738,14 @@ __global__ void __launch_bounds__(kTkThreads, 2)
         const Key128 kj = s_band_key[jj];
         rank += key_gt(kj, ki) || (key_eq(kj, ki) && s_band_idx[jj] < ci);
       }
-      if (rank < need && nch < 2) chosen[nch++] = ci;
+      if (rank < need) atomicOr(&s_bits[ci >> 5], 1u << (ci & 31));
     }
-    __syncthreads();  // every rank read the scores before any is overwritten
-    for (int x = 0; x < nch; ++x) s_row[chosen[x]] = kPlusInf;
   } else {
     // large band (many near-ties): exact radix select over the band, keys recomputed per
-    // pass, 16 passes of 8 bits over the biased 128-bit key
+    // pass, 16 passes of 8 bits over the biased 128-bit key (cells read from the score row)
     auto in_band = [&](int c) -> bool {
-      const float f = f_at(c);
-      return !(bd.L(f) > Ut) && bd.U(f) >= Lt;
+      const uint32_t k = fp16_order_key(__half_as_ushort(row[c]));
+      return k >= k_band && k < k_def;
     };
     auto bkey = [&](int c) -> unsigned __int128 {
       unsigned __int128 kb = (unsigned __int128)exact_key(s_qsum, kq + ((size_t)c * kGroups + g) * kD,
@@ -670,61 +769,62 @@ __global__ void __launch_bounds__(kTkThreads, 2)
       rem -= ab;
       pre |= (unsigned __int128)(unsigned)bin << shift;
     }
-    // take every band key above pre and the `rem` lowest-index cells equal to it; warp w
-    // scans the contiguous cell range [w * span, (w + 1) * span) so ties are met in order
+    // every band key above pre, and the `rem` lowest-index cells equal to it: warp w scans
+    // the contiguous range [w * span, (w + 1) * span), so ties are met in index order
+    __shared__ int s_wsum[nwarps];
     const int span = (n_kv + nwarps - 1) / nwarps;
-    const int c_begin = warp * span, c_end = min(n_kv, c_begin + span);
+    const int cb = warp * span, ce = min(n_kv, cb + span);
     int my_ties = 0;
-    for (int base = c_begin; base < c_end; base += 32) {
+    for (int base = cb; base < ce; base += 32) {
       const int c = base + lane;
-      const bool tie = c < c_end && in_band(c) && bkey(c) == pre;
+      const bool tie = c < ce && in_band(c) && bkey(c) == pre;
       my_ties += __popc(__ballot_sync(0xffffffffu, tie));
     }
     if (lane == 0) s_wsum[warp] = my_ties;
     __syncthreads();
     int before = 0;
-    for (int w = 0; w < warp; ++w) before += s_wsum[w];
-    __syncthreads();
-    for (int base = c_begin; base < c_end; base += 32) {
+    for (int x = 0; x < warp; ++x) before += s_wsum[x];
+    for (int base = cb; base < ce; base += 32) {
       const int c = base + lane;
       bool gt = false, tie = false;
-      if (c < c_end && in_band(c)) {
+      if (c < ce && in_band(c)) {
         const unsigned __int128 kb = bkey(c);
         gt = kb > pre;
         tie = kb == pre;
       }
-      const unsigned m = __ballot_sync(0xffffffffu, tie);
-      const int rank = before + __popc(m & ((1u << lane) - 1u));
-      before += __popc(m);
-      if (gt || (tie && rank < rem)) s_row[c] = kPlusInf;  // disjoint cells per thread: safe
+      const unsigned mm = __ballot_sync(0xffffffffu, tie);
+      const int rank = before + __popc(mm & ((1u << lane) - 1u));
+      before += __popc(mm);
+      if (gt || (tie && rank < rem)) atomicOr(&s_bits[c >> 5], 1u << (c & 31));
     }
   }
   __syncthreads();
 
-  // ---- emit ascending ids: warp w owns cells [w * span, (w + 1) * span)
-  const int span = (n_kv + nwarps - 1) / nwarps;
-  const int c_begin = warp * span, c_end = min(n_kv, c_begin + span);
-  int my = 0;
-  for (int base = c_begin; base < c_end; base += 32) {
-    const int c = base + lane;
-    my += __popc(__ballot_sync(0xffffffffu, c < c_end && (s_row[c] == kPlusInf || bd.L(f_at(c)) > Ut)));
+  // ---- emit ascending ids: surely-in cells (key >= k_def) plus the chosen band cells
+  const __half2 tdef = __half2half2(__ushort_as_half(key_to_bits(min(k_def, 0xFBFFu))));
+  uint32_t keep[V / 8];
+  int n_keep = 0;
+#pragma unroll
+  for (int m = 0; m < V / 8; ++m) {
+    const int c = c0 + 8 * m;
+    uint32_t k = (k_def <= 0xFBFFu) ? mask8(w[m], tdef, 0) : 0u;
+    if (c < n_kv) k |= (s_bits[c >> 5] >> (c & 31)) & 0xFFu;
+    keep[m] = k;
+    n_keep += __popc(k);
   }
-  if (lane == 0) s_wsum[warp] = my;
-  __syncthreads();
-  int pos = 0, total = 0;
-  for (int w = 0; w < nwarps; ++w) {
-    total += s_wsum[w];
-    if (w < warp) pos += s_wsum[w];
-  }
+  int total;
+  int pos = block_excl_scan(n_keep, s_red, &total);
   if (total != K && tid == 0) set_dev_status(status, QSA_DEV_BAND_OVERFLOW);
   int32_t* dst = ids + ((size_t)t * kGroups + g) * K;
-  for (int base = c_begin; base < c_end; base += 32) {
-    const int c = base + lane;
-    const bool keep = c < c_end && (s_row[c] == kPlusInf || bd.L(f_at(c)) > Ut);
-    const unsigned m = __ballot_sync(0xffffffffu, keep);
-    const int p = pos + __popc(m & ((1u << lane) - 1u));
-    if (keep && p < K) dst[p] = c;
-    pos += __popc(m);
+#pragma unroll
+  for (int m = 0; m < V / 8; ++m) {
+    uint32_t k = keep[m];
+    while (k) {
+      const int j = __ffs(k) - 1;
+      k &= k - 1;
+      if (pos < K) dst[pos] = c0 + 8 * m + j;
+      ++pos;
+    }
   }
 }
 
@@ -792,12 +892,17 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const dim3 grid(L.T_sel, kGroups);
-  const int smem = topk_smem_bytes(L.n_max);
-  if ((e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
-    return e;
-  topk_kernel<<<grid, kTkThreads, smem, stream>>>(sc, q, kq, ksc, eh, kmax, ids, L.t_sel, L.T_sel, L.n_pad, pos0,
+  auto run = [&](auto kern) -> cudaError_t {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmem);
+    if (err != cudaSuccess) return err;
+    kern<<<grid, kTkThreads, kTopkSmem, stream>>>(sc, q, kq, ksc, eh, kmax, ids, L.t_sel, L.T_sel, L.n_pad, pos0,
                                                   p.topk, p.sm_scale, status);
-  return cudaGetLastError();
+    return cudaGetLastError();
+  };
+  if (L.n_max <= 16 * kTkThreads) return run(topk_kernel<16>);
+  if (L.n_max <= 32 * kTkThreads) return run(topk_kernel<32>);
+  if (L.n_max <= 64 * kTkThreads) return run(topk_kernel<64>);
+  return run(topk_kernel<128>);
 }
 
 }  // namespace qsa
