@@ -129,9 +129,10 @@ def run_ours(args, rank, world, local_rank):
     xpC = [torch.empty((N_DEC, HEADS, D), device=device) for _ in range(LAYERS)]
     wsB = torch.empty(qsa.qsa_select_workspace_bytes(T_PREFILL, POS0_B, nB), dtype=torch.uint8, device=device)
     wsC = torch.empty(qsa.qsa_select_workspace_bytes(N_DEC, P_DEC, nC), dtype=torch.uint8, device=device)
+    pwsB = torch.empty(qsa.qsa_flash_prefill_workspace_bytes(T_PREFILL, POS0_B, nB), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-    # our kernel launches per step: A 1/layer; B select 4 + gather 1; C select 4 + partial 1 + merge 1
-    launches_per_step = LAYERS * (1 + 5 + 6)
+    # our kernel launches per step: A 1/layer; B select 4 + mirror 1 + gather 1; C select 4 + partial 1 + merge 1
+    launches_per_step = LAYERS * (1 + 6 + 6)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
@@ -152,7 +153,7 @@ def run_ours(args, rank, world, local_rank):
             qsa.qsa_select(d["q"], d["kq"], d["ksc"], nB, T_PREFILL, POS0_B, idsB[l], wsB)
             mark("Bf")
             qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nB, T_PREFILL, POS0_B, idsB[l],
-                                  outB[l])
+                                  outB[l], pwsB)
         mark("C0")
         for l in range(LAYERS):
             d = C[l]
@@ -226,7 +227,7 @@ def run_ours(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC,
-                      nA, nB, nC, cap, dist)
+                      pwsB, nA, nB, nC, cap, dist)
 
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = read_peaks()
     flopA = flops_prefill(T_PREFILL, 0)
@@ -276,8 +277,8 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC, nA, nB,
-            nC, cap, dist):
+def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC, pwsB,
+            nA, nB, nC, cap, dist):
     """Same step with every layer's inputs copied from pinned host memory and outputs copied back."""
     hostA = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in A]
     hostB = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in B]
@@ -301,7 +302,7 @@ def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, p
                 d[k].copy_(h[k], non_blocking=True)
             qsa.qsa_select(d["q"], d["kq"], d["ksc"], nB, T_PREFILL, POS0_B, idsB[l], wsB)
             qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nB, T_PREFILL, POS0_B, idsB[l],
-                                  outB[l])
+                                  outB[l], pwsB)
             hOutB[l].copy_(outB[l], non_blocking=True)
         for l in range(LAYERS):
             d, h = C[l], hostC[l]

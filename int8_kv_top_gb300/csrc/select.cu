@@ -263,14 +263,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     __half* dst_row = scores + ((size_t)g * T_sel + (row_valid ? r : 0)) * n_pad;
     bool dead = false;  // after a failed wait keep meeting the epilogue barrier, skip the work
+    const int sc_cell = et >> 2, sc_b = et & 3;  // this thread stages one scale per tile
+    auto load_scale = [&](int i) -> float {
+      const int c = (nt_begin + i) * kGN + sc_cell;
+      return (i < n_tiles && c < n_lim) ? __half2float(ksc[((size_t)c * kGroups + g) * kNB + sc_b]) : 0.f;
+    };
+    float sc_next = load_scale(0);
     for (int i = 0; i < n_tiles; ++i) {
       const int a = i & 1;
       const int n0 = (nt_begin + i) * kGN;
-      {
-        const int cell = et >> 2, b = et & 3;
-        const float v = (n0 + cell < n_lim) ? __half2float(ksc[((size_t)(n0 + cell) * kGroups + g) * kNB + b]) : 0.f;
-        reinterpret_cast<float*>(&s_scale[a][cell])[b] = v;
-      }
+      reinterpret_cast<float*>(&s_scale[a][sc_cell])[sc_b] = sc_next;
+      sc_next = load_scale(i + 1);  // one tile ahead: the load overlaps this tile's work
       epilogue_bar();
       if (!dead) dead = !mbar_wait_warp(&bars.acc_full[a], (i >> 1) & 1, status, &s_abort);
       if (dead) continue;
@@ -429,12 +432,9 @@ __device__ __forceinline__ int warp_append(bool pred, int* counter) {
   return pred ? base + __popc(m & ((1u << lane) - 1u)) : -1;
 }
 
-// Warp-aggregated histogram increment (lanes with equal bins add once).
+// Histogram increment (shared-memory atomics resolve same-bin lanes in hardware).
 __device__ __forceinline__ void warp_hist_add(bool pred, unsigned bin, unsigned* hist) {
-  const unsigned active = __ballot_sync(0xffffffffu, pred);
-  if (!pred) return;
-  const unsigned peers = __match_any_sync(active, bin);
-  if ((threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
+  if (pred) atomicAdd(&hist[bin], 1u);
 }
 
 // Bounds of the score error: a (absolute) and b (relative to the stored fp16 value).

@@ -27,7 +27,8 @@ QSA_ERR_DEVICE = -6
 N_GROUPS, HEADS_PER_GROUP, N_HEADS, HEAD_DIM, CHUNK, PART_STRIDE = 2, 12, 24, 256, 64, 258
 
 # every symbol include/qsa.h declares
-EXPORTS = ("qsa_last_error", "qsa_prep_quantize", "qsa_select_workspace_bytes", "qsa_select", "qsa_flash_prefill",
+EXPORTS = ("qsa_last_error", "qsa_prep_quantize", "qsa_select_workspace_bytes", "qsa_select",
+           "qsa_flash_prefill_workspace_bytes", "qsa_flash_prefill",
            "qsa_decode_partial", "qsa_merge", "qsa_check_device_status", "qsa_select_noalloc")
 
 
@@ -60,13 +61,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_select_workspace_bytes.argtypes = [I, I, I, PP]
     lib.qsa_select_workspace_bytes.restype = SZ
     lib.qsa_select.argtypes = [P, P, P, I, I, I, P, P, SZ, PP, P]
-    lib.qsa_flash_prefill.argtypes = [P, P, P, P, P, I, I, I, P, P, PP, P]
+    lib.qsa_flash_prefill_workspace_bytes.argtypes = [I, I, I, PP]
+    lib.qsa_flash_prefill_workspace_bytes.restype = SZ
+    lib.qsa_flash_prefill.argtypes = [P, P, P, P, P, I, I, I, P, P, P, SZ, PP, P]
     lib.qsa_decode_partial.argtypes = [P, P, P, P, P, I, I, I, P, P, P, I, PP, P]
     lib.qsa_merge.argtypes = [P, P, I, I, P, P]
     lib.qsa_check_device_status.argtypes = [P]
     lib.qsa_select_noalloc.argtypes = [P, P, P, I, I, I, P, PP, P]
     for name in EXPORTS:
-        if name not in ("qsa_last_error", "qsa_select_workspace_bytes"):
+        if name not in ("qsa_last_error", "qsa_select_workspace_bytes", "qsa_flash_prefill_workspace_bytes"):
             getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -125,9 +128,15 @@ def qsa_select_noalloc(q, kq, ksc, n_cells: int, T: int, pos0: int, ids, params=
                                      _stream(stream)))
 
 
-def qsa_flash_prefill(q, kq, vq, ksc, vsc, n_cells: int, T: int, pos0: int, ids, out, params=None, stream=None):
+def qsa_flash_prefill_workspace_bytes(T: int, pos0: int, n_cells: int, params=None) -> int:
+    return int(load().qsa_flash_prefill_workspace_bytes(T, pos0, n_cells, _params(params)))
+
+
+def qsa_flash_prefill(q, kq, vq, ksc, vsc, n_cells: int, T: int, pos0: int, ids, out, ws=None, params=None,
+                      stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(load().qsa_flash_prefill(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), n_cells, T, pos0, _ptr(ids),
-                                    _ptr(out), _params(params), _stream(stream)))
+                                    _ptr(out), _ptr(ws), ws_bytes, _params(params), _stream(stream)))
 
 
 def qsa_decode_partial(q, kq, vq, ksc, vsc, n_cells: int, N: int, pos0: int, ids, part, n_chunks,

@@ -40,9 +40,9 @@ FAKE = 1 << 20  # aligned, never dereferenced: every call below fails validation
 
 def test_null_and_misaligned_pointers(lib):
     P = ctypes.c_void_p
-    rc = lib.qsa_flash_prefill(None, P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, 4, 0, None, P(FAKE), None, None)
+    rc = lib.qsa_flash_prefill(None, P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, 4, 0, None, P(FAKE), None, 0, None, None)
     assert rc == qsa.QSA_ERR_INVALID_ARG and b"q is NULL" in lib.qsa_last_error()
-    rc = lib.qsa_flash_prefill(P(FAKE + 8), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, 4, 0, None, P(FAKE), None, None)
+    rc = lib.qsa_flash_prefill(P(FAKE + 8), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 10, 4, 0, None, P(FAKE), None, 0, None, None)
     assert rc == qsa.QSA_ERR_INVALID_ARG and b"aligned" in lib.qsa_last_error()
     rc = lib.qsa_merge(P(FAKE), None, 1, 33, P(FAKE), None)
     assert rc == qsa.QSA_ERR_INVALID_ARG
@@ -51,12 +51,17 @@ def test_null_and_misaligned_pointers(lib):
 def test_bad_sizes(lib):
     P = ctypes.c_void_p
     args = (P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE))
-    assert lib.qsa_flash_prefill(*args, 100, 0, 0, None, P(FAKE), None, None) == qsa.QSA_ERR_INVALID_ARG   # T = 0
-    assert lib.qsa_flash_prefill(*args, 100, 4, -1, None, P(FAKE), None, None) == qsa.QSA_ERR_INVALID_ARG  # pos0 < 0
-    assert lib.qsa_flash_prefill(*args, 100, 4, 97, None, P(FAKE), None, None) == qsa.QSA_ERR_INVALID_ARG  # cache small
+    assert lib.qsa_flash_prefill(*args, 100, 0, 0, None, P(FAKE), None, 0, None, None) == qsa.QSA_ERR_INVALID_ARG   # T = 0
+    assert lib.qsa_flash_prefill(*args, 100, 4, -1, None, P(FAKE), None, 0, None, None) == qsa.QSA_ERR_INVALID_ARG  # pos0 < 0
+    assert lib.qsa_flash_prefill(*args, 100, 4, 97, None, P(FAKE), None, 0, None, None) == qsa.QSA_ERR_INVALID_ARG  # cache small
     assert b"cache too small" in lib.qsa_last_error()
-    # tokens above the threshold need ids
-    assert lib.qsa_flash_prefill(*args, 3000, 4, 2500, None, P(FAKE), None, None) == qsa.QSA_ERR_INVALID_ARG
+    # tokens above the threshold need ids, then a workspace
+    assert lib.qsa_flash_prefill(*args, 3000, 4, 2500, None, P(FAKE), None, 0, None, None) == qsa.QSA_ERR_INVALID_ARG
+    need = lib.qsa_flash_prefill_workspace_bytes(4, 2500, 3000, None)
+    assert need == 2 * 2504 * 2 * 256 * 2
+    assert lib.qsa_flash_prefill(*args, 3000, 4, 2500, P(FAKE), P(FAKE), P(FAKE), need - 16, None, None) == \
+        qsa.QSA_ERR_WORKSPACE
+    assert lib.qsa_flash_prefill_workspace_bytes(4, 0, 100, None) == 0
     assert lib.qsa_merge(P(FAKE), P(FAKE), 0, 33, P(FAKE), None) == qsa.QSA_ERR_INVALID_ARG
     assert lib.qsa_merge(P(FAKE), P(FAKE), 1, 2000, P(FAKE), None) == qsa.QSA_ERR_UNSUPPORTED
     # decode: chunk_cap too small for the default set size (2051 cells -> 33 chunks)
@@ -68,7 +73,7 @@ def test_bad_sizes(lib):
 
 def test_bad_params(lib):
     P = ctypes.c_void_p
-    args = (P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 100, 4, 0, None, P(FAKE))
+    args = (P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 100, 4, 0, None, P(FAKE), None, 0)
     for bad in [(0, 2051, 0.0625), (2053, 2051, 0.0625), (4, 0, 0.0625), (4, 8, 0.0), (4, 8, -1.0),
                 (4, 8, float("inf"))]:
         p = qsa.qsa_params(*bad)

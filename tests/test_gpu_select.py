@@ -20,7 +20,9 @@ def gpu_select_prefill(inp, T, pos0, params=None, poison=True):
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") if nbytes else None
     qsa.qsa_select(d["q"], d["kq"], d["ksc"], n_cells, T, pos0, ids, ws, params)
     out = torch.full((T, 24, 256), float("nan"), dtype=torch.float16, device="cuda")
-    qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n_cells, T, pos0, ids, out, params)
+    pb = qsa.qsa_flash_prefill_workspace_bytes(T, pos0, n_cells, params)
+    pws = torch.empty(max(pb, 16), dtype=torch.uint8, device="cuda") if pb else None
+    qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n_cells, T, pos0, ids, out, pws, params)
     qsa.qsa_check_device_status()
     return ids.cpu().numpy(), out.float().cpu().numpy()
 
