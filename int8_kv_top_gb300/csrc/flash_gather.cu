@@ -182,8 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 1 && warp <= 3) {
     // ------------------------------------------------------------ gather producers
     const int pw = warp - 1;  // rows pw, pw + 3, ... of every 32-row group
-    bool ok = true;
-    for (int j = 0; ok && j < 2 * U; ++j) {
+    // ids of entry j's tile, lane l holding rows l, l+32, l+64, l+96 (-1: none); loaded one
+    // entry ahead so the copies never wait on them
+    auto load_ids = [&](int j, int (&dst)[4]) {
       int u, is_v;
       seq_entry(j, U, &u, &is_v);
       const int k = u / n_tiles, jl = u % n_tiles;
@@ -191,6 +192,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = t_begin + (it >> 1), g = it & 1;
       const int n_kv = pos0 + t + 1;
       const int32_t* idrow = ids + ((size_t)t * kGroups + g) * K;
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int slot = jl * kCells + 32 * x + lane;
+        int c = (slot < K) ? __ldg(idrow + slot) : -1;
+        if (c >= n_kv || (c < 0 && slot < K)) {
+          if (!is_v && pw == 0) set_dev_status(status, QSA_DEV_BAD_ID);
+          c = -1;
+        }
+        dst[x] = c;
+      }
+    };
+    int cur[4] = {-1, -1, -1, -1};
+    if (U > 0) load_ids(0, cur);
+    bool ok = true;
+    for (int j = 0; ok && j < 2 * U; ++j) {
+      int u, is_v;
+      seq_entry(j, U, &u, &is_v);
+      const int k = u / n_tiles, jl = u % n_tiles;
+      const int it = blockIdx.x + k * gridDim.x;
+      const int t = t_begin + (it >> 1), g = it & 1;
+      int nxt[4] = {-1, -1, -1, -1};
+      if (j + 1 < 2 * U) load_ids(j + 1, nxt);
       if (!is_v && jl == 0 && warp == 1) {
         // Q^T tile for this item: rows 0..11 = the group's heads (rows 12..15 stay zero)
         if (k >= 2 && !mbar_wait_warp(&bars.q_empty[k & 1], ((k >> 1) & 1) ^ 1, status, &s_abort)) ok = false;
@@ -215,22 +238,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint8_t* xb = smem + kOffX + buf * kTileBytes;
       const __half* src = is_v ? vhat : khat;
-      for (int r0 = 0; r0 < kCells; r0 += 32) {
-        const int slot = jl * kCells + r0 + lane;  // this lane's id: row r0 + lane
-        int c = (slot < K) ? __ldg(idrow + slot) : -1;
-        if (c >= n_kv || (c < 0 && slot < K)) {
-          if (!is_v && pw == 0) set_dev_status(status, QSA_DEV_BAD_ID);
-          c = -1;
-        }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
         for (int rr = pw; rr < 32; rr += 3) {
-          const int r = r0 + rr;
-          const int cell = __shfl_sync(0xffffffffu, c, rr);
+          const int r = 32 * x + rr;
+          const int cell = __shfl_sync(0xffffffffu, cur[x], rr);
           const int ch = lane;  // 32 chunks of 16 bytes = one 256-element fp16 row
           cp_async16_zfill(xb + (ch >> 3) * (kCells * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
                            src + ((size_t)(cell >= 0 ? cell : 0) * kGroups + g) * kD + ch * 8, cell >= 0);
         }
       }
       cp_async_arrive_noinc(&bars.x_full[buf]);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) cur[x] = nxt[x];
     }
     cp_async_wait_all();  // nothing of ours may land after the CTA exits
   } else if (warp >= 4) {

@@ -39,8 +39,8 @@ constexpr int kMaxCells = 65536;
 constexpr int kTkThreads = 512;
 constexpr int kCandCap = 2048;
 constexpr int kBandCap = 512;
-// hist 2 KB | qsum 2 KB | band keys + ids | candidate ids | selection bitmap
-constexpr int kTopkSmem = 4096 + kBandCap * 20 + kCandCap * 4 + kMaxCells / 8;
+// hist 2 KB | qsum 2 KB | band keys + ids | candidate ids + keys | selection bitmap
+constexpr int kTopkSmem = 4096 + kBandCap * 20 + kCandCap * 6 + kMaxCells / 8;
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -511,7 +511,8 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   Key128* s_band_key = reinterpret_cast<Key128*>(topk_smem + 4096);            // [kBandCap]
   int* s_band_idx = reinterpret_cast<int*>(s_band_key + kBandCap);             // [kBandCap]
   int* s_cand_idx = s_band_idx + kBandCap;                                     // [kCandCap]
-  unsigned* s_bits = reinterpret_cast<unsigned*>(s_cand_idx + kCandCap);       // [kMaxCells / 32]
+  uint16_t* s_cand_key = reinterpret_cast<uint16_t*>(s_cand_idx + kCandCap);   // [kCandCap]
+  unsigned* s_bits = reinterpret_cast<unsigned*>(s_cand_key + kCandCap);       // [kMaxCells / 32]
   __shared__ int s_red[64];
   __shared__ int s_tmp[8];
   __shared__ int s_cnt[2];          // 0: candidates, 1: band
@@ -564,9 +565,10 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
     }
     w[m] = x;
   }
-  auto half_bits = [](const uint4& x, int j) -> uint16_t {
-    const uint32_t* u = reinterpret_cast<const uint32_t*>(&x);
-    return (uint16_t)(u[j >> 1] >> (16 * (j & 1)));
+  auto half_bits = [](const uint4& x, int j) -> uint16_t {  // select chain: no local-memory indexing
+    const int wd = j >> 1;
+    const uint32_t v = wd == 0 ? x.x : wd == 1 ? x.y : wd == 2 ? x.z : x.w;
+    return (uint16_t)(v >> (16 * (j & 1)));
   };
   __syncthreads();
 
@@ -615,7 +617,10 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
         const int j = __ffs(in) - 1;
         in &= in - 1;
         const int slot = atomicAdd(&s_cnt[0], 1);
-        if (slot < kCandCap) s_cand_idx[slot] = c0 + 8 * m + j;
+        if (slot < kCandCap) {
+          s_cand_idx[slot] = c0 + 8 * m + j;
+          s_cand_key[slot] = (uint16_t)fp16_order_key(half_bits(w[m], j));
+        }
       }
     }
   }
@@ -632,13 +637,13 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
     if (bracket) {
       for (int base = warp * 32; base < Cn; base += kTkThreads) {
         const int i = base + lane;
-        warp_hist_add(i < Cn, i < Cn ? fp16_order_key(__half_as_ushort(row[s_cand_idx[i]])) >> 8 : 0u, s_hist);
+        warp_hist_add(i < Cn, i < Cn ? (uint32_t)s_cand_key[i] >> 8 : 0u, s_hist);
       }
       __syncthreads();
       b1 = find_bin_desc(s_hist, need_c, &ab1, s_tmp);
       for (int base = warp * 32; base < Cn; base += kTkThreads) {
         const int i = base + lane;
-        const uint32_t k = i < Cn ? fp16_order_key(__half_as_ushort(row[s_cand_idx[i]])) : 0u;
+        const uint32_t k = i < Cn ? (uint32_t)s_cand_key[i] : 0u;
         warp_hist_add(i < Cn && (int)(k >> 8) == b1, k & 0xFFu, s_hist + 256);
       }
       __syncthreads();
@@ -677,7 +682,7 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   if (bracket) {
     for (int i = tid; i < Cn; i += kTkThreads) {
       const int c = s_cand_idx[i];
-      const uint32_t k = fp16_order_key(__half_as_ushort(row[c]));
+      const uint32_t k = s_cand_key[i];
       if (k >= k_def) {
         ++n_def;
       } else if (k >= k_band) {
