@@ -203,39 +203,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         dst[x] = c;
       }
     };
-    int cur[4] = {-1, -1, -1, -1};
-    if (U > 0) load_ids(0, cur);
-    bool ok = true;
-    for (int j = 0; ok && j < 2 * U; ++j) {
+    // one entry's work, given its ids (returns false if a wait gave up)
+    auto produce = [&](int j, const int (&cur)[4]) -> bool {
       int u, is_v;
       seq_entry(j, U, &u, &is_v);
       const int k = u / n_tiles, jl = u % n_tiles;
       const int it = blockIdx.x + k * gridDim.x;
       const int t = t_begin + (it >> 1), g = it & 1;
-      int nxt[4] = {-1, -1, -1, -1};
-      if (j + 1 < 2 * U) load_ids(j + 1, nxt);
       if (!is_v && jl == 0 && warp == 1) {
         // Q^T tile for this item: rows 0..11 = the group's heads (rows 12..15 stay zero)
-        if (k >= 2 && !mbar_wait_warp(&bars.q_empty[k & 1], ((k >> 1) & 1) ^ 1, status, &s_abort)) ok = false;
-        if (ok) {
-          uint8_t* qb = smem + kOffQ + (k & 1) * kQBytes;
-          const __half* qt = q + ((size_t)t * kHeads + g * kHPG) * kD;
-          for (int x = lane; x < kHPG * 32; x += 32) {
-            const int hh = x >> 5, ch = x & 31;  // 16-byte chunk ch of row hh
-            const uint4 v = *reinterpret_cast<const uint4*>(qt + hh * kD + ch * 8);
-            *reinterpret_cast<uint4*>(qb + (ch >> 3) * (kNQ * 128) + hh * 128 + (((ch & 7) ^ (hh & 7)) << 4)) = v;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars.q_full[k & 1]);
+        if (k >= 2 && !mbar_wait_warp(&bars.q_empty[k & 1], ((k >> 1) & 1) ^ 1, status, &s_abort)) return false;
+        uint8_t* qb = smem + kOffQ + (k & 1) * kQBytes;
+        const __half* qt = q + ((size_t)t * kHeads + g * kHPG) * kD;
+        for (int x = lane; x < kHPG * 32; x += 32) {
+          const int hh = x >> 5, ch = x & 31;  // 16-byte chunk ch of row hh
+          const uint4 v = *reinterpret_cast<const uint4*>(qt + hh * kD + ch * 8);
+          *reinterpret_cast<uint4*>(qb + (ch >> 3) * (kNQ * 128) + hh * 128 + (((ch & 7) ^ (hh & 7)) << 4)) = v;
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.q_full[k & 1]);
       }
       const int buf = j % kNBuf;
-      const bool w_ok = (j < kNBuf) || mbar_wait_warp(&bars.x_empty[buf], ((j / kNBuf) & 1) ^ 1, status, &s_abort);
-      if (!ok || !w_ok) {
-        ok = false;
-        break;
-      }
+      if (j >= kNBuf && !mbar_wait_warp(&bars.x_empty[buf], ((j / kNBuf) & 1) ^ 1, status, &s_abort)) return false;
       uint8_t* xb = smem + kOffX + buf * kTileBytes;
       const __half* src = is_v ? vhat : khat;
 #pragma unroll
@@ -249,8 +239,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       cp_async_arrive_noinc(&bars.x_full[buf]);
-#pragma unroll
-      for (int x = 0; x < 4; ++x) cur[x] = nxt[x];
+      return true;
+    };
+    // ping-pong id sets: entry j+1's ids are in flight while entry j is issued
+    int ids_a[4] = {-1, -1, -1, -1}, ids_b[4] = {-1, -1, -1, -1};
+    if (U > 0) load_ids(0, ids_a);
+    for (int j = 0; j < 2 * U; j += 2) {
+      if (j + 1 < 2 * U) load_ids(j + 1, ids_b);
+      if (!produce(j, ids_a)) break;
+      if (j + 1 >= 2 * U) break;
+      if (j + 2 < 2 * U) load_ids(j + 2, ids_a);
+      if (!produce(j + 1, ids_b)) break;
     }
     cp_async_wait_all();  // nothing of ours may land after the CTA exits
   } else if (warp >= 4) {
@@ -272,13 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_part[h] = 0.f;
       }
       int last_v = -1;
+      int c_next = (i < K) ? idrow[i] : -1;  // id of this lane's cell in tile 0, then one tile ahead
       for (int jl = 0; jl < n_tiles; ++jl, ++u) {
-        const int slot = jl * kCells + i;
-        bool valid = slot < K;
-        if (valid) {
-          const int c = idrow[slot];
-          valid = c >= 0 && c < n_kv;
-        }
+        const int c_cur = c_next;
+        const bool valid = jl * kCells + i < K && c_cur >= 0 && c_cur < n_kv;
+        const int slot_next = (jl + 1) * kCells + i;
+        c_next = (jl + 1 < n_tiles && slot_next < K) ? idrow[slot_next] : -1;
         const bool w_ok = mbar_wait_warp(&bars.s_full[u & 1], (u >> 1) & 1, status, &s_abort);
         if (named_bar_any(1, 128, !w_ok)) { ok = false; break; }  // all four warps leave together
         tc_fence_after();
