@@ -17,7 +17,7 @@
 //        S^T[c][h]  = K^[c] . q[h]      A = K^ (128 cells, K-major)  B = Q^T (16 rows, 12 used)
 //        O^T[d][h] += V^[c][d] P[h][c]  A = V^ as MN-major (dims x cells)  B = P^T (K-major)
 //     warp 0      TMEM owner and single-thread UMMA issue
-//     warps 1-3   gather producers; three 64 KB tile buffers rotate in the order the MMAs
+//     warps 1-3, 8-11  gather producers; three 64 KB tile buffers rotate in the order the MMAs
 //                 consume them (K0, K1, V0, K2, V1, ...), so each load has ~1.5 tiles of lead;
 //                 warp 1 also stages each item's Q^T tile
 //     warps 4-7   one gathered cell per thread (TMEM lane): column-wise online softmax over
@@ -32,8 +32,9 @@ namespace {
 
 constexpr int kCells = 128;                  // gathered cells per tile (UMMA M)
 constexpr int kNQ = 16;                      // UMMA N: 12 heads + 4 zero rows
-constexpr int kThreads = 256;
-constexpr int kProdThreads = 96;             // warps 1-3
+constexpr int kThreads = 384;
+constexpr int kProdWarps = 7;                // warps 1-3 and 8-11
+constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kTileBytes = kCells * kD * 2;  // 64 KB fp16 tile
 constexpr int kQBytes = kNQ * kD * 2;        // 8 KB
 constexpr int kPBytes = kNQ * kCells * 2;    // 4 KB
@@ -179,9 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&bars.drain, 0, status);
     }
     __syncwarp();
-  } else if (warp >= 1 && warp <= 3) {
+  } else if ((warp >= 1 && warp <= 3) || warp >= 8) {
     // ------------------------------------------------------------ gather producers
-    const int pw = warp - 1;  // rows pw, pw + 3, ... of every 32-row group
+    const int pw = warp <= 3 ? warp - 1 : warp - 5;  // 0..6: rows pw, pw + 7, ... of every 32-row group
     // ids of entry j's tile, lane l holding rows l, l+32, l+64, l+96 (-1: none); loaded one
     // entry ahead so the copies never wait on them
     auto load_ids = [&](int j, int (&dst)[4]) {
@@ -228,14 +229,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j >= kNBuf && !mbar_wait_warp(&bars.x_empty[buf], ((j / kNBuf) & 1) ^ 1, status, &s_abort)) return false;
       uint8_t* xb = smem + kOffX + buf * kTileBytes;
       const __half* src = is_v ? vhat : khat;
+      // lane = 16-byte chunk of the row: its k-block and swizzle-free part of the offset
+      uint8_t* dst_l = xb + (lane >> 3) * (kCells * 128);
+      const __half* src_l = src + (size_t)g * kD + lane * 8;
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        for (int rr = pw; rr < 32; rr += 3) {
+        for (int rr = pw; rr < 32; rr += kProdWarps) {
           const int r = 32 * x + rr;
           const int cell = __shfl_sync(0xffffffffu, cur[x], rr);
-          const int ch = lane;  // 32 chunks of 16 bytes = one 256-element fp16 row
-          cp_async16_zfill(xb + (ch >> 3) * (kCells * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
-                           src + ((size_t)(cell >= 0 ? cell : 0) * kGroups + g) * kD + ch * 8, cell >= 0);
+          cp_async16_zfill(dst_l + r * 128 + (((lane & 7) ^ (r & 7)) << 4),
+                           src_l + (size_t)(cell >= 0 ? cell : 0) * (kGroups * kD), cell >= 0);
         }
       }
       cp_async_arrive_noinc(&bars.x_full[buf]);
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!produce(j + 1, ids_b)) break;
     }
     cp_async_wait_all();  // nothing of ours may land after the CTA exits
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp <= 7) {
     // ------------------------------------------------------------ softmax (thread = cell)
     const int quarter = warp & 3;
     const int i = quarter * 32 + lane;  // cell slot in the tile == TMEM lane
