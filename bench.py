@@ -130,9 +130,11 @@ def run_ours(args, rank, world, local_rank):
     wsB = torch.empty(qsa.qsa_select_workspace_bytes(T_PREFILL, POS0_B, nB), dtype=torch.uint8, device=device)
     wsC = torch.empty(qsa.qsa_select_workspace_bytes(N_DEC, P_DEC, nC), dtype=torch.uint8, device=device)
     pwsB = torch.empty(qsa.qsa_flash_prefill_workspace_bytes(T_PREFILL, POS0_B, nB), dtype=torch.uint8, device=device)
+    pwsA = torch.empty(qsa.qsa_flash_prefill_workspace_bytes(T_PREFILL, 0, nA), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-    # our kernel launches per step: A 1/layer; B select 4 + mirror 1 + gather 1; C select 4 + partial 1 + merge 1
-    launches_per_step = LAYERS * (1 + 6 + 6)
+    # our kernel launches per step: A mirror 1 + dense 1; B select 4 + mirror 1 + gather 1;
+    # C select 4 + partial 1 + merge 1
+    launches_per_step = LAYERS * (2 + 6 + 6)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
@@ -145,7 +147,7 @@ def run_ours(args, rank, world, local_rank):
         mark("A0")
         for l in range(LAYERS):
             d = A[l]
-            qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nA, T_PREFILL, 0, None, outA[l])
+            qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nA, T_PREFILL, 0, None, outA[l], pwsA)
         mark("A1")
         for l in range(LAYERS):
             d = B[l]
@@ -227,7 +229,7 @@ def run_ours(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC,
-                      pwsB, nA, nB, nC, cap, dist)
+                      pwsA, pwsB, nA, nB, nC, cap, dist)
 
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = read_peaks()
     flopA = flops_prefill(T_PREFILL, 0)
@@ -277,8 +279,8 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC, pwsB,
-            nA, nB, nC, cap, dist):
+def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC, pwsA,
+            pwsB, nA, nB, nC, cap, dist):
     """Same step with every layer's inputs copied from pinned host memory and outputs copied back."""
     hostA = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in A]
     hostB = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in B]
@@ -294,7 +296,7 @@ def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, p
             d, h = A[l], hostA[l]
             for k in d:
                 d[k].copy_(h[k], non_blocking=True)
-            qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nA, T_PREFILL, 0, None, outA[l])
+            qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nA, T_PREFILL, 0, None, outA[l], pwsA)
             hOutA[l].copy_(outA[l], non_blocking=True)
         for l in range(LAYERS):
             d, h = B[l], hostB[l]

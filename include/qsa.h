@@ -111,10 +111,9 @@ QSA_API int qsa_select(const uint16_t* q, const int8_t* kq, const uint16_t* ksc,
                int32_t* ids, void* ws, size_t ws_bytes, const qsa_params* params, void* stream);
 
 /*
- * Bytes of device workspace qsa_flash_prefill needs for a call with T tokens at pos0 (0
- * when every token of the call is at or under the identity threshold).  It holds the fp16
- * dequantised K and V rows of cells 0 .. pos0+T-1, written once per call and gathered by
- * the selected tokens: 2 * (pos0 + T) * 2 * 256 * 2 bytes.
+ * Bytes of device workspace qsa_flash_prefill needs for a call with T tokens at pos0: the
+ * fp16 dequantised K and V rows of cells 0 .. pos0+T-1, written once per call and read by
+ * every tile of the call, 2 * (pos0 + T) * 2 * 256 * 2 bytes.
  */
 QSA_API size_t qsa_flash_prefill_workspace_bytes(int T, int pos0, int n_cells, const qsa_params* params);
 
@@ -123,9 +122,9 @@ QSA_API size_t qsa_flash_prefill_workspace_bytes(int T, int pos0, int n_cells, c
  * what changed; "round 14 track b: qsa metadata hoist", decision):
  *   out[t,h,:] = sum_{c in set(t,g)} softmax_c(sm_scale * q[t,h,:] . k^[c,g,:]) * v^[c,g,:]
  * with set(t,g) = all causal cells when n_kv(t) <= identity_max (ids rows not read), else
- * ids[t][g][0..topk).  ids and ws may be NULL when every token of the call is at or under
- * the threshold; otherwise ws must hold qsa_flash_prefill_workspace_bytes(...) bytes and is
- * clobbered.  k^ = fp16(kq * ksc) and v^ = fp16(vq * vsc) (one rounding), fp16 operands, fp32
+ * ids[t][g][0..topk).  ids may be NULL when every token of the call is at or under the
+ * threshold.  ws must hold qsa_flash_prefill_workspace_bytes(...) bytes and is clobbered.
+ * k^ = fp16(kq * ksc) and v^ = fp16(vq * vsc) (one rounding), fp16 operands, fp32
  * accumulation and softmax, P rounded to fp16, fp16 out.  Ids outside [0, n_kv(t)) are
  * skipped and flagged in the status word.
  */

@@ -158,7 +158,7 @@ int qsa_select(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_c
 size_t qsa_flash_prefill_workspace_bytes(int T, int pos0, int n_cells, const qsa_params* params) {
   qsa::Params p;
   if (T <= 0 || pos0 < 0 || n_cells <= 0 || resolve_params(params, &p) != QSA_OK) return 0;
-  return qsa::gather_workspace_bytes(T, pos0, p);
+  return qsa::prefill_workspace_bytes(T, pos0);
 }
 
 int qsa_flash_prefill(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc, const uint16_t* vsc,
@@ -172,23 +172,26 @@ int qsa_flash_prefill(const uint16_t* q, const int8_t* kq, const int8_t* vq, con
   CHECK_PTR(vsc, "vsc");
   CHECK_PTR(out, "out");
   const int t_sel = qsa::first_selected_token(pos0, p.identity_max);
-  if (t_sel < T) {
-    CHECK_PTR(ids, "ids (needed: some tokens are above the identity threshold)");
-    const size_t need = qsa::gather_workspace_bytes(T, pos0, p);
-    if (!ws || ws_bytes < need)
-      return fail(QSA_ERR_WORKSPACE, "prefill workspace of %zu bytes given, %zu needed", ws ? ws_bytes : (size_t)0,
-                  need);
-    if (!aligned16(ws)) return fail(QSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
-  }
+  if (t_sel < T) CHECK_PTR(ids, "ids (needed: some tokens are above the identity threshold)");
+  const size_t need = qsa::prefill_workspace_bytes(T, pos0);
+  if (!ws || ws_bytes < need)
+    return fail(QSA_ERR_WORKSPACE, "prefill workspace of %zu bytes given, %zu needed", ws ? ws_bytes : (size_t)0,
+                need);
+  if (!aligned16(ws)) return fail(QSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
   int* st = status_ptr(&rc);
   if (!st) return rc;
   qsa::FlashArgs a{reinterpret_cast<const __half*>(q), kq, vq, reinterpret_cast<const __half*>(ksc),
                    reinterpret_cast<const __half*>(vsc), ids, reinterpret_cast<__half*>(out), n_cells, T, pos0, p, st};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int n = pos0 + T;
+  __half* khat = static_cast<__half*>(ws);
+  __half* vhat = khat + (size_t)n * QSA_N_GROUPS * QSA_HEAD_DIM;
+  cudaError_t e = qsa::launch_dequant_mirror(kq, vq, a.ksc, a.vsc, n, khat, vhat, s);
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_flash_prefill (fp16 mirror) launch");
   const int split = t_sel < T ? t_sel : T;
-  cudaError_t e = qsa::launch_flash_dense(a, 0, split, s);
+  e = qsa::launch_flash_dense(a, 0, split, khat, vhat, s);
   if (e != cudaSuccess) return cuda_fail(e, "qsa_flash_prefill (identity tokens) launch");
-  e = qsa::launch_flash_gather(a, split, T, ws, s);
+  e = qsa::launch_flash_gather(a, split, T, khat, vhat, s);
   if (e != cudaSuccess) return cuda_fail(e, "qsa_flash_prefill (selected tokens) launch");
   return ok();
 }

@@ -70,9 +70,14 @@ struct FlashArgs {
   int* status;
 };
 
-cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, cudaStream_t stream);
-size_t gather_workspace_bytes(int T, int pos0, Params p);
-cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, void* ws, cudaStream_t stream);
+// fp16 mirror of the cache cells 0 .. n-1 (K^ and V^), written once per prefill call.
+size_t prefill_workspace_bytes(int T, int pos0);
+cudaError_t launch_dequant_mirror(const int8_t* kq, const int8_t* vq, const __half* ksc, const __half* vsc, int n,
+                                  __half* khat, __half* vhat, cudaStream_t stream);
+cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
+                               cudaStream_t stream);
+cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
+                                cudaStream_t stream);
 
 cudaError_t launch_decode_partial(const __half* q, const int8_t* kq, const int8_t* vq, const __half* ksc,
                                   const __half* vsc, const int32_t* ids, float* part, int32_t* n_chunks,

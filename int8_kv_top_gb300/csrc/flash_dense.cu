@@ -1,5 +1,5 @@
 // qsa_flash_prefill, identity tokens (n_kv <= identity_max): dense causal attention of
-// fp16 queries over the int8 KV cache on the tcgen05 tensor cores.
+// fp16 queries over the KV cache on the tcgen05 tensor cores.
 //
 // The pages' qsa_flash runs one threadgroup per (KV head, token) over 64-cell chunks:
 // partial S for 12 heads, combine and scale by 1/16, max/exp per head, fp16 P, PV
@@ -8,10 +8,11 @@
 // n_kv <= 2051).  That design serves a GPU without a matrix unit big enough for a 128-row
 // tile.  Here the 12 heads of a group share their K/V rows, so a CTA owns a 128-row tile
 // of (token, head) pairs of one group, 32 tokens x 4 heads, and every 64-cell chunk is a
-// dense M=128 contraction:
+// dense M=128 contraction over the call's fp16 mirror of the cache (mirror.cu: each cell
+// dequantised once per call instead of once per tile that reads it):
 //
-//   warp 0      TMA: int8 K and V chunk tiles [64 cells][256] + their scale rows, 2-stage ring
-//   warps 8-15  dequantise int8 * fp16 scale -> fp16 into 128B-swizzled K^/V^ buffers
+//   warp 0      TMA: fp16 K^ and V^ chunk tiles, four 128B-swizzled boxes of [64 cells][64
+//               dims] each, which is exactly the UMMA operand layout; 3-stage ring
 //   warp 1      TMEM owner + single-thread UMMA issue:
 //                 S  = Q K^T   (A = Q from TMEM, B = K^ K-major)      M=128 N=64  K=256
 //                 O += P V^    (A = P from TMEM, B = V^ MN-major)     M=128 N=256 K=64
@@ -20,7 +21,6 @@
 //               (only when the running max grows by more than 2^8), final 1/l and fp16 out.
 //
 // TMEM columns: O [0,256)  S/P double buffer [256,320) [320,384)  Q [384,512).
-// Shared memory: int8 ring 2 x (32 KB codes + 2 KB scales), K^ 2 x 32 KB, V^ 2 x 32 KB (fp16).
 // Every mbarrier wait is bounded; a timeout sets the status word and the CTA drains.
 #include <cstring>
 
@@ -33,23 +33,17 @@ constexpr int kTok = 32;               // tokens per row tile
 constexpr int kHQ = 4;                 // heads per row tile
 constexpr int kRows = kTok * kHQ;      // 128 = UMMA M
 constexpr int kKV = 64;                // cells per chunk (UMMA N of QK^T)
-constexpr int kThreads = 512;
-constexpr int kI8Bytes = kKV * kD;     // one int8 tile (K or V), 16 KB
-constexpr int kHalfTile = kKV * kD * 2;  // one fp16 tile, 32 KB
-constexpr int kScaleBytes = kKV * kGroups * kNB * 2;     // [64 cells][2 groups][4] fp16, 1 KB
-constexpr int kStageBytes = 2 * kI8Bytes + 2 * kScaleBytes;  // K, V codes + K, V scales: 34 KB
-constexpr int kSmemI8 = 0;                                 // 2 stages
-constexpr int kSmemKh = kSmemI8 + 2 * kStageBytes;         // 68 KB
-constexpr int kSmemVh = kSmemKh + 2 * kHalfTile;           // 132 KB
-constexpr int kSmemTotal = kSmemVh + 2 * kHalfTile;        // 196 KB
-constexpr int kSmemAlloc = kSmemTotal + 1024;        // + alignment slack
+constexpr int kThreads = 256;
+constexpr int kStages = 3;
+constexpr int kHalfTile = kKV * kD * 2;           // one fp16 tile (K^ or V^), 32 KB
+constexpr int kStageBytes = 2 * kHalfTile;        // K^ then V^
+constexpr int kSmemTotal = kStages * kStageBytes;  // 192 KB
+constexpr int kSmemAlloc = kSmemTotal + 1024;      // + alignment slack
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct __align__(8) Bars {
-  uint64_t i8_full[2], i8_empty[2];
-  uint64_t kh_full[2], kh_empty[2];
-  uint64_t vh_full[2], vh_empty[2];
+  uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done[2], q_full, drain;  // o_done[i & 1]: PV(i) complete
 };
@@ -67,9 +61,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __global__ void __launch_bounds__(kThreads, 1)
     flash_dense_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                       const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_vs,
-                       const __half* __restrict__ q, __half* __restrict__ out, int pos0, int t_begin,
-                       int t_end, float scale_log2, int* status) {
+                       const __half* __restrict__ q, __half* __restrict__ out, int pos0, int t_begin, int t_end,
+                       float scale_log2, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Bars bars;
@@ -88,18 +81,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     s_abort = 0;
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bars.kv_full[i], 1);
+      mbar_init(&bars.kv_empty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.i8_full[i], 1);
-      mbar_init(&bars.i8_empty[i], 8);
-      mbar_init(&bars.kh_full[i], 8);
-      mbar_init(&bars.kh_empty[i], 1);
-      mbar_init(&bars.vh_full[i], 8);
-      mbar_init(&bars.vh_empty[i], 1);
       mbar_init(&bars.s_full[i], 1);
       mbar_init(&bars.p_full[i], 4);
+      mbar_init(&bars.o_done[i], 1);
     }
-    mbar_init(&bars.o_done[0], 1);
-    mbar_init(&bars.o_done[1], 1);
     mbar_init(&bars.q_full, 4);
     mbar_init(&bars.drain, 1);
     fence_mbar_init();
@@ -118,58 +108,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      tma_prefetch_desc(&map_ks);
-      tma_prefetch_desc(&map_vs);
       int issued = 0;
       for (int j = 0; j < J; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(&bars.i8_empty[s], ((j >> 1) & 1) ^ 1, status, &s_abort)) break;
-        uint8_t* dst = smem + kSmemI8 + s * kStageBytes;
-        mbar_arrive_expect_tx(&bars.i8_full[s], kStageBytes);
-        tma_load_3d(dst, &map_k, &bars.i8_full[s], 0, g, j * kKV);
-        tma_load_3d(dst + kI8Bytes, &map_v, &bars.i8_full[s], 0, g, j * kKV);
-        tma_load_2d(dst + 2 * kI8Bytes, &map_ks, &bars.i8_full[s], 0, j * kKV);
-        tma_load_2d(dst + 2 * kI8Bytes + kScaleBytes, &map_vs, &bars.i8_full[s], 0, j * kKV);
+        const int s = j % kStages;
+        if (j >= kStages && !mbar_wait(&bars.kv_empty[s], ((j / kStages) & 1) ^ 1, status, &s_abort)) break;
+        uint8_t* dst = smem + s * kStageBytes;
+        mbar_arrive_expect_tx(&bars.kv_full[s], kStageBytes);
+#pragma unroll
+        for (int blk = 0; blk < kNB; ++blk) {
+          tma_load_3d(dst + blk * (kKV * 128), &map_k, &bars.kv_full[s], blk * 64, g, j * kKV);
+          tma_load_3d(dst + kHalfTile + blk * (kKV * 128), &map_v, &bars.kv_full[s], blk * 64, g, j * kKV);
+        }
         issued = j + 1;
       }
-      // drain: the last load of each stage must have landed before the CTA exits
-      for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(&bars.i8_full[j & 1], (j >> 1) & 1, status);
+      // drain: the loads of the last stages must have landed before the CTA exits
+      for (int j = max(0, issued - kStages); j < issued; ++j)
+        mbar_wait(&bars.kv_full[j % kStages], (j / kStages) & 1, status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issue
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_f16_f32(kRows, kKV, 0, 0);
       const uint32_t idesc_pv = idesc_f16_f32(kRows, kD, 0, 1);
-      const uint32_t kh0 = smem_u32(smem + kSmemKh), vh0 = smem_u32(smem + kSmemVh);
+      const uint32_t st0 = smem_u32(smem);
       bool ok = mbar_wait(&bars.q_full, 0, status, &s_abort);  // Q rows are in TMEM
       tc_fence_after();
       auto issue_pv = [&](int i) -> bool {
-        const int b = i & 1;
+        const int b = i & 1, s = i % kStages;
         if (!mbar_wait(&bars.p_full[b], (i >> 1) & 1, status, &s_abort)) return false;
-        if (!mbar_wait(&bars.vh_full[b], (i >> 1) & 1, status, &s_abort)) return false;
         tc_fence_after();
-        const uint32_t vb = vh0 + b * kHalfTile;
+        const uint32_t vb = st0 + s * kStageBytes + kHalfTile;
 #pragma unroll
         for (int kk = 0; kk < kKV / 16; ++kk) {
           const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, kKV * 128, 1024);
           umma_ts(tmem + kColO, tmem + kColS + b * 64 + kk * 8, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bars.o_done[b]);
-        umma_commit(&bars.vh_empty[b]);
+        umma_commit(&bars.kv_empty[s]);
         return true;
       };
       for (int j = 0; ok && j < J; ++j) {
-        const int b = j & 1;
-        if (!mbar_wait(&bars.kh_full[b], (j >> 1) & 1, status, &s_abort)) { ok = false; break; }
+        const int b = j & 1, s = j % kStages;
+        if (!mbar_wait(&bars.kv_full[s], (j / kStages) & 1, status, &s_abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kb = kh0 + b * kHalfTile;
+        const uint32_t kb = st0 + s * kStageBytes;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint64_t bdesc = sdesc_sw128(kb + (kk >> 2) * (kKV * 128) + (kk & 3) * 32, 16, 1024);
           umma_ts(tmem + kColS + b * 64, tmem + kColQ + kk * 8, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars.s_full[b]);
-        umma_commit(&bars.kh_empty[b]);
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok) issue_pv(J - 1);
@@ -304,41 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ dequantise
-    const int dw = warp - 8;
-    const int blk = lane >> 3;
-    for (int j = 0; j < J; ++j) {
-      const int s = j & 1, b = j & 1;
-      if (!mbar_wait_warp(&bars.i8_full[s], (j >> 1) & 1, status, &s_abort)) break;
-      const uint8_t* src = smem + kSmemI8 + s * kStageBytes;
-      bool ok = true;
-#pragma unroll 1
-      for (int kv = 0; kv < 2; ++kv) {
-        uint64_t* empty = kv ? &bars.vh_empty[b] : &bars.kh_empty[b];
-        uint64_t* full = kv ? &bars.vh_full[b] : &bars.kh_full[b];
-        if (j >= 2 && !mbar_wait_warp(empty, ((j >> 1) & 1) ^ 1, status, &s_abort)) { ok = false; break; }
-        const __half* sc = reinterpret_cast<const __half*>(src + 2 * kI8Bytes + kv * kScaleBytes) + g * kNB + blk;
-        uint8_t* dstb = smem + (kv ? kSmemVh : kSmemKh) + b * kHalfTile;
-        const uint8_t* srcb = src + kv * kI8Bytes;
-#pragma unroll 2
-        for (int u = 0; u < kKV / 8; ++u) {
-          const int cell = dw + 8 * u;
-          const __half scale = sc[cell * kGroups * kNB];  // zero-filled past the cache end
-          const uint2 w = *reinterpret_cast<const uint2*>(srcb + cell * kD + lane * 8);
-          uint32_t o[4];
-          dequant8(w.x, w.y, __half2half2(scale), o);
-          const uint32_t off = blk * (kKV * 128) + cell * 128 + (((lane & 7) ^ (cell & 7)) << 4);
-          *reinterpret_cast<uint4*>(dstb + off) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.i8_empty[s]);
-      if (!ok) break;
-    }
   }
 
   tc_fence_before();
@@ -347,33 +300,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-bool make_scale_map(CUtensorMap* map, const __half* base, int n_cells) {
+// 3D map over a fp16 mirror [n][2][256]: box = 64 dims x 1 group x 64 cells, 128B swizzle.
+bool make_mirror_map(CUtensorMap* map, const __half* base, int n) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)(kGroups * kNB), (cuuint64_t)n_cells};
-  const cuuint64_t strides[1] = {(cuuint64_t)(kGroups * kNB * 2)};
-  const cuuint32_t box[2] = {(cuuint32_t)(kGroups * kNB), (cuuint32_t)kKV};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<__half*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool make_kv_map(CUtensorMap* map, const int8_t* base, int n_cells) {
-  EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kGroups, (cuuint64_t)n_cells};
-  const cuuint64_t strides[2] = {(cuuint64_t)kD, (cuuint64_t)kD * kGroups};
-  const cuuint32_t box[3] = {(cuuint32_t)kD, 1u, (cuuint32_t)kKV};
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kGroups, (cuuint64_t)n};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * kGroups * 2};
+  const cuuint32_t box[3] = {64u, 1u, (cuuint32_t)kKV};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<int8_t*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
-cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, cudaStream_t stream) {
+cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
+                               cudaStream_t stream) {
   if (t_end <= t_begin) return cudaSuccess;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -383,14 +326,13 @@ cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, cudaS
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  CUtensorMap mk, mv, mks, mvs;
-  if (!make_kv_map(&mk, a.kq, a.n_cells) || !make_kv_map(&mv, a.vq, a.n_cells) ||
-      !make_scale_map(&mks, a.ksc, a.n_cells) || !make_scale_map(&mvs, a.vsc, a.n_cells))
-    return cudaErrorInvalidValue;
+  const int n = a.pos0 + a.T;  // cells in the mirror
+  CUtensorMap mk, mv;
+  if (!make_mirror_map(&mk, khat, n) || !make_mirror_map(&mv, vhat, n)) return cudaErrorInvalidValue;
   const int n_ttiles = (t_end - t_begin + kTok - 1) / kTok;
   const float scale_log2 = a.p.sm_scale * kLog2e;
-  flash_dense_kernel<<<n_ttiles * 6, kThreads, kSmemAlloc, stream>>>(mk, mv, mks, mvs, a.q, a.out, a.pos0, t_begin,
-                                                                    t_end, scale_log2, a.status);
+  flash_dense_kernel<<<n_ttiles * 6, kThreads, kSmemAlloc, stream>>>(mk, mv, a.q, a.out, a.pos0, t_begin, t_end,
+                                                                    scale_log2, a.status);
   return cudaGetLastError();
 }
 

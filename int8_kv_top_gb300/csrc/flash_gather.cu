@@ -8,9 +8,8 @@
 // across tokens, while every cell of the cache is selected by many tokens (about 6% of
 // 1984 tokens per layer on random data).  Two launches therefore:
 //
-//  1. dequant_mirror: K^ = fp16(kq * ksc) and V^ = fp16(vq * vsc) once per call for the
-//     cells the call's tokens can see (the same rounding as the dense path), into a
-//     caller workspace in the cache's own [cell][group][256] layout.
+//  1. the fp16 mirror (mirror.cu): K^ = fp16(kq * ksc) and V^ = fp16(vq * vsc) once per
+//     call for the cells the call's tokens can see, in the cache's [cell][group][256] layout.
 //  2. flash_gather: per (token, group), the selected fp16 rows are gathered with 16-byte
 //     cp.async copies straight into 128B-swizzled UMMA operand tiles, and the MMA is swapped
 //     so the gathered cells form the 128-wide M side:
@@ -388,34 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
-// grid (ceil(n / 8), 2 groups), 256 threads: a warp per cell row, K and V.
-__global__ void __launch_bounds__(256)
-    dequant_mirror_kernel(const int8_t* __restrict__ kq, const int8_t* __restrict__ vq, const __half* __restrict__ ksc,
-                          const __half* __restrict__ vsc, int n, __half* __restrict__ khat, __half* __restrict__ vhat) {
-  const int g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x * 8 + warp;
-  if (c >= n) return;
-  const size_t row = ((size_t)c * kGroups + g) * kD + lane * 8;
-  const int blk = lane >> 3;
-  uint32_t o[4];
-  const uint2 wk = *reinterpret_cast<const uint2*>(kq + row);
-  dequant8(wk.x, wk.y, __half2half2(ksc[((size_t)c * kGroups + g) * kNB + blk]), o);
-  *reinterpret_cast<uint4*>(khat + row) = make_uint4(o[0], o[1], o[2], o[3]);
-  const uint2 wv = *reinterpret_cast<const uint2*>(vq + row);
-  dequant8(wv.x, wv.y, __half2half2(vsc[((size_t)c * kGroups + g) * kNB + blk]), o);
-  *reinterpret_cast<uint4*>(vhat + row) = make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 }  // namespace
 
-size_t gather_workspace_bytes(int T, int pos0, Params p) {
-  const int t_sel = first_selected_token(pos0, p.identity_max);
-  if (t_sel >= T) return 0;
-  const size_t n = (size_t)pos0 + T;  // cells any token of the call can see
-  return 2 * n * kGroups * kD * sizeof(__half);
-}
-
-cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, void* ws, cudaStream_t stream) {
+cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
+                                cudaStream_t stream) {
   if (t_end <= t_begin) return cudaSuccess;
   static bool attr_done[64] = {};
   static int n_sms[64] = {};
@@ -427,12 +402,6 @@ cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, void
     cudaDeviceGetAttribute(&n_sms[dev], cudaDevAttrMultiProcessorCount, dev);
     attr_done[dev] = true;
   }
-  const int n = a.pos0 + a.T;
-  __half* khat = static_cast<__half*>(ws);
-  __half* vhat = khat + (size_t)n * kGroups * kD;
-  dequant_mirror_kernel<<<dim3((n + 7) / 8, kGroups), 256, 0, stream>>>(a.kq, a.vq, a.ksc, a.vsc, n, khat, vhat);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   const int n_items = (t_end - t_begin) * kGroups;
   const int sms = (dev < 64 && n_sms[dev] > 0) ? n_sms[dev] : 148;
   const int grid = n_items < sms ? n_items : sms;

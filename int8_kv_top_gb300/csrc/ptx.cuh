@@ -77,6 +77,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (it > 4) __nanosleep(it < 64 ? 32 : 128);  // back off so waiting warps free the issue slots
     if ((it & 7u) == 0u) {
       if (abort && *abort) return false;
       if (globaltimer_ns() - t0 > kWaitBudgetNs) {

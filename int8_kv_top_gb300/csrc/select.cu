@@ -421,17 +421,6 @@ __device__ __forceinline__ int find_bin_desc(const unsigned* hist, int need, int
   return b;
 }
 
-// Warp-aggregated append of (this lane's) item to a shared list; returns its slot or -1.
-__device__ __forceinline__ int warp_append(bool pred, int* counter) {
-  const unsigned m = __ballot_sync(0xffffffffu, pred);
-  if (!m) return -1;
-  const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
-  int base = 0;
-  if (lane == leader) base = atomicAdd(counter, __popc(m));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  return pred ? base + __popc(m & ((1u << lane) - 1u)) : -1;
-}
-
 // Histogram increment (shared-memory atomics resolve same-bin lanes in hardware).
 __device__ __forceinline__ void warp_hist_add(bool pred, unsigned bin, unsigned* hist) {
   if (pred) atomicAdd(&hist[bin], 1u);

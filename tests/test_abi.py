@@ -61,7 +61,7 @@ def test_bad_sizes(lib):
     assert need == 2 * 2504 * 2 * 256 * 2
     assert lib.qsa_flash_prefill(*args, 3000, 4, 2500, P(FAKE), P(FAKE), P(FAKE), need - 16, None, None) == \
         qsa.QSA_ERR_WORKSPACE
-    assert lib.qsa_flash_prefill_workspace_bytes(4, 0, 100, None) == 0
+    assert lib.qsa_flash_prefill_workspace_bytes(4, 0, 100, None) == 2 * 4 * 2 * 256 * 2  # the fp16 mirror
     assert lib.qsa_merge(P(FAKE), P(FAKE), 0, 33, P(FAKE), None) == qsa.QSA_ERR_INVALID_ARG
     assert lib.qsa_merge(P(FAKE), P(FAKE), 1, 2000, P(FAKE), None) == qsa.QSA_ERR_UNSUPPORTED
     # decode: chunk_cap too small for the default set size (2051 cells -> 33 chunks)

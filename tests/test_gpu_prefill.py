@@ -14,7 +14,8 @@ def run_prefill(inp, T, pos0, ids=None, params=None):
     d = to_dev(inp)
     n_cells = inp["kq"].shape[0]
     out = torch.full((T, 24, 256), float("nan"), dtype=torch.float16, device="cuda")
-    qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n_cells, T, pos0, ids, out, None, params)
+    ws = torch.empty(qsa.qsa_flash_prefill_workspace_bytes(T, pos0, n_cells, params), dtype=torch.uint8, device="cuda")
+    qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n_cells, T, pos0, ids, out, ws, params)
     qsa.qsa_check_device_status()
     return out.float().cpu().numpy()
 
