@@ -16,8 +16,9 @@
 //   warp 1      TMEM owner + single-thread UMMA issue:
 //                 S  = Q K^T   (A = Q from TMEM, B = K^ K-major)      M=128 N=64  K=256
 //                 O += P V^    (A = P from TMEM, B = V^ MN-major)     M=128 N=256 K=64
-//   warps 4-7   one (token, head) row per thread: Q -> TMEM, online softmax on S in
-//               base-2 units (max, exp2, row sum), fp16 P -> TMEM over S, lazy O rescale
+//   warps 4-11  two warpgroups, one (token, head) row per thread in each, half of the
+//               columns each: Q -> TMEM, online softmax on S in base-2 units (max exchanged
+//               through shared memory, exp2, row sums), fp16 P -> TMEM over S, lazy O rescale
 //               (only when the running max grows by more than 2^8), final 1/l and fp16 out.
 //
 // TMEM columns: O [0,256)  S/P double buffer [256,320) [320,384)  Q [384,512).
@@ -33,7 +34,7 @@ constexpr int kTok = 32;               // tokens per row tile
 constexpr int kHQ = 4;                 // heads per row tile
 constexpr int kRows = kTok * kHQ;      // 128 = UMMA M
 constexpr int kKV = 64;                // cells per chunk (UMMA N of QK^T)
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kStages = 3;
 constexpr int kHalfTile = kKV * kD * 2;           // one fp16 tile (K^ or V^), 32 KB
 constexpr int kStageBytes = 2 * kHalfTile;        // K^ then V^
@@ -87,10 +88,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.p_full[i], 4);
+      mbar_init(&bars.p_full[i], 8);
       mbar_init(&bars.o_done[i], 1);
     }
-    mbar_init(&bars.q_full, 4);
+    mbar_init(&bars.q_full, 8);
     mbar_init(&bars.drain, 1);
     fence_mbar_init();
   }
@@ -166,8 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&bars.drain, 0, status);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax rows
+    // Two warpgroups share every row: warps 4-7 take S columns 0-31 of each chunk and O
+    // dims 0-127, warps 8-11 columns 32-63 and dims 128-255; they exchange half-row maxima
+    // and sums through shared memory.
+    __shared__ float s_xm[2][kRows];  // half-row maxima, then half-row sums
+    const int wg = warp >= 8 ? 1 : 0;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // TMEM lane == tile row
     const int tl = r >> 2, hl = r & 3;
@@ -177,11 +183,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_kv_row = row_valid ? pos0 + t + 1 : 0;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
 
-    // Q row -> TMEM columns [384, 512): 128 words of two fp16 (even dim in the low half)
+    // this warpgroup's half of the Q row -> TMEM columns [384 + 64 wg, 448 + 64 wg)
     {
-      const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)(row_valid ? t : t0) * kHeads + h) * kD);
+      const uint4* src =
+          reinterpret_cast<const uint4*>(q + ((size_t)(row_valid ? t : t0) * kHeads + h) * kD + wg * 128);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -191,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           w[i * 4 + 2] = v.z;
           w[i * 4 + 3] = v.w;
         }
-        tmem_st16(lane_base + kColQ + c * 16, w);
+        tmem_st16(lane_base + kColQ + wg * 64 + c * 16, w);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -199,96 +206,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars.q_full);
     }
 
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;  // l_run: this half of the row
     bool ok = true;
     for (int j = 0; j < J; ++j) {
       const int b = j & 1;
-      if (!mbar_wait_warp(&bars.s_full[b], (j >> 1) & 1, status, &s_abort)) { ok = false; break; }
+      const bool w_ok = mbar_wait_warp(&bars.s_full[b], (j >> 1) & 1, status, &s_abort);
+      if (named_bar_any(1, 256, !w_ok || !ok)) { ok = false; break; }  // both warpgroups leave together
       tc_fence_after();
-      uint32_t sr[64];
-      {
-        uint32_t a[32], c[32];
-        tmem_ld32(lane_base + kColS + b * 64, a);
-        tmem_ld32(lane_base + kColS + b * 64 + 32, c);
-        tmem_wait_ld();
+      uint32_t sr[32];
+      tmem_ld32(lane_base + kColS + b * 64 + wg * 32, sr);
+      tmem_wait_ld();
+      float s[32];
+      float m_half = -INFINITY;
+      const int lim = n_kv_row - j * kKV - wg * 32;  // cells i < lim are causal for this row
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sr[i] = a[i];
-          sr[32 + i] = c[i];
-        }
-      }
-      float s[64];
-      float m_tile = -INFINITY;
-      const int lim = n_kv_row - j * kKV;  // cells i < lim are causal for this row
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
+      for (int i = 0; i < 32; ++i) {
         s[i] = (i < lim) ? __uint_as_float(sr[i]) * scale_log2 : -INFINITY;
-        m_tile = fmaxf(m_tile, s[i]);
+        m_half = fmaxf(m_half, s[i]);
       }
+      s_xm[wg][r] = m_half;
+      named_bar_any(1, 256, false);
+      const float m_tile = fmaxf(m_half, s_xm[wg ^ 1][r]);
       const float m_new = fmaxf(m_run, m_tile);
       if (j == 0) {
         m_run = m_new;
       } else {
-        const bool need = m_new > m_run + kRescaleThreshold;
+        const bool need = m_new > m_run + kRescaleThreshold;  // identical in both warpgroups
         if (__any_sync(0xffffffffu, need)) {
           // O must hold every PV issued so far before it is rescaled in place
           // (alternating barriers: the commit after QK(j) already covered PV(j-2), so the
           // barrier of PV(j-1) is at most one phase behind)
-          if (!mbar_wait_warp(&bars.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, status, &s_abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const float f = need ? fast_exp2(m_run - m_new) : 1.f;
+          if (mbar_wait_warp(&bars.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, status, &s_abort)) {
+            tc_fence_after();
+            const float f = need ? fast_exp2(m_run - m_new) : 1.f;
 #pragma unroll 1
-          for (int c0 = 0; c0 < kD; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + kColO + c0, o);
-            tmem_wait_ld();
+            for (int c0 = wg * 128; c0 < wg * 128 + 128; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld32(lane_base + kColO + c0, o);
+              tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-            tmem_st32(lane_base + kColO + c0, o);
-          }
-          tmem_wait_st();
-          if (need) {
-            l_run *= f;
-            m_run = m_new;
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+              tmem_st32(lane_base + kColO + c0, o);
+            }
+            tmem_wait_st();
+            if (need) {
+              l_run *= f;
+              m_run = m_new;
+            }
+          } else {
+            ok = false;  // reported at the next tile's collective barrier
           }
         }
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      uint32_t pw[32];
+      uint32_t pw[16];
       float lsum = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 16; ++i) {
         const float p0 = fast_exp2(s[2 * i] - m_use), p1 = fast_exp2(s[2 * i + 1] - m_use);
         lsum += p0 + p1;
         pw[i] = pack_half2(p0, p1);
       }
       l_run += lsum;
-      tmem_st32(lane_base + kColS + b * 64, pw);
+      tmem_st16(lane_base + kColS + b * 64 + wg * 16, pw);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.p_full[b]);
     }
-    if (ok && mbar_wait_warp(&bars.o_done[(J - 1) & 1], ((J - 1) >> 1) & 1, status, &s_abort)) {
-      tc_fence_after();
-      const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      __half* dst = out + ((size_t)(row_valid ? t : 0) * kHeads + h) * kD;
+    if (!named_bar_any(1, 256, !ok)) {  // uniform: a failure in the last chunk is seen by all
+      s_xm[wg][r] = l_run;
+      named_bar_any(1, 256, false);
+      const float l_tot = l_run + s_xm[wg ^ 1][r];
+      const bool e_ok = mbar_wait_warp(&bars.o_done[(J - 1) & 1], ((J - 1) >> 1) & 1, status, &s_abort);
+      if (e_ok) {
+        tc_fence_after();
+        const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+        __half* dst = out + ((size_t)(row_valid ? t : 0) * kHeads + h) * kD;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kD; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + kColO + c0, o);
-        tmem_wait_ld();
-        uint32_t w[16];
+        for (int c0 = wg * 128; c0 < wg * 128 + 128; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + kColO + c0, o);
+          tmem_wait_ld();
+          uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_half2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (row_valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_half2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          if (row_valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
         }
       }
     }
