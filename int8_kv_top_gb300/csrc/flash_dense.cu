@@ -11,8 +11,9 @@
 // dense M=128 contraction over the call's fp16 mirror of the cache (mirror.cu: each cell
 // dequantised once per call instead of once per tile that reads it):
 //
-//   warp 0      TMA: fp16 K^ and V^ chunk tiles, four 128B-swizzled boxes of [64 cells][64
-//               dims] each, which is exactly the UMMA operand layout; 3-stage ring
+//   warps 0, 2  TMA: fp16 K^ and V^ chunk tiles, four 128B-swizzled boxes of [64 cells][64
+//               dims] each, which is exactly the UMMA operand layout; K^ in a 4-stage ring
+//               released by QK(j), V^ in a 2-stage ring released by PV(j)
 //   warp 1      TMEM owner + single-thread UMMA issue:
 //                 S  = Q K^T   (A = Q from TMEM, B = K^ K-major)      M=128 N=64  K=256
 //                 O += P V^    (A = P from TMEM, B = V^ MN-major)     M=128 N=256 K=64
@@ -35,16 +36,16 @@ constexpr int kHQ = 4;                 // heads per row tile
 constexpr int kRows = kTok * kHQ;      // 128 = UMMA M
 constexpr int kKV = 64;                // cells per chunk (UMMA N of QK^T)
 constexpr int kThreads = 384;
-constexpr int kStages = 3;
-constexpr int kHalfTile = kKV * kD * 2;           // one fp16 tile (K^ or V^), 32 KB
-constexpr int kStageBytes = 2 * kHalfTile;        // K^ then V^
-constexpr int kSmemTotal = kStages * kStageBytes;  // 192 KB
-constexpr int kSmemAlloc = kSmemTotal + 1024;      // + alignment slack
+constexpr int kKStages = 4, kVStages = 2;  // K^ freed by QK(j), V^ by PV(j): separate rings
+constexpr int kHalfTile = kKV * kD * 2;    // one fp16 tile (K^ or V^), 32 KB
+constexpr int kSmemV = kKStages * kHalfTile;                 // V ring after the K ring
+constexpr int kSmemTotal = (kKStages + kVStages) * kHalfTile;  // 192 KB
+constexpr int kSmemAlloc = kSmemTotal + 1024;                // + alignment slack
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct __align__(8) Bars {
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done[2], q_full, drain;  // o_done[i & 1]: PV(i) complete
 };
@@ -82,9 +83,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     s_abort = 0;
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bars.kv_full[i], 1);
-      mbar_init(&bars.kv_empty[i], 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&bars.k_full[i], 1);
+      mbar_init(&bars.k_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&bars.v_full[i], 1);
+      mbar_init(&bars.v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.s_full[i], 1);
@@ -104,61 +109,64 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ TMA producers (K^: warp 0, V^: warp 2)
     if (lane == 0) {
-      tma_prefetch_desc(&map_k);
-      tma_prefetch_desc(&map_v);
+      const bool is_v = warp == 2;
+      const CUtensorMap* map = is_v ? &map_v : &map_k;
+      const int nst = is_v ? kVStages : kKStages;
+      uint64_t* full = is_v ? bars.v_full : bars.k_full;
+      uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
+      uint8_t* ring = smem + (is_v ? kSmemV : 0);
+      tma_prefetch_desc(map);
       int issued = 0;
       for (int j = 0; j < J; ++j) {
-        const int s = j % kStages;
-        if (j >= kStages && !mbar_wait(&bars.kv_empty[s], ((j / kStages) & 1) ^ 1, status, &s_abort)) break;
-        uint8_t* dst = smem + s * kStageBytes;
-        mbar_arrive_expect_tx(&bars.kv_full[s], kStageBytes);
+        const int s = j % nst;
+        if (j >= nst && !mbar_wait(&empty[s], ((j / nst) & 1) ^ 1, status, &s_abort)) break;
+        uint8_t* dst = ring + s * kHalfTile;
+        mbar_arrive_expect_tx(&full[s], kHalfTile);
 #pragma unroll
-        for (int blk = 0; blk < kNB; ++blk) {
-          tma_load_3d(dst + blk * (kKV * 128), &map_k, &bars.kv_full[s], blk * 64, g, j * kKV);
-          tma_load_3d(dst + kHalfTile + blk * (kKV * 128), &map_v, &bars.kv_full[s], blk * 64, g, j * kKV);
-        }
+        for (int blk = 0; blk < kNB; ++blk) tma_load_3d(dst + blk * (kKV * 128), map, &full[s], blk * 64, g, j * kKV);
         issued = j + 1;
       }
       // drain: the loads of the last stages must have landed before the CTA exits
-      for (int j = max(0, issued - kStages); j < issued; ++j)
-        mbar_wait(&bars.kv_full[j % kStages], (j / kStages) & 1, status);
+      for (int j = max(0, issued - nst); j < issued; ++j) mbar_wait(&full[j % nst], (j / nst) & 1, status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issue
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_f16_f32(kRows, kKV, 0, 0);
       const uint32_t idesc_pv = idesc_f16_f32(kRows, kD, 0, 1);
-      const uint32_t st0 = smem_u32(smem);
+      const uint32_t k0 = smem_u32(smem), v0 = smem_u32(smem + kSmemV);
       bool ok = mbar_wait(&bars.q_full, 0, status, &s_abort);  // Q rows are in TMEM
       tc_fence_after();
       auto issue_pv = [&](int i) -> bool {
-        const int b = i & 1, s = i % kStages;
+        const int b = i & 1, s = i % kVStages;
         if (!mbar_wait(&bars.p_full[b], (i >> 1) & 1, status, &s_abort)) return false;
+        if (!mbar_wait(&bars.v_full[s], (i / kVStages) & 1, status, &s_abort)) return false;
         tc_fence_after();
-        const uint32_t vb = st0 + s * kStageBytes + kHalfTile;
+        const uint32_t vb = v0 + s * kHalfTile;
 #pragma unroll
         for (int kk = 0; kk < kKV / 16; ++kk) {
           const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, kKV * 128, 1024);
           umma_ts(tmem + kColO, tmem + kColS + b * 64 + kk * 8, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bars.o_done[b]);
-        umma_commit(&bars.kv_empty[s]);
+        umma_commit(&bars.v_empty[s]);
         return true;
       };
       for (int j = 0; ok && j < J; ++j) {
-        const int b = j & 1, s = j % kStages;
-        if (!mbar_wait(&bars.kv_full[s], (j / kStages) & 1, status, &s_abort)) { ok = false; break; }
+        const int b = j & 1, s = j % kKStages;
+        if (!mbar_wait(&bars.k_full[s], (j / kKStages) & 1, status, &s_abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kb = st0 + s * kStageBytes;
+        const uint32_t kb = k0 + s * kHalfTile;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint64_t bdesc = sdesc_sw128(kb + (kk >> 2) * (kKV * 128) + (kk & 3) * 32, 16, 1024);
           umma_ts(tmem + kColS + b * 64, tmem + kColQ + kk * 8, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars.s_full[b]);
+        umma_commit(&bars.k_empty[s]);
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok) issue_pv(J - 1);
