@@ -145,12 +145,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars.p_full[b], (i >> 1) & 1, status, &s_abort)) return false;
         if (!mbar_wait(&bars.v_full[s], (i / kVStages) & 1, status, &s_abort)) return false;
         tc_fence_after();
-        const uint32_t vb = v0 + s * kHalfTile;
+        // descriptor built once; the start-address field (bytes >> 4, low bits) advances per K step
+        const uint64_t vdesc = sdesc_sw128(v0 + s * kHalfTile, kKV * 128, 1024);
+        const uint32_t pcol = tmem + kColS + b * 64;
 #pragma unroll
-        for (int kk = 0; kk < kKV / 16; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, kKV * 128, 1024);
-          umma_ts(tmem + kColO, tmem + kColS + b * 64 + kk * 8, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kKV / 16; ++kk)
+          umma_ts(tmem + kColO, pcol + kk * 8, vdesc + (uint64_t)((kk * 2048) >> 4), idesc_pv,
+                  (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars.o_done[b]);
         umma_commit(&bars.v_empty[s]);
         return true;
@@ -159,12 +160,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = j & 1, s = j % kKStages;
         if (!mbar_wait(&bars.k_full[s], (j / kKStages) & 1, status, &s_abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kb = k0 + s * kHalfTile;
+        const uint64_t kdesc = sdesc_sw128(k0 + s * kHalfTile, 16, 1024);
+        const uint32_t scol = tmem + kColS + b * 64;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(kb + (kk >> 2) * (kKV * 128) + (kk & 3) * 32, 16, 1024);
-          umma_ts(tmem + kColS + b * 64, tmem + kColQ + kk * 8, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kD / 16; ++kk)
+          umma_ts(scol, tmem + kColQ + kk * 8, kdesc + (uint64_t)(((kk >> 2) * (kKV * 128) + (kk & 3) * 32) >> 4),
+                  idesc_qk, kk > 0 ? 1u : 0u);
         umma_commit(&bars.s_full[b]);
         umma_commit(&bars.k_empty[s]);
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }

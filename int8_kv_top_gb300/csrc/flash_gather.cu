@@ -144,13 +144,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (jl == 0 && !mbar_wait(&bars.q_full[k & 1], (k >> 1) & 1, status, &s_abort)) { ok = false; break; }
           if (!mbar_wait(&bars.x_full[buf], (j / kNBuf) & 1, status, &s_abort)) { ok = false; break; }
           tc_fence_after();
+          const uint64_t ad0 = sdesc_sw128(xb, 16, 1024), bd0 = sdesc_sw128(sQ + (k & 1) * kQBytes, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(xb + (kk >> 2) * (kCells * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd =
-                sdesc_sw128(sQ + (k & 1) * kQBytes + (kk >> 2) * (kNQ * 128) + (kk & 3) * 32, 16, 1024);
-            umma_ss(tmem + kColS + (u & 1) * 16, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kD / 16; ++kk)
+            umma_ss(tmem + kColS + (u & 1) * 16, ad0 + (uint64_t)(((kk >> 2) * (kCells * 128) + (kk & 3) * 32) >> 4),
+                    bd0 + (uint64_t)(((kk >> 2) * (kNQ * 128) + (kk & 3) * 32) >> 4), idesc_s, kk > 0 ? 1u : 0u);
           umma_commit(&bars.s_full[u & 1]);
           umma_commit(&bars.x_empty[buf]);
           if (jl == n_tiles - 1) umma_commit(&bars.q_empty[k & 1]);
@@ -163,14 +161,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&bars.p_full[b], (u >> 1) & 1, status, &s_abort)) { ok = false; break; }
           if (!mbar_wait(&bars.x_full[buf], (j / kNBuf) & 1, status, &s_abort)) { ok = false; break; }
           tc_fence_after();
+          const uint64_t av0 = sdesc_sw128(xb, kCells * 128, 1024), bp0 = sdesc_sw128(sP + b * kPBytes, 16, 1024);
 #pragma unroll
           for (int half = 0; half < 2; ++half)
 #pragma unroll
-            for (int kk = 0; kk < kCells / 16; ++kk) {
-              const uint64_t ad = sdesc_sw128(xb + half * 2 * (kCells * 128) + kk * 2048, kCells * 128, 1024);
-              const uint64_t bd = sdesc_sw128(sP + b * kPBytes + (kk >> 2) * (kNQ * 128) + (kk & 3) * 32, 16, 1024);
-              umma_ss(tmem + kColO + ob * 32 + half * 16, ad, bd, idesc_o, (jl > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kCells / 16; ++kk)
+              umma_ss(tmem + kColO + ob * 32 + half * 16,
+                      av0 + (uint64_t)((half * 2 * (kCells * 128) + kk * 2048) >> 4),
+                      bp0 + (uint64_t)(((kk >> 2) * (kNQ * 128) + (kk & 3) * 32) >> 4), idesc_o,
+                      (jl > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&bars.x_empty[buf]);
           umma_commit(&bars.o_done[b]);
         }

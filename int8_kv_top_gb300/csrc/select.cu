@@ -234,16 +234,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (i >= 2 && !mbar_wait(&bars.acc_empty[a], ((i >> 1) & 1) ^ 1, status, &s_abort)) { ok = false; break; }
         if (!mbar_wait(&bars.b_full[st], (i / kGStages) & 1, status, &s_abort)) { ok = false; break; }
         tc_fence_after();
+        const uint64_t ad0 = sdesc_sw128(a0, 16, 1024), bd0 = sdesc_sw128(b0 + st * kSmemBStage, 16, 1024);
 #pragma unroll
         for (int b = 0; b < kNB; ++b)
 #pragma unroll
           for (int part = 0; part < 2; ++part)  // hi_b then lo_b against the same codes
 #pragma unroll
-            for (int kk = 0; kk < kGK / 16; ++kk) {
-              const uint64_t ad = sdesc_sw128(a0 + (2 * b + part) * (kGM * 128) + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(b0 + st * kSmemBStage + b * (kGN * 128) + kk * 32, 16, 1024);
-              umma_ss(tmem + a * 256 + b * kGN, ad, bd, idesc, (part > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kGK / 16; ++kk)
+              umma_ss(tmem + a * 256 + b * kGN, ad0 + (uint64_t)(((2 * b + part) * (kGM * 128) + kk * 32) >> 4),
+                      bd0 + (uint64_t)((b * (kGN * 128) + kk * 32) >> 4), idesc, (part > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars.b_empty[st]);
         umma_commit(&bars.acc_full[a]);
       }
