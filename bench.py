@@ -43,6 +43,24 @@ def flops_prefill(T, pos0, topk=2048, idmax=2051):
     return 24 * cells * 256 * 4
 
 
+KERNEL_OF_FAMILY = {"dense_prefill": "flash_dense_kernel", "gather_prefill": "flash_gather_kernel"}
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None when the
+    kernel's source has changed since the counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+                return None
+        return rec["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
 def read_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -254,7 +272,8 @@ def run_ours(args, rank, world, local_rank):
     else:
         roof = dict(per_launch[dominant])
         roof["kernel"] = dominant
-    roof["traffic"] = None
+    roof["traffic"] = recorded_traffic(KERNEL_OF_FAMILY.get(dominant, ""))
+    roof["traffic_unit"] = "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"
     roof["peak_source"] = f"{peak_src}, sustained bf16 (f16 same rate)" if roof["unit"] == "TFLOP/s" else peak_src
 
     tokens = 2 * T_PREFILL * LAYERS
@@ -340,43 +359,78 @@ def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, p
 def oracle_sample(seconds_budget=20.0):
     """Time the CPU oracle, as it stands, on a bounded sample of the same workload.
 
-    The sample: a slice of tokens of layer 0 of workload A (identity prefill, every 31st
-    token of T=1984), 2 tokens of workload B (selection over ~31,984 cells + attention) and
-    the decode token of workload C; the per-layer time of the full workload is extrapolated
-    from the per-token times.  Returns (tokens/s per layer, description, cores)."""
+    The sample is taken from layer 0 of each workload:
+      A: tokens of the identity prefill T=1984 pos0=0 at a fixed stride;
+      B: the first tokens of the selected prefill T=1984 pos0=30000 (selection over
+         ~31,984 cells, then attention);
+      C: repeats of the decode token at P=8192.
+    Each part first runs a small calibration sample, then a sample sized to fill about a
+    third of `seconds_budget`.  The per-layer time of the full workload is extrapolated
+    from the per-cell (A) and per-token (B, C) times of the sized samples.
+    Returns (tokens/s per layer, description, cores, seconds spent)."""
     import oracle
     from int8_kv_top_gb300 import synth
 
     oracle.build()
     cores = os.cpu_count() or 1
+    part = seconds_budget / 3.0
+    spent = 0.0
+
     inpA = synth.layer_inputs(T_PREFILL, T_PREFILL, seed=5)
-    toksA = np.arange(0, T_PREFILL, 31, dtype=np.int32)
-    t0 = time.perf_counter()
-    oracle.prefill(inpA, T_PREFILL, 0, toks=toksA)
-    tA = time.perf_counter() - t0
-    cellsA = sum(t + 1 for t in toksA)
-    sec_per_cell_A = tA / cellsA
-    inpB = synth.layer_inputs(2, POS0_B + 2, seed=105)
-    t0 = time.perf_counter()
-    oracle.prefill(inpB, 2, POS0_B)
-    tB = (time.perf_counter() - t0) / 2
+
+    def run_a(stride):
+        toks = np.arange(0, T_PREFILL, stride, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.prefill(inpA, T_PREFILL, 0, toks=toks)
+        return time.perf_counter() - t0, int(sum(int(t) + 1 for t in toks)), len(toks)
+
+    dt, cells, _ = run_a(124)
+    spent += dt
+    cells_all = sum(t + 1 for t in range(T_PREFILL))
+    est_full = dt / cells * cells_all
+    stride = max(1, int(np.ceil(est_full / part)))
+    tA, cellsA, nA = run_a(stride)
+    spent += tA
+    full_A = tA / cellsA * cells_all
+
+    def run_b(n_tok):
+        inp = synth.layer_inputs(n_tok, POS0_B + n_tok, seed=105)
+        t0 = time.perf_counter()
+        oracle.prefill(inp, n_tok, POS0_B)
+        return time.perf_counter() - t0
+
+    nB0 = max(1, min(16, cores))
+    dt = run_b(nB0)
+    spent += dt
+    nB = int(max(nB0, min(T_PREFILL, part / (dt / nB0))))
+    tB = run_b(nB)
+    spent += tB
+    full_B = tB / nB * T_PREFILL
+
     inpC = synth.layer_inputs(N_DEC, P_DEC + N_DEC, seed=205)
     t0 = time.perf_counter()
     oracle.decode(inpC, N_DEC, P_DEC)
-    tC = time.perf_counter() - t0
-    full_A = sec_per_cell_A * sum(t + 1 for t in range(T_PREFILL))
-    full_B = tB * T_PREFILL
+    dt = time.perf_counter() - t0
+    spent += dt
+    reps = int(max(1, min(200, part / max(dt, 1e-6))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.decode(inpC, N_DEC, P_DEC)
+    tC = (time.perf_counter() - t0) / reps
+    spent += tC * reps
+
     per_layer = full_A + full_B + tC
     value = 2 * T_PREFILL / per_layer
-    desc = (f"layer-0 samples: {len(toksA)} tokens of T=1984 pos0=0 ({tA:.2f}s), 2 tokens of T=1984 pos0=30000 "
-            f"({2 * tB:.2f}s), 1 decode token P=8192 ({tC:.2f}s); per-layer time extrapolated by cells/tokens")
-    return value, desc, cores, tA + 2 * tB + tC
+    desc = (f"layer 0: {nA} tokens (stride {stride}) of T=1984 pos0=0 in {tA:.2f}s; the first {nB} tokens of "
+            f"T=1984 pos0=30000 in {tB:.2f}s; {reps} x the decode token at P=8192 in {tC * reps:.2f}s; per-layer "
+            f"time extrapolated by cells (A) and tokens (B, C); {cores} OpenMP threads")
+    return value, desc, cores, spent
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -393,8 +447,9 @@ def main():
             return
         vals = []
         desc, cores = "", 1
+        budget = max(3.0, min(20.0, 180.0 / max(1, args.warmup + args.steps)))
         for i in range(args.warmup + args.steps):
-            v, desc, cores, _ = oracle_sample()
+            v, desc, cores, _ = oracle_sample(budget)
             if i >= args.warmup:
                 vals.append(v)
         v = statistics.median(vals)
