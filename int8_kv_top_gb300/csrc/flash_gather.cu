@@ -15,43 +15,57 @@
 //     so the gathered cells form the 128-wide M side:
 //        S^T[c][h]  = K^[c] . q[h]      A = K^ (128 cells, K-major)  B = Q^T (16 rows, 12 used)
 //        O^T[d][h] += V^[c][d] P[h][c]  A = V^ as MN-major (dims x cells)  B = P^T (K-major)
-//     warp 0      TMEM owner and single-thread UMMA issue
-//     warps 1-3, 8-11  gather producers; three 64 KB tile buffers rotate in the order the MMAs
-//                 consume them (K0, K1, V0, K2, V1, ...), so each load has ~1.5 tiles of lead;
-//                 warp 1 also stages each item's Q^T tile
-//     warps 4-7   one gathered cell per thread (TMEM lane): column-wise online softmax over
-//                 the 128 cells (shuffle + shared-memory max per head, base-2 exponent),
-//                 fp16 P^T into shared memory, lazy O^T rescale, epilogue (thread = dim)
-// The CTA is persistent over (token, group) work items.  TMEM: S^T double buffer [0,32),
-// O^T double buffer (two 16-column halves for dims 0-127 / 128-255) [32,96).
+//
+// The gathers are bound by how many row reads each SM keeps in flight, so eleven producer
+// warps share every fill of one ring of 32 KB slots (half a K or V tile: 128 cells x 128
+// dims), filled in exactly the order the MMAs consume them and freed by the MMAs that read
+// them.  QK runs kLead tiles ahead of PV over kNS S^T / P^T buffers, so the K stream never
+// waits for the softmax of the tile before it.  Ids are ascending, so tile j of every item
+// covers about the same cell range; each item starts its walk at tile (item mod tiles), which
+// spreads the SMs' concurrent reads over the whole mirror instead of one window of it (the
+// online softmax does not depend on the order of the tiles).
+//     warp 0        TMEM owner and single-thread UMMA issue
+//     warps 1-3, 12-19  gather producers (warp 1 also stages each item's Q^T tile)
+//     warps 4-7     softmax for heads 0-5, warps 8-11 for heads 6-11: one gathered cell per
+//                   thread (TMEM lane), column-wise online softmax over the 128 cells
+//                   (shuffle + shared-memory max per head, base-2 exponent), fp16 P^T into
+//                   shared memory, lazy O^T rescale, epilogue (thread = dim)
+// The CTA is persistent over (token, group) work items.  TMEM: S^T buffers [0, 64), O^T
+// double buffer (two 16-column halves for dims 0-127 / 128-255) [64, 128).
 #include "common.cuh"
 
 namespace qsa {
 namespace {
 
-constexpr int kCells = 128;                  // gathered cells per tile (UMMA M)
-constexpr int kNQ = 16;                      // UMMA N: 12 heads + 4 zero rows
-constexpr int kThreads = 384;
-constexpr int kProdWarps = 7;                // warps 1-3 and 8-11
-constexpr int kProdThreads = kProdWarps * 32;
-constexpr int kTileBytes = kCells * kD * 2;  // 64 KB fp16 tile
-constexpr int kQBytes = kNQ * kD * 2;        // 8 KB
-constexpr int kPBytes = kNQ * kCells * 2;    // 4 KB
-constexpr int kNBuf = 3;
-constexpr int kOffX = 0, kOffQ = kNBuf * kTileBytes, kOffP = kOffQ + 2 * kQBytes;
-constexpr int kSmemTotal = kOffP + 2 * kPBytes;
+constexpr int kCells = 128;                // gathered cells per tile (UMMA M)
+constexpr int kNQ = 16;                    // UMMA N: 12 heads + 4 zero rows
+constexpr int kThreads = 640;
+constexpr int kProdWarps = 11;             // warps 1-3 and 12-19
+constexpr int kPerWarp = (kCells / 2 + kProdWarps - 1) / kProdWarps;  // copy instructions per warp and fill
+constexpr int kBlkBytes = kCells * 128;    // 16 KB: one 64-dim block of a tile
+constexpr int kSlotBytes = 2 * kBlkBytes;  // 32 KB: one 128-dim half of a K or V tile
+constexpr int kSlots = 6;
+constexpr int kNS = 4;                     // S^T and P^T buffers
+constexpr int kLead = 2;                   // QK(u + kLead) is issued before PV(u)
+constexpr int kQBytes = kNQ * kD * 2;      // 8 KB
+constexpr int kPBytes = kNQ * kCells * 2;  // 4 KB
+constexpr int kOffX = 0, kOffQ = kSlots * kSlotBytes;
+constexpr int kOffP = kOffQ + 2 * kQBytes;
+constexpr int kSmemTotal = kOffP + kNS * kPBytes;
 constexpr int kSmemAlloc = kSmemTotal + 1024;
-constexpr uint32_t kColS = 0, kColO = 32;
+constexpr uint32_t kColS = 0, kColO = kNS * 16;
+constexpr int kHPW = 6;  // heads per softmax warpgroup
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kNoSlot = -2147483647 - 1;  // marks tile slots past the end of an id row
+static_assert(kLead + 2 <= kNS, "S^T / P^T buffers must cover the QK lead");
 
 struct __align__(8) GBars {
-  uint64_t x_full[kNBuf], x_empty[kNBuf];
+  uint64_t x_full[kSlots], x_empty[kSlots];
   uint64_t q_full[2], q_empty[2];
-  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+  uint64_t s_full[kNS], p_full[kNS];
+  uint64_t o_done[kNS], o_free[2];  // o_done per tile mod kNS: a wait is never two phases behind
   uint64_t drain;
 };
-
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // 16-byte copy that writes zeros (and reads nothing) when `valid` is false.
 __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
@@ -60,20 +74,27 @@ __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, boo
                : "memory");
 }
 
-// Entry j of the load/consume sequence: K(0), K(1), V(0), K(2), V(1), ..., K(U-1), V(U-2), V(U-1).
-__device__ __forceinline__ void seq_entry(int j, int U, int* tile, int* is_v) {
-  if (j == 0) {
-    *tile = 0;
-    *is_v = 0;
-  } else if (j == 2 * U - 1) {
-    *tile = U - 1;
-    *is_v = 1;
-  } else if (j & 1) {  // j = 2u - 1 -> K(u), u >= 1
-    *tile = (j + 1) >> 1;
-    *is_v = 0;
-  } else {  // j = 2u -> V(u - 1)
-    *tile = (j >> 1) - 1;
-    *is_v = 1;
+__device__ __forceinline__ int pick4(const int (&v)[4], int x) {  // select chain: no local memory
+  return x == 0 ? v[0] : x == 1 ? v[1] : x == 2 ? v[2] : v[3];
+}
+
+// This warpgroup's six head columns (wg 0: 0-5, wg 1: 6-11) of a 16-column TMEM group.
+__device__ __forceinline__ void ld6(uint32_t taddr, int wg, uint32_t (&r)[kHPW]) {
+  if (wg == 0) {
+    tmem_ld4(taddr, r);
+    tmem_ld2(taddr + 4, r + 4);
+  } else {
+    tmem_ld2(taddr + 6, r);
+    tmem_ld4(taddr + 8, r + 2);
+  }
+}
+__device__ __forceinline__ void st6(uint32_t taddr, int wg, const uint32_t (&r)[kHPW]) {
+  if (wg == 0) {
+    tmem_st4(taddr, r);
+    tmem_st2(taddr + 4, r + 4);
+  } else {
+    tmem_st2(taddr + 6, r);
+    tmem_st4(taddr + 8, r + 2);
   }
 }
 
@@ -86,8 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ GBars bars;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ float s_red[2][4][kHPG];
-  __shared__ float s_l[4][kHPG];
+  __shared__ float s_red[2][2][4][kHPW];  // [warpgroup][tile parity][quarter][head]
+  __shared__ float s_l[2][4][kHPW];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (K + kCells - 1) / kCells;
@@ -96,27 +117,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     s_abort = 0;
-    for (int i = 0; i < kNBuf; ++i) {
-      mbar_init(&bars.x_full[i], kProdThreads);  // one cp.async completion arrival per producer
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&bars.x_full[i], kProdWarps * 32);  // one cp.async completion arrival per producer thread
       mbar_init(&bars.x_empty[i], 1);
+    }
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.p_full[i], 8);
+      mbar_init(&bars.o_done[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.q_full[i], 1);
       mbar_init(&bars.q_empty[i], 1);
-      mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.p_full[i], 4);
-      mbar_init(&bars.o_done[i], 1);
-      mbar_init(&bars.o_free[i], 4);
+      mbar_init(&bars.o_free[i], 8);
     }
     mbar_init(&bars.drain, 1);
     fence_mbar_init();
   }
-  // zero Q^T rows 12..15 and P^T rows 12..15 of both buffers (never written again)
-  for (int i = tid; i < 2 * (kQBytes + kPBytes) / 16; i += kThreads) {
-    const int qi = 2 * kQBytes / 16;
-    uint8_t* p = (i < qi) ? smem + kOffQ + i * 16 : smem + kOffP + (i - qi) * 16;
-    *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
-  }
+  // zero the Q^T and P^T buffers: rows 12..15 are never written again
+  for (int i = tid; i < (2 * kQBytes + kNS * kPBytes) / 16; i += kThreads)
+    *reinterpret_cast<uint4*>(smem + kOffQ + i * 16) = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 0) {
     tmem_alloc(&s_tmem, 128);
@@ -127,136 +147,182 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
+  // Raw ids of tile u for a producer warp: lane l holds slots l, l+32, l+64, l+96 (kNoSlot past
+  // the end of the id row).
+  // Loaded a tile ahead and checked only when used, so the loads overlap the copies.
+  auto load_ids = [&](int u, int (&dst)[4], int& g_out, int& nkv_out) {
+    const int k = u / n_tiles, jl = u % n_tiles;
+    const int it = blockIdx.x + k * gridDim.x;
+    const int t = t_begin + (it >> 1), g = it & 1;
+    const int32_t* idrow = ids + ((size_t)t * kGroups + g) * K;
+    const int pt = (jl + it) % n_tiles;  // tile order rotated per item (see above)
+    g_out = g;
+    nkv_out = pos0 + t + 1;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int slot = pt * kCells + 32 * x + lane;
+      dst[x] = (slot < K) ? __ldg(idrow + slot) : kNoSlot;
+    }
+  };
+  // Ids in [0, n_kv) stay, anything else becomes -1 (a zero row); a bad id in a real slot is
+  // reported once per tile by the reporting warp.
+  auto check_ids = [&](int (&v)[4], int n_kv, bool report) {
+    bool bad = false;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const bool ok = v[x] >= 0 && v[x] < n_kv;
+      bad |= !ok && v[x] != kNoSlot;
+      if (!ok) v[x] = -1;
+    }
+    if (report && __any_sync(0xffffffffu, bad) && lane == 0) set_dev_status(status, QSA_DEV_BAD_ID);
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ UMMA issue
     if (lane == 0) {
       const uint32_t idesc_s = idesc_f16_f32(kCells, kNQ, 0, 0);
       const uint32_t idesc_o = idesc_f16_f32(kCells, kNQ, 1, 0);
-      const uint32_t sX = smem_u32(smem + kOffX), sQ = smem_u32(smem + kOffQ), sP = smem_u32(smem + kOffP);
+      const uint32_t sX = smem_u32(smem + kOffX);
+      const uint32_t sQ = smem_u32(smem + kOffQ), sP = smem_u32(smem + kOffP);
+      int f = 0;  // fill counter: slot f % kSlots, in the producers' order
       bool ok = true;
-      for (int j = 0; ok && j < 2 * U; ++j) {
-        int u, is_v;
-        seq_entry(j, U, &u, &is_v);
-        const int k = u / n_tiles, jl = u % n_tiles;  // item (local) and tile within it
-        const int buf = j % kNBuf;
-        const uint32_t xb = sX + buf * kTileBytes;
-        if (!is_v) {
+      for (int s = 0; ok && s < U + kLead; ++s) {
+        if (s < U) {  // S^T(s) = K^(s) . Q^T: two fills of two 64-dim blocks (four K steps each)
+          const int k = s / n_tiles, jl = s % n_tiles;
           if (jl == 0 && !mbar_wait(&bars.q_full[k & 1], (k >> 1) & 1, status, &s_abort)) { ok = false; break; }
-          if (!mbar_wait(&bars.x_full[buf], (j / kNBuf) & 1, status, &s_abort)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t ad0 = sdesc_sw128(xb, 16, 1024), bd0 = sdesc_sw128(sQ + (k & 1) * kQBytes, 16, 1024);
+          const uint64_t bq0 = sdesc_sw128(sQ + (k & 1) * kQBytes, 16, 1024);
+          const uint32_t dS = tmem + kColS + (s % kNS) * 16;
+          for (int hf = 0; hf < 2; ++hf, ++f) {
+            const int slot = f % kSlots;
+            if (!mbar_wait(&bars.x_full[slot], (f / kSlots) & 1, status, &s_abort)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t a0 = sdesc_sw128(sX + slot * kSlotBytes, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            umma_ss(tmem + kColS + (u & 1) * 16, ad0 + (uint64_t)(((kk >> 2) * (kCells * 128) + (kk & 3) * 32) >> 4),
-                    bd0 + (uint64_t)(((kk >> 2) * (kNQ * 128) + (kk & 3) * 32) >> 4), idesc_s, kk > 0 ? 1u : 0u);
-          umma_commit(&bars.s_full[u & 1]);
-          umma_commit(&bars.x_empty[buf]);
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ss(dS, a0 + (uint64_t)(((kk >> 2) * kBlkBytes + (kk & 3) * 32) >> 4),
+                      bq0 + (uint64_t)(((2 * hf + (kk >> 2)) * (kNQ * 128) + (kk & 3) * 32) >> 4), idesc_s,
+                      (hf > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&bars.x_empty[slot]);
+          }
+          if (!ok) break;
+          umma_commit(&bars.s_full[s % kNS]);
           if (jl == n_tiles - 1) umma_commit(&bars.q_empty[k & 1]);
-        } else {
-          const int b = u & 1, ob = k & 1;
+        }
+        if (s >= kLead) {  // O^T += V^(u)^T . P^T(u): one fill per 128-dim half
+          const int u = s - kLead;
+          const int k = u / n_tiles, jl = u % n_tiles, ob = k & 1;
           if (jl == 0 && k >= 2 && !mbar_wait(&bars.o_free[ob], ((k >> 1) & 1) ^ 1, status, &s_abort)) {
             ok = false;
             break;
           }
-          if (!mbar_wait(&bars.p_full[b], (u >> 1) & 1, status, &s_abort)) { ok = false; break; }
-          if (!mbar_wait(&bars.x_full[buf], (j / kNBuf) & 1, status, &s_abort)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t av0 = sdesc_sw128(xb, kCells * 128, 1024), bp0 = sdesc_sw128(sP + b * kPBytes, 16, 1024);
-#pragma unroll
-          for (int half = 0; half < 2; ++half)
+          if (!mbar_wait(&bars.p_full[u % kNS], (u / kNS) & 1, status, &s_abort)) { ok = false; break; }
+          const uint64_t bp0 = sdesc_sw128(sP + (u % kNS) * kPBytes, 16, 1024);
+          for (int h = 0; h < 2; ++h, ++f) {
+            const int slot = f % kSlots;
+            if (!mbar_wait(&bars.x_full[slot], (f / kSlots) & 1, status, &s_abort)) { ok = false; break; }
+            tc_fence_after();
+            // MN-major A: the half's two 64-dim atoms 16 KB apart (LBO), 8-cell groups 1 KB apart
+            const uint64_t a0 = sdesc_sw128(sX + slot * kSlotBytes, kBlkBytes, 1024);
 #pragma unroll
             for (int kk = 0; kk < kCells / 16; ++kk)
-              umma_ss(tmem + kColO + ob * 32 + half * 16,
-                      av0 + (uint64_t)((half * 2 * (kCells * 128) + kk * 2048) >> 4),
+              umma_ss(tmem + kColO + ob * 32 + h * 16, a0 + (uint64_t)((kk * 2048) >> 4),
                       bp0 + (uint64_t)(((kk >> 2) * (kNQ * 128) + (kk & 3) * 32) >> 4), idesc_o,
                       (jl > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&bars.x_empty[buf]);
-          umma_commit(&bars.o_done[b]);
+            umma_commit(&bars.x_empty[slot]);
+          }
+          if (!ok) break;
+          umma_commit(&bars.o_done[u % kNS]);
         }
       }
       umma_commit(&bars.drain);
       mbar_wait(&bars.drain, 0, status);
     }
     __syncwarp();
-  } else if ((warp >= 1 && warp <= 3) || warp >= 8) {
+  } else if ((warp >= 1 && warp <= 3) || warp >= 12) {  // warps 12..19
     // ------------------------------------------------------------ gather producers
-    const int pw = warp <= 3 ? warp - 1 : warp - 5;  // 0..6: rows pw, pw + 7, ... of every 32-row group
-    // ids of entry j's tile, lane l holding rows l, l+32, l+64, l+96 (-1: none); loaded one
-    // entry ahead so the copies never wait on them
-    auto load_ids = [&](int j, int (&dst)[4]) {
-      int u, is_v;
-      seq_entry(j, U, &u, &is_v);
-      const int k = u / n_tiles, jl = u % n_tiles;
-      const int it = blockIdx.x + k * gridDim.x;
-      const int t = t_begin + (it >> 1), g = it & 1;
-      const int n_kv = pos0 + t + 1;
-      const int32_t* idrow = ids + ((size_t)t * kGroups + g) * K;
+    // Every fill is half a tile: 128 rows x 256 bytes.  Instruction i copies rows 2i, 2i+1
+    // (lane: row 2i + lane/16, chunk lane%16 of the half: 64-dim block (lane%16)/8, 16-byte
+    // chunk lane%8); warp pw takes i = pw, pw + 11, ...  All cells and addresses of a fill are
+    // resolved before its copies are issued back to back.  Fills follow the MMA order: per step
+    // s the two K halves of tile s, then the two V halves of tile s - kLead.
+    const int pw = warp <= 3 ? warp - 1 : warp - 9;  // 0..10
+    const int ch = lane & 15;
+    // ids of the tiles in use: tile s (K), s-1, s-2 (V when kLead = 2); next = tile s+1
+    int id0[4] = {-1, -1, -1, -1}, id1[4] = {-1, -1, -1, -1}, id2[4] = {-1, -1, -1, -1};
+    int idn[4] = {-1, -1, -1, -1};
+    int g0 = 0, g1 = 0, g2 = 0, gn = 0, nkvn = 0;
+    if (U > 0) load_ids(0, idn, gn, nkvn);
+    auto fill = [&](int f, const __half* base, int g, int h, const int (&cur)[4]) -> bool {
+      const int slot = f % kSlots;
+      if (f >= kSlots && !mbar_wait_warp(&bars.x_empty[slot], ((f / kSlots) & 1) ^ 1, status, &s_abort)) return false;
+      uint8_t* dst = smem + kOffX + slot * kSlotBytes + (ch >> 3) * kBlkBytes;
+      const __half* src_g = base + (size_t)g * kD + h * 128 + ch * 8;
+      int cell[kPerWarp];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int slot = jl * kCells + 32 * x + lane;
-        int c = (slot < K) ? __ldg(idrow + slot) : -1;
-        if (c >= n_kv || (c < 0 && slot < K)) {
-          if (!is_v && pw == 0) set_dev_status(status, QSA_DEV_BAD_ID);
-          c = -1;
-        }
-        dst[x] = c;
+      for (int m = 0; m < kPerWarp; ++m) {
+        const int i = pw + m * kProdWarps;  // warp-uniform
+        const int r = 2 * i + (lane >> 4);
+        cell[m] = __shfl_sync(0xffffffffu, pick4(cur, (i >> 4) & 3), r & 31);
       }
-    };
-    // one entry's work, given its ids (returns false if a wait gave up)
-    auto produce = [&](int j, const int (&cur)[4]) -> bool {
-      int u, is_v;
-      seq_entry(j, U, &u, &is_v);
-      const int k = u / n_tiles, jl = u % n_tiles;
-      const int it = blockIdx.x + k * gridDim.x;
-      const int t = t_begin + (it >> 1), g = it & 1;
-      if (!is_v && jl == 0 && warp == 1) {
-        // Q^T tile for this item: rows 0..11 = the group's heads (rows 12..15 stay zero)
-        if (k >= 2 && !mbar_wait_warp(&bars.q_empty[k & 1], ((k >> 1) & 1) ^ 1, status, &s_abort)) return false;
-        uint8_t* qb = smem + kOffQ + (k & 1) * kQBytes;
-        const __half* qt = q + ((size_t)t * kHeads + g * kHPG) * kD;
-        for (int x = lane; x < kHPG * 32; x += 32) {
-          const int hh = x >> 5, ch = x & 31;  // 16-byte chunk ch of row hh
-          const uint4 v = *reinterpret_cast<const uint4*>(qt + hh * kD + ch * 8);
-          *reinterpret_cast<uint4*>(qb + (ch >> 3) * (kNQ * 128) + hh * 128 + (((ch & 7) ^ (hh & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.q_full[k & 1]);
-      }
-      const int buf = j % kNBuf;
-      if (j >= kNBuf && !mbar_wait_warp(&bars.x_empty[buf], ((j / kNBuf) & 1) ^ 1, status, &s_abort)) return false;
-      uint8_t* xb = smem + kOffX + buf * kTileBytes;
-      const __half* src = is_v ? vhat : khat;
-      // lane = 16-byte chunk of the row: its k-block and swizzle-free part of the offset
-      uint8_t* dst_l = xb + (lane >> 3) * (kCells * 128);
-      const __half* src_l = src + (size_t)g * kD + lane * 8;
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        for (int rr = pw; rr < 32; rr += kProdWarps) {
-          const int r = 32 * x + rr;
-          const int cell = __shfl_sync(0xffffffffu, cur[x], rr);
-          cp_async16_zfill(dst_l + r * 128 + (((lane & 7) ^ (r & 7)) << 4),
-                           src_l + (size_t)(cell >= 0 ? cell : 0) * (kGroups * kD), cell >= 0);
+      for (int m = 0; m < kPerWarp; ++m) {
+        const int i = pw + m * kProdWarps;
+        if (i < kCells / 2) {
+          const int r = 2 * i + (lane >> 4);
+          cp_async16_zfill(dst + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
+                           src_g + (size_t)(cell[m] >= 0 ? cell[m] : 0) * (kGroups * kD), cell[m] >= 0);
         }
       }
-      cp_async_arrive_noinc(&bars.x_full[buf]);
+      cp_async_arrive_noinc(&bars.x_full[slot]);
       return true;
     };
-    // ping-pong id sets: entry j+1's ids are in flight while entry j is issued
-    int ids_a[4] = {-1, -1, -1, -1}, ids_b[4] = {-1, -1, -1, -1};
-    if (U > 0) load_ids(0, ids_a);
-    for (int j = 0; j < 2 * U; j += 2) {
-      if (j + 1 < 2 * U) load_ids(j + 1, ids_b);
-      if (!produce(j, ids_a)) break;
-      if (j + 1 >= 2 * U) break;
-      if (j + 2 < 2 * U) load_ids(j + 2, ids_a);
-      if (!produce(j + 1, ids_b)) break;
+    int f = 0;
+    bool ok = true;
+    for (int s = 0; ok && s < U + kLead; ++s) {
+      // rotate: tile s's ids become current, tile s+1's start loading
+      if (s < U) check_ids(idn, nkvn, pw == 0);  // tile s: loaded during the previous step
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        id2[x] = id1[x];
+        id1[x] = id0[x];
+        id0[x] = idn[x];
+      }
+      g2 = g1;
+      g1 = g0;
+      g0 = gn;
+      if (s + 1 < U) load_ids(s + 1, idn, gn, nkvn);
+      if (s < U) {
+        const int k = s / n_tiles, jl = s % n_tiles;
+        if (jl == 0 && warp == 1) {
+          // Q^T tile for this item: rows 0..11 = the group's heads (rows 12..15 stay zero)
+          const int it = blockIdx.x + k * gridDim.x;
+          const int t = t_begin + (it >> 1);
+          if (k >= 2 && !mbar_wait_warp(&bars.q_empty[k & 1], ((k >> 1) & 1) ^ 1, status, &s_abort)) break;
+          uint8_t* qb = smem + kOffQ + (k & 1) * kQBytes;
+          const __half* qt = q + ((size_t)t * kHeads + g0 * kHPG) * kD;
+          for (int x = lane; x < kHPG * 32; x += 32) {
+            const int hh = x >> 5, c16 = x & 31;  // 16-byte chunk c16 of row hh
+            const uint4 v = *reinterpret_cast<const uint4*>(qt + hh * kD + c16 * 8);
+            *reinterpret_cast<uint4*>(qb + (c16 >> 3) * (kNQ * 128) + hh * 128 + (((c16 & 7) ^ (hh & 7)) << 4)) = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.q_full[k & 1]);
+        }
+        if (!fill(f++, khat, g0, 0, id0) || !fill(f++, khat, g0, 1, id0)) { ok = false; break; }
+      }
+      if (s >= kLead) {
+        if (!fill(f++, vhat, g2, 0, id2) || !fill(f++, vhat, g2, 1, id2)) { ok = false; break; }
+      }
     }
     cp_async_wait_all();  // nothing of ours may land after the CTA exits
-  } else if (warp >= 4 && warp <= 7) {
+  } else if (warp >= 4 && warp <= 11) {
     // ------------------------------------------------------------ softmax (thread = cell)
+    const int wg = warp >= 8 ? 1 : 0;
     const int quarter = warp & 3;
     const int i = quarter * 32 + lane;  // cell slot in the tile == TMEM lane
+    const int h0 = wg * kHPW;           // this warpgroup's first head
+    const uint32_t bar_id = 1 + wg;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     uint8_t* sP = smem + kOffP;
     int u = 0;
@@ -265,117 +331,120 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = t_begin + (it >> 1), g = it & 1;
       const int n_kv = pos0 + t + 1;
       const int32_t* idrow = ids + ((size_t)t * kGroups + g) * K;
-      float m_run[kHPG], l_part[kHPG];
+      float m_run[kHPW], l_part[kHPW];
 #pragma unroll
-      for (int h = 0; h < kHPG; ++h) {
-        m_run[h] = -INFINITY;
-        l_part[h] = 0.f;
+      for (int j = 0; j < kHPW; ++j) {
+        m_run[j] = -INFINITY;
+        l_part[j] = 0.f;
       }
       int last_v = -1;
-      int c_next = (i < K) ? idrow[i] : -1;  // id of this lane's cell in tile 0, then one tile ahead
+      // the item's tiles are taken in rotated order, as the producers fill them
+      auto slot_of = [&](int jl) { return ((jl + it) % n_tiles) * kCells + i; };
+      int c_next = (slot_of(0) < K) ? idrow[slot_of(0)] : -1;  // this lane's id, one tile ahead
       for (int jl = 0; jl < n_tiles; ++jl, ++u) {
         const int c_cur = c_next;
-        const bool valid = jl * kCells + i < K && c_cur >= 0 && c_cur < n_kv;
-        const int slot_next = (jl + 1) * kCells + i;
+        const bool valid = slot_of(jl) < K && c_cur >= 0 && c_cur < n_kv;
+        const int slot_next = slot_of(jl + 1);
         c_next = (jl + 1 < n_tiles && slot_next < K) ? idrow[slot_next] : -1;
-        const bool w_ok = mbar_wait_warp(&bars.s_full[u & 1], (u >> 1) & 1, status, &s_abort);
-        if (named_bar_any(1, 128, !w_ok)) { ok = false; break; }  // all four warps leave together
+        const bool w_ok = mbar_wait_warp(&bars.s_full[u % kNS], (u / kNS) & 1, status, &s_abort);
+        if (named_bar_any(bar_id, 128, !w_ok)) { ok = false; break; }  // the warpgroup leaves together
         tc_fence_after();
-        uint32_t sr[16];
-        tmem_ld16(lane_base + kColS + (u & 1) * 16, sr);
+        uint32_t sr[kHPW];
+        ld6(lane_base + kColS + (u % kNS) * 16, wg, sr);
         tmem_wait_ld();
-        float s[kHPG];
+        float s[kHPW];
 #pragma unroll
-        for (int h = 0; h < kHPG; ++h) {
-          s[h] = valid ? __uint_as_float(sr[h]) * scale_log2 : -INFINITY;
-          float m = s[h];
+        for (int j = 0; j < kHPW; ++j) {
+          s[j] = valid ? __uint_as_float(sr[j]) * scale_log2 : -INFINITY;
+          float m = s[j];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          if (lane == 0) s_red[u & 1][quarter][h] = m;
+          if (lane == 0) s_red[wg][u & 1][quarter][j] = m;
         }
-        softmax_bar();
+        named_bar_any(bar_id, 128, false);
         bool need_any = false;
-        float alpha[kHPG];
+        float alpha[kHPW];
 #pragma unroll
-        for (int h = 0; h < kHPG; ++h) {
-          const float mt =
-              fmaxf(fmaxf(s_red[u & 1][0][h], s_red[u & 1][1][h]), fmaxf(s_red[u & 1][2][h], s_red[u & 1][3][h]));
-          const float mn = fmaxf(m_run[h], mt);
-          alpha[h] = 1.f;
+        for (int j = 0; j < kHPW; ++j) {
+          const float mt = fmaxf(fmaxf(s_red[wg][u & 1][0][j], s_red[wg][u & 1][1][j]),
+                                 fmaxf(s_red[wg][u & 1][2][j], s_red[wg][u & 1][3][j]));
+          const float mn = fmaxf(m_run[j], mt);
+          alpha[j] = 1.f;
           if (jl == 0) {
-            m_run[h] = mn;
-          } else if (mn > m_run[h] + kRescaleThreshold) {
-            alpha[h] = fast_exp2(m_run[h] - mn);
-            m_run[h] = mn;
+            m_run[j] = mn;
+          } else if (mn > m_run[j] + kRescaleThreshold) {
+            alpha[j] = fast_exp2(m_run[j] - mn);
+            m_run[j] = mn;
             need_any = true;
           }
         }
-        if (need_any) {  // uniform: every thread derived it from the same shared maxima
-          const bool r_ok = mbar_wait_warp(&bars.o_done[(u - 1) & 1], ((u - 1) >> 1) & 1, status, &s_abort);
-          if (named_bar_any(1, 128, !r_ok)) { ok = false; break; }
+        if (need_any) {  // uniform over the warpgroup: derived from the same shared maxima
+          const bool r_ok = mbar_wait_warp(&bars.o_done[(u - 1) % kNS], ((u - 1) / kNS) & 1, status, &s_abort);
+          if (named_bar_any(bar_id, 128, !r_ok)) { ok = false; break; }
           tc_fence_after();
-          uint32_t o[16];
+          uint32_t o[kHPW];
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const uint32_t col = kColO + (k & 1) * 32 + half * 16;
-            tmem_ld16(lane_base + col, o);
+            ld6(lane_base + col, wg, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < kHPG; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-            tmem_st16(lane_base + col, o);
+            for (int j = 0; j < kHPW; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[j]);
+            st6(lane_base + col, wg, o);
           }
           tmem_wait_st();
 #pragma unroll
-          for (int h = 0; h < kHPG; ++h) l_part[h] *= alpha[h];
+          for (int j = 0; j < kHPW; ++j) l_part[j] *= alpha[j];
         }
         // P^T[h][i] (K-major SW128: 64-cell blocks of [16 rows][128 B])
-        uint8_t* pb = sP + (u & 1) * kPBytes + (i >> 6) * (kNQ * 128);
+        uint8_t* pb = sP + (u % kNS) * kPBytes + (i >> 6) * (kNQ * 128);
 #pragma unroll
-        for (int h = 0; h < kHPG; ++h) {
-          const float mu = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
-          const float p = fast_exp2(s[h] - mu);
-          l_part[h] += p;
+        for (int j = 0; j < kHPW; ++j) {
+          const int h = h0 + j;
+          const float mu = (m_run[j] == -INFINITY) ? 0.f : m_run[j];
+          const float p = fast_exp2(s[j] - mu);
+          l_part[j] += p;
           *reinterpret_cast<__half*>(pb + h * 128 + ((((i & 63) >> 3) ^ (h & 7)) << 4) + (i & 7) * 2) =
               __float2half_rn(p);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.p_full[u & 1]);
+        if (lane == 0) mbar_arrive(&bars.p_full[u % kNS]);
         last_v = u;
       }
       if (!ok) break;
       // row sums over the 128 cell lanes
 #pragma unroll
-      for (int h = 0; h < kHPG; ++h) {
-        float l = l_part[h];
+      for (int j = 0; j < kHPW; ++j) {
+        float l = l_part[j];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) s_l[quarter][h] = l;
+        if (lane == 0) s_l[wg][quarter][j] = l;
       }
-      softmax_bar();
-      float inv_l[kHPG];
+      named_bar_any(bar_id, 128, false);
+      float inv_l[kHPW];
 #pragma unroll
-      for (int h = 0; h < kHPG; ++h) {
-        const float l = s_l[0][h] + s_l[1][h] + s_l[2][h] + s_l[3][h];
-        inv_l[h] = l > 0.f ? 1.f / l : 0.f;
+      for (int j = 0; j < kHPW; ++j) {
+        const float l = s_l[wg][0][j] + s_l[wg][1][j] + s_l[wg][2][j] + s_l[wg][3][j];
+        inv_l[j] = l > 0.f ? 1.f / l : 0.f;
       }
-      const bool e_ok = mbar_wait_warp(&bars.o_done[last_v & 1], (last_v >> 1) & 1, status, &s_abort);
-      if (named_bar_any(1, 128, !e_ok)) { ok = false; break; }
+      const bool e_ok = mbar_wait_warp(&bars.o_done[last_v % kNS], (last_v / kNS) & 1, status, &s_abort);
+      if (named_bar_any(bar_id, 128, !e_ok)) { ok = false; break; }
       tc_fence_after();
       // epilogue: thread = dim i (half 0) and 128 + i (half 1)
-      __half* orow = out + ((size_t)t * kHeads + g * kHPG) * kD;
+      __half* orow = out + ((size_t)t * kHeads + g * kHPG + h0) * kD;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t o[16];
-        tmem_ld16(lane_base + kColO + (k & 1) * 32 + half * 16, o);
+        uint32_t o[kHPW];
+        ld6(lane_base + kColO + (k & 1) * 32 + half * 16, wg, o);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < kHPG; ++h)
-          orow[h * kD + half * 128 + i] = __float2half_rn(__uint_as_float(o[h]) * inv_l[h]);
+        for (int j = 0; j < kHPW; ++j)
+          orow[j * kD + half * 128 + i] = __float2half_rn(__uint_as_float(o[j]) * inv_l[j]);
       }
       tc_fence_before();
-      softmax_bar();  // s_l may be rewritten by the next item only after everyone read it
+      named_bar_any(bar_id, 128, false);  // s_l may be rewritten by the next item only after everyone read it
       if (lane == 0) mbar_arrive(&bars.o_free[k & 1]);
     }
   }

@@ -79,71 +79,121 @@ __device__ __forceinline__ long long half_int24(uint16_t h) {
 }
 
 // ----------------------------------------------------------------- 1. prep
+// Round an exact integer multiple of 2^-24 (a = |value| * 2^24) to fp16, nearest-even.
+// Returns the fp16 magnitude bits and sets *r to the rounded magnitude in the same units.
+// Magnitudes below 2048 units are fp16 values already (subnormal below 1024, e = 1 above)
+// and their bit pattern is the integer itself; above, 11 significant bits are kept.
+__device__ __forceinline__ uint32_t units_to_half_mag(unsigned long long a, unsigned long long* r) {
+  if (a < 2048ull) {
+    *r = a;
+    return (uint32_t)a;
+  }
+  int s = 53 - __clzll((long long)a);  // bit length - 11 (>= 1)
+  unsigned long long mant = a >> s;
+  const unsigned long long rem = a & ((1ull << s) - 1), half = 1ull << (s - 1);
+  if (rem > half || (rem == half && (mant & 1ull))) ++mant;
+  if (mant == 2048ull) {
+    mant = 1024ull;
+    ++s;
+  }
+  const int e = s + 1;  // value = mant * 2^(e - 25), biased exponent e
+  if (e > 30) {         // beyond the fp16 range: infinity, like a rounding conversion
+    *r = a;
+    return 0x7C00u;
+  }
+  *r = mant << s;
+  return ((uint32_t)e << 10) | (uint32_t)(mant - 1024ull);
+}
+
+__device__ __forceinline__ __half signed_half(uint32_t mag_bits, bool neg) {
+  return __ushort_as_half((unsigned short)(mag_bits | (neg ? 0x8000u : 0u)));
+}
+
 // grid (T_pad, 2), 256 threads: thread = dim.  Row layout of qhl: for each 64-dim block b,
 // [hi_b (64) | lo_b (64)] at columns 128 b .. 128 b + 127, with Qsum = hi + lo + residual.
+// All arithmetic is exact in 64-bit integers (units of 2^-24): Qsum of 12 fp16 values is
+// below 2^44 units, and the block sums of |residual| and |hi| + |lo| stay below 2^51.
 __global__ void __launch_bounds__(256) prep_q_kernel(const __half* __restrict__ q, int t_sel, int T_sel, int T_pad,
                                                      __half* __restrict__ qhl, float* __restrict__ eh) {
   const int r = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
   __half hi = __ushort_as_half(0), lo = __ushort_as_half(0);
-  double e = 0.0;
+  long long e = 0, h_abs = 0;
   if (r < T_sel) {
-    const __half* qt = q + ((size_t)(t_sel + r) * kHeads + g * kHPG) * kD;
-    double s = 0.0;  // exact: 12 fp16 values fit the fp64 significand
+    const uint16_t* qt = reinterpret_cast<const uint16_t*>(q) + ((size_t)(t_sel + r) * kHeads + g * kHPG) * kD;
+    long long sum = 0;
 #pragma unroll
-    for (int h = 0; h < kHPG; ++h) s += (double)__half2float(qt[h * kD + d]);
-    hi = __double2half(s);
-    const double rest = s - (double)__half2float(hi);  // exact
-    lo = __double2half(rest);
-    e = rest - (double)__half2float(lo);  // exact residual
+    for (int h = 0; h < kHPG; ++h) sum += half_int24(__ldg(qt + h * kD + d));
+    unsigned long long rh, rl;
+    const bool neg = sum < 0;
+    const uint32_t hb = units_to_half_mag((unsigned long long)(neg ? -sum : sum), &rh);
+    hi = signed_half(hb, neg);
+    const long long rest = sum - (neg ? -(long long)rh : (long long)rh);  // exact
+    const bool neg2 = rest < 0;
+    const uint32_t lb = units_to_half_mag((unsigned long long)(neg2 ? -rest : rest), &rl);
+    lo = signed_half(lb, neg2);
+    e = rest - (neg2 ? -(long long)rl : (long long)rl);  // exact residual
+    if (e < 0) e = -e;
+    h_abs = (long long)rh + (long long)rl;
   }
   __half* dst = qhl + ((size_t)g * T_pad + r) * (2 * kD) + (d >> 6) * 128 + (d & 63);
   dst[0] = hi;
   dst[64] = lo;
   if (r >= T_sel) return;
-  // block norms over 64 dims = two warps: E_b = sum |residual|, H_b = sum (|hi| + |lo|)
-  double ae = fabs(e), ah = fabs((double)__half2float(hi)) + fabs((double)__half2float(lo));
+  // block sums over 64 dims = two warps: E_b = sum |residual|, H_b = sum (|hi| + |lo|)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    ae += __shfl_xor_sync(0xffffffffu, ae, o);
-    ah += __shfl_xor_sync(0xffffffffu, ah, o);
+    e += __shfl_xor_sync(0xffffffffu, e, o);
+    h_abs += __shfl_xor_sync(0xffffffffu, h_abs, o);
   }
-  __shared__ double s_e[8], s_h[8];
+  __shared__ long long s_e[8], s_h[8];
   const int w = d >> 5;
   if ((d & 31) == 0) {
-    s_e[w] = ae;
-    s_h[w] = ah;
+    s_e[w] = e;
+    s_h[w] = h_abs;
   }
   __syncthreads();
   if (d < kNB) {
     float* dst2 = eh + ((size_t)g * T_sel + r) * 8;
-    dst2[d] = __double2float_ru(s_e[2 * d] + s_e[2 * d + 1]);
-    dst2[kNB + d] = __double2float_ru(s_h[2 * d] + s_h[2 * d + 1]);
+    constexpr float kUnit = 5.9604644775390625e-8f;  // 2^-24, exact scaling
+    dst2[d] = __ll2float_ru(s_e[2 * d] + s_e[2 * d + 1]) * kUnit;
+    dst2[kNB + d] = __ll2float_ru(s_h[2 * d] + s_h[2 * d + 1]) * kUnit;
   }
 }
 
-// grid (n_pad / 8, 2), 256 threads: a warp per cell row, lane = 8 codes.
+// grid (min(n_pad / 8, kPrepKCtas), 2), 256 threads: a warp per cell row (lane = 8 codes),
+// CTAs striding over the rows.  Each CTA reduces its |ksc| maxima before one atomic per
+// scale block.
+constexpr int kPrepKCtas = 1024;
 __global__ void __launch_bounds__(256) prep_k_kernel(const int8_t* __restrict__ kq, const __half* __restrict__ ksc,
                                                      int n_max, int n_pad, __half* __restrict__ kc,
                                                      float* __restrict__ kmax) {
   const int g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x * 8 + warp;
   const int blk = lane >> 3;
-  uint4 outw = make_uint4(0, 0, 0, 0);
-  if (c < n_max) {
-    const uint2 w = *reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8);
-    uint32_t o[4];
-    dequant8(w.x, w.y, __half2half2(__ushort_as_half(0x3C00)), o);  // scale 1: exact codes
-    outw = make_uint4(o[0], o[1], o[2], o[3]);
-    if ((lane & 7) == 0) {
-      const float a = fabsf(__half2float(ksc[((size_t)c * kGroups + g) * kNB + blk]));
-      atomicMax(reinterpret_cast<int*>(kmax) + g * kNB + blk, __float_as_int(a));
+  float amax = 0.f;
+  for (int c = blockIdx.x * 8 + warp; c < n_pad; c += gridDim.x * 8) {
+    uint4 outw = make_uint4(0, 0, 0, 0);
+    if (c < n_max) {
+      const uint2 w = *reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8);
+      uint32_t o[4];
+      dequant8(w.x, w.y, __half2half2(__ushort_as_half(0x3C00)), o);  // scale 1: exact codes
+      outw = make_uint4(o[0], o[1], o[2], o[3]);
+      if ((lane & 7) == 0) amax = fmaxf(amax, fabsf(__half2float(ksc[((size_t)c * kGroups + g) * kNB + blk])));
     }
+    *reinterpret_cast<uint4*>(kc + ((size_t)g * n_pad + c) * kD + lane * 8) = outw;
   }
-  if (c < n_pad) *reinterpret_cast<uint4*>(kc + ((size_t)g * n_pad + c) * kD + lane * 8) = outw;
+  __shared__ float s_max[8][kNB];
+  if ((lane & 7) == 0) s_max[warp][blk] = amax;
+  __syncthreads();
+  if (threadIdx.x < kNB) {
+    float m = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) m = fmaxf(m, s_max[w][threadIdx.x]);
+    atomicMax(reinterpret_cast<int*>(kmax) + g * kNB + threadIdx.x, __float_as_int(m));
+  }
 }
 
 // ----------------------------------------------------------------- 2. score GEMM
-constexpr int kNtPerCta = 32;                  // 2048 cells per CTA
+constexpr int kNtPerCtaMax = 32;               // at most 2048 cells per CTA
 constexpr int kSmemA = kGM * kD * 2 * 2;       // 128 KB: 8 k-blocks (hi_b, lo_b) of [128 rows][64] SW128
 constexpr int kSmemBStage = kGN * kD * 2;      // 32 KB: 4 k-blocks of [64 cells][64] SW128
 constexpr int kScoreSmem = kSmemA + kGStages * kSmemBStage + 1024;
@@ -159,7 +209,7 @@ __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;"
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                  const __half* __restrict__ ksc, __half* __restrict__ scores, int T_sel, int T_pad, int n_pad,
-                 int n_base, int m_tiles, int n_chunks, float sm_scale, int* status) {
+                 int n_base, int m_tiles, int n_chunks, int nt_per_cta, float sm_scale, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ ScoreBars bars;
@@ -172,8 +222,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int r0 = m * kGM;
   const int r_last = min(r0 + kGM, T_sel) - 1;
   const int n_kv_hi = n_base + r_last + 1;  // cells the tile's last row can see
-  const int nt_begin = nch * kNtPerCta;
-  const int nt_end = min(nt_begin + kNtPerCta, (n_kv_hi + kGN - 1) / kGN);
+  const int nt_begin = nch * nt_per_cta;
+  const int nt_end = min(nt_begin + nt_per_cta, (n_kv_hi + kGN - 1) / kGN);
   const int n_tiles = nt_end - nt_begin;
   if (n_tiles <= 0) return;  // uniform over the CTA, before any allocation
 
@@ -315,6 +365,83 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ----------------------------------------------------------------- 2b. score for few rows
+// Decode-sized calls (at most kSmallRows selected rows) have no GEMM to feed the tensor
+// cores, so the same scores are computed on the CUDA cores straight from the int8 codes:
+// per 64-dim block S_b = sum over the block of (hi + lo) * kq in fp32 (128 exact products,
+// summed in a different order than the MMA but within the same bound), then
+// s~ = fp16(sm_scale * fma(ksc_3, S_3, fma(ksc_2, S_2, fma(ksc_1, S_1, ksc_0 * S_0)))),
+// the epilogue of the GEMM.  The kernel also takes kmax_b = max |ksc| (prep_k's job on the
+// GEMM path).  grid (ceil(n_max / 64), 2), 256 threads: warp = 8 cells, lane = 8 dims.
+constexpr int kSmallRows = 8;
+__global__ void __launch_bounds__(256) score_small_kernel(const int8_t* __restrict__ kq, const __half* __restrict__ ksc,
+                                                          const __half* __restrict__ qhl, int T_sel, int T_pad,
+                                                          int n_max, int n_pad, float sm_scale,
+                                                          __half* __restrict__ scores, float* __restrict__ kmax) {
+  __shared__ __align__(16) float s_hl[kSmallRows][2 * kD];  // per row: [hi_b | lo_b] per block b
+  __shared__ float s_max[8][kNB];
+  const int g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < T_sel * 2 * kD; i += 256)
+    s_hl[i / (2 * kD)][i % (2 * kD)] = __half2float(qhl[((size_t)g * T_pad + i / (2 * kD)) * (2 * kD) + i % (2 * kD)]);
+  __syncthreads();
+  const int blk = lane >> 3;
+  const int col = blk * 128 + (lane & 7) * 8;  // this lane's 8 hi values; lo at +64
+  float amax = 0.f;
+  for (int i = 0; i < 8; ++i) {
+    const int c = blockIdx.x * 64 + warp * 8 + i;
+    if (c >= n_max) break;  // uniform over the warp
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8));
+    float kf[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      kf[j] = (float)(int8_t)(w.x >> (8 * j));
+      kf[4 + j] = (float)(int8_t)(w.y >> (8 * j));
+    }
+    const float my_sc = __half2float(ksc[((size_t)c * kGroups + g) * kNB + blk]);
+    amax = fmaxf(amax, fabsf(my_sc));
+    const float sc0 = __shfl_sync(0xffffffffu, my_sc, 0), sc1 = __shfl_sync(0xffffffffu, my_sc, 8);
+    const float sc2 = __shfl_sync(0xffffffffu, my_sc, 16), sc3 = __shfl_sync(0xffffffffu, my_sc, 24);
+    for (int r = 0; r < T_sel; ++r) {
+      const float4* hp = reinterpret_cast<const float4*>(&s_hl[r][col]);
+      const float4 h0 = hp[0], h1 = hp[1], l0 = hp[16], l1 = hp[17];  // lo = hi + 64 floats
+      float p = h0.x * kf[0];
+      p = fmaf(h0.y, kf[1], p);
+      p = fmaf(h0.z, kf[2], p);
+      p = fmaf(h0.w, kf[3], p);
+      p = fmaf(h1.x, kf[4], p);
+      p = fmaf(h1.y, kf[5], p);
+      p = fmaf(h1.z, kf[6], p);
+      p = fmaf(h1.w, kf[7], p);
+      p = fmaf(l0.x, kf[0], p);
+      p = fmaf(l0.y, kf[1], p);
+      p = fmaf(l0.z, kf[2], p);
+      p = fmaf(l0.w, kf[3], p);
+      p = fmaf(l1.x, kf[4], p);
+      p = fmaf(l1.y, kf[5], p);
+      p = fmaf(l1.z, kf[6], p);
+      p = fmaf(l1.w, kf[7], p);
+      p += __shfl_xor_sync(0xffffffffu, p, 1);
+      p += __shfl_xor_sync(0xffffffffu, p, 2);
+      p += __shfl_xor_sync(0xffffffffu, p, 4);  // S_b on every lane of block b
+      const float S0 = __shfl_sync(0xffffffffu, p, 0), S1 = __shfl_sync(0xffffffffu, p, 8);
+      const float S2 = __shfl_sync(0xffffffffu, p, 16), S3 = __shfl_sync(0xffffffffu, p, 24);
+      float acc = fmaf(sc0, S0, 0.f);
+      acc = fmaf(sc1, S1, acc);
+      acc = fmaf(sc2, S2, acc);
+      acc = fmaf(sc3, S3, acc);
+      if (lane == 0) scores[((size_t)g * T_sel + r) * n_pad + c] = __float2half_rn(acc * sm_scale);
+    }
+  }
+  if ((lane & 7) == 0) s_max[warp][blk] = amax;
+  __syncthreads();
+  if (threadIdx.x < kNB) {
+    float m = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) m = fmaxf(m, s_max[w][threadIdx.x]);
+    atomicMax(reinterpret_cast<int*>(kmax) + g * kNB + threadIdx.x, __float_as_int(m));
+  }
 }
 
 // ----------------------------------------------------------------- 3. top-k
@@ -834,6 +961,39 @@ bool make_2d_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ou
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The score GEMM: CTAs of 128 rows x nt_per_cta 64-cell tiles; nt_per_cta shrinks for
+// short calls so that the grid still covers every SM twice.
+cudaError_t launch_score_gemm(const WsLayout& L, int pos0, __half* qhi, __half* kc, const __half* ksc, __half* sc,
+                              float sm_scale, int* status, cudaStream_t stream) {
+  static bool attr_done[64] = {};
+  static int n_sms[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t e;
+  if (dev < 64 && !attr_done[dev]) {
+    if ((e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem)) !=
+        cudaSuccess)
+      return e;
+    cudaDeviceGetAttribute(&n_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    attr_done[dev] = true;
+  }
+  const int sms = (dev < 64 && n_sms[dev] > 0) ? n_sms[dev] : 148;
+  CUtensorMap ma, mb;
+  if (!make_2d_map(&ma, qhi, 2 * kD, (uint64_t)kGroups * L.T_pad, kGK, kGM) ||
+      !make_2d_map(&mb, kc, kD, (uint64_t)kGroups * L.n_pad, kGK, kGN))
+    return cudaErrorInvalidValue;
+  const int m_tiles = L.T_pad / kGM;
+  const int n_tiles = L.n_pad / kGN;
+  const long long work = (long long)kGroups * m_tiles * n_tiles;
+  int nt_per = (int)((work + 2LL * sms - 1) / (2LL * sms));
+  nt_per = nt_per < 4 ? 4 : (nt_per > kNtPerCtaMax ? kNtPerCtaMax : nt_per);
+  const int n_chunks = (n_tiles + nt_per - 1) / nt_per;
+  const int n_base = pos0 + L.t_sel;  // n_kv of selected row r is n_base + r + 1
+  score_kernel<<<kGroups * m_tiles * n_chunks, kScoreThreads, kScoreSmem, stream>>>(
+      ma, mb, ksc, sc, L.T_sel, L.T_pad, L.n_pad, n_base, m_tiles, n_chunks, nt_per, sm_scale, status);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t select_workspace_bytes(int T, int pos0, int n_cells, Params p) {
@@ -859,29 +1019,15 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
   cudaError_t e = cudaMemsetAsync(kmax, 0, 8 * sizeof(float), stream);
   if (e != cudaSuccess) return e;
   prep_q_kernel<<<dim3(L.T_pad, kGroups), 256, 0, stream>>>(q, L.t_sel, L.T_sel, L.T_pad, qhi, eh);  // hi/lo
-  prep_k_kernel<<<dim3(L.n_pad / 8, kGroups), 256, 0, stream>>>(kq, ksc, L.n_max, L.n_pad, kc, kmax);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
-  static bool attr_done[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    if ((e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem)) !=
-        cudaSuccess)
-      return e;
-    attr_done[dev] = true;
+  if (L.T_sel <= kSmallRows) {
+    score_small_kernel<<<dim3((L.n_max + 63) / 64, kGroups), 256, 0, stream>>>(kq, ksc, qhi, L.T_sel, L.T_pad, L.n_max,
+                                                                           L.n_pad, p.sm_scale, sc, kmax);
+  } else {
+    prep_k_kernel<<<dim3(min(L.n_pad / 8, kPrepKCtas), kGroups), 256, 0, stream>>>(kq, ksc, L.n_max, L.n_pad, kc,
+                                                                                     kmax);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_score_gemm(L, pos0, qhi, kc, ksc, sc, p.sm_scale, status, stream)) != cudaSuccess) return e;
   }
-  CUtensorMap ma, mb;
-  if (!make_2d_map(&ma, qhi, 2 * kD, (uint64_t)kGroups * L.T_pad, kGK, kGM) ||
-      !make_2d_map(&mb, kc, kD, (uint64_t)kGroups * L.n_pad, kGK, kGN))
-    return cudaErrorInvalidValue;
-  const int m_tiles = L.T_pad / kGM;
-  const int n_tiles = L.n_pad / kGN;
-  const int n_chunks = (n_tiles + kNtPerCta - 1) / kNtPerCta;
-  const int n_base = pos0 + L.t_sel;  // n_kv of selected row r is n_base + r + 1
-  score_kernel<<<kGroups * m_tiles * n_chunks, kScoreThreads, kScoreSmem, stream>>>(ma, mb, ksc, sc, L.T_sel, L.T_pad, L.n_pad,
-                                                                         n_base, m_tiles, n_chunks, p.sm_scale,
-                                                                         status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const dim3 grid(L.T_sel, kGroups);
