@@ -17,15 +17,15 @@
 //        O^T[d][h] += V^[c][d] P[h][c]  A = V^ as MN-major (dims x cells)  B = P^T (K-major)
 //
 // The gathers are bound by how many row reads each SM keeps in flight, so eleven producer
-// warps share every fill of one ring of 32 KB slots (half a K or V tile: 128 cells x 128
-// dims), filled in exactly the order the MMAs consume them and freed by the MMAs that read
-// them.  QK runs kLead tiles ahead of PV over kNS S^T / P^T buffers, so the K stream never
+// warps take turns filling one ring of 32 KB slots (half a K or V tile: 128 cells x 128 dims),
+// each fill by a single warp so that fills complete independently; the slots are filled in
+// exactly the order the MMAs consume them and freed by the MMAs that read them.  QK runs kLead tiles ahead of PV over kNS S^T / P^T buffers, so the K stream never
 // waits for the softmax of the tile before it.  Ids are ascending, so tile j of every item
 // covers about the same cell range; each item starts its walk at tile (item mod tiles), which
 // spreads the SMs' concurrent reads over the whole mirror instead of one window of it (the
 // online softmax does not depend on the order of the tiles).
 //     warp 0        TMEM owner and single-thread UMMA issue
-//     warps 1-3, 12-19  gather producers (warp 1 also stages each item's Q^T tile)
+//     warps 1-3, 12-19  gather producers (warp 1 also starts each item's Q^T tile by TMA)
 //     warps 4-7     softmax for heads 0-5, warps 8-11 for heads 6-11: one gathered cell per
 //                   thread (TMEM lane), column-wise online softmax over the 128 cells
 //                   (shuffle + shared-memory max per head, base-2 exponent), fp16 P^T into
@@ -41,7 +41,6 @@ constexpr int kCells = 128;                // gathered cells per tile (UMMA M)
 constexpr int kNQ = 16;                    // UMMA N: 12 heads + 4 zero rows
 constexpr int kThreads = 640;
 constexpr int kProdWarps = 11;             // warps 1-3 and 12-19
-constexpr int kPerWarp = (kCells / 2 + kProdWarps - 1) / kProdWarps;  // copy instructions per warp and fill
 constexpr int kBlkBytes = kCells * 128;    // 16 KB: one 64-dim block of a tile
 constexpr int kSlotBytes = 2 * kBlkBytes;  // 32 KB: one 128-dim half of a K or V tile
 constexpr int kSlots = 6;
@@ -58,9 +57,12 @@ constexpr int kHPW = 6;  // heads per softmax warpgroup
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kNoSlot = -2147483647 - 1;  // marks tile slots past the end of an id row
 static_assert(kLead + 2 <= kNS, "S^T / P^T buffers must cover the QK lead");
+static_assert(2 * kSlots >= kProdWarps + 1, "x_empty keying must cover the producer round-robin");
 
 struct __align__(8) GBars {
-  uint64_t x_full[kSlots], x_empty[kSlots];
+  // x_empty is keyed by the consumed fill mod 2 * kSlots: the warp that refills a slot has, at
+  // its previous fill (11 earlier), seen fill f - 17 consumed, so no wait is two phases behind
+  uint64_t x_full[kSlots], x_empty[2 * kSlots];
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[kNS], p_full[kNS];
   uint64_t o_done[kNS], o_free[2];  // o_done per tile mod kNS: a wait is never two phases behind
@@ -99,7 +101,7 @@ __device__ __forceinline__ void st6(uint32_t taddr, int wg, const uint32_t (&r)[
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    flash_gather_kernel(const __half* __restrict__ q, const __half* __restrict__ khat,
+    flash_gather_kernel(const __grid_constant__ CUtensorMap map_q, const __half* __restrict__ khat,
                         const __half* __restrict__ vhat, const int32_t* __restrict__ ids, __half* __restrict__ out,
                         int pos0, int t_begin, int n_items, int K, float scale_log2, int* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -117,10 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     s_abort = 0;
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&bars.x_full[i], kProdWarps * 32);  // one cp.async completion arrival per producer thread
-      mbar_init(&bars.x_empty[i], 1);
-    }
+    for (int i = 0; i < kSlots; ++i) mbar_init(&bars.x_full[i], 32);  // the filling warp's cp.async arrivals
+    for (int i = 0; i < 2 * kSlots; ++i) mbar_init(&bars.x_empty[i], 1);
     for (int i = 0; i < kNS; ++i) {
       mbar_init(&bars.s_full[i], 1);
       mbar_init(&bars.p_full[i], 8);
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_ss(dS, a0 + (uint64_t)(((kk >> 2) * kBlkBytes + (kk & 3) * 32) >> 4),
                       bq0 + (uint64_t)(((2 * hf + (kk >> 2)) * (kNQ * 128) + (kk & 3) * 32) >> 4), idesc_s,
                       (hf > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&bars.x_empty[slot]);
+            umma_commit(&bars.x_empty[f % (2 * kSlots)]);
           }
           if (!ok) break;
           umma_commit(&bars.s_full[s % kNS]);
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_ss(tmem + kColO + ob * 32 + h * 16, a0 + (uint64_t)((kk * 2048) >> 4),
                       bp0 + (uint64_t)(((kk >> 2) * (kNQ * 128) + (kk & 3) * 32) >> 4), idesc_o,
                       (jl > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&bars.x_empty[slot]);
+            umma_commit(&bars.x_empty[f % (2 * kSlots)]);
           }
           if (!ok) break;
           umma_commit(&bars.o_done[u % kNS]);
@@ -240,10 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if ((warp >= 1 && warp <= 3) || warp >= 12) {  // warps 12..19
     // ------------------------------------------------------------ gather producers
-    // Every fill is half a tile: 128 rows x 256 bytes.  Instruction i copies rows 2i, 2i+1
-    // (lane: row 2i + lane/16, chunk lane%16 of the half: 64-dim block (lane%16)/8, 16-byte
-    // chunk lane%8); warp pw takes i = pw, pw + 11, ...  All cells and addresses of a fill are
-    // resolved before its copies are issued back to back.  Fills follow the MMA order: per step
+    // Every fill is half a tile: 128 rows x 256 bytes, all of it copied by one warp (fill f by
+    // producer warp f mod 11), so fills complete independently and several are in flight at
+    // once.  Instruction i copies rows 2i, 2i+1 (lane: row 2i + lane/16, chunk lane%16 of the
+    // half: 64-dim block (lane%16)/8, 16-byte chunk lane%8).  Fills follow the MMA order: per step
     // s the two K halves of tile s, then the two V halves of tile s - kLead.
     const int pw = warp <= 3 ? warp - 1 : warp - 9;  // 0..10
     const int ch = lane & 15;
@@ -253,22 +253,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g0 = 0, g1 = 0, g2 = 0, gn = 0, nkvn = 0;
     if (U > 0) load_ids(0, idn, gn, nkvn);
     auto fill = [&](int f, const __half* base, int g, int h, const int (&cur)[4]) -> bool {
+      if (f % kProdWarps != pw) return true;  // fills go round-robin over the producer warps
       const int slot = f % kSlots;
-      if (f >= kSlots && !mbar_wait_warp(&bars.x_empty[slot], ((f / kSlots) & 1) ^ 1, status, &s_abort)) return false;
+      if (f >= kSlots) {  // fill f - kSlots (same slot) consumed
+        const int e = f - kSlots;
+        if (!mbar_wait_warp(&bars.x_empty[e % (2 * kSlots)], (e / (2 * kSlots)) & 1, status, &s_abort)) return false;
+      }
       uint8_t* dst = smem + kOffX + slot * kSlotBytes + (ch >> 3) * kBlkBytes;
       const __half* src_g = base + (size_t)g * kD + h * 128 + ch * 8;
-      int cell[kPerWarp];
+      // instruction i copies rows 2i, 2i+1; cells are resolved eight instructions at a time
+#pragma unroll 1
+      for (int i0 = 0; i0 < kCells / 2; i0 += 8) {
+        const int sel = pick4(cur, (i0 >> 4) & 3);  // rows 2*i0 .. 2*i0 + 15 share one id register
+        int cell[8];
 #pragma unroll
-      for (int m = 0; m < kPerWarp; ++m) {
-        const int i = pw + m * kProdWarps;  // warp-uniform
-        const int r = 2 * i + (lane >> 4);
-        cell[m] = __shfl_sync(0xffffffffu, pick4(cur, (i >> 4) & 3), r & 31);
-      }
+        for (int m = 0; m < 8; ++m) cell[m] = __shfl_sync(0xffffffffu, sel, (2 * (i0 + m) + (lane >> 4)) & 31);
 #pragma unroll
-      for (int m = 0; m < kPerWarp; ++m) {
-        const int i = pw + m * kProdWarps;
-        if (i < kCells / 2) {
-          const int r = 2 * i + (lane >> 4);
+        for (int m = 0; m < 8; ++m) {
+          const int r = 2 * (i0 + m) + (lane >> 4);
           cp_async16_zfill(dst + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
                            src_g + (size_t)(cell[m] >= 0 ? cell[m] : 0) * (kGroups * kD), cell[m] >= 0);
         }
@@ -276,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp_async_arrive_noinc(&bars.x_full[slot]);
       return true;
     };
+    if (warp == 1 && lane == 0) tma_prefetch_desc(&map_q);
     int f = 0;
     bool ok = true;
     for (int s = 0; ok && s < U + kLead; ++s) {
@@ -294,20 +297,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (s < U) {
         const int k = s / n_tiles, jl = s % n_tiles;
         if (jl == 0 && warp == 1) {
-          // Q^T tile for this item: rows 0..11 = the group's heads (rows 12..15 stay zero)
+          // Q^T tile for this item by TMA: per 64-dim block the group's 12 head rows land as
+          // rows 0..11 of a 128B-swizzled [16][64] block (rows 12..15 stay zero)
           const int it = blockIdx.x + k * gridDim.x;
           const int t = t_begin + (it >> 1);
           if (k >= 2 && !mbar_wait_warp(&bars.q_empty[k & 1], ((k >> 1) & 1) ^ 1, status, &s_abort)) break;
-          uint8_t* qb = smem + kOffQ + (k & 1) * kQBytes;
-          const __half* qt = q + ((size_t)t * kHeads + g0 * kHPG) * kD;
-          for (int x = lane; x < kHPG * 32; x += 32) {
-            const int hh = x >> 5, c16 = x & 31;  // 16-byte chunk c16 of row hh
-            const uint4 v = *reinterpret_cast<const uint4*>(qt + hh * kD + c16 * 8);
-            *reinterpret_cast<uint4*>(qb + (c16 >> 3) * (kNQ * 128) + hh * 128 + (((c16 & 7) ^ (hh & 7)) << 4)) = v;
+          if (lane == 0) {
+            uint8_t* qb = smem + kOffQ + (k & 1) * kQBytes;
+            mbar_arrive_expect_tx(&bars.q_full[k & 1], kNB * kHPG * 128);
+#pragma unroll
+            for (int b = 0; b < kNB; ++b)
+              tma_load_2d(qb + b * (kNQ * 128), &map_q, &bars.q_full[k & 1], b * 64, t * kHeads + g0 * kHPG);
           }
-          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars.q_full[k & 1]);
         }
         if (!fill(f++, khat, g0, 0, id0) || !fill(f++, khat, g0, 1, id0)) { ok = false; break; }
       }
@@ -455,6 +457,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
+// q as rows (token * 24 + head) x 256 halves; boxes of 64 halves x 12 rows (one group's heads),
+// 128B swizzle.
+bool make_q_map(CUtensorMap* map, const __half* q, int T) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)T * kHeads};
+  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)kHPG};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(q), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
@@ -474,7 +490,9 @@ cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, cons
   const int sms = (dev < 64 && n_sms[dev] > 0) ? n_sms[dev] : 148;
   const int grid = n_items < sms ? n_items : sms;
   const float scale_log2 = a.p.sm_scale * kLog2e;
-  flash_gather_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(a.q, khat, vhat, a.ids, a.out, a.pos0, t_begin, n_items,
+  CUtensorMap mq;
+  if (!make_q_map(&mq, a.q, a.T)) return cudaErrorInvalidValue;
+  flash_gather_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, khat, vhat, a.ids, a.out, a.pos0, t_begin, n_items,
                                                               a.p.topk, scale_log2, a.status);
   return cudaGetLastError();
 }
