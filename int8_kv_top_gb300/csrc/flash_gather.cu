@@ -16,16 +16,18 @@
 //        S^T[c][h]  = K^[c] . q[h]      A = K^ (128 cells, K-major)  B = Q^T (16 rows, 12 used)
 //        O^T[d][h] += V^[c][d] P[h][c]  A = V^ as MN-major (dims x cells)  B = P^T (K-major)
 //
-// The gathers are bound by how many row reads each SM keeps in flight, so eleven producer
-// warps take turns filling one ring of 32 KB slots (half a K or V tile: 128 cells x 128 dims),
-// each fill by a single warp so that fills complete independently; the slots are filled in
-// exactly the order the MMAs consume them and freed by the MMAs that read them.  QK runs kLead tiles ahead of PV over kNS S^T / P^T buffers, so the K stream never
-// waits for the softmax of the tile before it.  Ids are ascending, so tile j of every item
-// covers about the same cell range; each item starts its walk at tile (item mod tiles), which
-// spreads the SMs' concurrent reads over the whole mirror instead of one window of it (the
-// online softmax does not depend on the order of the tiles).
-//     warp 0        TMEM owner and single-thread UMMA issue
-//     warps 1-3, 12-19  gather producers (warp 1 also starts each item's Q^T tile by TMA)
+// K and V have rings of their own (three 32 KB slots each: half a tile, 128 cells x 128
+// dims), each fed by a pool of five producer warps that take turns, one warp per fill, so
+// fills complete independently and several are in flight.  QK and PV are issued by two
+// threads, each waiting only for what its own MMAs read, so neither pays for the other's
+// barrier round trips; kNS S^T / P^T buffers decouple them.  Ids are ascending, so tile j of
+// every item covers about the same cell range; each item starts its walk at tile (item mod
+// tiles), which spreads the SMs' concurrent reads over the whole mirror (the online softmax
+// does not depend on the order of the tiles).
+//     warp 0        TMEM owner, QK issue (S^T = K^ . Q^T)
+//     warp 1        PV issue (O^T += V^^T . P^T)
+//     warps 2-3, 12-14  K producers (warp 2 also starts each item's Q^T tile by TMA)
+//     warps 15-19   V producers
 //     warps 4-7     softmax for heads 0-5, warps 8-11 for heads 6-11: one gathered cell per
 //                   thread (TMEM lane), column-wise online softmax over the 128 cells
 //                   (shuffle + shared-memory max per head, base-2 exponent), fp16 P^T into
@@ -40,15 +42,14 @@ namespace {
 constexpr int kCells = 128;                // gathered cells per tile (UMMA M)
 constexpr int kNQ = 16;                    // UMMA N: 12 heads + 4 zero rows
 constexpr int kThreads = 640;
-constexpr int kProdWarps = 11;             // warps 1-3 and 12-19
+constexpr int kPoolWarps = 5;              // warps per producer pool (K: 2-3, 12-14; V: 15-19)
 constexpr int kBlkBytes = kCells * 128;    // 16 KB: one 64-dim block of a tile
 constexpr int kSlotBytes = 2 * kBlkBytes;  // 32 KB: one 128-dim half of a K or V tile
-constexpr int kSlots = 6;
+constexpr int kRing = 3;                   // slots per ring
 constexpr int kNS = 4;                     // S^T and P^T buffers
-constexpr int kLead = 2;                   // QK(u + kLead) is issued before PV(u)
 constexpr int kQBytes = kNQ * kD * 2;      // 8 KB
 constexpr int kPBytes = kNQ * kCells * 2;  // 4 KB
-constexpr int kOffX = 0, kOffQ = kSlots * kSlotBytes;
+constexpr int kOffK = 0, kOffV = kRing * kSlotBytes, kOffQ = 2 * kRing * kSlotBytes;
 constexpr int kOffP = kOffQ + 2 * kQBytes;
 constexpr int kSmemTotal = kOffP + kNS * kPBytes;
 constexpr int kSmemAlloc = kSmemTotal + 1024;
@@ -56,17 +57,24 @@ constexpr uint32_t kColS = 0, kColO = kNS * 16;
 constexpr int kHPW = 6;  // heads per softmax warpgroup
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kNoSlot = -2147483647 - 1;  // marks tile slots past the end of an id row
-static_assert(kLead + 2 <= kNS, "S^T / P^T buffers must cover the QK lead");
-static_assert(2 * kSlots >= kProdWarps + 1, "x_empty keying must cover the producer round-robin");
+// A ring's empty barriers are keyed by the consumed fill mod 2 * kRing: a warp refilling the
+// slot of fill f saw, at its previous fill (kPoolWarps earlier), fill f - kPoolWarps - kRing
+// consumed, which covers the previous phase of the barrier it waits on.
+static_assert(kPoolWarps <= 2 * kRing, "empty-barrier keying must cover the producer round-robin");
+
+struct Ring {
+  uint64_t full[kRing], empty[2 * kRing];
+};
 
 struct __align__(8) GBars {
-  // x_empty is keyed by the consumed fill mod 2 * kSlots: the warp that refills a slot has, at
-  // its previous fill (11 earlier), seen fill f - 17 consumed, so no wait is two phases behind
-  uint64_t x_full[kSlots], x_empty[2 * kSlots];
+  Ring k, v;
   uint64_t q_full[2], q_empty[2];
-  uint64_t s_full[kNS], p_full[kNS];
-  uint64_t o_done[kNS], o_free[2];  // o_done per tile mod kNS: a wait is never two phases behind
-  uint64_t drain;
+  // p_free[u mod kNS] completes when PV(u) (and every PV before it) is done: it frees P^T(u)
+  // and tells the softmax O^T is up to date.  Every wait on it is at most one phase behind:
+  // the softmax waits for PV(u - kNS) at tile u, and for PV(u - 1) only later.
+  uint64_t s_full[kNS], s_free[kNS], p_full[kNS], p_free[kNS];
+  uint64_t o_free[2];
+  uint64_t drain_qk, drain_pv;
 };
 
 // 16-byte copy that writes zeros (and reads nothing) when `valid` is false.
@@ -119,19 +127,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     s_abort = 0;
-    for (int i = 0; i < kSlots; ++i) mbar_init(&bars.x_full[i], 32);  // the filling warp's cp.async arrivals
-    for (int i = 0; i < 2 * kSlots; ++i) mbar_init(&bars.x_empty[i], 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&bars.k.full[i], 32);  // the filling warp's cp.async arrivals
+      mbar_init(&bars.v.full[i], 32);
+    }
+    for (int i = 0; i < 2 * kRing; ++i) {
+      mbar_init(&bars.k.empty[i], 1);
+      mbar_init(&bars.v.empty[i], 1);
+    }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.s_free[i], 8);  // the softmax warps, once S^T is read
       mbar_init(&bars.p_full[i], 8);
-      mbar_init(&bars.o_done[i], 1);
+      mbar_init(&bars.p_free[i], 1);  // PV commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.q_full[i], 1);
       mbar_init(&bars.q_empty[i], 1);
       mbar_init(&bars.o_free[i], 8);
     }
-    mbar_init(&bars.drain, 1);
+    mbar_init(&bars.drain_qk, 1);
+    mbar_init(&bars.drain_pv, 1);
     fence_mbar_init();
   }
   // zero the Q^T and P^T buffers: rows 12..15 are never written again
@@ -178,89 +194,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ UMMA issue
+    // ------------------------------------------------------------ QK issue
     if (lane == 0) {
       const uint32_t idesc_s = idesc_f16_f32(kCells, kNQ, 0, 0);
-      const uint32_t idesc_o = idesc_f16_f32(kCells, kNQ, 1, 0);
-      const uint32_t sX = smem_u32(smem + kOffX);
-      const uint32_t sQ = smem_u32(smem + kOffQ), sP = smem_u32(smem + kOffP);
-      int f = 0;  // fill counter: slot f % kSlots, in the producers' order
-      bool ok = true;
-      for (int s = 0; ok && s < U + kLead; ++s) {
-        if (s < U) {  // S^T(s) = K^(s) . Q^T: two fills of two 64-dim blocks (four K steps each)
-          const int k = s / n_tiles, jl = s % n_tiles;
-          if (jl == 0 && !mbar_wait(&bars.q_full[k & 1], (k >> 1) & 1, status, &s_abort)) { ok = false; break; }
-          const uint64_t bq0 = sdesc_sw128(sQ + (k & 1) * kQBytes, 16, 1024);
-          const uint32_t dS = tmem + kColS + (s % kNS) * 16;
-          for (int hf = 0; hf < 2; ++hf, ++f) {
-            const int slot = f % kSlots;
-            if (!mbar_wait(&bars.x_full[slot], (f / kSlots) & 1, status, &s_abort)) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t a0 = sdesc_sw128(sX + slot * kSlotBytes, 16, 1024);
+      const uint32_t sK = smem_u32(smem + kOffK), sQ = smem_u32(smem + kOffQ);
+      int f = 0;  // K fill counter
+      for (int s = 0; s < U; ++s) {  // S^T(s) = K^(s) . Q^T: two fills of two 64-dim blocks each
+        const int k = s / n_tiles, jl = s % n_tiles;
+        if (jl == 0 && !mbar_wait(&bars.q_full[k & 1], (k >> 1) & 1, status, &s_abort)) break;
+        if (s >= kNS && !mbar_wait(&bars.s_free[s % kNS], ((s / kNS) - 1) & 1, status, &s_abort)) break;
+        const uint64_t bq0 = sdesc_sw128(sQ + (k & 1) * kQBytes, 16, 1024);
+        const uint32_t dS = tmem + kColS + (s % kNS) * 16;
+        bool ok = true;
+        for (int hf = 0; hf < 2; ++hf, ++f) {
+          const int slot = f % kRing;
+          if (!mbar_wait(&bars.k.full[slot], (f / kRing) & 1, status, &s_abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t a0 = sdesc_sw128(sK + slot * kSlotBytes, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_ss(dS, a0 + (uint64_t)(((kk >> 2) * kBlkBytes + (kk & 3) * 32) >> 4),
-                      bq0 + (uint64_t)(((2 * hf + (kk >> 2)) * (kNQ * 128) + (kk & 3) * 32) >> 4), idesc_s,
-                      (hf > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&bars.x_empty[f % (2 * kSlots)]);
-          }
-          if (!ok) break;
-          umma_commit(&bars.s_full[s % kNS]);
-          if (jl == n_tiles - 1) umma_commit(&bars.q_empty[k & 1]);
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(dS, a0 + (uint64_t)(((kk >> 2) * kBlkBytes + (kk & 3) * 32) >> 4),
+                    bq0 + (uint64_t)(((2 * hf + (kk >> 2)) * (kNQ * 128) + (kk & 3) * 32) >> 4), idesc_s,
+                    (hf > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&bars.k.empty[f % (2 * kRing)]);
         }
-        if (s >= kLead) {  // O^T += V^(u)^T . P^T(u): one fill per 128-dim half
-          const int u = s - kLead;
-          const int k = u / n_tiles, jl = u % n_tiles, ob = k & 1;
-          if (jl == 0 && k >= 2 && !mbar_wait(&bars.o_free[ob], ((k >> 1) & 1) ^ 1, status, &s_abort)) {
-            ok = false;
-            break;
-          }
-          if (!mbar_wait(&bars.p_full[u % kNS], (u / kNS) & 1, status, &s_abort)) { ok = false; break; }
-          const uint64_t bp0 = sdesc_sw128(sP + (u % kNS) * kPBytes, 16, 1024);
-          for (int h = 0; h < 2; ++h, ++f) {
-            const int slot = f % kSlots;
-            if (!mbar_wait(&bars.x_full[slot], (f / kSlots) & 1, status, &s_abort)) { ok = false; break; }
-            tc_fence_after();
-            // MN-major A: the half's two 64-dim atoms 16 KB apart (LBO), 8-cell groups 1 KB apart
-            const uint64_t a0 = sdesc_sw128(sX + slot * kSlotBytes, kBlkBytes, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kCells / 16; ++kk)
-              umma_ss(tmem + kColO + ob * 32 + h * 16, a0 + (uint64_t)((kk * 2048) >> 4),
-                      bp0 + (uint64_t)(((kk >> 2) * (kNQ * 128) + (kk & 3) * 32) >> 4), idesc_o,
-                      (jl > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&bars.x_empty[f % (2 * kSlots)]);
-          }
-          if (!ok) break;
-          umma_commit(&bars.o_done[u % kNS]);
-        }
+        if (!ok) break;
+        umma_commit(&bars.s_full[s % kNS]);
+        if (jl == n_tiles - 1) umma_commit(&bars.q_empty[k & 1]);
       }
-      umma_commit(&bars.drain);
-      mbar_wait(&bars.drain, 0, status);
+      umma_commit(&bars.drain_qk);
+      mbar_wait(&bars.drain_qk, 0, status);
     }
     __syncwarp();
-  } else if ((warp >= 1 && warp <= 3) || warp >= 12) {  // warps 12..19
-    // ------------------------------------------------------------ gather producers
-    // Every fill is half a tile: 128 rows x 256 bytes, all of it copied by one warp (fill f by
-    // producer warp f mod 11), so fills complete independently and several are in flight at
-    // once.  Instruction i copies rows 2i, 2i+1 (lane: row 2i + lane/16, chunk lane%16 of the
-    // half: 64-dim block (lane%16)/8, 16-byte chunk lane%8).  Fills follow the MMA order: per step
-    // s the two K halves of tile s, then the two V halves of tile s - kLead.
-    const int pw = warp <= 3 ? warp - 1 : warp - 9;  // 0..10
-    const int ch = lane & 15;
-    // ids of the tiles in use: tile s (K), s-1, s-2 (V when kLead = 2); next = tile s+1
-    int id0[4] = {-1, -1, -1, -1}, id1[4] = {-1, -1, -1, -1}, id2[4] = {-1, -1, -1, -1};
-    int idn[4] = {-1, -1, -1, -1};
-    int g0 = 0, g1 = 0, g2 = 0, gn = 0, nkvn = 0;
-    if (U > 0) load_ids(0, idn, gn, nkvn);
-    auto fill = [&](int f, const __half* base, int g, int h, const int (&cur)[4]) -> bool {
-      if (f % kProdWarps != pw) return true;  // fills go round-robin over the producer warps
-      const int slot = f % kSlots;
-      if (f >= kSlots) {  // fill f - kSlots (same slot) consumed
-        const int e = f - kSlots;
-        if (!mbar_wait_warp(&bars.x_empty[e % (2 * kSlots)], (e / (2 * kSlots)) & 1, status, &s_abort)) return false;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ PV issue
+    if (lane == 0) {
+      const uint32_t idesc_o = idesc_f16_f32(kCells, kNQ, 1, 0);
+      const uint32_t sV = smem_u32(smem + kOffV), sP = smem_u32(smem + kOffP);
+      int f = 0;  // V fill counter
+      for (int u = 0; u < U; ++u) {  // O^T += V^(u)^T . P^T(u): one fill per 128-dim half
+        const int k = u / n_tiles, jl = u % n_tiles, ob = k & 1;
+        if (jl == 0 && k >= 2 && !mbar_wait(&bars.o_free[ob], ((k >> 1) & 1) ^ 1, status, &s_abort)) break;
+        if (!mbar_wait(&bars.p_full[u % kNS], (u / kNS) & 1, status, &s_abort)) break;
+        const uint64_t bp0 = sdesc_sw128(sP + (u % kNS) * kPBytes, 16, 1024);
+        bool ok = true;
+        for (int h = 0; h < 2; ++h, ++f) {
+          const int slot = f % kRing;
+          if (!mbar_wait(&bars.v.full[slot], (f / kRing) & 1, status, &s_abort)) { ok = false; break; }
+          tc_fence_after();
+          // MN-major A: the half's two 64-dim atoms 16 KB apart (LBO), 8-cell groups 1 KB apart
+          const uint64_t a0 = sdesc_sw128(sV + slot * kSlotBytes, kBlkBytes, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kCells / 16; ++kk)
+            umma_ss(tmem + kColO + ob * 32 + h * 16, a0 + (uint64_t)((kk * 2048) >> 4),
+                    bp0 + (uint64_t)(((kk >> 2) * (kNQ * 128) + (kk & 3) * 32) >> 4), idesc_o,
+                    (jl > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&bars.v.empty[f % (2 * kRing)]);
+        }
+        if (!ok) break;
+        umma_commit(&bars.p_free[u % kNS]);
       }
-      uint8_t* dst = smem + kOffX + slot * kSlotBytes + (ch >> 3) * kBlkBytes;
-      const __half* src_g = base + (size_t)g * kD + h * 128 + ch * 8;
+      umma_commit(&bars.drain_pv);
+      mbar_wait(&bars.drain_pv, 0, status);
+    }
+    __syncwarp();
+  } else if ((warp >= 2 && warp <= 3) || warp >= 12) {
+    // ------------------------------------------------------------ gather producers
+    // Every fill is half a tile: 128 rows x 256 bytes, all of it copied by one warp of the
+    // ring's pool (fill f by pool warp f mod 5).  Instruction i copies rows 2i, 2i+1 (lane:
+    // row 2i + lane/16, chunk lane%16 of the half: 64-dim block (lane%16)/8, 16-byte chunk
+    // lane%8).
+    const bool is_v = warp >= 15;
+    const int pw = is_v ? warp - 15 : (warp <= 3 ? warp - 2 : warp - 10);  // 0..4 in the pool
+    Ring& ring = is_v ? bars.v : bars.k;
+    uint8_t* ring_base = smem + (is_v ? kOffV : kOffK);
+    const __half* base = is_v ? vhat : khat;
+    const int ch = lane & 15;
+    int cur[4] = {-1, -1, -1, -1}, nxt[4] = {-1, -1, -1, -1};
+    int g_cur = 0, g_nxt = 0, nkv_nxt = 0;
+    if (U > 0) load_ids(0, nxt, g_nxt, nkv_nxt);
+    if (warp == 2 && lane == 0) tma_prefetch_desc(&map_q);
+    auto fill = [&](int f, int h) -> bool {
+      if (f % kPoolWarps != pw) return true;  // fills go round-robin over the pool
+      const int slot = f % kRing;
+      if (f >= kRing) {  // fill f - kRing (same slot) consumed
+        const int e = f - kRing;
+        if (!mbar_wait_warp(&ring.empty[e % (2 * kRing)], (e / (2 * kRing)) & 1, status, &s_abort)) return false;
+      }
+      uint8_t* dst = ring_base + slot * kSlotBytes + (ch >> 3) * kBlkBytes;
+      const __half* src_g = base + (size_t)g_cur * kD + h * 128 + ch * 8;
       // instruction i copies rows 2i, 2i+1; cells are resolved eight instructions at a time
 #pragma unroll 1
       for (int i0 = 0; i0 < kCells / 2; i0 += 8) {
@@ -275,47 +297,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                            src_g + (size_t)(cell[m] >= 0 ? cell[m] : 0) * (kGroups * kD), cell[m] >= 0);
         }
       }
-      cp_async_arrive_noinc(&bars.x_full[slot]);
+      cp_async_arrive_noinc(&ring.full[slot]);
       return true;
     };
-    if (warp == 1 && lane == 0) tma_prefetch_desc(&map_q);
     int f = 0;
-    bool ok = true;
-    for (int s = 0; ok && s < U + kLead; ++s) {
-      // rotate: tile s's ids become current, tile s+1's start loading
-      if (s < U) check_ids(idn, nkvn, pw == 0);  // tile s: loaded during the previous step
+    for (int s = 0; s < U; ++s) {
+      check_ids(nxt, nkv_nxt, warp == 2);  // tile s: loaded during the previous step
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        id2[x] = id1[x];
-        id1[x] = id0[x];
-        id0[x] = idn[x];
-      }
-      g2 = g1;
-      g1 = g0;
-      g0 = gn;
-      if (s + 1 < U) load_ids(s + 1, idn, gn, nkvn);
-      if (s < U) {
-        const int k = s / n_tiles, jl = s % n_tiles;
-        if (jl == 0 && warp == 1) {
-          // Q^T tile for this item by TMA: per 64-dim block the group's 12 head rows land as
-          // rows 0..11 of a 128B-swizzled [16][64] block (rows 12..15 stay zero)
-          const int it = blockIdx.x + k * gridDim.x;
-          const int t = t_begin + (it >> 1);
-          if (k >= 2 && !mbar_wait_warp(&bars.q_empty[k & 1], ((k >> 1) & 1) ^ 1, status, &s_abort)) break;
-          if (lane == 0) {
-            uint8_t* qb = smem + kOffQ + (k & 1) * kQBytes;
-            mbar_arrive_expect_tx(&bars.q_full[k & 1], kNB * kHPG * 128);
+      for (int x = 0; x < 4; ++x) cur[x] = nxt[x];
+      g_cur = g_nxt;
+      if (s + 1 < U) load_ids(s + 1, nxt, g_nxt, nkv_nxt);
+      const int k = s / n_tiles, jl = s % n_tiles;
+      if (jl == 0 && warp == 2) {
+        // Q^T tile for this item by TMA: per 64-dim block the group's 12 head rows land as
+        // rows 0..11 of a 128B-swizzled [16][64] block (rows 12..15 stay zero)
+        const int it = blockIdx.x + k * gridDim.x;
+        const int t = t_begin + (it >> 1);
+        if (k >= 2 && !mbar_wait_warp(&bars.q_empty[k & 1], ((k >> 1) & 1) ^ 1, status, &s_abort)) break;
+        if (lane == 0) {
+          uint8_t* qb = smem + kOffQ + (k & 1) * kQBytes;
+          mbar_arrive_expect_tx(&bars.q_full[k & 1], kNB * kHPG * 128);
 #pragma unroll
-            for (int b = 0; b < kNB; ++b)
-              tma_load_2d(qb + b * (kNQ * 128), &map_q, &bars.q_full[k & 1], b * 64, t * kHeads + g0 * kHPG);
-          }
-          __syncwarp();
+          for (int b = 0; b < kNB; ++b)
+            tma_load_2d(qb + b * (kNQ * 128), &map_q, &bars.q_full[k & 1], b * 64, t * kHeads + g_cur * kHPG);
         }
-        if (!fill(f++, khat, g0, 0, id0) || !fill(f++, khat, g0, 1, id0)) { ok = false; break; }
+        __syncwarp();
       }
-      if (s >= kLead) {
-        if (!fill(f++, vhat, g2, 0, id2) || !fill(f++, vhat, g2, 1, id2)) { ok = false; break; }
-      }
+      if (!fill(f++, 0) || !fill(f++, 1)) break;
     }
     cp_async_wait_all();  // nothing of ours may land after the CTA exits
   } else if (warp >= 4 && warp <= 11) {
@@ -354,6 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sr[kHPW];
         ld6(lane_base + kColS + (u % kNS) * 16, wg, sr);
         tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.s_free[u % kNS]);  // QK(u + kNS) may overwrite S^T(u)
         float s[kHPW];
 #pragma unroll
         for (int j = 0; j < kHPW; ++j) {
@@ -381,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (need_any) {  // uniform over the warpgroup: derived from the same shared maxima
-          const bool r_ok = mbar_wait_warp(&bars.o_done[(u - 1) % kNS], ((u - 1) / kNS) & 1, status, &s_abort);
+          const bool r_ok = mbar_wait_warp(&bars.p_free[(u - 1) % kNS], ((u - 1) / kNS) & 1, status, &s_abort);
           if (named_bar_any(bar_id, 128, !r_ok)) { ok = false; break; }
           tc_fence_after();
           uint32_t o[kHPW];
@@ -397,6 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
 #pragma unroll
           for (int j = 0; j < kHPW; ++j) l_part[j] *= alpha[j];
+        }
+        // P^T(u) reuses the buffer of P^T(u - kNS): PV(u - kNS) must be done with it
+        if (u >= kNS) {
+          const bool f_ok = mbar_wait_warp(&bars.p_free[u % kNS], ((u / kNS) - 1) & 1, status, &s_abort);
+          if (named_bar_any(bar_id, 128, !f_ok)) { ok = false; break; }
         }
         // P^T[h][i] (K-major SW128: 64-cell blocks of [16 rows][128 B])
         uint8_t* pb = sP + (u % kNS) * kPBytes + (i >> 6) * (kNQ * 128);
@@ -431,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float l = s_l[wg][0][j] + s_l[wg][1][j] + s_l[wg][2][j] + s_l[wg][3][j];
         inv_l[j] = l > 0.f ? 1.f / l : 0.f;
       }
-      const bool e_ok = mbar_wait_warp(&bars.o_done[last_v % kNS], (last_v / kNS) & 1, status, &s_abort);
+      const bool e_ok = mbar_wait_warp(&bars.p_free[last_v % kNS], (last_v / kNS) & 1, status, &s_abort);
       if (named_bar_any(bar_id, 128, !e_ok)) { ok = false; break; }
       tc_fence_after();
       // epilogue: thread = dim i (half 0) and 128 + i (half 1)
