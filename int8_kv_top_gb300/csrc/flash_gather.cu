@@ -17,8 +17,8 @@
 //        O^T[d][h] += V^[c][d] P[h][c]  A = V^ as MN-major (dims x cells)  B = P^T (K-major)
 //
 // K and V have rings of their own (three 32 KB slots each: half a tile, 128 cells x 128
-// dims), each fed by a pool of five producer warps that take turns, one warp per fill, so
-// fills complete independently and several are in flight.  QK and PV are issued by two
+// dims), each fed by a pool of three producer warp pairs that take turns, one pair per fill,
+// so fills complete independently and several are in flight.  QK and PV are issued by two
 // threads, each waiting only for what its own MMAs read, so neither pays for the other's
 // barrier round trips; kNS S^T / P^T buffers decouple them.  Ids are ascending, so tile j of
 // every item covers about the same cell range; each item starts its walk at tile (item mod
@@ -26,8 +26,8 @@
 // does not depend on the order of the tiles).
 //     warp 0        TMEM owner, QK issue (S^T = K^ . Q^T)
 //     warp 1        PV issue (O^T += V^^T . P^T)
-//     warps 2-3, 12-14  K producers (warp 2 also starts each item's Q^T tile by TMA)
-//     warps 15-19   V producers
+//     warps 2-3, 12-15  K producers (warp 2 also starts each item's Q^T tile by TMA)
+//     warps 16-21   V producers
 //     warps 4-7     softmax for heads 0-5, warps 8-11 for heads 6-11: one gathered cell per
 //                   thread (TMEM lane), column-wise online softmax over the 128 cells
 //                   (shuffle + shared-memory max per head, base-2 exponent), fp16 P^T into
@@ -41,8 +41,8 @@ namespace {
 
 constexpr int kCells = 128;                // gathered cells per tile (UMMA M)
 constexpr int kNQ = 16;                    // UMMA N: 12 heads + 4 zero rows
-constexpr int kThreads = 640;
-constexpr int kPoolWarps = 5;              // warps per producer pool (K: 2-3, 12-14; V: 15-19)
+constexpr int kThreads = 704;
+constexpr int kPoolPairs = 3;              // warp pairs per producer pool (K: 2-3, 12-15; V: 16-21)
 constexpr int kBlkBytes = kCells * 128;    // 16 KB: one 64-dim block of a tile
 constexpr int kSlotBytes = 2 * kBlkBytes;  // 32 KB: one 128-dim half of a K or V tile
 constexpr int kRing = 3;                   // slots per ring
@@ -57,10 +57,10 @@ constexpr uint32_t kColS = 0, kColO = kNS * 16;
 constexpr int kHPW = 6;  // heads per softmax warpgroup
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kNoSlot = -2147483647 - 1;  // marks tile slots past the end of an id row
-// A ring's empty barriers are keyed by the consumed fill mod 2 * kRing: a warp refilling the
-// slot of fill f saw, at its previous fill (kPoolWarps earlier), fill f - kPoolWarps - kRing
+// A ring's empty barriers are keyed by the consumed fill mod 2 * kRing: a warp pair refilling
+// the slot of fill f saw, at its previous fill (kPoolPairs earlier), fill f - kPoolPairs - kRing
 // consumed, which covers the previous phase of the barrier it waits on.
-static_assert(kPoolWarps <= 2 * kRing, "empty-barrier keying must cover the producer round-robin");
+static_assert(kPoolPairs <= 2 * kRing, "empty-barrier keying must cover the producer round-robin");
 
 struct Ring {
   uint64_t full[kRing], empty[2 * kRing];
@@ -128,8 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     s_abort = 0;
     for (int i = 0; i < kRing; ++i) {
-      mbar_init(&bars.k.full[i], 32);  // the filling warp's cp.async arrivals
-      mbar_init(&bars.v.full[i], 32);
+      mbar_init(&bars.k.full[i], 64);  // the filling warp pair's cp.async arrivals
+      mbar_init(&bars.v.full[i], 64);
     }
     for (int i = 0; i < 2 * kRing; ++i) {
       mbar_init(&bars.k.empty[i], 1);
@@ -260,12 +260,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if ((warp >= 2 && warp <= 3) || warp >= 12) {
     // ------------------------------------------------------------ gather producers
-    // Every fill is half a tile: 128 rows x 256 bytes, all of it copied by one warp of the
-    // ring's pool (fill f by pool warp f mod 5).  Instruction i copies rows 2i, 2i+1 (lane:
-    // row 2i + lane/16, chunk lane%16 of the half: 64-dim block (lane%16)/8, 16-byte chunk
-    // lane%8).
-    const bool is_v = warp >= 15;
-    const int pw = is_v ? warp - 15 : (warp <= 3 ? warp - 2 : warp - 10);  // 0..4 in the pool
+    // Every fill is half a tile: 128 rows x 256 bytes, copied by one warp pair of the ring's
+    // pool (fill f by pair f mod 3; each warp of the pair takes 64 rows).  Instruction i copies
+    // rows 2i, 2i+1 (lane: row 2i + lane/16, chunk lane%16 of the half: 64-dim block
+    // (lane%16)/8, 16-byte chunk lane%8).
+    const bool is_v = warp >= 16;
+    const int pw = is_v ? warp - 16 : (warp <= 3 ? warp - 2 : warp - 10);  // 0..5 in the pool
+    const int pair = pw >> 1, half_rows = pw & 1;
     Ring& ring = is_v ? bars.v : bars.k;
     uint8_t* ring_base = smem + (is_v ? kOffV : kOffK);
     const __half* base = is_v ? vhat : khat;
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (U > 0) load_ids(0, nxt, g_nxt, nkv_nxt);
     if (warp == 2 && lane == 0) tma_prefetch_desc(&map_q);
     auto fill = [&](int f, int h) -> bool {
-      if (f % kPoolWarps != pw) return true;  // fills go round-robin over the pool
+      if (f % kPoolPairs != pair) return true;  // fills go round-robin over the pool's pairs
       const int slot = f % kRing;
       if (f >= kRing) {  // fill f - kRing (same slot) consumed
         const int e = f - kRing;
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const __half* src_g = base + (size_t)g_cur * kD + h * 128 + ch * 8;
       // instruction i copies rows 2i, 2i+1; cells are resolved eight instructions at a time
 #pragma unroll 1
-      for (int i0 = 0; i0 < kCells / 2; i0 += 8) {
+      for (int i0 = half_rows * (kCells / 4); i0 < (half_rows + 1) * (kCells / 4); i0 += 8) {
         const int sel = pick4(cur, (i0 >> 4) & 3);  // rows 2*i0 .. 2*i0 + 15 share one id register
         int cell[8];
 #pragma unroll
