@@ -12,17 +12,19 @@
 // dequantised once per call instead of once per tile that reads it):
 //
 //   warps 0, 2  TMA: fp16 K^ and V^ chunk tiles, four 128B-swizzled boxes of [64 cells][64
-//               dims] each, which is exactly the UMMA operand layout; K^ in a 4-stage ring
-//               released by QK(j), V^ in a 2-stage ring released by PV(j)
-//   warp 1      TMEM owner + single-thread UMMA issue:
-//                 S  = Q K^T   (A = Q from TMEM, B = K^ K-major)      M=128 N=64  K=256
-//                 O += P V^    (A = P from TMEM, B = V^ MN-major)     M=128 N=256 K=64
+//               dims] each, which is exactly the UMMA operand layout; K^ in a 3-stage ring
+//               released by QK(j), V^ in a 2-stage ring released by PV(j); warp 0 also loads
+//               the Q tile, four boxes of [32 tokens][4 heads][64 dims]
+//   warp 1      TMEM owner + QK issue:   S  = Q K^T  (A = Q K-major, B = K^ K-major)  M=128 N=64  K=256
+//   warp 3      PV issue:                O += P V^   (A = P from TMEM, B = V^ MN-major) M=128 N=256 K=64
 //   warps 4-11  two warpgroups, one (token, head) row per thread in each, half of the
-//               columns each: Q -> TMEM, online softmax on S in base-2 units (max exchanged
-//               through shared memory, exp2, row sums), fp16 P -> TMEM over S, lazy O rescale
-//               (only when the running max grows by more than 2^8), final 1/l and fp16 out.
+//               columns each: online softmax on S in base-2 units (max exchanged through
+//               shared memory, exp2, row sums), fp16 P -> TMEM over S, lazy O rescale (only
+//               when the running max grows by more than 2^8), final 1/l and fp16 out.
+// QK and PV are issued by two threads so that neither waits for the other's barrier round
+// trips; four S/P buffers let QK run up to four chunks ahead of PV.
 //
-// TMEM columns: O [0,256)  S/P double buffer [256,320) [320,384)  Q [384,512).
+// TMEM columns: O [0,256)  S/P buffers [256 + 64 b, 320 + 64 b), b = 0..3.
 // Every mbarrier wait is bounded; a timeout sets the status word and the CTA drains.
 #include <cstring>
 
@@ -36,18 +38,24 @@ constexpr int kHQ = 4;                 // heads per row tile
 constexpr int kRows = kTok * kHQ;      // 128 = UMMA M
 constexpr int kKV = 64;                // cells per chunk (UMMA N of QK^T)
 constexpr int kThreads = 384;
-constexpr int kKStages = 4, kVStages = 2;  // K^ freed by QK(j), V^ by PV(j): separate rings
+constexpr int kKStages = 3, kVStages = 2;  // K^ freed by QK(j), V^ by PV(j): separate rings
+constexpr int kNS = 4;                     // S/P buffers
 constexpr int kHalfTile = kKV * kD * 2;    // one fp16 tile (K^ or V^), 32 KB
-constexpr int kSmemV = kKStages * kHalfTile;                 // V ring after the K ring
-constexpr int kSmemTotal = (kKStages + kVStages) * kHalfTile;  // 192 KB
-constexpr int kSmemAlloc = kSmemTotal + 1024;                // + alignment slack
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
+constexpr int kSmemV = kKStages * kHalfTile;                   // V ring after the K ring
+constexpr int kSmemQ = (kKStages + kVStages) * kHalfTile;      // Q tile: 4 blocks of [128 rows][128 B]
+constexpr int kQBytes = kRows * kD * 2;                        // 64 KB
+constexpr int kSmemTotal = kSmemQ + kQBytes;                   // 224 KB
+constexpr int kSmemAlloc = kSmemTotal + 1024;                  // + alignment slack
+constexpr uint32_t kColO = 0, kColS = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct __align__(8) Bars {
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_done[2], q_full, drain;  // o_done[i & 1]: PV(i) complete
+  // pv_done[i mod kNS]: PV(i) complete (frees S/P buffer i mod kNS, and O holds every PV <= i).
+  // Waits are never two phases behind: QK(j) waits for PV(j - kNS), the softmax for PV(j - 1)
+  // only after QK(j) (hence PV(j - kNS)) is done.
+  uint64_t s_full[kNS], p_full[kNS], pv_done[kNS];
+  uint64_t q_full, drain_qk, drain_pv;
 };
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -63,8 +71,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __global__ void __launch_bounds__(kThreads, 1)
     flash_dense_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                       const __half* __restrict__ q, __half* __restrict__ out, int pos0, int t_begin, int t_end,
-                       float scale_log2, int* status) {
+                       const __grid_constant__ CUtensorMap map_q, __half* __restrict__ out, int pos0, int t_begin,
+                       int t_end, float scale_log2, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Bars bars;
@@ -91,13 +99,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.v_full[i], 1);
       mbar_init(&bars.v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNS; ++i) {
       mbar_init(&bars.s_full[i], 1);
       mbar_init(&bars.p_full[i], 8);
-      mbar_init(&bars.o_done[i], 1);
+      mbar_init(&bars.pv_done[i], 1);
     }
-    mbar_init(&bars.q_full, 8);
-    mbar_init(&bars.drain, 1);
+    mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.drain_qk, 1);
+    mbar_init(&bars.drain_pv, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -110,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == 0 || warp == 2) {
-    // ------------------------------------------------------------ TMA producers (K^: warp 0, V^: warp 2)
+    // ------------------------------------------------------------ TMA producers (K^ + Q: warp 0, V^: warp 2)
     if (lane == 0) {
       const bool is_v = warp == 2;
       const CUtensorMap* map = is_v ? &map_v : &map_k;
@@ -119,6 +128,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
       uint8_t* ring = smem + (is_v ? kSmemV : 0);
       tma_prefetch_desc(map);
+      if (!is_v) {  // Q tile: rows = 32 tokens x 4 heads (token-major), 64 dims per box
+        tma_prefetch_desc(&map_q);
+        mbar_arrive_expect_tx(&bars.q_full, kQBytes);
+#pragma unroll
+        for (int blk = 0; blk < kNB; ++blk)
+          tma_load_3d(smem + kSmemQ + blk * (kRows * 128), &map_q, &bars.q_full, blk * 64, g * kHPG + hq * kHQ, t0);
+      }
       int issued = 0;
       for (int j = 0; j < J; ++j) {
         const int s = j % nst;
@@ -131,19 +147,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // drain: the loads of the last stages must have landed before the CTA exits
       for (int j = max(0, issued - nst); j < issued; ++j) mbar_wait(&full[j % nst], (j / nst) & 1, status);
+      if (!is_v) mbar_wait(&bars.q_full, 0, status);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ UMMA issue
+    // ------------------------------------------------------------ QK issue
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_f16_f32(kRows, kKV, 0, 0);
+      const uint32_t k0 = smem_u32(smem);
+      const uint64_t qdesc = sdesc_sw128(smem_u32(smem + kSmemQ), 16, 1024);
+      bool ok = mbar_wait(&bars.q_full, 0, status, &s_abort);
+      for (int j = 0; ok && j < J; ++j) {
+        const int b = j % kNS, s = j % kKStages;
+        if (j >= kNS && !mbar_wait(&bars.pv_done[b], ((j / kNS) - 1) & 1, status, &s_abort)) break;  // P(j - 4) read
+        if (!mbar_wait(&bars.k_full[s], (j / kKStages) & 1, status, &s_abort)) break;
+        tc_fence_after();
+        const uint64_t kdesc = sdesc_sw128(k0 + s * kHalfTile, 16, 1024);
+        const uint32_t scol = tmem + kColS + b * 64;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          umma_ss(scol, qdesc + (uint64_t)(((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                  kdesc + (uint64_t)(((kk >> 2) * (kKV * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
+        umma_commit(&bars.s_full[b]);
+        umma_commit(&bars.k_empty[s]);
+      }
+      // drain: everything issued must complete before TMEM is released
+      umma_commit(&bars.drain_qk);
+      mbar_wait(&bars.drain_qk, 0, status);
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ PV issue
+    if (lane == 0) {
       const uint32_t idesc_pv = idesc_f16_f32(kRows, kD, 0, 1);
-      const uint32_t k0 = smem_u32(smem), v0 = smem_u32(smem + kSmemV);
-      bool ok = mbar_wait(&bars.q_full, 0, status, &s_abort);  // Q rows are in TMEM
-      tc_fence_after();
-      auto issue_pv = [&](int i) -> bool {
-        const int b = i & 1, s = i % kVStages;
-        if (!mbar_wait(&bars.p_full[b], (i >> 1) & 1, status, &s_abort)) return false;
-        if (!mbar_wait(&bars.v_full[s], (i / kVStages) & 1, status, &s_abort)) return false;
+      const uint32_t v0 = smem_u32(smem + kSmemV);
+      for (int i = 0; i < J; ++i) {
+        const int b = i % kNS, s = i % kVStages;
+        if (!mbar_wait(&bars.p_full[b], (i / kNS) & 1, status, &s_abort)) break;
+        if (!mbar_wait(&bars.v_full[s], (i / kVStages) & 1, status, &s_abort)) break;
         tc_fence_after();
         // descriptor built once; the start-address field (bytes >> 4, low bits) advances per K step
         const uint64_t vdesc = sdesc_sw128(v0 + s * kHalfTile, kKV * 128, 1024);
@@ -152,28 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kKV / 16; ++kk)
           umma_ts(tmem + kColO, pcol + kk * 8, vdesc + (uint64_t)((kk * 2048) >> 4), idesc_pv,
                   (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars.o_done[b]);
+        umma_commit(&bars.pv_done[b]);
         umma_commit(&bars.v_empty[s]);
-        return true;
-      };
-      for (int j = 0; ok && j < J; ++j) {
-        const int b = j & 1, s = j % kKStages;
-        if (!mbar_wait(&bars.k_full[s], (j / kKStages) & 1, status, &s_abort)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t kdesc = sdesc_sw128(k0 + s * kHalfTile, 16, 1024);
-        const uint32_t scol = tmem + kColS + b * 64;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          umma_ts(scol, tmem + kColQ + kk * 8, kdesc + (uint64_t)(((kk >> 2) * (kKV * 128) + (kk & 3) * 32) >> 4),
-                  idesc_qk, kk > 0 ? 1u : 0u);
-        umma_commit(&bars.s_full[b]);
-        umma_commit(&bars.k_empty[s]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
-      if (ok) issue_pv(J - 1);
-      // drain: everything issued must complete before TMEM is released
-      umma_commit(&bars.drain);
-      mbar_wait(&bars.drain, 0, status);
+      umma_commit(&bars.drain_pv);
+      mbar_wait(&bars.drain_pv, 0, status);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -192,34 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_kv_row = row_valid ? pos0 + t + 1 : 0;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
 
-    // this warpgroup's half of the Q row -> TMEM columns [384 + 64 wg, 448 + 64 wg)
-    {
-      const uint4* src =
-          reinterpret_cast<const uint4*>(q + ((size_t)(row_valid ? t : t0) * kHeads + h) * kD + wg * 128);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 v = row_valid ? src[c * 4 + i] : make_uint4(0, 0, 0, 0);
-          w[i * 4 + 0] = v.x;
-          w[i * 4 + 1] = v.y;
-          w[i * 4 + 2] = v.z;
-          w[i * 4 + 3] = v.w;
-        }
-        tmem_st16(lane_base + kColQ + wg * 64 + c * 16, w);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.q_full);
-    }
-
     float m_run = -INFINITY, l_run = 0.f;  // l_run: this half of the row
     bool ok = true;
     for (int j = 0; j < J; ++j) {
-      const int b = j & 1;
-      const bool w_ok = mbar_wait_warp(&bars.s_full[b], (j >> 1) & 1, status, &s_abort);
+      const int b = j % kNS;
+      const bool w_ok = mbar_wait_warp(&bars.s_full[b], (j / kNS) & 1, status, &s_abort);
       if (named_bar_any(1, 256, !w_ok || !ok)) { ok = false; break; }  // both warpgroups leave together
       tc_fence_after();
       uint32_t sr[32];
@@ -243,9 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need = m_new > m_run + kRescaleThreshold;  // identical in both warpgroups
         if (__any_sync(0xffffffffu, need)) {
           // O must hold every PV issued so far before it is rescaled in place
-          // (alternating barriers: the commit after QK(j) already covered PV(j-2), so the
-          // barrier of PV(j-1) is at most one phase behind)
-          if (mbar_wait_warp(&bars.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, status, &s_abort)) {
+          if (mbar_wait_warp(&bars.pv_done[(j - 1) % kNS], ((j - 1) / kNS) & 1, status, &s_abort)) {
             tc_fence_after();
             const float f = need ? fast_exp2(m_run - m_new) : 1.f;
 #pragma unroll 1
@@ -287,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_xm[wg][r] = l_run;
       named_bar_any(1, 256, false);
       const float l_tot = l_run + s_xm[wg ^ 1][r];
-      const bool e_ok = mbar_wait_warp(&bars.o_done[(J - 1) & 1], ((J - 1) >> 1) & 1, status, &s_abort);
+      const bool e_ok = mbar_wait_warp(&bars.pv_done[(J - 1) % kNS], ((J - 1) / kNS) & 1, status, &s_abort);
       if (e_ok) {
         tc_fence_after();
         const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
@@ -330,6 +328,21 @@ bool make_mirror_map(CUtensorMap* map, const __half* base, int n) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3D map over q [T][24][256]: box = 64 dims x 4 heads x 32 tokens, 128B swizzle; the box
+// lands as the [128 rows][64 dims] block of a row tile (row = token * 4 + head).  Tokens past
+// T read as zeros.
+bool make_q_map(CUtensorMap* map, const __half* q, int T) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kHeads, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * kHeads * 2};
+  const cuuint32_t box[3] = {64u, (cuuint32_t)kHQ, (cuuint32_t)kTok};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(q), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
@@ -344,11 +357,12 @@ cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const
     attr_done[dev] = true;
   }
   const int n = a.pos0 + a.T;  // cells in the mirror
-  CUtensorMap mk, mv;
-  if (!make_mirror_map(&mk, khat, n) || !make_mirror_map(&mv, vhat, n)) return cudaErrorInvalidValue;
+  CUtensorMap mk, mv, mq;
+  if (!make_mirror_map(&mk, khat, n) || !make_mirror_map(&mv, vhat, n) || !make_q_map(&mq, a.q, a.T))
+    return cudaErrorInvalidValue;
   const int n_ttiles = (t_end - t_begin + kTok - 1) / kTok;
   const float scale_log2 = a.p.sm_scale * kLog2e;
-  flash_dense_kernel<<<n_ttiles * 6, kThreads, kSmemAlloc, stream>>>(mk, mv, a.q, a.out, a.pos0, t_begin, t_end,
+  flash_dense_kernel<<<n_ttiles * 6, kThreads, kSmemAlloc, stream>>>(mk, mv, mq, a.out, a.pos0, t_begin, t_end,
                                                                     scale_log2, a.status);
   return cudaGetLastError();
 }

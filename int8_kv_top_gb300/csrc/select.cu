@@ -598,15 +598,23 @@ __device__ __forceinline__ uint32_t mask8(const uint4& w, __half2 th, int strict
   return m;
 }
 
-// Smallest order key k in [1, 0xFBFF+...] with pred(k), pred monotone (false .. true).
+// Smallest finite order key k (0x0400 .. 0xFBFF) with pred(k), 0xFC00 if none; pred monotone
+// (false .. true).  Called by all 32 lanes of a warp: each round tests 32 evenly spaced keys up to hi
+// and keeps the gap where pred turns true, so four rounds cover the 63,488 finite keys.
 template <class P>
-__device__ uint32_t first_key(P pred) {
-  uint32_t lo = 0x0400u, hi = 0xFBFFu;  // finite fp16 values: -65504 .. 65504
-  if (!pred(hi)) return 0xFC00u;        // none
+__device__ uint32_t first_key_warp(P pred) {
+  const uint32_t lane = threadIdx.x & 31u;
+  uint32_t lo = 0x0400u, hi = 0xFBFFu;  // answer in [lo, hi] while pred(hi)
+  if (!pred(hi)) return 0xFC00u;        // none (uniform: every lane evaluates the same key)
   while (lo < hi) {
-    const uint32_t mid = (lo + hi) >> 1;
-    if (pred(mid)) hi = mid;
-    else lo = mid + 1;
+    const uint32_t step = (hi - lo + 30u) / 31u;  // lane 31 reaches hi
+    const uint32_t k = lo + lane * step;
+    const unsigned b = __ballot_sync(0xffffffffu, k >= hi || pred(k));
+    const uint32_t first = (uint32_t)__ffs(b) - 1u;  // exists: lanes past hi vote true
+    if (first == 0u) return lo;                      // pred(lo)
+    const uint32_t nhi = lo + first * step;
+    lo = lo + (first - 1u) * step + 1u;              // pred false at lo + (first - 1) step
+    hi = nhi < hi ? nhi : hi;
   }
   return lo;
 }
@@ -728,13 +736,27 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
       const uint32_t gt = mask8(w[m], thi, 1);
       above += __popc(gt);
       uint32_t in = mask8(w[m], tlo, 0) & ~gt;  // key_lo <= key <= key_hi (padding is -inf)
-      while (in) {
-        const int j = __ffs(in) - 1;
-        in &= in - 1;
-        const int slot = atomicAdd(&s_cnt[0], 1);
-        if (slot < kCandCap) {
-          s_cand_idx[slot] = c0 + 8 * m + j;
-          s_cand_key[slot] = (uint16_t)fp16_order_key(half_bits(w[m], j));
+      // one shared-memory atomic per warp: lanes take consecutive ranges of candidate slots
+      const int n = __popc(in);
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int tot = __shfl_sync(0xffffffffu, incl, 31);
+      if (tot) {  // warp-uniform
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&s_cnt[0], tot);
+        int slot = __shfl_sync(0xffffffffu, base, 0) + incl - n;
+        while (in) {
+          const int j = __ffs(in) - 1;
+          in &= in - 1;
+          if (slot < kCandCap) {
+            s_cand_idx[slot] = c0 + 8 * m + j;
+            s_cand_key[slot] = (uint16_t)fp16_order_key(half_bits(w[m], j));
+          }
+          ++slot;
         }
       }
     }
@@ -782,12 +804,16 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   }
 
   // ---- thresholds: surely in <=> key >= k_def, undecided <=> k_band <= key < k_def
-  if (tid == 0) {
+  if (warp == 0) {
     const Bound bd = s_bound;
     const float tau = order_key_to_float(tau_key);
     const float Ut = bd.U(tau), Lt = bd.L(tau);
-    s_thr[0] = first_key([&](uint32_t k) { return bd.L(order_key_to_float(k)) > Ut; });
-    s_thr[1] = first_key([&](uint32_t k) { return bd.U(order_key_to_float(k)) >= Lt; });
+    const uint32_t k0 = first_key_warp([&](uint32_t k) { return bd.L(order_key_to_float(k)) > Ut; });
+    const uint32_t k1 = first_key_warp([&](uint32_t k) { return bd.U(order_key_to_float(k)) >= Lt; });
+    if (lane == 0) {
+      s_thr[0] = k0;
+      s_thr[1] = k1;
+    }
   }
   __syncthreads();
   const uint32_t k_def = s_thr[0], k_band = s_thr[1];
