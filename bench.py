@@ -256,10 +256,14 @@ def run_ours(args, rank, world, local_rank):
         "dense_prefill": {"bound": "tensor", "achieved": flopA / (fam["dense_prefill"] / LAYERS * 1e-3) / 1e12,
                           "peak": bf16_tf_sus, "unit": "TFLOP/s"},
         "gather_prefill": {"bound": "tensor", "achieved": flopB / (fam["gather_prefill"] / LAYERS * 1e-3) / 1e12,
-                           "peak": bf16_tf_sus, "unit": "TFLOP/s"},
+                           "peak": bf16_tf_sus, "unit": "TFLOP/s",
+                           # the selected rows are gathered from L2: T x 2 groups x 2048 cells x 1 KB (K^ + V^ fp16)
+                           "l2_gather_gbs": T_PREFILL * 2 * 2048 * 1024 / (fam["gather_prefill"] / LAYERS * 1e-3) / 1e9},
     }
     for v in per_launch.values():
         v["frac"] = v["achieved"] / v["peak"]
+    for k, v in per_launch.items():
+        v["traffic"] = recorded_traffic(KERNEL_OF_FAMILY[k])
     dominant = max(("dense_prefill", "gather_prefill", "select_B"), key=lambda k: fam[k])
     if dominant == "select_B":
         # select moves the score matrix through HBM: written once (fp16) and read once, plus K codes
