@@ -61,6 +61,22 @@ def recorded_traffic(kernel):
         return None
 
 
+def max_over_ranks(x, dist, device):
+    """The slowest rank's time: every rank contributes x, every rank gets the maximum."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(ms_per_step, world):
+    """Prefill tokens/s per layer of the whole job: each of `world` replicas runs the full step
+    (2 x 1984 prefill tokens in each of the 12 layers) in ms_per_step (the max over ranks)."""
+    return 2 * T_PREFILL * LAYERS / (ms_per_step * 1e-3) / LAYERS * world
+
+
 def read_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -213,10 +229,7 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop() if sampler else None
     qsa.qsa_check_device_status()
     total_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, device)
     ms_step = total_ms / args.steps
 
     # ---- per-kernel-family times from the marks (averaged over steps)
@@ -280,8 +293,7 @@ def run_ours(args, rank, world, local_rank):
     roof["traffic_unit"] = "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"
     roof["peak_source"] = f"{peak_src}, sustained bf16 (f16 same rate)" if roof["unit"] == "TFLOP/s" else peak_src
 
-    tokens = 2 * T_PREFILL * LAYERS
-    value = tokens / (ms_step * 1e-3) / LAYERS * world
+    value = whole_job_rate(ms_step, world)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -351,12 +363,9 @@ def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, p
     e1.record(stream)
     torch.cuda.synchronize(device)
     ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, device)
     world = dist.get_world_size() if dist else 1
-    value = 2 * T_PREFILL * LAYERS / (ms * 1e-3) / LAYERS * world
+    value = whole_job_rate(ms, world)
     return {"value": value, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
