@@ -15,7 +15,7 @@
 //  2. score:   tcgen05 GEMM with one TMEM accumulator per 64-dim scale block:
 //                S_b[t][c] = sum_{d in b} (hi + lo)[t][d] * kq[c][d]   (products exact in fp32)
 //              epilogue  s~[t][c] = fp16(sm_scale * sum_b ksc[c][b] * S_b[t][c]).
-//              128-row x 64-cell tiles, TMA-fed 4-stage ring, two accumulator sets.
+//              128-row x 64-cell tiles, TMA-fed 3-stage ring, two accumulator sets.
 //  3. topk:    one 512-thread CTA per (token, group) holds the row's scores in registers.
 //              |s~ - s| <= a + b|s~| rigorously (a: fp16 rounding of Qsum and fp32
 //              accumulation, from E_b, H_b, kmax; b: fp16 storage), and U(f) = f + a + b|f|,
@@ -34,7 +34,7 @@ namespace qsa {
 namespace {
 
 // ----------------------------------------------------------------- workspace layout
-constexpr int kGM = 128, kGN = 64, kGK = 64, kGStages = 2;
+constexpr int kGM = 128, kGN = 64, kGK = 64, kGStages = 3;
 constexpr int kMaxCells = 65536;
 constexpr int kTkThreads = 512;
 constexpr int kCandCap = 2048;
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // epilogue: warps 4-7 take cells 0-31 of each 64-cell tile, warps 8-11 cells 32-63
-    __shared__ float4 s_scale[2][kGN];  // the tile's K scales of group g, per accumulator set
+    __shared__ __half s_scale[2][kGN][kNB];  // the tile's fp16 K scales of group g, per accumulator set
     const int quarter = warp & 3, c0 = (warp >= 8) ? 32 : 0;
     const int et = tid - 128;  // 0..255
     const int r = r0 + quarter * 32 + lane;
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     for (int i = 0; i < n_tiles; ++i) {
       const int a = i & 1;
       const int n0 = (nt_begin + i) * kGN;
-      reinterpret_cast<float*>(&s_scale[a][sc_cell])[sc_b] = sc_next;
+      s_scale[a][sc_cell][sc_b] = __float2half_rn(sc_next);  // an fp16 value: exact
       sc_next = load_scale(i + 1);  // one tile ahead: the load overlaps this tile's work
       epilogue_bar();
       if (!dead) dead = !mbar_wait_warp(&bars.acc_full[a], (i >> 1) & 1, status, &s_abort);
@@ -337,9 +337,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float4 sc = s_scale[a][c0 + j];
-          const float sb = (b == 0) ? sc.x : (b == 1) ? sc.y : (b == 2) ? sc.z : sc.w;
-          acc[j] = fmaf(sb, __uint_as_float(v[j]), acc[j]);
+          acc[j] = fmaf(__half2float(s_scale[a][c0 + j][b]), __uint_as_float(v[j]), acc[j]);
         }
       }
       tc_fence_before();
@@ -852,27 +850,41 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   const int need = K - A;  // 1 <= need <= B by construction
 
   if (B <= kBandCap) {
-    // exact keys, one warp per band cell: lane = 8 codes of block lane/8
-    for (int i = warp; i < B; i += nwarps) {
-      const int c = s_band_idx[i];
-      const uint2 x = *reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8);
-      long long part = 0;
+    // exact keys, a warp per band cell (lane = 8 codes of block lane/8), kBatch cells per warp
+    // at a time: each cell's code row and its block scales are loaded together, before use
+    constexpr int kBatch = V >= 64 ? 1 : 4;  // the row held in registers leaves less room at V = 64
+    for (int i0 = warp; i0 < B; i0 += kBatch * nwarps) {
+      uint2 x[kBatch];
+      uint32_t sc[kBatch];
 #pragma unroll
-      for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + by] * (long long)(int8_t)(x.x >> (8 * by));
+      for (int m = 0; m < kBatch; ++m) {
+        const int i = i0 + m * nwarps;
+        const int c = i < B ? s_band_idx[i] : 0;
+        x[m] = *reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8);
+        sc[m] = __half_as_ushort(ksc[((size_t)c * kGroups + g) * kNB + (lane >> 3)]);  // this lane's block scale
+      }
 #pragma unroll
-      for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + 4 + by] * (long long)(int8_t)(x.y >> (8 * by));
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      part += __shfl_xor_sync(0xffffffffu, part, 4);
-      const long long p1 = __shfl_sync(0xffffffffu, part, 8), p2 = __shfl_sync(0xffffffffu, part, 16),
-                      p3 = __shfl_sync(0xffffffffu, part, 24);
-      if (lane == 0) {
-        const __half* sr = ksc + ((size_t)c * kGroups + g) * kNB;
-        __int128 k128 = (__int128)half_int24(__half_as_ushort(sr[0])) * part;
-        k128 += (__int128)half_int24(__half_as_ushort(sr[1])) * p1;
-        k128 += (__int128)half_int24(__half_as_ushort(sr[2])) * p2;
-        k128 += (__int128)half_int24(__half_as_ushort(sr[3])) * p3;
-        s_band_key[i] = split128(k128);
+      for (int m = 0; m < kBatch; ++m) {
+        long long part = 0;
+#pragma unroll
+        for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + by] * (long long)(int8_t)(x[m].x >> (8 * by));
+#pragma unroll
+        for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + 4 + by] * (long long)(int8_t)(x[m].y >> (8 * by));
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        part += __shfl_xor_sync(0xffffffffu, part, 4);  // block sum on every lane of the block
+        const long long p1 = __shfl_sync(0xffffffffu, part, 8), p2 = __shfl_sync(0xffffffffu, part, 16),
+                        p3 = __shfl_sync(0xffffffffu, part, 24);
+        const uint32_t s1 = __shfl_sync(0xffffffffu, sc[m], 8), s2 = __shfl_sync(0xffffffffu, sc[m], 16),
+                       s3 = __shfl_sync(0xffffffffu, sc[m], 24);
+        const int i = i0 + m * nwarps;
+        if (lane == 0 && i < B) {
+          __int128 k128 = (__int128)half_int24((uint16_t)sc[m]) * part;
+          k128 += (__int128)half_int24((uint16_t)s1) * p1;
+          k128 += (__int128)half_int24((uint16_t)s2) * p2;
+          k128 += (__int128)half_int24((uint16_t)s3) * p3;
+          s_band_key[i] = split128(k128);
+        }
       }
     }
     __syncthreads();
