@@ -316,7 +316,8 @@ def run_ours(args, rank, world, local_rank):
 
 def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC, pwsA,
             pwsB, nA, nB, nC, cap, dist):
-    """Same step with every layer's inputs copied from pinned host memory and outputs copied back."""
+    """Same step with every layer's inputs copied from pinned host memory and outputs copied back,
+    all inside the timed region; copies overlap the kernels of other layers."""
     hostA = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in A]
     hostB = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in B]
     hostC = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in C]
@@ -326,30 +327,52 @@ def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, p
     h2d = sum(v.numel() * v.element_size() for hs in (hostA, hostB, hostC) for d in hs for v in d.values())
     d2h = sum(o.numel() * o.element_size() for o in hOutA + hOutB + hXp)
 
-    def step():
-        for l in range(LAYERS):
-            d, h = A[l], hostA[l]
-            for k in d:
-                d[k].copy_(h[k], non_blocking=True)
-            qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nA, T_PREFILL, 0, None, outA[l], pwsA)
-            hOutA[l].copy_(outA[l], non_blocking=True)
-        for l in range(LAYERS):
-            d, h = B[l], hostB[l]
-            for k in d:
-                d[k].copy_(h[k], non_blocking=True)
+    # one job per layer and workload: (device inputs, host inputs, compute, device output, host output)
+    jobs = []
+    for l in range(LAYERS):
+        jobs.append((A[l], hostA[l], lambda d, l=l: qsa.qsa_flash_prefill(
+            d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nA, T_PREFILL, 0, None, outA[l], pwsA), outA[l], hOutA[l]))
+    for l in range(LAYERS):
+        def run_b(d, l=l):
             qsa.qsa_select(d["q"], d["kq"], d["ksc"], nB, T_PREFILL, POS0_B, idsB[l], wsB)
             qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nB, T_PREFILL, POS0_B, idsB[l],
                                   outB[l], pwsB)
-            hOutB[l].copy_(outB[l], non_blocking=True)
-        for l in range(LAYERS):
-            d, h = C[l], hostC[l]
-            for k in d:
-                d[k].copy_(h[k], non_blocking=True)
+        jobs.append((B[l], hostB[l], run_b, outB[l], hOutB[l]))
+    for l in range(LAYERS):
+        def run_c(d, l=l):
             qsa.qsa_select(d["q"], d["kq"], d["ksc"], nC, N_DEC, P_DEC, idsC[l], wsC)
             qsa.qsa_decode_partial(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nC, N_DEC, P_DEC, idsC[l], partC,
                                    nchC, cap)
             qsa.qsa_merge(partC, nchC, N_DEC, cap, xpC[l])
-            hXp[l].copy_(xpC[l], non_blocking=True)
+        jobs.append((C[l], hostC[l], run_c, xpC[l], hXp[l]))
+
+    # Copies run on their own streams so that they overlap the kernels of other layers: job j's
+    # inputs go up on h2d_s, its kernels run on the compute stream once they have landed, and its
+    # output comes back on d2h_s.  A job's device buffers are reused next step only after its
+    # kernels (for the inputs) and its read-back (for the output) are done.
+    h2d_s, d2h_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    ev_in, ev_done, ev_out = [ev() for _ in jobs], [ev() for _ in jobs], [ev() for _ in jobs]
+    for e in ev_done + ev_out:
+        e.record(stream)
+
+    def step():
+        for j, (d, h, _, _, _) in enumerate(jobs):
+            h2d_s.wait_event(ev_done[j])
+            with torch.cuda.stream(h2d_s):
+                for k in d:
+                    d[k].copy_(h[k], non_blocking=True)
+            ev_in[j].record(h2d_s)
+        for j, (d, _, run, out, hout) in enumerate(jobs):
+            stream.wait_event(ev_in[j])
+            stream.wait_event(ev_out[j])
+            run(d)
+            ev_done[j].record(stream)
+            d2h_s.wait_event(ev_done[j])
+            with torch.cuda.stream(d2h_s):
+                hout.copy_(out, non_blocking=True)
+            ev_out[j].record(d2h_s)
+        stream.wait_event(ev_out[-1])  # the step ends when its last result is back on the host
 
     for _ in range(max(1, args.warmup)):
         step()
@@ -358,6 +381,8 @@ def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, p
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    h2d_s.wait_event(e0)
+    d2h_s.wait_event(e0)
     for _ in range(args.steps):
         step()
     e1.record(stream)
