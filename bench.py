@@ -5,6 +5,8 @@ One step = 12 QSA layers (distinct, seeded synthetic buffers per layer) of each 
   B  prefill  T=1984 at pos0=30000  (31,984-cell cache, top-2048)       qsa_select + qsa_flash_prefill
   C  decode   N=1 at P=8192         (top-2048, 64-cell split)           qsa_select + qsa_decode_partial + qsa_merge
 value = prefill tokens per second per layer over the whole step: (1984 + 1984) * 12 / (12 * step time).
+The timed steps replay one CUDA graph per workload (captured from the same API calls); --eager
+times the calls themselves.
 
 python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 Under torchrun (N > 1) every rank runs the same step on its own GPU (replicas, weak scaling)
@@ -172,17 +174,24 @@ def run_ours(args, rank, world, local_rank):
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
-    def step(marks=None):
+    def mark_in(marks):
         def mark(name):
             if marks is not None:
                 e = ev()
                 e.record(stream)
                 marks.append((name, e))
+        return mark
+
+    def sec_a(marks=None):
+        mark = mark_in(marks)
         mark("A0")
         for l in range(LAYERS):
             d = A[l]
             qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nA, T_PREFILL, 0, None, outA[l], pwsA)
         mark("A1")
+
+    def sec_b(marks=None):
+        mark = mark_in(marks)
         for l in range(LAYERS):
             d = B[l]
             mark("Bs")
@@ -191,6 +200,9 @@ def run_ours(args, rank, world, local_rank):
             qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nB, T_PREFILL, POS0_B, idsB[l],
                                   outB[l], pwsB)
         mark("C0")
+
+    def sec_c(marks=None):
+        mark = mark_in(marks)
         for l in range(LAYERS):
             d = C[l]
             mark("Cs")
@@ -202,9 +214,34 @@ def run_ours(args, rank, world, local_rank):
             qsa.qsa_merge(partC, nchC, N_DEC, cap, xpC[l])
         mark("C1")
 
+    def step(marks=None):
+        sec_a(marks)
+        sec_b(marks)
+        sec_c(marks)
+
     for _ in range(args.warmup):
         step()
     qsa.qsa_check_device_status()
+
+    # The timed steps replay one CUDA graph per workload (the same kernels on the same resident
+    # buffers, without the per-call host work); eager steps with events between the calls give
+    # the per-kernel-family breakdown afterwards.
+    graphs = None
+    if not args.eager:
+        try:
+            graphs = []
+            for sec in (sec_a, sec_b, sec_c):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    sec()
+                graphs.append(g)
+            for g in graphs:
+                g.replay()
+            torch.cuda.synchronize(device)
+            qsa.qsa_check_device_status()
+        except Exception as exc:  # capture not available: time the eager calls instead
+            print(f"graph capture failed ({exc}); timing eager calls", file=sys.stderr)
+            graphs = None
 
     dist = None
     if world > 1:
@@ -213,17 +250,30 @@ def run_ours(args, rank, world, local_rank):
     sampler = ClockSampler(local_rank, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
         if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None
     all_marks = []
+    sec_ms = [0.0, 0.0, 0.0]
     if dist:
         dist.barrier()
     torch.cuda.synchronize(device)
     e0, e1 = ev(), ev()
     e0.record(stream)
+    sec_events = []
     for _ in range(args.steps):
-        marks = []
-        step(marks)
-        all_marks.append(marks)
+        if graphs:
+            evs = [ev() for _ in range(4)]
+            for i, g in enumerate(graphs):
+                evs[i].record(stream)
+                g.replay()
+            evs[3].record(stream)
+            sec_events.append(evs)
+        else:
+            marks = []
+            step(marks)
+            all_marks.append(marks)
     e1.record(stream)
     torch.cuda.synchronize(device)
+    for evs in sec_events:
+        for i in range(3):
+            sec_ms[i] += evs[i].elapsed_time(evs[i + 1]) / args.steps
     if dist:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
@@ -231,6 +281,14 @@ def run_ours(args, rank, world, local_rank):
     total_ms = e0.elapsed_time(e1)
     total_ms = max_over_ranks(total_ms, dist, device)
     ms_step = total_ms / args.steps
+
+    if graphs:  # eager marked steps for the per-kernel-family breakdown (outside the timed region)
+        for _ in range(min(args.steps, 5)):
+            marks = []
+            step(marks)
+            all_marks.append(marks)
+        torch.cuda.synchronize(device)
+        qsa.qsa_check_device_status()
 
     # ---- per-kernel-family times from the marks (averaged over steps)
     fam = {"dense_prefill": 0.0, "select_B": 0.0, "gather_prefill": 0.0, "select_C": 0.0, "decode_partial": 0.0,
@@ -254,7 +312,13 @@ def run_ours(args, rank, world, local_rank):
             elif n == "Cm":
                 fam["merge"] += dt
             del nxt
-    fam = {k: v / args.steps for k, v in fam.items()}  # ms per step (12 launches each)
+    fam = {k: v / max(1, len(all_marks)) for k, v in fam.items()}  # ms per step (12 launches each)
+    # per-workload times of the timed steps: graph replays when available, else the eager marks
+    if graphs:
+        sec = {"A": sec_ms[0], "B": sec_ms[1], "C": sec_ms[2]}
+    else:
+        sec = {"A": fam["dense_prefill"], "B": fam["select_B"] + fam["gather_prefill"],
+               "C": fam["select_C"] + fam["decode_partial"] + fam["merge"]}
 
     # ---- e2e: same step through the public API from pinned host buffers
     e2e = None
@@ -266,7 +330,7 @@ def run_ours(args, rank, world, local_rank):
     flopA = flops_prefill(T_PREFILL, 0)
     flopB = flops_prefill(T_PREFILL, POS0_B)
     per_launch = {
-        "dense_prefill": {"bound": "tensor", "achieved": flopA / (fam["dense_prefill"] / LAYERS * 1e-3) / 1e12,
+        "dense_prefill": {"bound": "tensor", "achieved": flopA / (sec["A"] / LAYERS * 1e-3) / 1e12,
                           "peak": bf16_tf_sus, "unit": "TFLOP/s"},
         "gather_prefill": {"bound": "tensor", "achieved": flopB / (fam["gather_prefill"] / LAYERS * 1e-3) / 1e12,
                            "peak": bf16_tf_sus, "unit": "TFLOP/s",
@@ -304,9 +368,12 @@ def run_ours(args, rank, world, local_rank):
                    "heads": "2 KV x 12 q, dim 256", "l2": "inputs larger than L2 (12 distinct layer buffer sets)",
                    "parallelism": f"replicas x{world}"},
         "breakdown_ms_per_step": fam,
-        "prefill_identity_us_per_layer": fam["dense_prefill"] / LAYERS * 1e3,
-        "prefill_selected_us_per_layer": (fam["select_B"] + fam["gather_prefill"]) / LAYERS * 1e3,
-        "decode_us_per_token_per_layer": (fam["select_C"] + fam["decode_partial"] + fam["merge"]) / LAYERS * 1e3 / N_DEC,
+        "breakdown_timing": "eager calls, CUDA events between them",
+        "timing": "CUDA graph replay per workload" if graphs else "eager calls",
+        "workload_ms_per_step": sec,
+        "prefill_identity_us_per_layer": sec["A"] / LAYERS * 1e3,
+        "prefill_selected_us_per_layer": sec["B"] / LAYERS * 1e3,
+        "decode_us_per_token_per_layer": sec["C"] / LAYERS * 1e3 / N_DEC,
         "roofline": roof, "roofline_per_kernel": per_launch,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks, "e2e": e2e,
@@ -473,6 +540,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager API calls instead of CUDA graph replays")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
