@@ -367,29 +367,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.s_free[u % kNS]);  // QK(u + kNS) may overwrite S^T(u)
         float s[kHPW];
+        bool high = jl == 0;  // the item's first tile always sets the running maxima
 #pragma unroll
         for (int j = 0; j < kHPW; ++j) {
           s[j] = valid ? __uint_as_float(sr[j]) * scale_log2 : -INFINITY;
-          float m = s[j];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          if (lane == 0) s_red[wg][u & 1][quarter][j] = m;
+          high |= s[j] > m_run[j] + kRescaleThreshold;
         }
-        named_bar_any(bar_id, 128, false);
+        // The column maxima are needed only when some score of the tile exceeds its head's running
+        // maximum by more than the rescale threshold: otherwise P = exp2(s - m_run) <= 2^8 as
+        // with any lazily rescaled tile, and one barrier-reduction replaces the shuffle maxima.
         bool need_any = false;
         float alpha[kHPW];
 #pragma unroll
-        for (int j = 0; j < kHPW; ++j) {
-          const float mt = fmaxf(fmaxf(s_red[wg][u & 1][0][j], s_red[wg][u & 1][1][j]),
-                                 fmaxf(s_red[wg][u & 1][2][j], s_red[wg][u & 1][3][j]));
-          const float mn = fmaxf(m_run[j], mt);
-          alpha[j] = 1.f;
-          if (jl == 0) {
-            m_run[j] = mn;
-          } else if (mn > m_run[j] + kRescaleThreshold) {
-            alpha[j] = fast_exp2(m_run[j] - mn);
-            m_run[j] = mn;
-            need_any = true;
+        for (int j = 0; j < kHPW; ++j) alpha[j] = 1.f;
+        if (named_bar_any(bar_id, 128, high)) {  // uniform over the warpgroup
+#pragma unroll
+          for (int j = 0; j < kHPW; ++j) {
+            float m = s[j];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) s_red[wg][u & 1][quarter][j] = m;
+          }
+          named_bar_any(bar_id, 128, false);
+#pragma unroll
+          for (int j = 0; j < kHPW; ++j) {
+            const float mt = fmaxf(fmaxf(s_red[wg][u & 1][0][j], s_red[wg][u & 1][1][j]),
+                                   fmaxf(s_red[wg][u & 1][2][j], s_red[wg][u & 1][3][j]));
+            const float mn = fmaxf(m_run[j], mt);
+            if (jl == 0) {
+              m_run[j] = mn;
+            } else if (mn > m_run[j] + kRescaleThreshold) {
+              alpha[j] = fast_exp2(m_run[j] - mn);
+              m_run[j] = mn;
+              need_any = true;
+            }
           }
         }
         if (need_any) {  // uniform over the warpgroup: derived from the same shared maxima
