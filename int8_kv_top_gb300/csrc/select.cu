@@ -387,17 +387,27 @@ __global__ void __launch_bounds__(256) score_small_kernel(const int8_t* __restri
   const int blk = lane >> 3;
   const int col = blk * 128 + (lane & 7) * 8;  // this lane's 8 hi values; lo at +64
   float amax = 0.f;
+  // the warp's 8 cells: codes and scales all loaded before any use, so their latencies overlap
+  uint2 wk[8];
+  __half hs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int c = min(blockIdx.x * 64 + warp * 8 + i, n_max - 1);  // clamped: rows past n_max are not used
+    wk[i] = __ldg(reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8));
+    hs[i] = ksc[((size_t)c * kGroups + g) * kNB + blk];
+  }
+#pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int c = blockIdx.x * 64 + warp * 8 + i;
     if (c >= n_max) break;  // uniform over the warp
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8));
+    const uint2 w = wk[i];
     float kf[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       kf[j] = (float)(int8_t)(w.x >> (8 * j));
       kf[4 + j] = (float)(int8_t)(w.y >> (8 * j));
     }
-    const float my_sc = __half2float(ksc[((size_t)c * kGroups + g) * kNB + blk]);
+    const float my_sc = __half2float(hs[i]);
     amax = fmaxf(amax, fabsf(my_sc));
     const float sc0 = __shfl_sync(0xffffffffu, my_sc, 0), sc1 = __shfl_sync(0xffffffffu, my_sc, 8);
     const float sc2 = __shfl_sync(0xffffffffu, my_sc, 16), sc3 = __shfl_sync(0xffffffffu, my_sc, 24);
@@ -1056,7 +1066,9 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
 
   cudaError_t e = cudaMemsetAsync(kmax, 0, 8 * sizeof(float), stream);
   if (e != cudaSuccess) return e;
-  prep_q_kernel<<<dim3(L.T_pad, kGroups), 256, 0, stream>>>(q, L.t_sel, L.T_sel, L.T_pad, qhi, eh);  // hi/lo
+  // hi/lo rows; the padding rows only feed the GEMM, so the few-rows path skips them
+  const int q_rows = L.T_sel <= kSmallRows ? L.T_sel : L.T_pad;
+  prep_q_kernel<<<dim3(q_rows, kGroups), 256, 0, stream>>>(q, L.t_sel, L.T_sel, L.T_pad, qhi, eh);
   if (L.T_sel <= kSmallRows) {
     score_small_kernel<<<dim3((L.n_max + 63) / 64, kGroups), 256, 0, stream>>>(kq, ksc, qhi, L.T_sel, L.T_pad, L.n_max,
                                                                            L.n_pad, p.sm_scale, sc, kmax);

@@ -10,7 +10,8 @@ from tests.qsa_testutil import assert_close
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("n_chunks,cap", [([33], 33), ([1, 2, 17, 33], 33), ([32, 32, 32, 33], 33), ([5], 7)])
+@pytest.mark.parametrize("n_chunks,cap", [([33], 33), ([1, 2, 17, 33], 33), ([32, 32, 32, 33], 33), ([5], 7),
+                                          ([64, 65, 100, 3, 70], 100)])
 def test_merge_matches_oracle(n_chunks, cap):
     part = synth.merge_partials(n_chunks, cap, seed=sum(n_chunks))
     ref = oracle.merge_f32(part, n_chunks)
