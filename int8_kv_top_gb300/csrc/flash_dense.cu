@@ -9,23 +9,38 @@
 // tile.  Here the 12 heads of a group share their K/V rows, so a CTA owns a 128-row tile
 // of (token, head) pairs of one group, 32 tokens x 4 heads, and every 64-cell chunk is a
 // dense M=128 contraction over the call's fp16 mirror of the cache (mirror.cu: each cell
-// dequantised once per call instead of once per tile that reads it):
+// dequantised once per call instead of once per tile that reads it).
 //
-//   warps 0, 2  TMA: fp16 K^ and V^ chunk tiles, four 128B-swizzled boxes of [64 cells][64
-//               dims] each, which is exactly the UMMA operand layout; K^ in a 3-stage ring
-//               released by QK(j), V^ in a 2-stage ring released by PV(j); warp 0 also loads
-//               the Q tile, four boxes of [32 tokens][4 heads][64 dims]
-//   warp 1      TMEM owner + QK issue:   S  = Q K^T  (A = Q K-major, B = K^ K-major)  M=128 N=64  K=256
-//   warp 3      PV issue:                O += P V^   (A = P from TMEM, B = V^ MN-major) M=128 N=256 K=64
-//   warps 4-11  two warpgroups, one (token, head) row per thread in each, half of the
-//               columns each: online softmax on S in base-2 units (max exchanged through
-//               shared memory, exp2, row sums), fp16 P -> TMEM over S, lazy O rescale (only
-//               when the running max grows by more than 2^8), final 1/l and fp16 out.
-// QK and PV are issued by two threads so that neither waits for the other's barrier round
-// trips; four S/P buffers let QK run up to four chunks ahead of PV.
+// Two CTAs of a cluster form a pair over 64 consecutive tokens (rank 0 the first 32, rank 1
+// the next 32; same group and head quad) and the cache is taken in 128-cell super-chunks, each
+// ONE M=256 x N=128 contraction issued by rank 0 with .cta_group::2: each CTA holds its own 128
+// Q rows, half of the K^ super-chunk (64 cells) and half of the V^ super-chunk (128 dims), and
+// the hardware shares the B halves between the two SMs.  A chain of N=64 K16 steps runs at
+// about 52 cycles each against 32 of arithmetic, N=128 at about 67 against 64, so the wide QK
+// keeps the tensor pipe near its rate; per SM and 128 cells the shared-memory traffic is 96 KB
+// of QK operands, 32 KB of PV operand and 64 KB of TMA writes.
 //
-// TMEM columns: O [0,256)  S/P buffers [256 + 64 b, 320 + 64 b), b = 0..3.
-// Every mbarrier wait is bounded; a timeout sets the status word and the CTA drains.
+//   warps 0, 2  TMA (both CTAs): this CTA's K^ half (four 128B-swizzled boxes of [64 cells]
+//               [64 dims]) into a 3-stage ring and V^ half (two boxes of [128 cells][64 dims])
+//               into a 2-stage ring, released by the pair MMA's multicast commit; warp 0 also
+//               loads the Q tile, four boxes of [32 tokens][4 heads][64 dims]
+//   warp 1      TMEM (pair allocation in both CTAs); rank 0: MMA issue, in the order
+//               QK(0), QK(1), PV(0), QK(2), PV(1), ...
+//                 S = Q K^T  (A = Q K-major, B = K^ K-major)  M=256 N=128 K=256
+//                 O += P V^  (A = P from TMEM, B = V^ MN-major)  M=256 N=256 K=128
+//               rank 1: forwards its Q and K^ arrivals to rank 0's barriers
+//   warp 3      rank 1: forwards its V^ arrivals
+//   warps 4-11  (both CTAs) two warpgroups, one (token, head) row per thread in each, half
+//               of the columns each: online softmax on S in base-2 units (max exchanged
+//               through shared memory, exp2, row sums), fp16 P -> TMEM over S, lazy O rescale
+//               (only when the running max grows by more than 2^8), final 1/l and fp16 out;
+//               P ready is signalled on rank 0's barrier.
+// Two S/P buffers let QK(j + 1) run while super-chunk j is in the softmax.
+//
+// TMEM columns (each CTA): O [0,256)  S/P buffers [256 + 128 b, 384 + 128 b), b = 0, 1.
+// Every mbarrier wait is bounded; a timeout sets the status word and both CTAs drain to the
+// closing cluster barrier.
+#include <algorithm>
 #include <cstring>
 
 #include "common.cuh"
@@ -33,30 +48,57 @@
 namespace qsa {
 namespace {
 
-constexpr int kTok = 32;               // tokens per row tile
-constexpr int kHQ = 4;                 // heads per row tile
-constexpr int kRows = kTok * kHQ;      // 128 = UMMA M
-constexpr int kKV = 64;                // cells per chunk (UMMA N of QK^T)
+constexpr int kTok = 32;               // tokens per CTA tile
+constexpr int kHQ = 4;                 // heads per tile
+constexpr int kRows = kTok * kHQ;      // 128 rows per CTA, 256 per pair (UMMA M)
+constexpr int kKV = 128;               // cells per super-chunk (UMMA N of QK^T)
 constexpr int kThreads = 384;
 constexpr int kKStages = 3, kVStages = 2;  // K^ freed by QK(j), V^ by PV(j): separate rings
-constexpr int kNS = 4;                     // S/P buffers
-constexpr int kHalfTile = kKV * kD * 2;    // one fp16 tile (K^ or V^), 32 KB
-constexpr int kSmemV = kKStages * kHalfTile;                   // V ring after the K ring
-constexpr int kSmemQ = (kKStages + kVStages) * kHalfTile;      // Q tile: 4 blocks of [128 rows][128 B]
-constexpr int kQBytes = kRows * kD * 2;                        // 64 KB
-constexpr int kSmemTotal = kSmemQ + kQBytes;                   // 224 KB
-constexpr int kSmemAlloc = kSmemTotal + 1024;                  // + alignment slack
+constexpr int kNS = 2;                     // S/P buffers
+constexpr int kHalfK = (kKV / 2) * kD * 2;   // this CTA's K^ half: 64 cells x 256 dims fp16, 32 KB
+constexpr int kHalfV = kKV * (kD / 2) * 2;   // this CTA's V^ half: 128 cells x 128 dims fp16, 32 KB
+constexpr int kSmemV = kKStages * kHalfK;                 // V ring after the K ring
+constexpr int kSmemQ = kSmemV + kVStages * kHalfV;        // Q tile: 4 blocks of [128 rows][128 B]
+constexpr int kQBytes = kRows * kD * 2;                   // 64 KB
+constexpr int kSmemTotal = kSmemQ + kQBytes;              // 224 KB
+constexpr int kSmemAlloc = kSmemTotal + 1024;             // + alignment slack
 constexpr uint32_t kColO = 0, kColS = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint16_t kBothCtas = 0x3;
 
+// Same layout in both CTAs.  Rank 0's k_full / v_full / q_full complete on its own TMA bytes
+// plus two arrivals (its producer's, and rank 1's forwarder once rank 1's half has landed);
+// rank 1's complete on its own bytes and one arrival.  k_empty / v_empty / s_full / pv_done
+// receive the pair MMA's multicast commits in both CTAs; p_full (rank 0) counts the 16
+// softmax warps of the pair.
 struct __align__(8) Bars {
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   // pv_done[i mod kNS]: PV(i) complete (frees S/P buffer i mod kNS, and O holds every PV <= i).
   // Waits are never two phases behind: QK(j) waits for PV(j - kNS), the softmax for PV(j - 1)
   // only after QK(j) (hence PV(j - kNS)) is done.
   uint64_t s_full[kNS], p_full[kNS], pv_done[kNS];
-  uint64_t q_full, drain_qk, drain_pv;
+  uint64_t q_full, q_empty, o_free, drain;  // q_empty: last QK of an item done; o_free (rank 0): O read out
 };
+
+// Items (pair of 32-token tiles, group, head quad), heaviest (latest tokens) first; a
+// cluster takes every nC-th item in snake order so that the clusters' loads even out.
+struct Item {
+  int g, hq, t0p, J;  // t0p: first token of the pair; J: super-chunks
+};
+__device__ __forceinline__ Item item_at(int q, int n_pairs, int t_begin, int t_end, int pos0) {
+  Item it;
+  const int pair = n_pairs - 1 - q / 6;
+  it.g = (q % 6) / 3;
+  it.hq = q % 3;
+  it.t0p = t_begin + pair * 2 * kTok;
+  const int t_last_pair = min(it.t0p + 2 * kTok, t_end) - 1;
+  it.J = (pos0 + t_last_pair + 1 + kKV - 1) / kKV;
+  return it;
+}
+__device__ __forceinline__ int item_of(int c, int nC, int n, int n_items) {
+  const int q = n * nC + ((n & 1) ? nC - 1 - c : c);
+  return q < n_items ? q : -1;
+}
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   uint32_t a[16], b[16];
@@ -69,7 +111,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   tmem_st16(taddr + 16, b);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     flash_dense_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                        const __grid_constant__ CUtensorMap map_q, __half* __restrict__ out, int pos0, int t_begin,
                        int t_end, float scale_log2, int* status) {
@@ -80,212 +122,330 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
   const int n_ttiles = (t_end - t_begin + kTok - 1) / kTok;
-  const int item = blockIdx.x;
-  const int ttile = n_ttiles - 1 - item / 6;  // heaviest (latest) token tiles first
-  const int g = (item % 6) / 3, hq = item % 3;
-  const int t0 = t_begin + ttile * kTok;
-  const int t_last = min(t0 + kTok, t_end) - 1;
-  const int n_kv_max = pos0 + t_last + 1;
-  const int J = (n_kv_max + kKV - 1) / kKV;
+  const int n_pairs = (n_ttiles + 1) / 2;
+  const int n_items = n_pairs * 6;
+  const int c = blockIdx.x >> 1, nC = gridDim.x >> 1;
 
   if (tid == 0) {
     s_abort = 0;
+    const uint32_t n_in = rank == 0 ? 2u : 1u;  // arrivals that complete a full barrier
     for (int i = 0; i < kKStages; ++i) {
-      mbar_init(&bars.k_full[i], 1);
+      mbar_init(&bars.k_full[i], n_in);
       mbar_init(&bars.k_empty[i], 1);
     }
     for (int i = 0; i < kVStages; ++i) {
-      mbar_init(&bars.v_full[i], 1);
+      mbar_init(&bars.v_full[i], n_in);
       mbar_init(&bars.v_empty[i], 1);
     }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.p_full[i], 8);
+      mbar_init(&bars.p_full[i], 16);
       mbar_init(&bars.pv_done[i], 1);
     }
-    mbar_init(&bars.q_full, 1);
-    mbar_init(&bars.drain_qk, 1);
-    mbar_init(&bars.drain_pv, 1);
+    mbar_init(&bars.q_full, n_in);
+    mbar_init(&bars.q_empty, 1);
+    mbar_init(&bars.o_free, 16);
+    mbar_init(&bars.drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&s_tmem, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(&s_tmem, 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive or commit
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
+  // Global super-chunk index gj (over this cluster's items) drives every ring's stage and phase.
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ TMA producers (K^ + Q: warp 0, V^: warp 2)
     if (lane == 0) {
       const bool is_v = warp == 2;
       const CUtensorMap* map = is_v ? &map_v : &map_k;
       const int nst = is_v ? kVStages : kKStages;
+      const uint32_t bytes = is_v ? kHalfV : kHalfK;
       uint64_t* full = is_v ? bars.v_full : bars.k_full;
       uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
       uint8_t* ring = smem + (is_v ? kSmemV : 0);
       tma_prefetch_desc(map);
-      if (!is_v) {  // Q tile: rows = 32 tokens x 4 heads (token-major), 64 dims per box
-        tma_prefetch_desc(&map_q);
-        mbar_arrive_expect_tx(&bars.q_full, kQBytes);
+      if (!is_v) tma_prefetch_desc(&map_q);
+      int gj = 0, n = 0;
+      bool ok = true;
+      for (; ok; ++n) {
+        const int q = item_of(c, nC, n, n_items);
+        if (q < 0) break;
+        const Item it = item_at(q, n_pairs, t_begin, t_end, pos0);
+        if (!is_v) {  // Q tile (rows = 32 tokens x 4 heads, token-major), once the last QK of the previous item is done
+          if (n > 0 && !mbar_wait(&bars.q_empty, (n - 1) & 1, status, &s_abort)) break;
+          mbar_arrive_expect_tx(&bars.q_full, kQBytes);
 #pragma unroll
-        for (int blk = 0; blk < kNB; ++blk)
-          tma_load_3d(smem + kSmemQ + blk * (kRows * 128), &map_q, &bars.q_full, blk * 64, g * kHPG + hq * kHQ, t0);
-      }
-      int issued = 0;
-      for (int j = 0; j < J; ++j) {
-        const int s = j % nst;
-        if (j >= nst && !mbar_wait(&empty[s], ((j / nst) & 1) ^ 1, status, &s_abort)) break;
-        uint8_t* dst = ring + s * kHalfTile;
-        mbar_arrive_expect_tx(&full[s], kHalfTile);
+          for (int blk = 0; blk < kNB; ++blk)
+            tma_load_3d(smem + kSmemQ + blk * (kRows * 128), &map_q, &bars.q_full, blk * 64, it.g * kHPG + it.hq * kHQ,
+                        it.t0p + (int)rank * kTok);
+        }
+        for (int j = 0; j < it.J; ++j, ++gj) {
+          const int s = gj % nst;
+          if (gj >= nst && !mbar_wait(&empty[s], ((gj / nst) & 1) ^ 1, status, &s_abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = ring + s * bytes;
+          mbar_arrive_expect_tx(&full[s], bytes);
+          if (is_v) {  // dims 128 rank .. 128 rank + 127 of the super-chunk's cells
 #pragma unroll
-        for (int blk = 0; blk < kNB; ++blk) tma_load_3d(dst + blk * (kKV * 128), map, &full[s], blk * 64, g, j * kKV);
-        issued = j + 1;
+            for (int blk = 0; blk < 2; ++blk)
+              tma_load_3d(dst + blk * (kKV * 128), map, &full[s], (int)rank * 128 + blk * 64, it.g, j * kKV);
+          } else {     // cells 128 j + 64 rank .. + 63, all dims
+#pragma unroll
+            for (int blk = 0; blk < kNB; ++blk)
+              tma_load_3d(dst + blk * ((kKV / 2) * 128), map, &full[s], blk * 64, it.g, j * kKV + (int)rank * (kKV / 2));
+          }
+        }
       }
-      // drain: the loads of the last stages must have landed before the CTA exits
-      for (int j = max(0, issued - nst); j < issued; ++j) mbar_wait(&full[j % nst], (j / nst) & 1, status);
-      if (!is_v) mbar_wait(&bars.q_full, 0, status);
+      // drain: this CTA's last loads must have landed before it exits
+      for (int k = max(0, gj - nst); k < gj; ++k) mbar_wait(&full[k % nst], (k / nst) & 1, status);
+      if (!is_v && n > 0) mbar_wait(&bars.q_full, (n - 1) & 1, status);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ QK issue
+  } else if (warp == 1 && rank == 1) {
+    // ------------------------------------------------------------ rank 1: forward Q and K^ arrivals
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_f16_f32(kRows, kKV, 0, 0);
-      const uint32_t k0 = smem_u32(smem);
-      const uint64_t qdesc = sdesc_sw128(smem_u32(smem + kSmemQ), 16, 1024);
-      bool ok = mbar_wait(&bars.q_full, 0, status, &s_abort);
-      for (int j = 0; ok && j < J; ++j) {
-        const int b = j % kNS, s = j % kKStages;
-        if (j >= kNS && !mbar_wait(&bars.pv_done[b], ((j / kNS) - 1) & 1, status, &s_abort)) break;  // P(j - 4) read
-        if (!mbar_wait(&bars.k_full[s], (j / kKStages) & 1, status, &s_abort)) break;
-        tc_fence_after();
-        const uint64_t kdesc = sdesc_sw128(k0 + s * kHalfTile, 16, 1024);
-        const uint32_t scol = tmem + kColS + b * 64;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          umma_ss(scol, qdesc + (uint64_t)(((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
-                  kdesc + (uint64_t)(((kk >> 2) * (kKV * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
-        umma_commit(&bars.s_full[b]);
-        umma_commit(&bars.k_empty[s]);
+      const uint32_t q_rem = mapa_shared(smem_u32(&bars.q_full), 0);
+      const uint32_t k_rem = mapa_shared(smem_u32(&bars.k_full[0]), 0);
+      int gj = 0;
+      bool ok = true;
+      for (int n = 0; ok; ++n) {
+        const int q = item_of(c, nC, n, n_items);
+        if (q < 0) break;
+        const Item it = item_at(q, n_pairs, t_begin, t_end, pos0);
+        if (!mbar_wait(&bars.q_full, n & 1, status, &s_abort)) break;
+        mbar_arrive_cluster(q_rem);
+        for (int j = 0; j < it.J; ++j, ++gj) {
+          const int s = gj % kKStages;
+          if (!mbar_wait(&bars.k_full[s], (gj / kKStages) & 1, status, &s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(k_rem + 8u * (uint32_t)s);
+        }
       }
-      // drain: everything issued must complete before TMEM is released
-      umma_commit(&bars.drain_qk);
-      mbar_wait(&bars.drain_qk, 0, status);
     }
     __syncwarp();
-  } else if (warp == 3) {
-    // ------------------------------------------------------------ PV issue
+  } else if (warp == 3 && rank == 1) {
+    // ------------------------------------------------------------ rank 1: forward V^ arrivals
     if (lane == 0) {
-      const uint32_t idesc_pv = idesc_f16_f32(kRows, kD, 0, 1);
-      const uint32_t v0 = smem_u32(smem + kSmemV);
-      for (int i = 0; i < J; ++i) {
-        const int b = i % kNS, s = i % kVStages;
-        if (!mbar_wait(&bars.p_full[b], (i / kNS) & 1, status, &s_abort)) break;
-        if (!mbar_wait(&bars.v_full[s], (i / kVStages) & 1, status, &s_abort)) break;
+      const uint32_t v_rem = mapa_shared(smem_u32(&bars.v_full[0]), 0);
+      int gj = 0;
+      bool ok = true;
+      for (int n = 0; ok; ++n) {
+        const int q = item_of(c, nC, n, n_items);
+        if (q < 0) break;
+        const Item it = item_at(q, n_pairs, t_begin, t_end, pos0);
+        for (int j = 0; j < it.J; ++j, ++gj) {
+          const int s = gj % kVStages;
+          if (!mbar_wait(&bars.v_full[s], (gj / kVStages) & 1, status, &s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(v_rem + 8u * (uint32_t)s);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ rank 0: MMA issue
+    // One thread issues QK(j + 1) before PV(j), so the in-order tensor pipe never holds the
+    // S of the next super-chunk behind a PV: QK(j + 1) needs its buffer back from PV(j - 1)
+    // (the two share no accumulator, so that completion is awaited), PV(j) needs P(j).
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_f16_f32(2 * kRows, kKV, 0, 0);
+      const uint32_t idesc_pv = idesc_f16_f32(2 * kRows, kD, 0, 1);
+      const uint32_t k0 = smem_u32(smem), v0 = smem_u32(smem + kSmemV);
+      const uint64_t qdesc = sdesc_sw128(smem_u32(smem + kSmemQ), 16, 1024);
+      // gj: global super-chunk index (rings, buffers and phases); a PV with restart = true
+      // overwrites O, so the previous item's O must have been read out (o_free)
+      auto issue_qk = [&](int gj) -> bool {
+        const int b = gj % kNS, s = gj % kKStages;
+        if (gj >= kNS && !mbar_wait(&bars.pv_done[b], ((gj / kNS) - 1) & 1, status, &s_abort)) return false;
+        if (!mbar_wait(&bars.k_full[s], (gj / kKStages) & 1, status, &s_abort)) return false;
+        tc_fence_after();
+        const uint64_t kdesc = sdesc_sw128(k0 + s * kHalfK, 16, 1024);
+        const uint32_t scol = tmem + kColS + b * kKV;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          umma2_ss(scol, qdesc + (uint64_t)(((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                   kdesc + (uint64_t)(((kk >> 2) * ((kKV / 2) * 128) + (kk & 3) * 32) >> 4), idesc_qk,
+                   kk > 0 ? 1u : 0u);
+        umma2_commit(&bars.s_full[b], kBothCtas);
+        umma2_commit(&bars.k_empty[s], kBothCtas);
+        return true;
+      };
+      auto issue_pv = [&](int gj, bool restart) -> bool {
+        const int b = gj % kNS, s = gj % kVStages;
+        if (!mbar_wait(&bars.p_full[b], (gj / kNS) & 1, status, &s_abort)) return false;
+        if (!mbar_wait(&bars.v_full[s], (gj / kVStages) & 1, status, &s_abort)) return false;
         tc_fence_after();
         // descriptor built once; the start-address field (bytes >> 4, low bits) advances per K step
-        const uint64_t vdesc = sdesc_sw128(v0 + s * kHalfTile, kKV * 128, 1024);
-        const uint32_t pcol = tmem + kColS + b * 64;
+        const uint64_t vdesc = sdesc_sw128(v0 + s * kHalfV, kKV * 128, 1024);
+        const uint32_t pcol = tmem + kColS + b * kKV;
 #pragma unroll
         for (int kk = 0; kk < kKV / 16; ++kk)
-          umma_ts(tmem + kColO, pcol + kk * 8, vdesc + (uint64_t)((kk * 2048) >> 4), idesc_pv,
-                  (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars.pv_done[b]);
-        umma_commit(&bars.v_empty[s]);
+          umma2_ts(tmem + kColO, pcol + kk * 8, vdesc + (uint64_t)((kk * 2048) >> 4), idesc_pv,
+                   (!restart || kk > 0) ? 1u : 0u);
+        umma2_commit(&bars.pv_done[b], kBothCtas);
+        umma2_commit(&bars.v_empty[s], kBothCtas);
+        return true;
+      };
+      bool ok = true;
+      int base = 0;
+      for (int n = 0; ok; ++n) {
+        const int q = item_of(c, nC, n, n_items);
+        if (q < 0) break;
+        const int J = item_at(q, n_pairs, t_begin, t_end, pos0).J;
+        ok = mbar_wait(&bars.q_full, n & 1, status, &s_abort) && issue_qk(base);
+        if (ok && J == 1) umma2_commit(&bars.q_empty, kBothCtas);  // Q no longer read
+        for (int j = 0; ok && j < J; ++j) {
+          if (j + 1 < J) {
+            ok = issue_qk(base + j + 1);
+            if (ok && j + 2 == J) umma2_commit(&bars.q_empty, kBothCtas);
+          }
+          if (ok && j == 0 && n > 0) ok = mbar_wait(&bars.o_free, (n - 1) & 1, status, &s_abort);
+          ok = ok && issue_pv(base + j, j == 0);
+        }
+        base += J;
       }
-      umma_commit(&bars.drain_pv);
-      mbar_wait(&bars.drain_pv, 0, status);
+      // drain: everything issued must complete before TMEM is released
+      umma2_commit(&bars.drain, 0x1);
+      mbar_wait(&bars.drain, 0, status);
     }
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax rows
-    // Two warpgroups share every row: warps 4-7 take S columns 0-31 of each chunk and O
-    // dims 0-127, warps 8-11 columns 32-63 and dims 128-255; they exchange half-row maxima
-    // and sums through shared memory.
+    // Two warpgroups share every row: warps 4-7 take S columns 0-63 of each super-chunk and O
+    // dims 0-127, warps 8-11 columns 64-127 and dims 128-255; they exchange half-row maxima
+    // (when needed) and sums through shared memory.
     __shared__ float s_xm[2][kRows];  // half-row maxima, then half-row sums
     const int wg = warp >= 8 ? 1 : 0;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // TMEM lane == tile row
     const int tl = r >> 2, hl = r & 3;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t p_full0 = mapa_shared(smem_u32(&bars.p_full[0]), 0);  // rank 0's p_full[0]
+    const uint32_t o_free0 = mapa_shared(smem_u32(&bars.o_free), 0);     // rank 0's o_free
+    bool ok = true;
+    int base = 0;  // global index of the item's first super-chunk
+    for (int n = 0; ok; ++n) {
+    const int q = item_of(c, nC, n, n_items);
+    if (q < 0) break;
+    const Item it = item_at(q, n_pairs, t_begin, t_end, pos0);
+    const int J = it.J;
+    const int t0 = it.t0p + (int)rank * kTok;         // this CTA's first token
+    const int t_last = min(t0 + kTok, t_end) - 1;      // < t0 for an empty tile
     const int t = t0 + tl;
     const bool row_valid = t <= t_last;
-    const int h = g * kHPG + hq * kHQ + hl;
+    const int h = it.g * kHPG + it.hq * kHQ + hl;
     const int n_kv_row = row_valid ? pos0 + t + 1 : 0;
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
 
-    float m_run = -INFINITY, l_run = 0.f;  // l_run: this half of the row
-    bool ok = true;
+    float m_run = -INFINITY, l_run = 0.f;  // m_run in log2 units; l_run: this half of the row
     for (int j = 0; j < J; ++j) {
-      const int b = j % kNS;
-      const bool w_ok = mbar_wait_warp(&bars.s_full[b], (j / kNS) & 1, status, &s_abort);
-      if (named_bar_any(1, 256, !w_ok || !ok)) { ok = false; break; }  // both warpgroups leave together
+      const int gj = base + j, b = gj % kNS;
+      const bool w_ok = mbar_wait_warp(&bars.s_full[b], (gj / kNS) & 1, status, &s_abort);
       tc_fence_after();
-      uint32_t sr[32];
-      tmem_ld32(lane_base + kColS + b * 64 + wg * 32, sr);
+      uint32_t sa[32], sb[32];
+      tmem_ld32(lane_base + kColS + b * kKV + wg * 64, sa);
+      tmem_ld32(lane_base + kColS + b * kKV + wg * 64 + 32, sb);
       tmem_wait_ld();
-      float s[32];
-      float m_half = -INFINITY;
-      const int lim = n_kv_row - j * kKV - wg * 32;  // cells i < lim are causal for this row
+      // raw scores; non-causal cells (only near the diagonal) become -inf
+      float s[64];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        s[i] = (i < lim) ? __uint_as_float(sr[i]) * scale_log2 : -INFINITY;
-        m_half = fmaxf(m_half, s[i]);
+        s[i] = __uint_as_float(sa[i]);
+        s[32 + i] = __uint_as_float(sb[i]);
       }
-      s_xm[wg][r] = m_half;
-      named_bar_any(1, 256, false);
-      const float m_tile = fmaxf(m_half, s_xm[wg ^ 1][r]);
-      const float m_new = fmaxf(m_run, m_tile);
-      if (j == 0) {
-        m_run = m_new;
-      } else {
-        const bool need = m_new > m_run + kRescaleThreshold;  // identical in both warpgroups
-        if (__any_sync(0xffffffffu, need)) {
-          // O must hold every PV issued so far before it is rescaled in place
-          if (mbar_wait_warp(&bars.pv_done[(j - 1) % kNS], ((j - 1) / kNS) & 1, status, &s_abort)) {
-            tc_fence_after();
-            const float f = need ? fast_exp2(m_run - m_new) : 1.f;
-#pragma unroll 1
-            for (int c0 = wg * 128; c0 < wg * 128 + 128; c0 += 32) {
-              uint32_t o[32];
-              tmem_ld32(lane_base + kColO + c0, o);
-              tmem_wait_ld();
+      const int lim = n_kv_row - j * kKV - wg * 64;  // cells i < lim are causal for this row
+      if (lim < 64) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-              tmem_st32(lane_base + kColO + c0, o);
+        for (int i = 0; i < 64; ++i) s[i] = (i < lim) ? s[i] : -INFINITY;
+      }
+      float mx[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mx[i] = fmaxf(s[i], s[i + 32]);
+#pragma unroll
+      for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) mx[i] = fmaxf(mx[i], mx[i + w]);
+      const float m_half = mx[0] * scale_log2;  // scale > 0 keeps the order
+      const bool fail = !w_ok || !ok;
+      // One barrier reduction per super-chunk (it also orders every S read of the tile before
+      // the P stores, which overwrite the first half of the buffer): the half-row maxima are
+      // exchanged only when some row crosses its running maximum by the threshold, and at j = 0.
+      if (named_bar_any(1, 256, fail || j == 0 || m_half > m_run + kRescaleThreshold)) {
+        s_xm[wg][r] = m_half;
+        if (named_bar_any(1, 256, fail)) { ok = false; break; }  // both warpgroups leave together
+        const float m_new = fmaxf(m_run, fmaxf(m_half, s_xm[wg ^ 1][r]));
+        if (j == 0) {
+          m_run = m_new;
+        } else {
+          const bool need = m_new > m_run + kRescaleThreshold;  // identical in both warpgroups
+          if (__any_sync(0xffffffffu, need)) {
+            // O must hold every PV issued so far before it is rescaled in place
+            if (mbar_wait_warp(&bars.pv_done[(gj - 1) % kNS], ((gj - 1) / kNS) & 1, status, &s_abort)) {
+              tc_fence_after();
+              const float f = need ? fast_exp2(m_run - m_new) : 1.f;
+#pragma unroll 1
+              for (int c0 = wg * 128; c0 < wg * 128 + 128; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(lane_base + kColO + c0, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+                tmem_st32(lane_base + kColO + c0, o);
+              }
+              tmem_wait_st();
+              if (need) {
+                l_run *= f;
+                m_run = m_new;
+              }
+            } else {
+              ok = false;  // reported at the next super-chunk's barrier reduction
             }
-            tmem_wait_st();
-            if (need) {
-              l_run *= f;
-              m_run = m_new;
-            }
-          } else {
-            ok = false;  // reported at the next tile's collective barrier
           }
         }
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      uint32_t pw[16];
+      uint32_t pa[16], pb[16];
       float lsum = 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float p0 = fast_exp2(s[2 * i] - m_use), p1 = fast_exp2(s[2 * i + 1] - m_use);
-        lsum += p0 + p1;
-        pw[i] = pack_half2(p0, p1);
+        const float p0 = fast_exp2(fmaf(s[2 * i], scale_log2, -m_use));
+        const float p1 = fast_exp2(fmaf(s[2 * i + 1], scale_log2, -m_use));
+        const float p2 = fast_exp2(fmaf(s[32 + 2 * i], scale_log2, -m_use));
+        const float p3 = fast_exp2(fmaf(s[33 + 2 * i], scale_log2, -m_use));
+        lsum += (p0 + p1) + (p2 + p3);
+        pa[i] = pack_half2(p0, p1);
+        pb[i] = pack_half2(p2, p3);
       }
       l_run += lsum;
-      tmem_st16(lane_base + kColS + b * 64 + wg * 16, pw);
+      tmem_st16(lane_base + kColS + b * kKV + wg * 32, pa);
+      tmem_st16(lane_base + kColS + b * kKV + wg * 32 + 16, pb);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_full[b]);
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(&bars.p_full[b]);
+        else mbar_arrive_cluster(p_full0 + 8u * (uint32_t)b);
+      }
     }
-    if (!named_bar_any(1, 256, !ok)) {  // uniform: a failure in the last chunk is seen by all
+    if (named_bar_any(1, 256, !ok)) {  // uniform: a failure in the last chunk is seen by all
+      ok = false;
+    } else {
       s_xm[wg][r] = l_run;
       named_bar_any(1, 256, false);
       const float l_tot = l_run + s_xm[wg ^ 1][r];
-      const bool e_ok = mbar_wait_warp(&bars.pv_done[(J - 1) % kNS], ((J - 1) / kNS) & 1, status, &s_abort);
+      const int gl = base + J - 1;
+      const bool e_ok = mbar_wait_warp(&bars.pv_done[gl % kNS], (gl / kNS) & 1, status, &s_abort);
       if (e_ok) {
         tc_fence_after();
         const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
@@ -305,23 +465,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
           }
         }
+        // O is read out: the next item's first PV may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive(&bars.o_free);
+          else mbar_arrive_cluster(o_free0);
+        }
+      } else {
+        ok = false;
       }
+    }
+    // the epilogue wait is per warp: all 256 threads agree before the next item's barriers
+    if (named_bar_any(1, 256, !ok)) ok = false;
+    base += J;
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // rank 0's MMAs have drained; neither CTA leaves while the other may read its memory
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1) tmem_dealloc_pair(tmem, 512);
 }
 
-// 3D map over a fp16 mirror [n][2][256]: box = 64 dims x 1 group x 64 cells, 128B swizzle.
-bool make_mirror_map(CUtensorMap* map, const __half* base, int n) {
+// 3D map over a fp16 mirror [n][2][256]: box = 64 dims x 1 group x `box_cells` cells, 128B swizzle.
+bool make_mirror_map(CUtensorMap* map, const __half* base, int n, int box_cells) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kGroups, (cuuint64_t)n};
   const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * kGroups * 2};
-  const cuuint32_t box[3] = {64u, 1u, (cuuint32_t)kKV};
+  const cuuint32_t box[3] = {64u, 1u, (cuuint32_t)box_cells};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -348,22 +521,34 @@ bool make_q_map(CUtensorMap* map, const __half* q, int T) {
 cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
                                cudaStream_t stream) {
   if (t_end <= t_begin) return cudaSuccess;
-  static bool attr_done[64] = {};
+  // per device: the shared-memory attribute and how many CTA pairs fit on the GPU at once
+  static int max_clusters[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (max_clusters[dev] == 0) {
     cudaError_t e = cudaFuncSetAttribute(flash_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemAlloc;
+    int nc = 0;
+    e = cudaOccupancyMaxActiveClusters(&nc, flash_dense_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (nc < 1) return cudaErrorInvalidConfiguration;
+    max_clusters[dev] = nc;
   }
   const int n = a.pos0 + a.T;  // cells in the mirror
   CUtensorMap mk, mv, mq;
-  if (!make_mirror_map(&mk, khat, n) || !make_mirror_map(&mv, vhat, n) || !make_q_map(&mq, a.q, a.T))
+  if (!make_mirror_map(&mk, khat, n, kKV / 2) || !make_mirror_map(&mv, vhat, n, kKV) || !make_q_map(&mq, a.q, a.T))
     return cudaErrorInvalidValue;
   const int n_ttiles = (t_end - t_begin + kTok - 1) / kTok;
   const float scale_log2 = a.p.sm_scale * kLog2e;
-  flash_dense_kernel<<<n_ttiles * 6, kThreads, kSmemAlloc, stream>>>(mk, mv, mq, a.out, a.pos0, t_begin, t_end,
-                                                                    scale_log2, a.status);
+  const int n_items = (n_ttiles + 1) / 2 * 6;  // (pair of tiles, group, head quad)
+  const int n_clusters = std::min(max_clusters[dev], n_items);  // persistent: each takes items in snake order
+  flash_dense_kernel<<<n_clusters * 2, kThreads, kSmemAlloc, stream>>>(mk, mv, mq, a.out, a.pos0, t_begin, t_end,
+                                                                      scale_log2, a.status);
   return cudaGetLastError();
 }
 
