@@ -594,6 +594,8 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_red, int* total) {
 }
 
 // 8-bit mask of the halves of w (cell 8m + j -> bit j) that are >= th (cmp = 0) or > th (1).
+// Each packed compare gives 0xFFFF per true half; bits 0 and 16 of compare i go to bits 2i and
+// 16 + 2i, and one fold moves the high halves down to the odd bits 2i + 1.
 __device__ __forceinline__ uint32_t mask8(const uint4& w, __half2 th, int strict) {
   const uint32_t* u = reinterpret_cast<const uint32_t*>(&w);
   uint32_t m = 0;
@@ -601,9 +603,9 @@ __device__ __forceinline__ uint32_t mask8(const uint4& w, __half2 th, int strict
   for (int i = 0; i < 4; ++i) {
     const __half2 h = *reinterpret_cast<const __half2*>(&u[i]);
     const uint32_t x = strict ? __hgt2_mask(h, th) : __hge2_mask(h, th);
-    m |= ((x & 1u) | ((x >> 15) & 2u)) << (2 * i);
+    m |= (x & 0x00010001u) << (2 * i);
   }
-  return m;
+  return (m | (m >> 15)) & 0xFFu;
 }
 
 // Smallest finite order key k (0x0400 .. 0xFBFF) with pred(k), 0xFC00 if none; pred monotone
@@ -739,27 +741,35 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   if (bracket) {
     const __half2 thi = __half2half2(__ushort_as_half(key_to_bits(key_hi)));
     const __half2 tlo = __half2half2(__ushort_as_half(key_to_bits(key_lo)));
+    // key_lo <= key <= key_hi (padding is -inf): 8-cell masks packed four to a register
+    uint32_t in[(V / 8 + 3) / 4] = {};
+    int n = 0;
 #pragma unroll
     for (int m = 0; m < V / 8; ++m) {
       const uint32_t gt = mask8(w[m], thi, 1);
       above += __popc(gt);
-      uint32_t in = mask8(w[m], tlo, 0) & ~gt;  // key_lo <= key <= key_hi (padding is -inf)
-      // one shared-memory atomic per warp: lanes take consecutive ranges of candidate slots
-      const int n = __popc(in);
-      int incl = n;
+      const uint32_t msk = mask8(w[m], tlo, 0) & ~gt;
+      in[m >> 2] |= msk << (8 * (m & 3));
+      n += __popc(msk);
+    }
+    // one scan and one shared-memory atomic per warp: lanes take consecutive ranges of slots
+    int incl = n;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int tot = __shfl_sync(0xffffffffu, incl, 31);
-      if (tot) {  // warp-uniform
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&s_cnt[0], tot);
-        int slot = __shfl_sync(0xffffffffu, base, 0) + incl - n;
-        while (in) {
-          const int j = __ffs(in) - 1;
-          in &= in - 1;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    if (tot) {  // warp-uniform
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&s_cnt[0], tot);
+      int slot = __shfl_sync(0xffffffffu, base, 0) + incl - n;
+#pragma unroll
+      for (int m = 0; m < V / 8; ++m) {
+        uint32_t bits = (in[m >> 2] >> (8 * (m & 3))) & 0xFFu;
+        while (bits) {
+          const int j = __ffs(bits) - 1;
+          bits &= bits - 1;
           if (slot < kCandCap) {
             s_cand_idx[slot] = c0 + 8 * m + j;
             s_cand_key[slot] = (uint16_t)fp16_order_key(half_bits(w[m], j));
