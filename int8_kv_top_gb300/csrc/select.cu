@@ -40,7 +40,8 @@ constexpr int kTkThreads = 512;
 constexpr int kCandCap = 2048;
 constexpr int kBandCap = 512;
 // hist 2 KB | qsum 2 KB | band keys + ids | candidate ids + keys | selection bitmap
-constexpr int kTopkSmem = 4096 + kBandCap * 20 + kCandCap * 6 + kMaxCells / 8;
+constexpr int kStageRows = 64;  // band cells whose code rows are staged in shared memory at once
+constexpr int kTopkSmem = 4096 + kBandCap * 20 + kCandCap * 6 + kMaxCells / 8 + kStageRows * (kD + 8);
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -646,6 +647,8 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   int* s_cand_idx = s_band_idx + kBandCap;                                     // [kCandCap]
   uint16_t* s_cand_key = reinterpret_cast<uint16_t*>(s_cand_idx + kCandCap);   // [kCandCap]
   unsigned* s_bits = reinterpret_cast<unsigned*>(s_cand_key + kCandCap);       // [kMaxCells / 32]
+  int8_t* s_stage = reinterpret_cast<int8_t*>(s_bits + kMaxCells / 32);          // [kStageRows][256] codes
+  uint2* s_stage_sc = reinterpret_cast<uint2*>(s_stage + kStageRows * kD);       // [kStageRows] 4 fp16 scales
   __shared__ int s_red[64];
   __shared__ int s_tmp[8];
   __shared__ int s_cnt[2];          // 0: candidates, 1: band
@@ -870,44 +873,44 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   const int need = K - A;  // 1 <= need <= B by construction
 
   if (B <= kBandCap) {
-    // exact keys, a warp per band cell (lane = 8 codes of block lane/8), kBatch cells per warp
-    // at a time: each cell's code row and its block scales are loaded together, before use
-    constexpr int kBatch = V >= 64 ? 1 : 4;  // the row held in registers leaves less room at V = 64
-    for (int i0 = warp; i0 < B; i0 += kBatch * nwarps) {
-      uint2 x[kBatch];
-      uint32_t sc[kBatch];
-#pragma unroll
-      for (int m = 0; m < kBatch; ++m) {
-        const int i = i0 + m * nwarps;
-        const int c = i < B ? s_band_idx[i] : 0;
-        x[m] = *reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8);
-        sc[m] = __half_as_ushort(ksc[((size_t)c * kGroups + g) * kNB + (lane >> 3)]);  // this lane's block scale
+    // exact keys: the band cells' code rows and scales are staged in shared memory by the
+    // whole CTA in one round of copies (kStageRows at a time), then a warp per cell (lane = 8
+    // codes of block lane / 8) forms the 64-bit block sums and the 128-bit key
+    for (int i0 = 0; i0 < B; i0 += kStageRows) {
+      const int nb = min(kStageRows, B - i0);
+      for (int x = tid; x < nb * 16; x += kTkThreads) {
+        const int c = s_band_idx[i0 + (x >> 4)];
+        cp_async16(s_stage + (x >> 4) * kD + (x & 15) * 16, kq + ((size_t)c * kGroups + g) * kD + (x & 15) * 16);
       }
-#pragma unroll
-      for (int m = 0; m < kBatch; ++m) {
+      for (int x = tid; x < nb; x += kTkThreads) {
+        const int c = s_band_idx[i0 + x];
+        s_stage_sc[x] = *reinterpret_cast<const uint2*>(ksc + ((size_t)c * kGroups + g) * kNB);
+      }
+      cp_async_wait_all();
+      __syncthreads();
+      for (int i = warp; i < nb; i += nwarps) {
+        const uint2 x = *reinterpret_cast<const uint2*>(s_stage + i * kD + lane * 8);
         long long part = 0;
 #pragma unroll
-        for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + by] * (long long)(int8_t)(x[m].x >> (8 * by));
+        for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + by] * (long long)(int8_t)(x.x >> (8 * by));
 #pragma unroll
-        for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + 4 + by] * (long long)(int8_t)(x[m].y >> (8 * by));
+        for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + 4 + by] * (long long)(int8_t)(x.y >> (8 * by));
         part += __shfl_xor_sync(0xffffffffu, part, 1);
         part += __shfl_xor_sync(0xffffffffu, part, 2);
         part += __shfl_xor_sync(0xffffffffu, part, 4);  // block sum on every lane of the block
         const long long p1 = __shfl_sync(0xffffffffu, part, 8), p2 = __shfl_sync(0xffffffffu, part, 16),
                         p3 = __shfl_sync(0xffffffffu, part, 24);
-        const uint32_t s1 = __shfl_sync(0xffffffffu, sc[m], 8), s2 = __shfl_sync(0xffffffffu, sc[m], 16),
-                       s3 = __shfl_sync(0xffffffffu, sc[m], 24);
-        const int i = i0 + m * nwarps;
-        if (lane == 0 && i < B) {
-          __int128 k128 = (__int128)half_int24((uint16_t)sc[m]) * part;
-          k128 += (__int128)half_int24((uint16_t)s1) * p1;
-          k128 += (__int128)half_int24((uint16_t)s2) * p2;
-          k128 += (__int128)half_int24((uint16_t)s3) * p3;
-          s_band_key[i] = split128(k128);
+        if (lane == 0) {
+          const uint2 sw = s_stage_sc[i];
+          __int128 k128 = (__int128)half_int24((uint16_t)(sw.x & 0xFFFFu)) * part;
+          k128 += (__int128)half_int24((uint16_t)(sw.x >> 16)) * p1;
+          k128 += (__int128)half_int24((uint16_t)(sw.y & 0xFFFFu)) * p2;
+          k128 += (__int128)half_int24((uint16_t)(sw.y >> 16)) * p3;
+          s_band_key[i0 + i] = split128(k128);
         }
       }
+      __syncthreads();  // the staging area is reused by the next round
     }
-    __syncthreads();
     for (int i = tid; i < B; i += kTkThreads) {
       const Key128 ki = s_band_key[i];
       const int ci = s_band_idx[i];
