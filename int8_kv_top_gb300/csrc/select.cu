@@ -40,6 +40,7 @@ constexpr int kTkThreads = 512;
 constexpr int kCandCap = 2048;
 constexpr int kBandCap = 512;
 // hist 2 KB | qsum 2 KB | band keys + ids | candidate ids + keys | selection bitmap
+constexpr int kSmallRows = 8;   // calls with at most this many selected rows score on the CUDA cores
 constexpr int kStageRows = 64;  // band cells whose code rows are staged in shared memory at once
 constexpr int kTopkSmem = 4096 + kBandCap * 20 + kCandCap * 6 + kMaxCells / 8 + kStageRows * (kD + 8);
 
@@ -47,7 +48,7 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 
 struct WsLayout {
   int t_sel, T_sel, T_pad, n_max, n_pad;
-  size_t off_kmax, off_eh, off_qhi, off_kc, off_scores, total;
+  size_t off_kmax, off_hist1, zero_bytes, off_eh, off_qhi, off_kc, off_scores, total;
 };
 
 WsLayout ws_layout(int T, int pos0, Params p) {
@@ -59,7 +60,12 @@ WsLayout ws_layout(int T, int pos0, Params p) {
   L.n_pad = (int)align_up((size_t)L.n_max, 256);
   size_t o = 0;
   L.off_kmax = o;
-  o = align_up(o + 8 * sizeof(float), 1024);
+  L.off_hist1 = o + 8 * sizeof(float);
+  // few-row calls: per (group, row) 256-bin histograms of the scores' high key bytes, which
+  // score_small_kernel fills for topk_kernel; zeroed together with kmax
+  const size_t hist_bytes = L.T_sel <= kSmallRows ? (size_t)kGroups * L.T_sel * 256 * sizeof(unsigned) : 0;
+  L.zero_bytes = 8 * sizeof(float) + hist_bytes;
+  o = align_up(o + L.zero_bytes, 1024);
   L.off_eh = o;
   o = align_up(o + (size_t)kGroups * L.T_sel * 8 * sizeof(float), 1024);
   L.off_qhi = o;
@@ -366,6 +372,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// Unsigned key with the order of the fp16 values (finite values and -inf).
+__device__ __forceinline__ uint32_t fp16_order_key(uint16_t b) {
+  return (b & 0x8000u) ? (uint32_t)(~b & 0xFFFFu) : (uint32_t)(b | 0x8000u);
+}
+
 // ----------------------------------------------------------------- 2b. score for few rows
 // Decode-sized calls (at most kSmallRows selected rows) have no GEMM to feed the tensor
 // cores, so the same scores are computed on the CUDA cores straight from the int8 codes:
@@ -373,15 +384,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // summed in a different order than the MMA but within the same bound), then
 // s~ = fp16(sm_scale * fma(ksc_3, S_3, fma(ksc_2, S_2, fma(ksc_1, S_1, ksc_0 * S_0)))),
 // the epilogue of the GEMM.  The kernel also takes kmax_b = max |ksc| (prep_k's job on the
-// GEMM path).  grid (ceil(n_max / 64), 2), 256 threads: warp = 8 cells, lane = 8 dims.
-constexpr int kSmallRows = 8;
+// GEMM path), and for each row the 256-bin histogram of the high byte of its scores' order keys
+// over the row's causal cells (counted in shared memory, one global atomic per non-empty bin),
+// so that topk_kernel starts from the k-th largest score's bin.  grid (ceil(n_max / 64), 2),
+// 256 threads: warp = 8 cells, lane = 8 dims.
 __global__ void __launch_bounds__(256) score_small_kernel(const int8_t* __restrict__ kq, const __half* __restrict__ ksc,
                                                           const __half* __restrict__ qhl, int T_sel, int T_pad,
-                                                          int n_max, int n_pad, float sm_scale,
-                                                          __half* __restrict__ scores, float* __restrict__ kmax) {
+                                                          int n_max, int n_pad, int n_base, float sm_scale,
+                                                          __half* __restrict__ scores, float* __restrict__ kmax,
+                                                          unsigned* __restrict__ hist1) {
   __shared__ __align__(16) float s_hl[kSmallRows][2 * kD];  // per row: [hi_b | lo_b] per block b
   __shared__ float s_max[8][kNB];
+  __shared__ unsigned s_h1[kSmallRows][256];
   const int g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < T_sel * 256; i += 256) s_h1[i >> 8][i & 255] = 0u;
   for (int i = threadIdx.x; i < T_sel * 2 * kD; i += 256)
     s_hl[i / (2 * kD)][i % (2 * kD)] = __half2float(qhl[((size_t)g * T_pad + i / (2 * kD)) * (2 * kD) + i % (2 * kD)]);
   __syncthreads();
@@ -440,7 +456,11 @@ __global__ void __launch_bounds__(256) score_small_kernel(const int8_t* __restri
       acc = fmaf(sc1, S1, acc);
       acc = fmaf(sc2, S2, acc);
       acc = fmaf(sc3, S3, acc);
-      if (lane == 0) scores[((size_t)g * T_sel + r) * n_pad + c] = __float2half_rn(acc * sm_scale);
+      if (lane == 0) {
+        const __half sv = __float2half_rn(acc * sm_scale);
+        scores[((size_t)g * T_sel + r) * n_pad + c] = sv;
+        if (c < n_base + r + 1) atomicAdd(&s_h1[r][fp16_order_key(__half_as_ushort(sv)) >> 8], 1u);
+      }
     }
   }
   if ((lane & 7) == 0) s_max[warp][blk] = amax;
@@ -450,6 +470,10 @@ __global__ void __launch_bounds__(256) score_small_kernel(const int8_t* __restri
 #pragma unroll
     for (int w = 0; w < 8; ++w) m = fmaxf(m, s_max[w][threadIdx.x]);
     atomicMax(reinterpret_cast<int*>(kmax) + g * kNB + threadIdx.x, __float_as_int(m));
+  }
+  for (int i = threadIdx.x; i < T_sel * 256; i += 256) {
+    const unsigned v = s_h1[i >> 8][i & 255];
+    if (v) atomicAdd(hist1 + ((size_t)g * T_sel + (i >> 8)) * 256 + (i & 255), v);
   }
 }
 
@@ -485,9 +509,6 @@ __device__ __forceinline__ __int128 exact_key(const long long* __restrict__ s_qs
   return key;
 }
 
-__device__ __forceinline__ uint32_t fp16_order_key(uint16_t b) {
-  return (b & 0x8000u) ? (uint32_t)(~b & 0xFFFFu) : (uint32_t)(b | 0x8000u);
-}
 __device__ __forceinline__ uint16_t key_to_bits(uint32_t k) {
   return (k & 0x8000u) ? (uint16_t)(k & 0x7FFFu) : (uint16_t)(~k & 0xFFFFu);
 }
@@ -637,8 +658,8 @@ template <int V>
 __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
     topk_kernel(const __half* __restrict__ scores, const __half* __restrict__ q, const int8_t* __restrict__ kq,
                 const __half* __restrict__ ksc, const float* __restrict__ eh, const float* __restrict__ kmax,
-                int32_t* __restrict__ ids, int t_sel, int T_sel, int n_pad, int pos0, int K, float sm_scale,
-                int* status) {
+                const unsigned* __restrict__ hist1, int32_t* __restrict__ ids, int t_sel, int T_sel, int n_pad,
+                int pos0, int K, float sm_scale, int* status) {
   extern __shared__ __align__(16) uint8_t topk_smem[];
   unsigned* s_hist = reinterpret_cast<unsigned*>(topk_smem);                   // [2][256]
   long long* s_qsum = reinterpret_cast<long long*>(topk_smem + 2048);          // [256]
@@ -711,7 +732,9 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   // ---- tau: bracket from a 1-in-8 sample (cells 0, 8, 16, ...), then one compare pass
   const int n_samp = (n_kv + 7) / 8;
   uint32_t key_hi = 0xFBFFu, key_lo = 0x0400u;  // finite range
-  bool bracket = n_samp >= 64;
+  // with the row's high-byte histogram given (few-row calls), the k-th largest key is found
+  // from it directly and no bracket is needed
+  bool bracket = hist1 == nullptr && n_samp >= 64;
   if (bracket) {
     const float ks = (float)K * n_samp / n_kv;
     const int margin = (int)(3.f * sqrtf(ks) + 16.f);
@@ -782,7 +805,7 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
       }
     }
   }
-  const int A0 = block_sum(above, s_red);
+  const int A0 = bracket ? block_sum(above, s_red) : 0;
   const int Cn = s_cnt[0];
   const int need_c = K - A0;
   bracket = bracket && Cn <= kCandCap && need_c >= 1 && need_c <= Cn;
@@ -806,6 +829,22 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
       }
       __syncthreads();
       b2 = find_bin_desc(s_hist + 256, need_c - ab1, &ab2, s_tmp);
+    } else if (hist1 != nullptr) {
+      const unsigned* h1 = hist1 + ((size_t)g * T_sel + r) * 256;
+      for (int i = tid; i < 256; i += kTkThreads) s_hist[i] = h1[i];
+      __syncthreads();
+      b1 = find_bin_desc(s_hist, K, &ab1, s_tmp);
+      // low byte of the keys in bin b1, from the row held in registers
+#pragma unroll
+      for (int m = 0; m < V / 8; ++m) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t k = fp16_order_key(half_bits(w[m], j));
+          if (c0 + 8 * m + j < n_kv && (int)(k >> 8) == b1) atomicAdd(&s_hist[256 + (k & 0xFFu)], 1u);
+        }
+      }
+      __syncthreads();
+      b2 = find_bin_desc(s_hist + 256, K - ab1, &ab2, s_tmp);
     } else {
       for (int c = tid; c < n_kv; c += kTkThreads) atomicAdd(&s_hist[fp16_order_key(__half_as_ushort(row[c])) >> 8], 1u);
       __syncthreads();
@@ -1077,14 +1116,15 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
   __half* kc = reinterpret_cast<__half*>(base + L.off_kc);
   __half* sc = reinterpret_cast<__half*>(base + L.off_scores);
 
-  cudaError_t e = cudaMemsetAsync(kmax, 0, 8 * sizeof(float), stream);
+  unsigned* hist1 = reinterpret_cast<unsigned*>(base + L.off_hist1);
+  cudaError_t e = cudaMemsetAsync(kmax, 0, L.zero_bytes, stream);  // kmax and (few-row calls) the histograms
   if (e != cudaSuccess) return e;
   // hi/lo rows; the padding rows only feed the GEMM, so the few-rows path skips them
   const int q_rows = L.T_sel <= kSmallRows ? L.T_sel : L.T_pad;
   prep_q_kernel<<<dim3(q_rows, kGroups), 256, 0, stream>>>(q, L.t_sel, L.T_sel, L.T_pad, qhi, eh);
   if (L.T_sel <= kSmallRows) {
-    score_small_kernel<<<dim3((L.n_max + 63) / 64, kGroups), 256, 0, stream>>>(kq, ksc, qhi, L.T_sel, L.T_pad, L.n_max,
-                                                                           L.n_pad, p.sm_scale, sc, kmax);
+    score_small_kernel<<<dim3((L.n_max + 63) / 64, kGroups), 256, 0, stream>>>(
+        kq, ksc, qhi, L.T_sel, L.T_pad, L.n_max, L.n_pad, pos0 + L.t_sel, p.sm_scale, sc, kmax, hist1);
   } else {
     prep_k_kernel<<<dim3(min(L.n_pad / 8, kPrepKCtas), kGroups), 256, 0, stream>>>(kq, ksc, L.n_max, L.n_pad, kc,
                                                                                      kmax);
@@ -1097,7 +1137,8 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
   auto run = [&](auto kern) -> cudaError_t {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmem);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kTkThreads, kTopkSmem, stream>>>(sc, q, kq, ksc, eh, kmax, ids, L.t_sel, L.T_sel, L.n_pad, pos0,
+    kern<<<grid, kTkThreads, kTopkSmem, stream>>>(sc, q, kq, ksc, eh, kmax, L.T_sel <= kSmallRows ? hist1 : nullptr,
+                                                  ids, L.t_sel, L.T_sel, L.n_pad, pos0,
                                                   p.topk, p.sm_scale, status);
     return cudaGetLastError();
   };
