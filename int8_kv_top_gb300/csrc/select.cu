@@ -120,51 +120,62 @@ __device__ __forceinline__ __half signed_half(uint32_t mag_bits, bool neg) {
 // [hi_b (64) | lo_b (64)] at columns 128 b .. 128 b + 127, with Qsum = hi + lo + residual.
 // All arithmetic is exact in 64-bit integers (units of 2^-24): Qsum of 12 fp16 values is
 // below 2^44 units, and the block sums of |residual| and |hi| + |lo| stay below 2^51.
-__global__ void __launch_bounds__(256) prep_q_kernel(const __half* __restrict__ q, int t_sel, int T_sel, int T_pad,
-                                                     __half* __restrict__ qhl, float* __restrict__ eh) {
-  const int r = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
-  __half hi = __ushort_as_half(0), lo = __ushort_as_half(0);
-  long long e = 0, h_abs = 0;
-  if (r < T_sel) {
-    const uint16_t* qt = reinterpret_cast<const uint16_t*>(q) + ((size_t)(t_sel + r) * kHeads + g * kHPG) * kD;
-    long long sum = 0;
+// Qsum_d = sum of the group's 12 query heads at dim d for token t (exact, units of 2^-24), split
+// into hi = fp16(Qsum) and lo = fp16(Qsum - hi); e = |Qsum - hi - lo| and h = |hi| + |lo|.
+__device__ __forceinline__ void qsum_split(const __half* __restrict__ q, int t, int g, int d, __half& hi, __half& lo,
+                                           long long& e, long long& h_abs) {
+  const uint16_t* qt = reinterpret_cast<const uint16_t*>(q) + ((size_t)t * kHeads + g * kHPG) * kD;
+  long long sum = 0;
 #pragma unroll
-    for (int h = 0; h < kHPG; ++h) sum += half_int24(__ldg(qt + h * kD + d));
-    unsigned long long rh, rl;
-    const bool neg = sum < 0;
-    const uint32_t hb = units_to_half_mag((unsigned long long)(neg ? -sum : sum), &rh);
-    hi = signed_half(hb, neg);
-    const long long rest = sum - (neg ? -(long long)rh : (long long)rh);  // exact
-    const bool neg2 = rest < 0;
-    const uint32_t lb = units_to_half_mag((unsigned long long)(neg2 ? -rest : rest), &rl);
-    lo = signed_half(lb, neg2);
-    e = rest - (neg2 ? -(long long)rl : (long long)rl);  // exact residual
-    if (e < 0) e = -e;
-    h_abs = (long long)rh + (long long)rl;
-  }
-  __half* dst = qhl + ((size_t)g * T_pad + r) * (2 * kD) + (d >> 6) * 128 + (d & 63);
-  dst[0] = hi;
-  dst[64] = lo;
-  if (r >= T_sel) return;
-  // block sums over 64 dims = two warps: E_b = sum |residual|, H_b = sum (|hi| + |lo|)
+  for (int h = 0; h < kHPG; ++h) sum += half_int24(__ldg(qt + h * kD + d));
+  unsigned long long rh, rl;
+  const bool neg = sum < 0;
+  const uint32_t hb = units_to_half_mag((unsigned long long)(neg ? -sum : sum), &rh);
+  hi = signed_half(hb, neg);
+  const long long rest = sum - (neg ? -(long long)rh : (long long)rh);  // exact
+  const bool neg2 = rest < 0;
+  const uint32_t lb = units_to_half_mag((unsigned long long)(neg2 ? -rest : rest), &rl);
+  lo = signed_half(lb, neg2);
+  e = rest - (neg2 ? -(long long)rl : (long long)rl);  // exact residual
+  if (e < 0) e = -e;
+  h_abs = (long long)rh + (long long)rl;
+}
+
+// E_b = sum |residual| and H_b = sum (|hi| + |lo|) over each 64-dim block (two warps), one
+// row, 256 threads (thread = dim); threads 0-3 write eh[0..3] = E_b and eh[4..7] = H_b.
+__device__ __forceinline__ void write_eh(long long e, long long h_abs, float* __restrict__ eh_row,
+                                         long long* s_e, long long* s_h) {
+  const int d = threadIdx.x;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     e += __shfl_xor_sync(0xffffffffu, e, o);
     h_abs += __shfl_xor_sync(0xffffffffu, h_abs, o);
   }
-  __shared__ long long s_e[8], s_h[8];
-  const int w = d >> 5;
   if ((d & 31) == 0) {
-    s_e[w] = e;
-    s_h[w] = h_abs;
+    s_e[d >> 5] = e;
+    s_h[d >> 5] = h_abs;
   }
   __syncthreads();
   if (d < kNB) {
-    float* dst2 = eh + ((size_t)g * T_sel + r) * 8;
     constexpr float kUnit = 5.9604644775390625e-8f;  // 2^-24, exact scaling
-    dst2[d] = __ll2float_ru(s_e[2 * d] + s_e[2 * d + 1]) * kUnit;
-    dst2[kNB + d] = __ll2float_ru(s_h[2 * d] + s_h[2 * d + 1]) * kUnit;
+    eh_row[d] = __ll2float_ru(s_e[2 * d] + s_e[2 * d + 1]) * kUnit;
+    eh_row[kNB + d] = __ll2float_ru(s_h[2 * d] + s_h[2 * d + 1]) * kUnit;
   }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(256) prep_q_kernel(const __half* __restrict__ q, int t_sel, int T_sel, int T_pad,
+                                                     __half* __restrict__ qhl, float* __restrict__ eh) {
+  const int r = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
+  __half hi = __ushort_as_half(0), lo = __ushort_as_half(0);
+  long long e = 0, h_abs = 0;
+  if (r < T_sel) qsum_split(q, t_sel + r, g, d, hi, lo, e, h_abs);
+  __half* dst = qhl + ((size_t)g * T_pad + r) * (2 * kD) + (d >> 6) * 128 + (d & 63);
+  dst[0] = hi;
+  dst[64] = lo;
+  if (r >= T_sel) return;
+  __shared__ long long s_e[8], s_h[8];
+  write_eh(e, h_abs, eh + ((size_t)g * T_sel + r) * 8, s_e, s_h);
 }
 
 // grid (min(n_pad / 8, kPrepKCtas), 2), 256 threads: a warp per cell row (lane = 8 codes),
@@ -389,17 +400,38 @@ __device__ __forceinline__ uint32_t fp16_order_key(uint16_t b) {
 // so that topk_kernel starts from the k-th largest score's bin.  grid (ceil(n_max / 64), 2),
 // 256 threads: warp = 8 cells, lane = 8 dims.
 __global__ void __launch_bounds__(256) score_small_kernel(const int8_t* __restrict__ kq, const __half* __restrict__ ksc,
-                                                          const __half* __restrict__ qhl, int T_sel, int T_pad,
-                                                          int n_max, int n_pad, int n_base, float sm_scale,
+                                                          const __half* __restrict__ q, int t_sel, int T_sel, int n_max,
+                                                          int n_pad, int n_base, float sm_scale,
                                                           __half* __restrict__ scores, float* __restrict__ kmax,
-                                                          unsigned* __restrict__ hist1) {
+                                                          unsigned* __restrict__ hist1, float* __restrict__ eh) {
   __shared__ __align__(16) float s_hl[kSmallRows][2 * kD];  // per row: [hi_b | lo_b] per block b
   __shared__ float s_max[8][kNB];
   __shared__ unsigned s_h1[kSmallRows][256];
+  __shared__ long long s_e[8], s_h[8];
   const int g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < T_sel * 256; i += 256) s_h1[i >> 8][i & 255] = 0u;
-  for (int i = threadIdx.x; i < T_sel * 2 * kD; i += 256)
-    s_hl[i / (2 * kD)][i % (2 * kD)] = __half2float(qhl[((size_t)g * T_pad + i / (2 * kD)) * (2 * kD) + i % (2 * kD)]);
+  // the rows' Qsum hi/lo split (prep_q's arithmetic), thread = dim, all rows' loads in flight
+  // together; CTA 0 also writes E_b, H_b
+  long long e[kSmallRows], h_abs[kSmallRows];
+  {
+    const int d = threadIdx.x;
+#pragma unroll
+    for (int r = 0; r < kSmallRows; ++r) {
+      e[r] = 0;
+      h_abs[r] = 0;
+      if (r < T_sel) {
+        __half hi, lo;
+        qsum_split(q, t_sel + r, g, d, hi, lo, e[r], h_abs[r]);
+        s_hl[r][(d >> 6) * 128 + (d & 63)] = __half2float(hi);
+        s_hl[r][(d >> 6) * 128 + 64 + (d & 63)] = __half2float(lo);
+      }
+    }
+  }
+  if (blockIdx.x == 0) {
+#pragma unroll
+    for (int r = 0; r < kSmallRows; ++r)
+      if (r < T_sel) write_eh(e[r], h_abs[r], eh + ((size_t)g * T_sel + r) * 8, s_e, s_h);
+  }
   __syncthreads();
   const int blk = lane >> 3;
   const int col = blk * 128 + (lane & 7) * 8;  // this lane's 8 hi values; lo at +64
@@ -1119,13 +1151,11 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
   unsigned* hist1 = reinterpret_cast<unsigned*>(base + L.off_hist1);
   cudaError_t e = cudaMemsetAsync(kmax, 0, L.zero_bytes, stream);  // kmax and (few-row calls) the histograms
   if (e != cudaSuccess) return e;
-  // hi/lo rows; the padding rows only feed the GEMM, so the few-rows path skips them
-  const int q_rows = L.T_sel <= kSmallRows ? L.T_sel : L.T_pad;
-  prep_q_kernel<<<dim3(q_rows, kGroups), 256, 0, stream>>>(q, L.t_sel, L.T_sel, L.T_pad, qhi, eh);
-  if (L.T_sel <= kSmallRows) {
+  if (L.T_sel <= kSmallRows) {  // the few-rows path forms the Qsum split itself
     score_small_kernel<<<dim3((L.n_max + 63) / 64, kGroups), 256, 0, stream>>>(
-        kq, ksc, qhi, L.T_sel, L.T_pad, L.n_max, L.n_pad, pos0 + L.t_sel, p.sm_scale, sc, kmax, hist1);
+        kq, ksc, q, L.t_sel, L.T_sel, L.n_max, L.n_pad, pos0 + L.t_sel, p.sm_scale, sc, kmax, hist1, eh);
   } else {
+    prep_q_kernel<<<dim3(L.T_pad, kGroups), 256, 0, stream>>>(q, L.t_sel, L.T_sel, L.T_pad, qhi, eh);  // hi/lo
     prep_k_kernel<<<dim3(min(L.n_pad / 8, kPrepKCtas), kGroups), 256, 0, stream>>>(kq, ksc, L.n_max, L.n_pad, kc,
                                                                                      kmax);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
