@@ -959,26 +959,45 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
       }
       cp_async_wait_all();
       __syncthreads();
-      for (int i = warp; i < nb; i += nwarps) {
-        const uint2 x = *reinterpret_cast<const uint2*>(s_stage + i * kD + lane * 8);
-        long long part = 0;
+      // four cells per warp, 8 lanes per cell: lane j of a cell takes dims 32 j .. 32 j + 31 (two
+      // lanes per 64-dim block); the four block terms sc_b * S_b (128-bit) are formed on four
+      // lanes at once and summed across them
+      const int cs = lane >> 3, j = lane & 7;
+      for (int ib = warp * 4; ib < nb; ib += nwarps * 4) {
+        const int i = ib + cs;
+        const bool have = i < nb;
+        long long part0 = 0, part1 = 0;
+        if (have) {
+          const uint4* src = reinterpret_cast<const uint4*>(s_stage + i * kD + j * 32);
+          const uint4 xa = src[0], xb = src[1];
+          const uint32_t wv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+          const long long* qs = s_qsum + j * 32;
 #pragma unroll
-        for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + by] * (long long)(int8_t)(x.x >> (8 * by));
+          for (int u = 0; u < 8; ++u)
 #pragma unroll
-        for (int by = 0; by < 4; ++by) part += s_qsum[lane * 8 + 4 + by] * (long long)(int8_t)(x.y >> (8 * by));
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        part += __shfl_xor_sync(0xffffffffu, part, 4);  // block sum on every lane of the block
-        const long long p1 = __shfl_sync(0xffffffffu, part, 8), p2 = __shfl_sync(0xffffffffu, part, 16),
-                        p3 = __shfl_sync(0xffffffffu, part, 24);
-        if (lane == 0) {
-          const uint2 sw = s_stage_sc[i];
-          __int128 k128 = (__int128)half_int24((uint16_t)(sw.x & 0xFFFFu)) * part;
-          k128 += (__int128)half_int24((uint16_t)(sw.x >> 16)) * p1;
-          k128 += (__int128)half_int24((uint16_t)(sw.y & 0xFFFFu)) * p2;
-          k128 += (__int128)half_int24((uint16_t)(sw.y >> 16)) * p3;
-          s_band_key[i0 + i] = split128(k128);
+            for (int by = 0; by < 4; by += 2) {
+              part0 += qs[4 * u + by] * (long long)(int8_t)(wv[u] >> (8 * by));
+              part1 += qs[4 * u + by + 1] * (long long)(int8_t)(wv[u] >> (8 * by + 8));
+            }
         }
+        long long part = part0 + part1;
+        part += __shfl_xor_sync(0xffffffffu, part, 1);  // S_b on both lanes of block b = j / 2
+        __int128 k128 = 0;
+        if (have && (j & 1) == 0) {
+          const uint2 sw = s_stage_sc[i];
+          const uint32_t word = (j >> 2) ? sw.y : sw.x;
+          k128 = (__int128)half_int24((uint16_t)(word >> (16 * ((j >> 1) & 1)))) * part;
+        }
+        // sum the four block terms of the cell (lanes j = 0, 2, 4, 6)
+#pragma unroll
+        for (int o = 2; o <= 4; o <<= 1) {
+          const unsigned long long lo = (unsigned long long)k128;
+          const long long hi = (long long)(k128 >> 64);
+          const unsigned long long lo2 = __shfl_xor_sync(0xffffffffu, lo, o);
+          const long long hi2 = __shfl_xor_sync(0xffffffffu, hi, o);
+          k128 += (__int128)(((unsigned __int128)(unsigned long long)hi2 << 64) | lo2);
+        }
+        if (have && j == 0) s_band_key[i0 + i] = split128(k128);
       }
       __syncthreads();  // the staging area is reused by the next round
     }
