@@ -39,6 +39,8 @@ def check_ids(ids_gpu, ids_ref, T, pos0, idmax):
     (8, 2050, None),                   # default budget boundary: n_kv 2051 identity, 2052 selected
     (96, 1984, None),                  # mixed-budget window at pos0 = 1984
     (32, 2050, None),
+    (10, 2050, None),                  # 9 selected rows: the smallest call on the score GEMM path
+    (5, 160, (40, 71, 1 / 16)),        # few-row path (histogram-seeded top-k) with a small budget
 ])
 def test_select_and_prefill_small(T, pos0, params):
     inp = synth.layer_inputs(T, pos0 + T, seed=T * 7 + pos0)
