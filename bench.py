@@ -168,9 +168,10 @@ def run_ours(args, rank, world, local_rank):
     pwsB = torch.empty(qsa.qsa_flash_prefill_workspace_bytes(T_PREFILL, POS0_B, nB), dtype=torch.uint8, device=device)
     pwsA = torch.empty(qsa.qsa_flash_prefill_workspace_bytes(T_PREFILL, 0, nA), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-    # our kernel launches per step: A mirror 1 + dense 1; B select 4 + mirror 1 + gather 1;
-    # C select 4 + partial 1 + merge 1
-    launches_per_step = LAYERS * (2 + 6 + 6)
+    # our kernel launches per step (the select workspace memset is not counted):
+    # A mirror 1 + dense 1; B select 4 (prep_q, prep_k, score, top-k) + mirror 1 + gather 1;
+    # C select 2 (score_small, top-k) + partial 1 + merge 1
+    launches_per_step = LAYERS * (2 + 6 + 4)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
