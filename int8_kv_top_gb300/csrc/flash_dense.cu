@@ -330,7 +330,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int wg = warp >= 8 ? 1 : 0;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // TMEM lane == tile row
-    const int tl = r >> 2, hl = r & 3;
+    const int tl = r >> 2;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t p_full0 = mapa_shared(smem_u32(&bars.p_full[0]), 0);  // rank 0's p_full[0]
     const uint32_t o_free0 = mapa_shared(smem_u32(&bars.o_free), 0);     // rank 0's o_free
@@ -345,7 +345,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int t_last = min(t0 + kTok, t_end) - 1;      // < t0 for an empty tile
     const int t = t0 + tl;
     const bool row_valid = t <= t_last;
-    const int h = it.g * kHPG + it.hq * kHQ + hl;
     const int n_kv_row = row_valid ? pos0 + t + 1 : 0;
 
     float m_run = -INFINITY, l_run = 0.f;  // m_run in log2 units; l_run: this half of the row
@@ -449,20 +448,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (e_ok) {
         tc_fence_after();
         const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
-        __half* dst = out + ((size_t)(row_valid ? t : 0) * kHeads + h) * kD;
+        // The 4 lanes of a group hold the 4 heads of one token, whose output rows are adjacent.
+        // Per 64 dims each lane packs its row into 4 blocks of 16 dims (32 B); a two-step
+        // butterfly gives lane g block g of all 4 rows, and each 32-byte store of a warp then
+        // writes 8 whole 128-byte row segments instead of 32 scattered pieces.
+        const int g0 = lane & 1, g1 = (lane >> 1) & 1, gq = lane & 3;
+        const int tok = t0 + quarter * 8 + (lane >> 2);
+        const bool tok_valid = tok <= t_last;
+        __half* gdst = out + ((size_t)(tok_valid ? tok : 0) * kHeads + it.g * kHPG + it.hq * kHQ) * kD + 16 * gq;
 #pragma unroll 1
-        for (int c0 = wg * 128; c0 < wg * 128 + 128; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + kColO + c0, o);
+        for (int c0 = wg * 128; c0 < wg * 128 + 128; c0 += 64) {
+          uint32_t oa[32], ob[32];
+          tmem_ld32(lane_base + kColO + c0, oa);
+          tmem_ld32(lane_base + kColO + c0 + 32, ob);
           tmem_wait_ld();
-          uint32_t w[16];
+          uint32_t B[32];  // block b (dims c0 + 16 b ..) = words 8 b .. 8 b + 7
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_half2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          if (row_valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+          for (int i = 0; i < 16; ++i) {
+            B[i] = pack_half2(__uint_as_float(oa[2 * i]) * inv_l, __uint_as_float(oa[2 * i + 1]) * inv_l);
+            B[16 + i] = pack_half2(__uint_as_float(ob[2 * i]) * inv_l, __uint_as_float(ob[2 * i + 1]) * inv_l);
+          }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int b1 = 0; b1 < 2; ++b1)  // blocks (b1, 1 - g0) to and from lane ^ 1
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t x0 = B[(2 * b1) * 8 + i], x1 = B[(2 * b1 + 1) * 8 + i];
+              const uint32_t got = __shfl_xor_sync(0xffffffffu, g0 ? x0 : x1, 1);
+              B[(2 * b1) * 8 + i] = g0 ? got : x0;
+              B[(2 * b1 + 1) * 8 + i] = g0 ? x1 : got;
+            }
+#pragma unroll
+          for (int e0 = 0; e0 < 2; ++e0)  // blocks (1 - g1, e0) to and from lane ^ 2
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t x0 = B[e0 * 8 + i], x1 = B[(2 + e0) * 8 + i];
+              const uint32_t got = __shfl_xor_sync(0xffffffffu, g1 ? x0 : x1, 2);
+              B[e0 * 8 + i] = g1 ? got : x0;
+              B[(2 + e0) * 8 + i] = g1 ? x1 : got;
+            }
+          if (tok_valid) {  // block e = dims c0 + 16 gq .. of head e's row
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(gdst + e * kD + c0),
+                           "r"(B[8 * e]), "r"(B[8 * e + 1]), "r"(B[8 * e + 2]), "r"(B[8 * e + 3]), "r"(B[8 * e + 4]),
+                           "r"(B[8 * e + 5]), "r"(B[8 * e + 6]), "r"(B[8 * e + 7])
+                           : "memory");
           }
         }
         // O is read out: the next item's first PV may overwrite it
