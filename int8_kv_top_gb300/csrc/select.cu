@@ -324,11 +324,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int quarter = warp & 3, c0 = (warp >= 8) ? 32 : 0;
     const int et = tid - 128;  // 0..255
     const int r = r0 + quarter * 32 + lane;
-    const bool row_valid = r < T_sel;
-    const int n_kv = row_valid ? n_base + r + 1 : 0;
     const int n_lim = n_base + T_sel;  // cells that exist for this call
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    __half* dst_row = scores + ((size_t)g * T_sel + (row_valid ? r : 0)) * n_pad;
     bool dead = false;  // after a failed wait keep meeting the epilogue barrier, skip the work
     const int sc_cell = et >> 2, sc_b = et & 3;  // this thread stages one scale per tile
     auto load_scale = [&](int i) -> float {
@@ -362,17 +359,36 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.acc_empty[a]);
       const int cell0 = n0 + c0;
-      if (row_valid && cell0 < n_kv) {
-        uint32_t w[16];
+      // Lanes 2j and 2j + 1 hold adjacent rows: they swap 32-byte halves so that each holds 16
+      // cells (half g0) of both rows, and each 32-byte store of the warp then writes 16 row
+      // segments of 64 bytes instead of 32 scattered 16-byte pieces.
+      uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = pack_half2(acc[2 * j] * sm_scale, acc[2 * j + 1] * sm_scale);
-        if (cell0 + 32 <= n_kv) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst_row + cell0);
+      for (int j = 0; j < 16; ++j) w[j] = pack_half2(acc[2 * j] * sm_scale, acc[2 * j + 1] * sm_scale);
+      const int g0 = lane & 1;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-        } else {
-          const __half* hw = reinterpret_cast<const __half*>(w);
-          for (int j = 0; j < n_kv - cell0; ++j) dst_row[cell0 + j] = hw[j];
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t x0 = w[i], x1 = w[8 + i];
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, g0 ? x0 : x1, 1);
+        w[i] = g0 ? got : x0;
+        w[8 + i] = g0 ? x1 : got;
+      }
+      const int cb = cell0 + 16 * g0;  // w[8 e .. 8 e + 7]: cells cb .. cb + 15 of row (r & ~1) + e
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int rr = (r & ~1) + e;
+        const int nk = rr < T_sel ? n_base + rr + 1 : 0;  // that row's causal cells
+        if (cb < nk) {
+          __half* dp = scores + ((size_t)g * T_sel + rr) * n_pad + cb;
+          if (cb + 16 <= nk) {
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dp), "r"(w[8 * e]),
+                         "r"(w[8 * e + 1]), "r"(w[8 * e + 2]), "r"(w[8 * e + 3]), "r"(w[8 * e + 4]), "r"(w[8 * e + 5]),
+                         "r"(w[8 * e + 6]), "r"(w[8 * e + 7])
+                         : "memory");
+          } else {
+            const __half* hw = reinterpret_cast<const __half*>(w + 8 * e);
+            for (int j = 0; j < nk - cb; ++j) dp[j] = hw[j];
+          }
         }
       }
     }
