@@ -320,7 +320,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // epilogue: warps 4-7 take cells 0-31 of each 64-cell tile, warps 8-11 cells 32-63
-    __shared__ __half s_scale[2][kGN][kNB];  // the tile's fp16 K scales of group g, per accumulator set
+    // the tile's fp16 K scales of group g, per accumulator set, block-major so that a block's 32
+    // cells come in as four 16-byte broadcast loads
+    __shared__ __align__(16) __half s_scale[2][kNB][kGN];
     const int quarter = warp & 3, c0 = (warp >= 8) ? 32 : 0;
     const int et = tid - 128;  // 0..255
     const int r = r0 + quarter * 32 + lane;
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     for (int i = 0; i < n_tiles; ++i) {
       const int a = i & 1;
       const int n0 = (nt_begin + i) * kGN;
-      s_scale[a][sc_cell][sc_b] = __float2half_rn(sc_next);  // an fp16 value: exact
+      s_scale[a][sc_b][sc_cell] = __float2half_rn(sc_next);  // an fp16 value: exact
       sc_next = load_scale(i + 1);  // one tile ahead: the load overlaps this tile's work
       epilogue_bar();
       if (!dead) dead = !mbar_wait_warp(&bars.acc_full[a], (i >> 1) & 1, status, &s_abort);
@@ -349,10 +351,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (int b = 0; b < kNB; ++b) {
         uint32_t v[32];
         tmem_ld32(lane_base + a * 256 + b * kGN + c0, v);
-        tmem_wait_ld();
+        uint4 sv[4];  // this block's scales of the warpgroup's 32 cells
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          acc[j] = fmaf(__half2float(s_scale[a][c0 + j][b]), __uint_as_float(v[j]), acc[j]);
+        for (int q4 = 0; q4 < 4; ++q4) sv[q4] = reinterpret_cast<const uint4*>(&s_scale[a][b][c0])[q4];
+        tmem_wait_ld();
+        const __half2* sc2 = reinterpret_cast<const __half2*>(sv);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 sf = __half22float2(sc2[j]);
+          acc[2 * j] = fmaf(sf.x, __uint_as_float(v[2 * j]), acc[2 * j]);
+          acc[2 * j + 1] = fmaf(sf.y, __uint_as_float(v[2 * j + 1]), acc[2 * j + 1]);
         }
       }
       tc_fence_before();
