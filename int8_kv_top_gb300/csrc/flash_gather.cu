@@ -210,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = f % kRing;
           if (!mbar_wait(&bars.k.full[slot], (f / kRing) & 1, status, &s_abort)) { ok = false; break; }
           tc_fence_after();
+          fence_proxy_async_smem();  // the fill's cp.async writes (generic proxy) before the MMA reads them
           const uint64_t a0 = sdesc_sw128(sK + slot * kSlotBytes, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -242,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = f % kRing;
           if (!mbar_wait(&bars.v.full[slot], (f / kRing) & 1, status, &s_abort)) { ok = false; break; }
           tc_fence_after();
+          fence_proxy_async_smem();
           // MN-major A: the half's two 64-dim atoms 16 KB apart (LBO), 8-cell groups 1 KB apart
           const uint64_t a0 = sdesc_sw128(sV + slot * kSlotBytes, kBlkBytes, 1024);
 #pragma unroll
