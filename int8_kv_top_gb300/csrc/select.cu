@@ -34,7 +34,7 @@ namespace qsa {
 namespace {
 
 // ----------------------------------------------------------------- workspace layout
-constexpr int kGM = 128, kGN = 64, kGK = 64, kGStages = 3;
+constexpr int kGM = 128, kGN = 128, kGK = 64, kGStages = 5;
 constexpr int kMaxCells = 65536;
 constexpr int kTkThreads = 512;
 constexpr int kCandCap = 2048;
@@ -211,13 +211,19 @@ __global__ void __launch_bounds__(256) prep_k_kernel(const int8_t* __restrict__ 
 }
 
 // ----------------------------------------------------------------- 2. score GEMM
-constexpr int kNtPerCtaMax = 32;               // at most 2048 cells per CTA
+// CTA: 128 rows x nt_per_cta tiles of 128 cells.  TMEM holds one M128 x N128 fp32 accumulator per
+// 64-dim scale block (4 x 128 columns).  The B operand is staged one 64-dim block at a time
+// ([128 cells][64] SW128, 16 KB) in a kGStages ring; per block the MMA issuer runs hi_b then
+// lo_b against the same codes (8 K16 steps) and commits that block's accumulator.  The epilogue
+// frees each block's accumulator as soon as it has loaded it, so the next tile's MMAs on block b
+// wait only for that load, not for the whole epilogue: no second accumulator set is needed.
+constexpr int kNtPerCtaMax = 16;               // at most 2048 cells per CTA
 constexpr int kSmemA = kGM * kD * 2 * 2;       // 128 KB: 8 k-blocks (hi_b, lo_b) of [128 rows][64] SW128
-constexpr int kSmemBStage = kGN * kD * 2;      // 32 KB: 4 k-blocks of [64 cells][64] SW128
+constexpr int kSmemBStage = kGN * kGK * 2;     // 16 KB: one 64-dim block of [128 cells][64] SW128
 constexpr int kScoreSmem = kSmemA + kGStages * kSmemBStage + 1024;
 
 struct __align__(8) ScoreBars {
-  uint64_t a_full, b_full[kGStages], b_empty[kGStages], acc_full[2], acc_empty[2], drain;
+  uint64_t a_full, b_full[kGStages], b_empty[kGStages], acc_full[kNB], acc_empty[kNB], drain;
 };
 
 constexpr int kScoreThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-11 epilogue
@@ -252,9 +258,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       mbar_init(&bars.b_full[i], 1);
       mbar_init(&bars.b_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.acc_full[i], 1);
-      mbar_init(&bars.acc_empty[i], 8);
+    for (int b = 0; b < kNB; ++b) {
+      mbar_init(&bars.acc_full[b], 1);
+      mbar_init(&bars.acc_empty[b], 8);  // the 8 epilogue warps, once they have loaded block b
     }
     mbar_init(&bars.drain, 1);
     fence_mbar_init();
@@ -269,6 +275,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const uint32_t tmem = s_tmem;
   uint8_t* sA = smem;
   uint8_t* sB = smem + kSmemA;
+  const int n_blocks = n_tiles * kNB;  // B stages this CTA consumes: (tile, 64-dim block)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -278,18 +285,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (int kb = 0; kb < 2 * kD / kGK; ++kb)
         tma_load_2d(sA + kb * (kGM * 128), &map_a, &bars.a_full, kb * kGK, g * T_pad + r0);
       int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % kGStages;
-        if (i >= kGStages && !mbar_wait(&bars.b_empty[st], ((i / kGStages) & 1) ^ 1, status, &s_abort)) break;
+      for (int j = 0; j < n_blocks; ++j) {
+        const int st = j % kGStages;
+        if (j >= kGStages && !mbar_wait(&bars.b_empty[st], ((j / kGStages) & 1) ^ 1, status, &s_abort)) break;
         mbar_arrive_expect_tx(&bars.b_full[st], kSmemBStage);
-        for (int kb = 0; kb < kD / kGK; ++kb)
-          tma_load_2d(sB + st * kSmemBStage + kb * (kGN * 128), &map_b, &bars.b_full[st], kb * kGK,
-                      g * n_pad + (nt_begin + i) * kGN);
-        issued = i + 1;
+        tma_load_2d(sB + st * kSmemBStage, &map_b, &bars.b_full[st], (j % kNB) * kGK,
+                    g * n_pad + (nt_begin + j / kNB) * kGN);
+        issued = j + 1;
       }
       mbar_wait(&bars.a_full, 0, status);
-      for (int i = max(0, issued - kGStages); i < issued; ++i)
-        mbar_wait(&bars.b_full[i % kGStages], (i / kGStages) & 1, status);
+      for (int j = max(0, issued - kGStages); j < issued; ++j)
+        mbar_wait(&bars.b_full[j % kGStages], (j / kGStages) & 1, status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -297,105 +303,117 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
       bool ok = mbar_wait(&bars.a_full, 0, status, &s_abort);
       tc_fence_after();
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int a = i & 1, st = i % kGStages;
-        if (i >= 2 && !mbar_wait(&bars.acc_empty[a], ((i >> 1) & 1) ^ 1, status, &s_abort)) { ok = false; break; }
-        if (!mbar_wait(&bars.b_full[st], (i / kGStages) & 1, status, &s_abort)) { ok = false; break; }
+      const uint64_t ad0 = sdesc_sw128(a0, 16, 1024);
+      for (int j = 0; ok && j < n_blocks; ++j) {
+        const int i = j / kNB, b = j % kNB, st = j % kGStages;
+        if (i >= 1 && !mbar_wait(&bars.acc_empty[b], (i - 1) & 1, status, &s_abort)) { ok = false; break; }
+        if (!mbar_wait(&bars.b_full[st], (j / kGStages) & 1, status, &s_abort)) { ok = false; break; }
         tc_fence_after();
-        const uint64_t ad0 = sdesc_sw128(a0, 16, 1024), bd0 = sdesc_sw128(b0 + st * kSmemBStage, 16, 1024);
+        const uint64_t bd0 = sdesc_sw128(b0 + st * kSmemBStage, 16, 1024);
 #pragma unroll
-        for (int b = 0; b < kNB; ++b)
+        for (int part = 0; part < 2; ++part)  // hi_b then lo_b against the same codes
 #pragma unroll
-          for (int part = 0; part < 2; ++part)  // hi_b then lo_b against the same codes
-#pragma unroll
-            for (int kk = 0; kk < kGK / 16; ++kk)
-              umma_ss(tmem + a * 256 + b * kGN, ad0 + (uint64_t)(((2 * b + part) * (kGM * 128) + kk * 32) >> 4),
-                      bd0 + (uint64_t)((b * (kGN * 128) + kk * 32) >> 4), idesc, (part > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kGK / 16; ++kk)
+            umma_ss(tmem + b * kGN, ad0 + (uint64_t)(((2 * b + part) * (kGM * 128) + kk * 32) >> 4),
+                    bd0 + (uint64_t)((kk * 32) >> 4), idesc, (part > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars.b_empty[st]);
-        umma_commit(&bars.acc_full[a]);
+        umma_commit(&bars.acc_full[b]);
       }
       umma_commit(&bars.drain);
       mbar_wait(&bars.drain, 0, status);
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // epilogue: warps 4-7 take cells 0-31 of each 64-cell tile, warps 8-11 cells 32-63
-    // the tile's fp16 K scales of group g, per accumulator set, block-major so that a block's 32
-    // cells come in as four 16-byte broadcast loads
-    __shared__ __align__(16) __half s_scale[2][kNB][kGN];
-    const int quarter = warp & 3, c0 = (warp >= 8) ? 32 : 0;
+    // epilogue: warps 4-7 take cells 0-63 of each 128-cell tile, warps 8-11 cells 64-127; thread
+    // = row.  The tile's K scales of group g are staged as fp32, block-major, one tile ahead, so
+    // that a block's 64 cells come in as sixteen 16-byte broadcast loads.
+    __shared__ __align__(16) float s_scale[2][kNB][kGN];
+    const int quarter = warp & 3, c0 = (warp >= 8) ? 64 : 0;
     const int et = tid - 128;  // 0..255
     const int r = r0 + quarter * 32 + lane;
     const int n_lim = n_base + T_sel;  // cells that exist for this call
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     bool dead = false;  // after a failed wait keep meeting the epilogue barrier, skip the work
-    const int sc_cell = et >> 2, sc_b = et & 3;  // this thread stages one scale per tile
-    auto load_scale = [&](int i) -> float {
-      const int c = (nt_begin + i) * kGN + sc_cell;
-      return (i < n_tiles && c < n_lim) ? __half2float(ksc[((size_t)c * kGroups + g) * kNB + sc_b]) : 0.f;
+    auto load_scales = [&](int i, float (&dst)[2]) {  // this thread stages two scales per tile
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int e = et + 256 * x, cell = e >> 2, b = e & 3;
+        const int c = (nt_begin + i) * kGN + cell;
+        dst[x] = (i < n_tiles && c < n_lim) ? __half2float(ksc[((size_t)c * kGroups + g) * kNB + b]) : 0.f;
+      }
     };
-    float sc_next = load_scale(0);
+    float sc_next[2];
+    load_scales(0, sc_next);
     for (int i = 0; i < n_tiles; ++i) {
       const int a = i & 1;
       const int n0 = (nt_begin + i) * kGN;
-      s_scale[a][sc_b][sc_cell] = __float2half_rn(sc_next);  // an fp16 value: exact
-      sc_next = load_scale(i + 1);  // one tile ahead: the load overlaps this tile's work
-      epilogue_bar();
-      if (!dead) dead = !mbar_wait_warp(&bars.acc_full[a], (i >> 1) & 1, status, &s_abort);
-      if (dead) continue;
-      tc_fence_after();
-      float acc[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+      for (int x = 0; x < 2; ++x) {
+        const int e = et + 256 * x;
+        s_scale[a][e & 3][e >> 2] = sc_next[x];
+      }
+      load_scales(i + 1, sc_next);  // one tile ahead: the loads overlap this tile's work
+      epilogue_bar();
+      float acc[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[j] = 0.f;
 #pragma unroll
       for (int b = 0; b < kNB; ++b) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + a * 256 + b * kGN + c0, v);
-        uint4 sv[4];  // this block's scales of the warpgroup's 32 cells
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) sv[q4] = reinterpret_cast<const uint4*>(&s_scale[a][b][c0])[q4];
+        if (!dead) dead = !mbar_wait_warp(&bars.acc_full[b], i & 1, status, &s_abort);
+        if (dead) continue;
+        tc_fence_after();
+        uint32_t v[2][32];
+        tmem_ld32(lane_base + b * kGN + c0, v[0]);
+        tmem_ld32(lane_base + b * kGN + c0 + 32, v[1]);
         tmem_wait_ld();
-        const __half2* sc2 = reinterpret_cast<const __half2*>(sv);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.acc_empty[b]);  // the next tile's block-b MMAs may start
+        const float4* sv = reinterpret_cast<const float4*>(&s_scale[a][b][c0]);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float2 sf = __half22float2(sc2[j]);
-          acc[2 * j] = fmaf(sf.x, __uint_as_float(v[2 * j]), acc[2 * j]);
-          acc[2 * j + 1] = fmaf(sf.y, __uint_as_float(v[2 * j + 1]), acc[2 * j + 1]);
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const float4 s4 = sv[q4];
+          const int j = 4 * q4;
+          acc[j] = fmaf(s4.x, __uint_as_float(v[j >> 5][j & 31]), acc[j]);
+          acc[j + 1] = fmaf(s4.y, __uint_as_float(v[(j + 1) >> 5][(j + 1) & 31]), acc[j + 1]);
+          acc[j + 2] = fmaf(s4.z, __uint_as_float(v[(j + 2) >> 5][(j + 2) & 31]), acc[j + 2]);
+          acc[j + 3] = fmaf(s4.w, __uint_as_float(v[(j + 3) >> 5][(j + 3) & 31]), acc[j + 3]);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.acc_empty[a]);
-      const int cell0 = n0 + c0;
-      // Lanes 2j and 2j + 1 hold adjacent rows: they swap 32-byte halves so that each holds 16
-      // cells (half g0) of both rows, and each 32-byte store of the warp then writes 16 row
-      // segments of 64 bytes instead of 32 scattered 16-byte pieces.
-      uint32_t w[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) w[j] = pack_half2(acc[2 * j] * sm_scale, acc[2 * j + 1] * sm_scale);
+      if (dead) continue;
+      // Per 32 cells, lanes 2j and 2j + 1 (adjacent rows) swap 32-byte halves so that each holds
+      // 16 cells of both rows, and each 32-byte store of the warp writes 16 row segments of 64
+      // bytes instead of 32 scattered 16-byte pieces.
       const int g0 = lane & 1;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t x0 = w[i], x1 = w[8 + i];
-        const uint32_t got = __shfl_xor_sync(0xffffffffu, g0 ? x0 : x1, 1);
-        w[i] = g0 ? got : x0;
-        w[8 + i] = g0 ? x1 : got;
-      }
-      const int cb = cell0 + 16 * g0;  // w[8 e .. 8 e + 7]: cells cb .. cb + 15 of row (r & ~1) + e
+      for (int h32 = 0; h32 < 2; ++h32) {
+        uint32_t w[16];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int rr = (r & ~1) + e;
-        const int nk = rr < T_sel ? n_base + rr + 1 : 0;  // that row's causal cells
-        if (cb < nk) {
-          __half* dp = scores + ((size_t)g * T_sel + rr) * n_pad + cb;
-          if (cb + 16 <= nk) {
-            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dp), "r"(w[8 * e]),
-                         "r"(w[8 * e + 1]), "r"(w[8 * e + 2]), "r"(w[8 * e + 3]), "r"(w[8 * e + 4]), "r"(w[8 * e + 5]),
-                         "r"(w[8 * e + 6]), "r"(w[8 * e + 7])
-                         : "memory");
-          } else {
-            const __half* hw = reinterpret_cast<const __half*>(w + 8 * e);
-            for (int j = 0; j < nk - cb; ++j) dp[j] = hw[j];
+        for (int j = 0; j < 16; ++j)
+          w[j] = pack_half2(acc[32 * h32 + 2 * j] * sm_scale, acc[32 * h32 + 2 * j + 1] * sm_scale);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          const uint32_t x0 = w[x], x1 = w[8 + x];
+          const uint32_t got = __shfl_xor_sync(0xffffffffu, g0 ? x0 : x1, 1);
+          w[x] = g0 ? got : x0;
+          w[8 + x] = g0 ? x1 : got;
+        }
+        const int cb = n0 + c0 + 32 * h32 + 16 * g0;  // w[8 e .. 8 e + 7]: cells cb .. cb + 15 of row (r & ~1) + e
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int rr = (r & ~1) + e;
+          const int nk = rr < T_sel ? n_base + rr + 1 : 0;  // that row's causal cells
+          if (cb < nk) {
+            __half* dp = scores + ((size_t)g * T_sel + rr) * n_pad + cb;
+            if (cb + 16 <= nk) {
+              asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dp), "r"(w[8 * e]),
+                           "r"(w[8 * e + 1]), "r"(w[8 * e + 2]), "r"(w[8 * e + 3]), "r"(w[8 * e + 4]),
+                           "r"(w[8 * e + 5]), "r"(w[8 * e + 6]), "r"(w[8 * e + 7])
+                           : "memory");
+            } else {
+              const __half* hw = reinterpret_cast<const __half*>(w + 8 * e);
+              for (int j = 0; j < nk - cb; ++j) dp[j] = hw[j];
+            }
           }
         }
       }
@@ -1136,8 +1154,9 @@ bool make_2d_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ou
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The score GEMM: CTAs of 128 rows x nt_per_cta 64-cell tiles; nt_per_cta shrinks for
-// short calls so that the grid still covers every SM twice.
+// The score GEMM: CTAs of 128 rows x nt_per_cta 128-cell tiles (one CTA per SM).  nt_per_cta is
+// the one in [4, kNtPerCtaMax] with the shortest span in tile times, ceil(CTAs / SMs) x nt_per_cta,
+// so that the last wave of CTAs is nearly full.
 cudaError_t launch_score_gemm(const WsLayout& L, int pos0, __half* qhi, __half* kc, const __half* ksc, __half* sc,
                               float sm_scale, int* status, cudaStream_t stream) {
   static bool attr_done[64] = {};
@@ -1159,9 +1178,16 @@ cudaError_t launch_score_gemm(const WsLayout& L, int pos0, __half* qhi, __half* 
     return cudaErrorInvalidValue;
   const int m_tiles = L.T_pad / kGM;
   const int n_tiles = L.n_pad / kGN;
-  const long long work = (long long)kGroups * m_tiles * n_tiles;
-  int nt_per = (int)((work + 2LL * sms - 1) / (2LL * sms));
-  nt_per = nt_per < 4 ? 4 : (nt_per > kNtPerCtaMax ? kNtPerCtaMax : nt_per);
+  int nt_per = kNtPerCtaMax;
+  long long best = -1;
+  for (int x = kNtPerCtaMax; x >= 4; --x) {
+    const long long ctas = (long long)kGroups * m_tiles * ((n_tiles + x - 1) / x);
+    const long long span = (ctas + sms - 1) / sms * x;
+    if (best < 0 || span < best) {
+      best = span;
+      nt_per = x;
+    }
+  }
   const int n_chunks = (n_tiles + nt_per - 1) / nt_per;
   const int n_base = pos0 + L.t_sel;  // n_kv of selected row r is n_base + r + 1
   score_kernel<<<kGroups * m_tiles * n_chunks, kScoreThreads, kScoreSmem, stream>>>(
