@@ -39,10 +39,14 @@ constexpr int kMaxCells = 65536;
 constexpr int kTkThreads = 512;
 constexpr int kCandCap = 2048;
 constexpr int kBandCap = 512;
-// hist 2 KB | qsum 2 KB | band keys + ids | candidate ids + keys | selection bitmap
+// hist 2 KB | qsum (padded) | band keys + ids | candidate ids + keys | selection bitmap | staged band rows
 constexpr int kSmallRows = 8;   // calls with at most this many selected rows score on the CUDA cores
 constexpr int kStageRows = 64;  // band cells whose code rows are staged in shared memory at once
-constexpr int kTopkSmem = 4096 + kBandCap * 20 + kCandCap * 6 + kMaxCells / 8 + kStageRows * (kD + 8);
+// Qsum_d sits at slot d + d / 32: the 8 lanes that form one cell's exact key read dims 32 j + t
+// (j = 0..7) at the same time, which without the pad would all fall in one bank.
+constexpr int kQsumSlots = kD + kD / 32;
+constexpr int kOffBandKey = 2048 + kQsumSlots * 8;  // 4160, 16-byte aligned
+constexpr int kTopkSmem = kOffBandKey + kBandCap * 20 + kCandCap * 6 + kMaxCells / 8 + kStageRows * (kD + 8);
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -576,7 +580,7 @@ __device__ __forceinline__ __int128 exact_key(const long long* __restrict__ s_qs
       for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int by = 0; by < 4; ++by)
-          acc += s_qsum[b * kBlk + i * 16 + j * 4 + by] * (long long)(int8_t)(ws[j] >> (8 * by));
+          acc += s_qsum[b * (kBlk + 2) + (i >> 1) + i * 16 + j * 4 + by] * (long long)(int8_t)(ws[j] >> (8 * by));
     }
     key += (__int128)half_int24(__half_as_ushort(srow[b])) * (__int128)acc;
   }
@@ -736,8 +740,8 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
                 int pos0, int K, float sm_scale, int* status) {
   extern __shared__ __align__(16) uint8_t topk_smem[];
   unsigned* s_hist = reinterpret_cast<unsigned*>(topk_smem);                   // [2][256]
-  long long* s_qsum = reinterpret_cast<long long*>(topk_smem + 2048);          // [256]
-  Key128* s_band_key = reinterpret_cast<Key128*>(topk_smem + 4096);            // [kBandCap]
+  long long* s_qsum = reinterpret_cast<long long*>(topk_smem + 2048);          // [kQsumSlots], padded
+  Key128* s_band_key = reinterpret_cast<Key128*>(topk_smem + kOffBandKey);     // [kBandCap]
   int* s_band_idx = reinterpret_cast<int*>(s_band_key + kBandCap);             // [kBandCap]
   int* s_cand_idx = s_band_idx + kBandCap;                                     // [kCandCap]
   uint16_t* s_cand_key = reinterpret_cast<uint16_t*>(s_cand_idx + kCandCap);   // [kCandCap]
@@ -761,7 +765,7 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
     const __half* qt = q + ((size_t)t * kHeads + g * kHPG) * kD + tid;
 #pragma unroll
     for (int h = 0; h < kHPG; ++h) sq += half_int24(__half_as_ushort(qt[h * kD]));
-    s_qsum[tid] = sq;
+    s_qsum[tid + (tid >> 5)] = sq;
   }
   for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
   for (int i = tid; i < (n_kv + 31) / 32; i += kTkThreads) s_bits[i] = 0u;
@@ -1013,7 +1017,7 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
           const uint4* src = reinterpret_cast<const uint4*>(s_stage + i * kD + j * 32);
           const uint4 xa = src[0], xb = src[1];
           const uint32_t wv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-          const long long* qs = s_qsum + j * 32;
+          const long long* qs = s_qsum + j * 33;  // dims 32 j .. 32 j + 31 (padded slots)
 #pragma unroll
           for (int u = 0; u < 8; ++u)
 #pragma unroll
@@ -1043,15 +1047,17 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
       }
       __syncthreads();  // the staging area is reused by the next round
     }
-    for (int i = tid; i < B; i += kTkThreads) {
+    // rank of each band cell by (key desc, index asc): a warp per cell, lanes over the band
+    for (int i = warp; i < B; i += nwarps) {
       const Key128 ki = s_band_key[i];
       const int ci = s_band_idx[i];
       int rank = 0;
-      for (int jj = 0; jj < B; ++jj) {
+      for (int jj = lane; jj < B; jj += 32) {
         const Key128 kj = s_band_key[jj];
         rank += key_gt(kj, ki) || (key_eq(kj, ki) && s_band_idx[jj] < ci);
       }
-      if (rank < need) atomicOr(&s_bits[ci >> 5], 1u << (ci & 31));
+      rank = __reduce_add_sync(0xffffffffu, rank);
+      if (lane == 0 && rank < need) atomicOr(&s_bits[ci >> 5], 1u << (ci & 31));
     }
   } else {
     // large band (many near-ties): exact radix select over the band, keys recomputed per
