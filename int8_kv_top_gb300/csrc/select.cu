@@ -37,16 +37,20 @@ namespace {
 constexpr int kGM = 128, kGN = 128, kGK = 64, kGStages = 5;
 constexpr int kMaxCells = 65536;
 constexpr int kTkThreads = 512;
+static_assert(kTkThreads >= 256, "top-k stages a 256-entry histogram and 256 Qsum dims one per thread");
 constexpr int kCandCap = 2048;
 constexpr int kBandCap = 512;
 // hist 2 KB | qsum (padded) | band keys + ids | candidate ids + keys | selection bitmap | staged band rows
 constexpr int kSmallRows = 8;   // calls with at most this many selected rows score on the CUDA cores
 constexpr int kStageRows = 64;  // band cells whose code rows are staged in shared memory at once
+// Staged code rows are kD + 16 bytes apart, so the four cells a warp keys at once start in
+// different banks.
+constexpr int kStageStride = kD + 16;
 // Qsum_d sits at slot d + d / 32: the 8 lanes that form one cell's exact key read dims 32 j + t
 // (j = 0..7) at the same time, which without the pad would all fall in one bank.
 constexpr int kQsumSlots = kD + kD / 32;
 constexpr int kOffBandKey = 2048 + kQsumSlots * 8;  // 4160, 16-byte aligned
-constexpr int kTopkSmem = kOffBandKey + kBandCap * 20 + kCandCap * 6 + kMaxCells / 8 + kStageRows * (kD + 8);
+constexpr int kTopkSmem = kOffBandKey + kBandCap * 20 + kCandCap * 6 + kMaxCells / 8 + kStageRows * (kStageStride + 8);
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -612,15 +616,15 @@ __device__ __forceinline__ int block_sum(int v, int* s_red) {
 // Find the bin holding the `need`-th largest element given a 256-bin histogram in smem
 // (bins scanned from high to low).  Returns the bin and sets *above = count in higher bins.
 __device__ __forceinline__ int find_bin_desc(const unsigned* hist, int need, int* above, int* s_tmp) {
-  // warp 0: lane l owns bins 255-8l .. 248-8l (descending)
+  // warp 0: lane l owns bins 255-8l .. 248-8l (descending), read as two 16-byte words
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    int cnt[8], sum = 0;
+    const uint4* h4 = reinterpret_cast<const uint4*>(hist + 248 - 8 * lane);
+    const uint4 lo4 = h4[0], hi4 = h4[1];  // bins 248-8l .. 251-8l, 252-8l .. 255-8l
+    const int cnt[8] = {(int)hi4.w, (int)hi4.z, (int)hi4.y, (int)hi4.x, (int)lo4.w, (int)lo4.z, (int)lo4.y, (int)lo4.x};
+    int sum = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      cnt[i] = (int)hist[255 - 8 * lane - i];
-      sum += cnt[i];
-    }
+    for (int i = 0; i < 8; ++i) sum += cnt[i];
     int incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -746,8 +750,8 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   int* s_cand_idx = s_band_idx + kBandCap;                                     // [kCandCap]
   uint16_t* s_cand_key = reinterpret_cast<uint16_t*>(s_cand_idx + kCandCap);   // [kCandCap]
   unsigned* s_bits = reinterpret_cast<unsigned*>(s_cand_key + kCandCap);       // [kMaxCells / 32]
-  int8_t* s_stage = reinterpret_cast<int8_t*>(s_bits + kMaxCells / 32);          // [kStageRows][256] codes
-  uint2* s_stage_sc = reinterpret_cast<uint2*>(s_stage + kStageRows * kD);       // [kStageRows] 4 fp16 scales
+  int8_t* s_stage = reinterpret_cast<int8_t*>(s_bits + kMaxCells / 32);          // [kStageRows][kStageStride] codes
+  uint2* s_stage_sc = reinterpret_cast<uint2*>(s_stage + kStageRows * kStageStride);  // [kStageRows] 4 fp16 scales
   __shared__ int s_red[64];
   __shared__ int s_tmp[8];
   __shared__ int s_cnt[2];          // 0: candidates, 1: band
@@ -759,6 +763,8 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   const int t = t_sel + r;
   const int n_kv = pos0 + t + 1;
   const __half* row = scores + ((size_t)g * T_sel + r) * n_pad;
+  // few-row calls: the row's high-byte histogram, loaded now so its latency overlaps the row's
+  const unsigned h1_pre = (hist1 != nullptr && tid < 256) ? __ldg(hist1 + ((size_t)g * T_sel + r) * 256 + tid) : 0u;
 
   if (tid < kD) {  // exact Qsum in units of 2^-24
     long long sq = 0;
@@ -908,8 +914,7 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
       __syncthreads();
       b2 = find_bin_desc(s_hist + 256, need_c - ab1, &ab2, s_tmp);
     } else if (hist1 != nullptr) {
-      const unsigned* h1 = hist1 + ((size_t)g * T_sel + r) * 256;
-      for (int i = tid; i < 256; i += kTkThreads) s_hist[i] = h1[i];
+      if (tid < 256) s_hist[tid] = h1_pre;
       __syncthreads();
       b1 = find_bin_desc(s_hist, K, &ab1, s_tmp);
       // low byte of the keys in bin b1, from the row held in registers
@@ -942,16 +947,13 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   }
 
   // ---- thresholds: surely in <=> key >= k_def, undecided <=> k_band <= key < k_def
-  if (warp == 0) {
+  if (warp < 2) {  // the two thresholds are searched by two warps at once
     const Bound bd = s_bound;
     const float tau = order_key_to_float(tau_key);
     const float Ut = bd.U(tau), Lt = bd.L(tau);
-    const uint32_t k0 = first_key_warp([&](uint32_t k) { return bd.L(order_key_to_float(k)) > Ut; });
-    const uint32_t k1 = first_key_warp([&](uint32_t k) { return bd.U(order_key_to_float(k)) >= Lt; });
-    if (lane == 0) {
-      s_thr[0] = k0;
-      s_thr[1] = k1;
-    }
+    const uint32_t kt = warp == 0 ? first_key_warp([&](uint32_t k) { return bd.L(order_key_to_float(k)) > Ut; })
+                                  : first_key_warp([&](uint32_t k) { return bd.U(order_key_to_float(k)) >= Lt; });
+    if (lane == 0) s_thr[warp] = kt;
   }
   __syncthreads();
   const uint32_t k_def = s_thr[0], k_band = s_thr[1];
@@ -997,7 +999,8 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
       const int nb = min(kStageRows, B - i0);
       for (int x = tid; x < nb * 16; x += kTkThreads) {
         const int c = s_band_idx[i0 + (x >> 4)];
-        cp_async16(s_stage + (x >> 4) * kD + (x & 15) * 16, kq + ((size_t)c * kGroups + g) * kD + (x & 15) * 16);
+        cp_async16(s_stage + (x >> 4) * kStageStride + (x & 15) * 16,
+                   kq + ((size_t)c * kGroups + g) * kD + (x & 15) * 16);
       }
       for (int x = tid; x < nb; x += kTkThreads) {
         const int c = s_band_idx[i0 + x];
@@ -1014,7 +1017,7 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
         const bool have = i < nb;
         long long part0 = 0, part1 = 0;
         if (have) {
-          const uint4* src = reinterpret_cast<const uint4*>(s_stage + i * kD + j * 32);
+          const uint4* src = reinterpret_cast<const uint4*>(s_stage + i * kStageStride + j * 32);
           const uint4 xa = src[0], xb = src[1];
           const uint32_t wv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
           const long long* qs = s_qsum + j * 33;  // dims 32 j .. 32 j + 31 (padded slots)
