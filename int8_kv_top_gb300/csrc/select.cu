@@ -758,7 +758,10 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   __shared__ uint32_t s_thr[2];     // order keys: surely-in threshold, band threshold
   __shared__ Bound s_bound;
 
-  const int r = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // rows are taken last-written first: the score kernel writes group 1's last rows last, and those
+  // are the ones most likely still in L2 when the first wave of this kernel starts
+  const int r = gridDim.x - 1 - blockIdx.x, g = gridDim.y - 1 - blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int nwarps = kTkThreads / 32;
   const int t = t_sel + r;
   const int n_kv = pos0 + t + 1;
