@@ -6,8 +6,9 @@
 // contract and delivered change).  The score of cell c for token t and group g is the sum
 // over the group's 12 heads of sm_scale * q . k^, equal scores going to the lower index.
 //
-// GB300 design (four launches on the caller's stream):
-//  1. prep_q:  Qsum = sum_h q over the group's 12 heads, exact in fp64, split as
+// GB300 design (four launches on the caller's stream; calls with at most kSmallRows selected
+// rows use two, score_small_kernel in place of 1 and 2):
+//  1. prep_q:  Qsum = sum_h q over the group's 12 heads, exact in 64-bit integers, split as
 //              hi = fp16(Qsum), lo = fp16(Qsum - hi); per 64-dim block the residual norm
 //              E_b = sum |Qsum - hi - lo| and H_b = sum (|hi| + |lo|).
 //     prep_k:  int8 K codes as fp16 (exact integers) for every cell a selected token can
@@ -15,7 +16,9 @@
 //  2. score:   tcgen05 GEMM with one TMEM accumulator per 64-dim scale block:
 //                S_b[t][c] = sum_{d in b} (hi + lo)[t][d] * kq[c][d]   (products exact in fp32)
 //              epilogue  s~[t][c] = fp16(sm_scale * sum_b ksc[c][b] * S_b[t][c]).
-//              128-row x 64-cell tiles, TMA-fed 3-stage ring, two accumulator sets.
+//              128-row x 128-cell tiles; B is staged one 64-dim block at a time in a TMA-fed
+//              ring, and each block's accumulator is released as soon as the epilogue has
+//              loaded it.
 //  3. topk:    one 512-thread CTA per (token, group) holds the row's scores in registers.
 //              |s~ - s| <= a + b|s~| rigorously (a: fp16 rounding of Qsum and fp32
 //              accumulation, from E_b, H_b, kmax; b: fp16 storage), and U(f) = f + a + b|f|,
