@@ -7,9 +7,29 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "ptx.cuh"
 
 namespace qsa {
+
+// Launch with programmatic stream serialization (see pdl_begin): the kernel may start while the
+// previous kernel on `stream` finishes, and waits for it inside pdl_begin().
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 constexpr int kGroups = 2;         // KV heads
 constexpr int kHPG = 12;           // query heads per KV head

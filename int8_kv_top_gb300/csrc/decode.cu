@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(
   __shared__ float s_s[kHPC][kChunk];           // logits
   __shared__ __align__(16) float4 s_e[kChunk];  // per cell: exp(s - m) of the 3 heads, .w unused
 
+  pdl_begin();
   const int k = blockIdx.x, g = blockIdx.y / kHS, hq = blockIdx.y % kHS, t = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h0 = g * kHPG + hq * kHPC;  // first query head of this CTA
@@ -185,9 +186,8 @@ cudaError_t launch_decode_partial(const __half* q, const int8_t* kq, const int8_
                                   cudaStream_t stream) {
   (void)n_cells;
   dim3 grid(chunk_cap, kGroups * kHS, N);
-  decode_partial_kernel<<<grid, kDecThreads, 0, stream>>>(q, kq, vq, ksc, vsc, ids, part, n_chunks, chunk_cap, pos0,
-                                                         p, status);
-  return cudaGetLastError();
+  return launch_pdl(decode_partial_kernel, grid, dim3(kDecThreads), 0, stream, q, kq, vq, ksc, vsc, ids, part, n_chunks,
+                    chunk_cap, pos0, p, status);
 }
 
 }  // namespace qsa

@@ -158,6 +158,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive or commit
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  pdl_begin();
 
   // Global super-chunk index gj (over this cluster's items) drives every ring's stage and phase.
   if (warp == 0 || warp == 2) {
@@ -577,9 +578,8 @@ cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const
   const float scale_log2 = a.p.sm_scale * kLog2e;
   const int n_items = (n_ttiles + 1) / 2 * 6;  // (pair of tiles, group, head quad)
   const int n_clusters = std::min(max_clusters[dev], n_items);  // persistent: each takes items in snake order
-  flash_dense_kernel<<<n_clusters * 2, kThreads, kSmemAlloc, stream>>>(mk, mv, mq, a.out, a.pos0, t_begin, t_end,
-                                                                      scale_log2, a.status);
-  return cudaGetLastError();
+  return launch_pdl(flash_dense_kernel, dim3(n_clusters * 2), dim3(kThreads), kSmemAlloc, stream, mk, mv, mq, a.out,
+                    a.pos0, t_begin, t_end, scale_log2, a.status);
 }
 
 }  // namespace qsa

@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  pdl_begin();
 
   // Raw ids of tile u for a producer warp: lane l holds slots l, l+32, l+64, l+96 (kNoSlot past
   // the end of the id row).
@@ -522,9 +523,8 @@ cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, cons
   const float scale_log2 = a.p.sm_scale * kLog2e;
   CUtensorMap mq;
   if (!make_q_map(&mq, a.q, a.T)) return cudaErrorInvalidValue;
-  flash_gather_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, khat, vhat, a.ids, a.out, a.pos0, t_begin, n_items,
-                                                              a.p.topk, scale_log2, a.status);
-  return cudaGetLastError();
+  return launch_pdl(flash_gather_kernel, dim3(grid), dim3(kThreads), kSmemAlloc, stream, mq, khat, vhat, a.ids, a.out,
+                    a.pos0, t_begin, n_items, a.p.topk, scale_log2, a.status);
 }
 
 }  // namespace qsa

@@ -23,6 +23,7 @@ constexpr int kMaxChunks = 1024;
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __restrict__ part,
                                                               const int32_t* __restrict__ n_chunks, int chunk_cap,
                                                               float* __restrict__ xp, int* status) {
+  pdl_begin();
   const int t = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
   const int tid = threadIdx.x, lane = tid & 31;
   const size_t cs = (size_t)kHeads * kPartStride;  // chunk stride
@@ -89,8 +90,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
 cudaError_t launch_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp, int* status,
                          cudaStream_t stream) {
   if (chunk_cap > kMaxChunks) return cudaErrorInvalidValue;
-  merge_kernel<<<N * kHeads, kMergeThreads, 0, stream>>>(part, n_chunks, chunk_cap, xp, status);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, dim3(N * kHeads), dim3(kMergeThreads), 0, stream, part, n_chunks, chunk_cap, xp,
+                    status);
 }
 
 }  // namespace qsa

@@ -15,6 +15,7 @@ namespace {
 __global__ void __launch_bounds__(256)
     dequant_mirror_kernel(const int8_t* __restrict__ kq, const int8_t* __restrict__ vq, const __half* __restrict__ ksc,
                           const __half* __restrict__ vsc, int n, __half* __restrict__ khat, __half* __restrict__ vhat) {
+  pdl_begin();
   const int g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * 8 + warp;
   if (c >= n) return;
@@ -39,8 +40,8 @@ size_t prefill_workspace_bytes(int T, int pos0) {
 cudaError_t launch_dequant_mirror(const int8_t* kq, const int8_t* vq, const __half* ksc, const __half* vsc, int n,
                                   __half* khat, __half* vhat, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
-  dequant_mirror_kernel<<<dim3((n + 7) / 8, kGroups), 256, 0, stream>>>(kq, vq, ksc, vsc, n, khat, vhat);
-  return cudaGetLastError();
+  return launch_pdl(dequant_mirror_kernel, dim3((n + 7) / 8, kGroups), dim3(256), 0, stream, kq, vq, ksc, vsc, n, khat,
+                    vhat);
 }
 
 }  // namespace qsa

@@ -124,6 +124,17 @@ __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t nthreads, bo
   return r != 0;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of this library is launched with programmatic stream serialization (launch_pdl),
+// so its launch may overlap the end of the previous kernel on the stream.  Each kernel calls
+// pdl_begin() before its first access to global memory: the wait returns once the previous grid
+// has completed and its writes are visible, so stream order holds for every read and write after
+// it.  Only CTA-local setup (shared-memory barriers, TMEM allocation, tensor map prefetch from
+// kernel parameters) may come before it.  No kernel triggers its dependents early: CTAs of the
+// next kernel waiting beside running ones slowed the latency-bound kernels (the one-CTA decode
+// top-k most).
+__device__ __forceinline__ void pdl_begin() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -14,6 +14,7 @@ namespace {
 
 __global__ void __launch_bounds__(256) quantize_kernel(const __half* __restrict__ x, int64_t n_blocks,
                                                        int8_t* __restrict__ xq, __half* __restrict__ xsc) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); blk < n_blocks; blk += warps) {
@@ -42,8 +43,7 @@ cudaError_t launch_quantize(const __half* x, int64_t n_rows, int8_t* xq, __half*
   if (n_blocks == 0) return cudaSuccess;
   const int64_t want = (n_blocks + 7) / 8;
   const int grid = (int)(want < 152 * 32 ? want : 152 * 32);
-  quantize_kernel<<<grid, 256, 0, stream>>>(x, n_blocks, xq, xsc);
-  return cudaGetLastError();
+  return launch_pdl(quantize_kernel, dim3(grid), dim3(256), 0, stream, x, n_blocks, xq, xsc);
 }
 
 }  // namespace qsa

@@ -177,6 +177,7 @@ __device__ __forceinline__ void write_eh(long long e, long long h_abs, float* __
 
 __global__ void __launch_bounds__(256) prep_q_kernel(const __half* __restrict__ q, int t_sel, int T_sel, int T_pad,
                                                      __half* __restrict__ qhl, float* __restrict__ eh) {
+  pdl_begin();
   const int r = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
   __half hi = __ushort_as_half(0), lo = __ushort_as_half(0);
   long long e = 0, h_abs = 0;
@@ -196,6 +197,7 @@ constexpr int kPrepKCtas = 1024;
 __global__ void __launch_bounds__(256) prep_k_kernel(const int8_t* __restrict__ kq, const __half* __restrict__ ksc,
                                                      int n_max, int n_pad, __half* __restrict__ kc,
                                                      float* __restrict__ kmax) {
+  pdl_begin();
   const int g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int blk = lane >> 3;
   float amax = 0.f;
@@ -260,7 +262,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int nt_begin = nch * nt_per_cta;
   const int nt_end = min(nt_begin + nt_per_cta, (n_kv_hi + kGN - 1) / kGN);
   const int n_tiles = nt_end - nt_begin;
-  if (n_tiles <= 0) return;  // uniform over the CTA, before any allocation
+  if (n_tiles <= 0) {  // uniform over the CTA, before any allocation
+    pdl_begin();         // still waits, so the grid never completes ahead of the kernel before it
+    return;
+  }
 
   if (tid == 0) {
     s_abort = 0;
@@ -284,6 +289,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  pdl_begin();
   uint8_t* sA = smem;
   uint8_t* sB = smem + kSmemA;
   const int n_blocks = n_tiles * kNB;  // B stages this CTA consumes: (tile, 64-dim block)
@@ -461,6 +467,7 @@ __global__ void __launch_bounds__(256) score_small_kernel(const int8_t* __restri
   __shared__ float s_max[8][kNB];
   __shared__ unsigned s_h1[kSmallRows][256];
   __shared__ long long s_e[8], s_h[8];
+  pdl_begin();
   const int g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < T_sel * 256; i += 256) s_h1[i >> 8][i & 255] = 0u;
   // the rows' Qsum hi/lo split (prep_q's arithmetic), thread = dim, all rows' loads in flight
@@ -745,6 +752,7 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
                 const __half* __restrict__ ksc, const float* __restrict__ eh, const float* __restrict__ kmax,
                 const unsigned* __restrict__ hist1, int32_t* __restrict__ ids, int t_sel, int T_sel, int n_pad,
                 int pos0, int K, float sm_scale, int* status) {
+  pdl_begin();
   extern __shared__ __align__(16) uint8_t topk_smem[];
   unsigned* s_hist = reinterpret_cast<unsigned*>(topk_smem);                   // [2][256]
   long long* s_qsum = reinterpret_cast<long long*>(topk_smem + 2048);          // [kQsumSlots], padded
@@ -1205,9 +1213,8 @@ cudaError_t launch_score_gemm(const WsLayout& L, int pos0, __half* qhi, __half* 
   }
   const int n_chunks = (n_tiles + nt_per - 1) / nt_per;
   const int n_base = pos0 + L.t_sel;  // n_kv of selected row r is n_base + r + 1
-  score_kernel<<<kGroups * m_tiles * n_chunks, kScoreThreads, kScoreSmem, stream>>>(
-      ma, mb, ksc, sc, L.T_sel, L.T_pad, L.n_pad, n_base, m_tiles, n_chunks, nt_per, sm_scale, status);
-  return cudaGetLastError();
+  return launch_pdl(score_kernel, dim3(kGroups * m_tiles * n_chunks), dim3(kScoreThreads), kScoreSmem, stream, ma, mb,
+                    ksc, sc, L.T_sel, L.T_pad, L.n_pad, n_base, m_tiles, n_chunks, nt_per, sm_scale, status);
 }
 
 }  // namespace
@@ -1236,13 +1243,16 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
   cudaError_t e = cudaMemsetAsync(kmax, 0, L.zero_bytes, stream);  // kmax and (few-row calls) the histograms
   if (e != cudaSuccess) return e;
   if (L.T_sel <= kSmallRows) {  // the few-rows path forms the Qsum split itself
-    score_small_kernel<<<dim3((L.n_max + 63) / 64, kGroups), 256, 0, stream>>>(
-        kq, ksc, q, L.t_sel, L.T_sel, L.n_max, L.n_pad, pos0 + L.t_sel, p.sm_scale, sc, kmax, hist1, eh);
+    e = launch_pdl(score_small_kernel, dim3((L.n_max + 63) / 64, kGroups), dim3(256), 0, stream, kq, ksc, q, L.t_sel,
+                   L.T_sel, L.n_max, L.n_pad, pos0 + L.t_sel, p.sm_scale, sc, kmax, hist1, eh);
+    if (e != cudaSuccess) return e;
   } else {
-    prep_q_kernel<<<dim3(L.T_pad, kGroups), 256, 0, stream>>>(q, L.t_sel, L.T_sel, L.T_pad, qhi, eh);  // hi/lo
-    prep_k_kernel<<<dim3(min(L.n_pad / 8, kPrepKCtas), kGroups), 256, 0, stream>>>(kq, ksc, L.n_max, L.n_pad, kc,
-                                                                                     kmax);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_pdl(prep_q_kernel, dim3(L.T_pad, kGroups), dim3(256), 0, stream, q, L.t_sel, L.T_sel, L.T_pad, qhi,
+                   eh);  // hi/lo
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(prep_k_kernel, dim3(min(L.n_pad / 8, kPrepKCtas), kGroups), dim3(256), 0, stream, kq, ksc, L.n_max,
+                   L.n_pad, kc, kmax);
+    if (e != cudaSuccess) return e;
     if ((e = launch_score_gemm(L, pos0, qhi, kc, ksc, sc, p.sm_scale, status, stream)) != cudaSuccess) return e;
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1251,10 +1261,9 @@ cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, 
   auto run = [&](auto kern) -> cudaError_t {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmem);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kTkThreads, kTopkSmem, stream>>>(sc, q, kq, ksc, eh, kmax, L.T_sel <= kSmallRows ? hist1 : nullptr,
-                                                  ids, L.t_sel, L.T_sel, L.n_pad, pos0,
-                                                  p.topk, p.sm_scale, status);
-    return cudaGetLastError();
+    const unsigned* h1 = L.T_sel <= kSmallRows ? hist1 : nullptr;
+    return launch_pdl(kern, grid, dim3(kTkThreads), kTopkSmem, stream, sc, q, kq, ksc, eh, kmax, h1, ids, L.t_sel,
+                      L.T_sel, L.n_pad, pos0, p.topk, p.sm_scale, status);
   };
   if (L.n_max <= 16 * kTkThreads) return run(topk_kernel<16>);
   if (L.n_max <= 32 * kTkThreads) return run(topk_kernel<32>);
