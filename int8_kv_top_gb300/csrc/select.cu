@@ -625,41 +625,49 @@ __device__ __forceinline__ int block_sum(int v, int* s_red) {
 
 // Find the bin holding the `need`-th largest element given a 256-bin histogram in smem
 // (bins scanned from high to low).  Returns the bin and sets *above = count in higher bins.
+// One warp: the bin (counting down from 255) that holds the need-th largest element of `hist`,
+// and how many elements lie in higher bins; bin -1 if there is none.  Lane l owns bins
+// 255-8l .. 248-8l, read as two 16-byte words.
+__device__ __forceinline__ void warp_find_bin(const unsigned* hist, int need, int lane, int& found, int& found_above) {
+  const uint4* h4 = reinterpret_cast<const uint4*>(hist + 248 - 8 * lane);
+  const uint4 lo4 = h4[0], hi4 = h4[1];  // bins 248-8l .. 251-8l, 252-8l .. 255-8l
+  const int cnt[8] = {(int)hi4.w, (int)hi4.z, (int)hi4.y, (int)hi4.x, (int)lo4.w, (int)lo4.z, (int)lo4.y, (int)lo4.x};
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sum += cnt[i];
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int run = incl - sum;  // elements in higher bins than this lane's first
+  found = -1;
+  found_above = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (found < 0 && run < need && run + cnt[i] >= need) {
+      found = 255 - 8 * lane - i;
+      found_above = run;
+    }
+    run += cnt[i];
+  }
+  const unsigned who = __ballot_sync(0xffffffffu, found >= 0);
+  if (who) {
+    const int src = __ffs(who) - 1;
+    found = __shfl_sync(0xffffffffu, found, src);
+    found_above = __shfl_sync(0xffffffffu, found_above, src);
+  }
+}
+
+// Block-wide: warp 0 searches, every thread gets the bin and the count above it.
 __device__ __forceinline__ int find_bin_desc(const unsigned* hist, int need, int* above, int* s_tmp) {
-  // warp 0: lane l owns bins 255-8l .. 248-8l (descending), read as two 16-byte words
   if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const uint4* h4 = reinterpret_cast<const uint4*>(hist + 248 - 8 * lane);
-    const uint4 lo4 = h4[0], hi4 = h4[1];  // bins 248-8l .. 251-8l, 252-8l .. 255-8l
-    const int cnt[8] = {(int)hi4.w, (int)hi4.z, (int)hi4.y, (int)hi4.x, (int)lo4.w, (int)lo4.z, (int)lo4.y, (int)lo4.x};
-    int sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sum += cnt[i];
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    int run = incl - sum;  // elements in higher bins than this lane's first
-    int found = -1, found_above = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (found < 0 && run < need && run + cnt[i] >= need) {
-        found = 255 - 8 * lane - i;
-        found_above = run;
-      }
-      run += cnt[i];
-    }
-    const unsigned who = __ballot_sync(0xffffffffu, found >= 0);
-    if (who) {
-      const int src = __ffs(who) - 1;
-      found = __shfl_sync(0xffffffffu, found, src);
-      found_above = __shfl_sync(0xffffffffu, found_above, src);
-    }
-    if (lane == 0) {
-      s_tmp[0] = found;
-      s_tmp[1] = found_above;
+    int f, fa;
+    warp_find_bin(hist, need, threadIdx.x, f, fa);
+    if (threadIdx.x == 0) {
+      s_tmp[0] = f;
+      s_tmp[1] = fa;
     }
   }
   __syncthreads();
@@ -667,6 +675,27 @@ __device__ __forceinline__ int find_bin_desc(const unsigned* hist, int need, int
   *above = s_tmp[1];
   __syncthreads();
   return b;
+}
+
+// Two independent searches at once: warp 0 on (h0, need0), warp 1 on (h1, need1).  A search whose
+// use flag is false (uniform) reports bin -1 and 0 above.
+__device__ __forceinline__ void find_bin_desc2(const unsigned* h0, int need0, bool use0, const unsigned* h1, int need1,
+                                               bool use1, int* b0, int* above0, int* b1, int* above1, int* s_tmp) {
+  const int w = threadIdx.x >> 5;
+  if (w < 2) {
+    int f = -1, fa = 0;
+    if (w == 0 ? use0 : use1) warp_find_bin(w == 0 ? h0 : h1, w == 0 ? need0 : need1, threadIdx.x & 31, f, fa);
+    if ((threadIdx.x & 31) == 0) {
+      s_tmp[2 * w] = f;
+      s_tmp[2 * w + 1] = fa;
+    }
+  }
+  __syncthreads();
+  *b0 = s_tmp[0];
+  *above0 = s_tmp[1];
+  *b1 = s_tmp[2];
+  *above1 = s_tmp[3];
+  __syncthreads();
 }
 
 // Histogram increment (shared-memory atomics resolve same-bin lanes in hardware).
@@ -843,8 +872,7 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
       warp_hist_add(c0 + 8 * m < n_kv, fp16_order_key(half_bits(w[m], 0)) >> 8, s_hist);
     __syncthreads();
     int ab_hi = 0, ab_lo = 0, b_hi = -1, b_lo = -1;
-    if (r_hi >= 1) b_hi = find_bin_desc(s_hist, r_hi, &ab_hi, s_tmp);
-    if (r_lo <= n_samp) b_lo = find_bin_desc(s_hist, r_lo, &ab_lo, s_tmp);
+    find_bin_desc2(s_hist, r_hi, r_hi >= 1, s_hist, r_lo, r_lo <= n_samp, &b_hi, &ab_hi, &b_lo, &ab_lo, s_tmp);
     for (int i = tid; i < 512; i += kTkThreads) s_hist[i] = 0u;
     __syncthreads();
 #pragma unroll
@@ -855,9 +883,11 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
       warp_hist_add(v && (int)(k >> 8) == b_lo, k & 0xFFu, s_hist + 256);
     }
     __syncthreads();
-    int dummy;
-    if (b_hi >= 0) key_hi = ((uint32_t)b_hi << 8) | (uint32_t)find_bin_desc(s_hist, r_hi - ab_hi, &dummy, s_tmp);
-    if (b_lo >= 0) key_lo = ((uint32_t)b_lo << 8) | (uint32_t)find_bin_desc(s_hist + 256, r_lo - ab_lo, &dummy, s_tmp);
+    int f_hi, f_lo, dummy0, dummy1;
+    find_bin_desc2(s_hist, r_hi - ab_hi, b_hi >= 0, s_hist + 256, r_lo - ab_lo, b_lo >= 0, &f_hi, &dummy0, &f_lo, &dummy1,
+                   s_tmp);
+    if (b_hi >= 0) key_hi = ((uint32_t)b_hi << 8) | (uint32_t)f_hi;
+    if (b_lo >= 0) key_lo = ((uint32_t)b_lo << 8) | (uint32_t)f_lo;
     key_hi = min(key_hi, 0xFBFFu);
     key_lo = max(key_lo, 0x0400u);
   }
