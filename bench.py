@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -91,9 +92,11 @@ def read_peaks():
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
-    def __init__(self, index, path):
+    def __init__(self, index, path, keep=True):
         self.path = path
+        self.keep = keep  # False: the CSV is a temporary file, removed once read
         self.proc = None
+        self.f = None
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -101,8 +104,18 @@ class ClockSampler:
             self.f = open(path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={q}", "--format=csv,noheader",
                                           "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
-        except Exception:
+        except Exception:  # no nvidia-smi: no clock record
             self.proc = None
+            if self.f:
+                self.f.close()
+            self._discard()
+
+    def _discard(self):
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
 
     def stop(self):
         if self.proc is None:
@@ -113,6 +126,12 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
+        try:
+            return self._summary()
+        finally:
+            self._discard()
+
+    def _summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
@@ -248,8 +267,10 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
     # ---- timed region: K steps, barrier + sync on both sides
-    sampler = ClockSampler(local_rank, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
-        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None
+    # nvidia-smi samples of the timed region go to --clocks-csv if given, else to a temporary file
+    clocks_path = args.clocks_csv.replace("{rank}", str(rank)) if args.clocks_csv else \
+        os.path.join(tempfile.gettempdir(), f"qsa_bench_clocks_rank{rank}_{os.getpid()}.csv")
+    sampler = ClockSampler(local_rank, clocks_path, keep=bool(args.clocks_csv))
     all_marks = []
     sec_ms = [0.0, 0.0, 0.0]
     if dist:
@@ -542,6 +563,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager API calls instead of CUDA graph replays")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="also keep the nvidia-smi samples of the timed region in this CSV ({rank} is replaced)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
