@@ -1,6 +1,7 @@
 // Shared constants, the int8 -> fp16 dequantisation step and the internal launcher
 // interface between the C ABI (api.cu) and the kernel translation units.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>

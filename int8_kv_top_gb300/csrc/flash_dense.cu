@@ -552,12 +552,14 @@ bool make_q_map(CUtensorMap* map, const __half* q, int T) {
 cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
                                cudaStream_t stream) {
   if (t_end <= t_begin) return cudaSuccess;
-  // per device: the shared-memory attribute and how many CTA pairs fit on the GPU at once
-  static int max_clusters[64] = {};
+  // per device, set once (0 = not yet): the shared-memory attribute and how many CTA pairs fit on
+  // the GPU at once; threads that race here both set the same attribute and store the same count
+  static std::atomic<int> max_clusters[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64) return cudaErrorInvalidDevice;
-  if (max_clusters[dev] == 0) {
+  int n_clusters_max = max_clusters[dev].load(std::memory_order_acquire);
+  if (n_clusters_max == 0) {
     cudaError_t e = cudaFuncSetAttribute(flash_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -568,7 +570,8 @@ cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const
     e = cudaOccupancyMaxActiveClusters(&nc, flash_dense_kernel, &cfg);
     if (e != cudaSuccess) return e;
     if (nc < 1) return cudaErrorInvalidConfiguration;
-    max_clusters[dev] = nc;
+    max_clusters[dev].store(nc, std::memory_order_release);
+    n_clusters_max = nc;
   }
   const int n = a.pos0 + a.T;  // cells in the mirror
   CUtensorMap mk, mv, mq;
@@ -577,7 +580,7 @@ cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const
   const int n_ttiles = (t_end - t_begin + kTok - 1) / kTok;
   const float scale_log2 = a.p.sm_scale * kLog2e;
   const int n_items = (n_ttiles + 1) / 2 * 6;  // (pair of tiles, group, head quad)
-  const int n_clusters = std::min(max_clusters[dev], n_items);  // persistent: each takes items in snake order
+  const int n_clusters = std::min(n_clusters_max, n_items);  // persistent: each takes items in snake order
   return launch_pdl(flash_dense_kernel, dim3(n_clusters * 2), dim3(kThreads), kSmemAlloc, stream, mk, mv, mq, a.out,
                     a.pos0, t_begin, t_end, scale_log2, a.status);
 }

@@ -507,18 +507,21 @@ bool make_q_map(CUtensorMap* map, const __half* q, int T) {
 cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
                                 cudaStream_t stream) {
   if (t_end <= t_begin) return cudaSuccess;
-  static bool attr_done[64] = {};
-  static int n_sms[64] = {};
+  // per device, set once (0 = not yet): the shared-memory attribute is set and the SM count read;
+  // threads that race here both set the same attribute and store the same count
+  static std::atomic<int> n_sms[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  int sms = n_sms[dev].load(std::memory_order_acquire);
+  if (sms == 0) {
     cudaError_t e = cudaFuncSetAttribute(flash_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
-    cudaDeviceGetAttribute(&n_sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    attr_done[dev] = true;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (sms < 1) return cudaErrorInvalidConfiguration;
+    n_sms[dev].store(sms, std::memory_order_release);
   }
   const int n_items = (t_end - t_begin) * kGroups;
-  const int sms = (dev < 64 && n_sms[dev] > 0) ? n_sms[dev] : 148;
   const int grid = n_items < sms ? n_items : sms;
   const float scale_log2 = a.p.sm_scale * kLog2e;
   CUtensorMap mq;

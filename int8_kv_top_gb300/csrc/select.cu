@@ -1212,19 +1212,22 @@ bool make_2d_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ou
 // so that the last wave of CTAs is nearly full.
 cudaError_t launch_score_gemm(const WsLayout& L, int pos0, __half* qhi, __half* kc, const __half* ksc, __half* sc,
                               float sm_scale, int* status, cudaStream_t stream) {
-  static bool attr_done[64] = {};
-  static int n_sms[64] = {};
+  // per device, set once (0 = not yet): the shared-memory attribute is set and the SM count read;
+  // threads that race here both set the same attribute and store the same count
+  static std::atomic<int> n_sms[64];
   int dev = 0;
   cudaGetDevice(&dev);
+  if (dev >= 64) return cudaErrorInvalidDevice;
   cudaError_t e;
-  if (dev < 64 && !attr_done[dev]) {
+  int sms = n_sms[dev].load(std::memory_order_acquire);
+  if (sms == 0) {
     if ((e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem)) !=
         cudaSuccess)
       return e;
-    cudaDeviceGetAttribute(&n_sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    attr_done[dev] = true;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (sms < 1) return cudaErrorInvalidConfiguration;
+    n_sms[dev].store(sms, std::memory_order_release);
   }
-  const int sms = (dev < 64 && n_sms[dev] > 0) ? n_sms[dev] : 148;
   CUtensorMap ma, mb;
   if (!make_2d_map(&ma, qhi, 2 * kD, (uint64_t)kGroups * L.T_pad, kGK, kGM) ||
       !make_2d_map(&mb, kc, kD, (uint64_t)kGroups * L.n_pad, kGK, kGN))
