@@ -91,3 +91,23 @@ def test_select_rejects_missing_workspace(lib):
         assert rc == qsa.QSA_ERR_WORKSPACE
     # under the threshold nothing is needed or launched
     assert lib.qsa_select(P(FAKE), P(FAKE), P(FAKE), 100, 4, 0, None, None, 0, None, None) == qsa.QSA_OK
+
+
+def test_select_workspace_covers_the_score_rows(lib):
+    # the workspace holds (at least) the fp16 score row of every selected token and group, one row
+    # per token whose n_kv = pos0 + t + 1 exceeds identity_max, padded to whole 256-cell blocks;
+    # it grows with T and pos0, and is a whole number of 1 KB blocks
+    prev = {}
+    for pos0 in (2040, 8192, 30000):
+        for T in (1, 8, 9, 64, 512, 1984):
+            n = pos0 + T
+            need = lib.qsa_select_workspace_bytes(T, pos0, n, None)
+            t_sel = max(0, 2051 - pos0)
+            T_sel = max(0, T - t_sel)
+            n_pad = -(-n // 256) * 256
+            assert need >= 2 * T_sel * n_pad * 2, (T, pos0)
+            assert need % 1024 == 0
+            if pos0 in prev:
+                assert need >= prev[pos0], (T, pos0)
+            prev[pos0] = need
+    assert lib.qsa_select_workspace_bytes(512, 30000, 30512, None) >= lib.qsa_select_workspace_bytes(512, 8192, 8704, None)
