@@ -16,6 +16,10 @@
  *    and one device status word per device (see qsa_check_device_status).
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the
  *    legacy default stream) and never synchronize, except qsa_check_device_status.
+ *    Kernels are launched with programmatic stream serialization: a kernel may be
+ *    scheduled while the work before it on the stream finishes, but it waits for that
+ *    work to complete before it reads or writes any memory, so ordering against the
+ *    caller's earlier and later work on the stream is as with ordinary launches.
  *  - Return value: QSA_OK, or a negative QSA_ERR_* code with qsa_last_error() set.
  *    Argument errors are detected on the host before anything is launched.
  *
