@@ -4,9 +4,12 @@ One step = 12 QSA layers (distinct, seeded synthetic buffers per layer) of each 
   A  prefill  T=1984 at pos0=0      (identity: every causal cell)       qsa_flash_prefill
   B  prefill  T=1984 at pos0=30000  (31,984-cell cache, top-2048)       qsa_select + qsa_flash_prefill
   C  decode   N=1 at P=8192         (top-2048, 64-cell split)           qsa_select + qsa_decode_partial + qsa_merge
-value = prefill tokens per second per layer over the whole step: (1984 + 1984) * 12 / (12 * step time).
+value = identity-prefill tokens per second per layer (T=1984, the pages' own convention: tokens of
+the window / time of one layer), from the A part of the timed steps, times the number of replicas.
 The timed steps replay one CUDA graph per workload (captured from the same API calls); --eager
-times the calls themselves.
+times the calls themselves.  After the timed steps, every configuration of the workload list is
+timed on its own (CUDA graphs of the API calls, L2 flushed before each replay) and reported under
+"configs" with the per-call roofline fractions.
 
 python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 Under torchrun (N > 1) every rank runs the same step on its own GPU (replicas, weak scaling)
@@ -34,7 +37,7 @@ POS0_B = 30000
 N_DEC, P_DEC = 1, 8192
 HEADS, D = 24, 256
 METRIC = "prefill tokens/s per QSA layer (T=1984) + decode us/token; % tensor/HBM roofline"
-UNIT = "tokens/s per layer"
+UNIT = "tokens/s per layer (identity prefill T=1984)"
 
 
 def flops_prefill(T, pos0, topk=2048, idmax=2051):
@@ -74,10 +77,10 @@ def max_over_ranks(x, dist, device):
     return float(t.item())
 
 
-def whole_job_rate(ms_per_step, world):
-    """Prefill tokens/s per layer of the whole job: each of `world` replicas runs the full step
-    (2 x 1984 prefill tokens in each of the 12 layers) in ms_per_step (the max over ranks)."""
-    return 2 * T_PREFILL * LAYERS / (ms_per_step * 1e-3) / LAYERS * world
+def whole_job_rate(ms_per_layer_set, world):
+    """Identity-prefill tokens/s per layer of the whole job: each of `world` replicas runs the 12
+    identity-prefill layers of T=1984 tokens in ms_per_layer_set (the max over ranks)."""
+    return T_PREFILL / (ms_per_layer_set * 1e-3 / LAYERS) * world
 
 
 def read_peaks():
@@ -351,11 +354,14 @@ def run_ours(args, rank, world, local_rank):
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = read_peaks()
     flopA = flops_prefill(T_PREFILL, 0)
     flopB = flops_prefill(T_PREFILL, POS0_B)
+    # kernels are timed inside steps of about a millisecond or less: the burst peaks apply
     per_launch = {
         "dense_prefill": {"bound": "tensor", "achieved": flopA / (sec["A"] / LAYERS * 1e-3) / 1e12,
-                          "peak": bf16_tf_sus, "unit": "TFLOP/s"},
+                          "peak": bf16_tf, "unit": "TFLOP/s",
+                          "call": "qsa_flash_prefill T=1984 pos0=0 (fp16 mirror + flash_dense_kernel), graph-timed"},
         "gather_prefill": {"bound": "tensor", "achieved": flopB / (fam["gather_prefill"] / LAYERS * 1e-3) / 1e12,
-                           "peak": bf16_tf_sus, "unit": "TFLOP/s",
+                           "peak": bf16_tf, "unit": "TFLOP/s",
+                           "call": "qsa_flash_prefill T=1984 pos0=30000 (fp16 mirror + flash_gather_kernel), eager",
                            # the selected rows are gathered from L2: T x 2 groups x 2048 cells x 1 KB (K^ + V^ fp16)
                            "l2_gather_gbs": T_PREFILL * 2 * 2048 * 1024 / (fam["gather_prefill"] / LAYERS * 1e-3) / 1e9},
     }
@@ -363,32 +369,31 @@ def run_ours(args, rank, world, local_rank):
         v["frac"] = v["achieved"] / v["peak"]
     for k, v in per_launch.items():
         v["traffic"] = recorded_traffic(KERNEL_OF_FAMILY[k])
-    dominant = max(("dense_prefill", "gather_prefill", "select_B"), key=lambda k: fam[k])
-    if dominant == "select_B":
-        # select moves the score matrix through HBM: written once (fp16) and read once, plus K codes
-        T_sel = T_PREFILL
-        n_avg = POS0_B + (T_PREFILL + 1) / 2
-        bytes_sel = 2 * T_sel * n_avg * 2 * 2 + 2 * nB * (256 + 8) + 2 * nB * 512
-        roof = {"bound": "hbm", "achieved": bytes_sel / (fam["select_B"] / LAYERS * 1e-3) / 1e9, "peak": hbm_gbs,
-                "unit": "GB/s", "kernel": "qsa_select (4 launches)"}
-        roof["frac"] = roof["achieved"] / roof["peak"]
-    else:
-        roof = dict(per_launch[dominant])
-        roof["kernel"] = dominant
-    roof["traffic"] = recorded_traffic(KERNEL_OF_FAMILY.get(dominant, ""))
+    dominant = max(("dense_prefill", "gather_prefill"), key=lambda k: fam[k])
+    roof = dict(per_launch[dominant])
+    roof["kernel"] = KERNEL_OF_FAMILY[dominant]
     roof["traffic_unit"] = "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"
-    roof["peak_source"] = f"{peak_src}, sustained bf16 (f16 same rate)" if roof["unit"] == "TFLOP/s" else peak_src
+    roof["peak_source"] = f"{peak_src}, burst bf16 (f16 same rate)"
 
-    value = whole_job_rate(ms_step, world)
+    configs = None
+    if not args.no_configs:
+        configs = measure_configs(torch, qsa, synth, device, stream, (hbm_gbs, bf16_tf), A, B)
+        for k in ("select_prefill", "decode_select", "decode_partial", "merge"):
+            if k in configs.get("hbm_calls", {}):
+                per_launch[k] = configs["hbm_calls"][k]
+
+    value = whole_job_rate(max_over_ranks(sec["A"], dist, device), world)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 operands, f32 accumulate", "data": "synthetic (seeded; q~N(0,1) fp16, int8 K/V uniform "
         "[-127,127], fp16 scales U[0.005,0.02])",
-        "config": {"workload": "12 QSA layers x {prefill T=1984 pos0=0 (identity); prefill T=1984 pos0=30000 "
-                               "(31984-cell cache, top-2048); decode N=1 P=8192}", "layers": LAYERS,
+        "config": {"workload": "prefill T=1984 pos0=0, 12 QSA layers (identity ids; the value); each timed step "
+                               "also runs 12 layers of prefill T=1984 pos0=30000 (31984-cell cache, top-2048) and "
+                               "12 layers of decode N=1 P=8192", "layers": LAYERS,
                    "heads": "2 KV x 12 q, dim 256", "l2": "inputs larger than L2 (12 distinct layer buffer sets)",
                    "parallelism": f"replicas x{world}"},
+        "value_definition": "T / (time of one identity-prefill layer), T = 1984, times replicas",
         "breakdown_ms_per_step": fam,
         "breakdown_timing": "eager calls, CUDA events between them",
         "timing": "CUDA graph replay per workload" if graphs else "eager calls",
@@ -397,22 +402,218 @@ def run_ours(args, rank, world, local_rank):
         "prefill_selected_us_per_layer": sec["B"] / LAYERS * 1e3,
         "decode_us_per_token_per_layer": sec["C"] / LAYERS * 1e3 / N_DEC,
         "roofline": roof, "roofline_per_kernel": per_launch,
+        "configs": configs,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks, "e2e": e2e,
     }
     return line
 
 
+def _graph_us(torch, device, stream, fn, reps, flush):
+    """fn() captured in one CUDA graph, replayed `reps` times, each replay after an L2 flush (a
+    256 MB write) outside the timed events.  Returns (median, min) replay time in microseconds."""
+    fn()
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize(device)
+    evs = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize(device)
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    del g
+    return statistics.median(us), us[0]
+
+
+def _roof(achieved, peak, unit, bound):
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak}
+
+
+def measure_configs(torch, qsa, synth, device, stream, peaks, A, B, reps=10):
+    """Every configuration of the workload list timed on its own, with the per-call roofline.
+
+    0: prefill T=96 pos0=0, 1 layer; 1: T=512 pos0=0, 12 layers; 2: T=1984 pos0=0, 12 layers;
+    3: T=1984 pos0=30000 over 31,984 cells, select and prefill, 12 layers; 4: decode N in {1, 4} x
+    P in {512, 2048, 8192}, select / partial / merge and their total, 12 layers.  Tensor fractions
+    count only causal or selected cells; HBM fractions count the bytes the method must move, each
+    needed cell once per call (distinct (cell, group) rows, from the ids the call produced)."""
+    hbm_gbs, tf_burst = peaks
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    res = {"timing": "CUDA graph of the API calls over 12 distinct layer buffer sets (1 for config 0); median of "
+                     f"{reps} replays, L2 flushed (256 MB write) before each replay outside the timed events",
+           "peaks": {"hbm_gbs": hbm_gbs, "bf16_tflops_burst": tf_burst}}
+    gt = lambda fn: _graph_us(torch, device, stream, fn, reps, flush)  # noqa: E731
+    up = lambda inp: {k: torch.from_numpy(v).to(device) for k, v in inp.items()}  # noqa: E731
+
+    def prefill_set(T, pos0, bufs, ids=None):
+        n = pos0 + T
+        outs = [torch.empty((T, HEADS, D), dtype=torch.float16, device=device) for _ in bufs]
+        ws = torch.empty(qsa.qsa_flash_prefill_workspace_bytes(T, pos0, n), dtype=torch.uint8, device=device)
+
+        def fn():
+            for l, d in enumerate(bufs):
+                qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n, T, pos0,
+                                      None if ids is None else ids[l], outs[l], ws)
+        return fn
+
+    def prefill_entry(T, pos0, layers, med, mn):
+        fl = flops_prefill(T, pos0)
+        per_layer = med / layers
+        return {"T": T, "pos0": pos0, "layers": layers, "us_per_layer": per_layer, "us_per_layer_min": mn / layers,
+                "ms_per_layers": med * 1e-3, "tokens_per_s_per_layer": T / (per_layer * 1e-6),
+                "gflop_per_layer": fl / 1e9,
+                "tensor": _roof(fl / (per_layer * 1e-6) / 1e12, tf_burst, "TFLOP/s", "tensor")}
+
+    # configs 0-2: identity prefill
+    b0 = [up(synth.layer_inputs(96, 96, seed=5))]
+    res["config0"] = prefill_entry(96, 0, 1, *gt(prefill_set(96, 0, b0)))
+    b1 = [up(synth.layer_inputs(512, 512, seed=5 + l)) for l in range(LAYERS)]
+    res["config1"] = prefill_entry(512, 0, LAYERS, *gt(prefill_set(512, 0, b1)))
+    res["config2"] = prefill_entry(T_PREFILL, 0, LAYERS, *gt(prefill_set(T_PREFILL, 0, A)))
+    del b0, b1
+
+    # config 3: select, then the gathered prefill, and both
+    nB = POS0_B + T_PREFILL
+    idsB = [torch.empty((T_PREFILL, 2, 2048), dtype=torch.int32, device=device) for _ in range(LAYERS)]
+    wsB = torch.empty(qsa.qsa_select_workspace_bytes(T_PREFILL, POS0_B, nB), dtype=torch.uint8, device=device)
+
+    def sel3():
+        for l, d in enumerate(B):
+            qsa.qsa_select(d["q"], d["kq"], d["ksc"], nB, T_PREFILL, POS0_B, idsB[l], wsB)
+    fl3 = prefill_set(T_PREFILL, POS0_B, B, idsB)
+    s_med, s_min = gt(sel3)
+    f_med, f_min = gt(fl3)
+    b_med, b_min = gt(lambda: (sel3(), fl3()))
+    e3 = prefill_entry(T_PREFILL, POS0_B, LAYERS, b_med, b_min)
+    e3["n_cells"] = nB
+    sel_bytes = nB * 2 * 264 + T_PREFILL * HEADS * D * 2 + T_PREFILL * 2 * 2048 * 4
+    e3["select_us_per_layer"] = s_med / LAYERS
+    e3["select_hbm"] = _roof(sel_bytes / (s_med / LAYERS * 1e-6) / 1e9, hbm_gbs, "GB/s", "hbm")
+    e3["select_hbm"]["bytes"] = sel_bytes
+    e3["select_hbm"]["bytes_note"] = ("K codes and scales of every cell (both groups), q, ids; the fp16 score "
+                                      "matrix this implementation writes and reads back is not counted")
+    e3["select_tensor"] = _roof(2 * 2 * (POS0_B * T_PREFILL + T_PREFILL * (T_PREFILL + 1) // 2) * 256
+                                / (s_med / LAYERS * 1e-6) / 1e12, tf_burst, "TFLOP/s", "tensor")
+    e3["select_tensor"]["flop_note"] = "Qsum form: 2 x 256 per (token, group, causal cell)"
+    e3["flash_us_per_layer"] = f_med / LAYERS
+    e3["flash_tensor"] = _roof(flops_prefill(T_PREFILL, POS0_B) / (f_med / LAYERS * 1e-6) / 1e12, tf_burst,
+                               "TFLOP/s", "tensor")
+    res["config3"] = e3
+    hbm_calls = {"select_prefill": dict(e3["select_hbm"], call="qsa_select T=1984 pos0=30000")}
+
+    # config 4: decode
+    cap = qsa.chunk_cap_for()
+    dec = {}
+    for N in (1, 4):
+        for P in (512, 2048, 8192):
+            n = P + N
+            bufs = [up(synth.layer_inputs(N, n, seed=2000 + 10 * N + P + l)) for l in range(LAYERS)]
+            ids = [torch.full((N, 2, 2048), -1, dtype=torch.int32, device=device) for _ in range(LAYERS)]
+            part = [torch.empty((N, cap, HEADS, 258), device=device) for _ in range(LAYERS)]
+            nch = [torch.empty(N, dtype=torch.int32, device=device) for _ in range(LAYERS)]
+            xp = [torch.empty((N, HEADS, D), device=device) for _ in range(LAYERS)]
+            wsz = qsa.qsa_select_workspace_bytes(N, P, n)
+            ws = torch.empty(max(wsz, 16), dtype=torch.uint8, device=device)
+            any_sel = n > 2051
+
+            def fsel():
+                for l, d in enumerate(bufs):
+                    qsa.qsa_select(d["q"], d["kq"], d["ksc"], n, N, P, ids[l], ws)
+
+            def fpart():
+                for l, d in enumerate(bufs):
+                    qsa.qsa_decode_partial(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n, N, P,
+                                           ids[l] if any_sel else None, part[l], nch[l], cap)
+
+            def fmerge():
+                for l in range(LAYERS):
+                    qsa.qsa_merge(part[l], nch[l], N, cap, xp[l])
+            fsel()
+            fpart()
+            torch.cuda.synchronize(device)
+            qsa.qsa_check_device_status()
+            # distinct (cell, group) rows each call must read, and the partial chunks it writes
+            ids0 = ids[0].cpu().numpy()
+            rows, chunks = 0, 0
+            for g in range(2):
+                cells = set()
+                for t in range(N):
+                    n_kv = P + t + 1
+                    if n_kv <= 2051:
+                        cells.update(range(n_kv))
+                        chunks += (n_kv + 63) // 64 if g == 0 else 0
+                    else:
+                        cells.update(int(c) for c in ids0[t, g])
+                        chunks += 2048 // 64 if g == 0 else 0
+                rows += len(cells)
+            n_sel_tok = sum(1 for t in range(N) if P + t + 1 > 2051)
+            by_sel = n * 2 * 264 + N * HEADS * D * 2 + n_sel_tok * 2 * 2048 * 4 if any_sel else 0
+            by_part = rows * 528 + N * HEADS * D * 2 + chunks * HEADS * 258 * 4
+            by_merge = chunks * HEADS * 258 * 4 + N * HEADS * D * 4
+            e = {"N": N, "P": P}
+            for name, fn, by in (("select", fsel, by_sel), ("partial", fpart, by_part), ("merge", fmerge, by_merge)):
+                if name == "select" and not any_sel:
+                    e[name] = {"us_per_call": 0.0, "note": "no token above the identity threshold: nothing launched"}
+                    continue
+                med, _ = gt(fn)
+                per_call = med / LAYERS
+                e[name] = {"us_per_call": per_call, "us_per_token": per_call / N, "bytes": by,
+                           "hbm": _roof(by / (per_call * 1e-6) / 1e9, hbm_gbs, "GB/s", "hbm")}
+            med, _ = gt(lambda: (fsel() if any_sel else None, fpart(), fmerge()))
+            # the layer as a whole: K of every cell once (selection), V of the selected rows (K and V of
+            # every cell when no token selects), q, the merged output and the ids
+            kv_bytes = n * 2 * 264 + rows * 264 if any_sel else rows * 528
+            tot_bytes = kv_bytes + N * HEADS * D * 2 + N * HEADS * D * 4 + n_sel_tok * 2 * 2048 * 4
+            e["total"] = {"us_per_call": med / LAYERS, "us_per_token_per_layer": med / LAYERS / N,
+                          "bytes": tot_bytes, "bytes_note": "each needed input row read once, the merged output "
+                          "and the ids written once (partials between the calls not counted)",
+                          "hbm": _roof(tot_bytes / (med / LAYERS * 1e-6) / 1e9, hbm_gbs, "GB/s", "hbm")}
+            dec[f"N{N}_P{P}"] = e
+            if N == 1 and P == 8192:
+                for k, name in (("decode_select", "select"), ("decode_partial", "partial"), ("merge", "merge")):
+                    hbm_calls[k] = dict(e[name]["hbm"], call=f"{name} N=1 P=8192", us_per_call=e[name]["us_per_call"])
+            del bufs, ids, part, nch, xp, ws
+    res["config4_decode"] = dec
+    res["hbm_calls"] = hbm_calls
+    return res
+
+
 def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC, pwsA,
             pwsB, nA, nB, nC, cap, dist):
-    """Same step with every layer's inputs copied from pinned host memory and outputs copied back,
-    all inside the timed region; copies overlap the kernels of other layers."""
+    """The value's workload (12 identity-prefill layers, T=1984) through the public API with every
+    layer's inputs copied from pinned host memory and its output copied back inside the timed region
+    (copies overlap the kernels of other layers), then the same for the whole step (all three
+    workloads) for context."""
+    head = _e2e_leg(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC,
+                    pwsA, pwsB, nA, nB, nC, cap, dist, "A")
+    full = _e2e_leg(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC,
+                    pwsA, pwsB, nA, nB, nC, cap, dist, "ABC")
+    world = dist.get_world_size() if dist else 1
+    return {"value": whole_job_rate(head["ms"], world), "unit": UNIT, "ms_per_12_layers": head["ms"],
+            "h2d_bytes_per_step": head["h2d"], "d2h_bytes_per_step": head["d2h"],
+            "whole_step": {"ms_per_step": full["ms"], "h2d_bytes_per_step": full["h2d"],
+                           "d2h_bytes_per_step": full["d2h"],
+                           "workload": "12 layers each of prefill T=1984 pos0=0, prefill T=1984 pos0=30000 and "
+                                       "decode N=1 P=8192, with host copies"}}
+
+
+def _e2e_leg(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC, pwsA,
+             pwsB, nA, nB, nC, cap, dist, which):
+    """One end-to-end leg over the workloads named in `which`; returns ms per step and copy bytes."""
     hostA = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in A]
-    hostB = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in B]
-    hostC = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in C]
+    hostB = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in B] if "B" in which else []
+    hostC = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in C] if "C" in which else []
     hOutA = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outA]
-    hOutB = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outB]
-    hXp = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in xpC]
+    hOutB = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outB] if "B" in which else []
+    hXp = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in xpC] if "C" in which else []
     h2d = sum(v.numel() * v.element_size() for hs in (hostA, hostB, hostC) for d in hs for v in d.values())
     d2h = sum(o.numel() * o.element_size() for o in hOutA + hOutB + hXp)
 
@@ -421,13 +622,13 @@ def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, p
     for l in range(LAYERS):
         jobs.append((A[l], hostA[l], lambda d, l=l: qsa.qsa_flash_prefill(
             d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nA, T_PREFILL, 0, None, outA[l], pwsA), outA[l], hOutA[l]))
-    for l in range(LAYERS):
+    for l in range(LAYERS if "B" in which else 0):
         def run_b(d, l=l):
             qsa.qsa_select(d["q"], d["kq"], d["ksc"], nB, T_PREFILL, POS0_B, idsB[l], wsB)
             qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nB, T_PREFILL, POS0_B, idsB[l],
                                   outB[l], pwsB)
         jobs.append((B[l], hostB[l], run_b, outB[l], hOutB[l]))
-    for l in range(LAYERS):
+    for l in range(LAYERS if "C" in which else 0):
         def run_c(d, l=l):
             qsa.qsa_select(d["q"], d["kq"], d["ksc"], nC, N_DEC, P_DEC, idsC[l], wsC)
             qsa.qsa_decode_partial(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nC, N_DEC, P_DEC, idsC[l], partC,
@@ -478,9 +679,7 @@ def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, p
     torch.cuda.synchronize(device)
     ms = e0.elapsed_time(e1) / args.steps
     ms = max_over_ranks(ms, dist, device)
-    world = dist.get_world_size() if dist else 1
-    value = whole_job_rate(ms, world)
-    return {"value": value, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    return {"ms": ms, "h2d": h2d, "d2h": d2h}
 
 
 def oracle_sample(seconds_budget=20.0):
@@ -554,6 +753,56 @@ def oracle_sample(seconds_budget=20.0):
     return value, desc, cores, spent
 
 
+PROFILE_CASES = ("dense", "gather", "select", "decode")
+
+
+def run_profile_case(args):
+    """Run one workload's API calls (args.steps times after args.warmup) for an ncu capture; prints
+    nothing but a done line.  dense: prefill T=1984 pos0=0; select / gather: the select or the
+    gathered prefill of T=1984 at pos0=30000; decode: select + partial + merge at N=1, P=8192.
+    One layer's buffers, so the capture holds well under a GB on the device."""
+    import torch
+
+    from int8_kv_top_gb300 import qsa, synth
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    qsa.load()
+    case = args.profile
+    if case == "dense":
+        T, pos0 = T_PREFILL, 0
+    elif case in ("select", "gather"):
+        T, pos0 = T_PREFILL, POS0_B
+    else:
+        T, pos0 = N_DEC, P_DEC
+    n = pos0 + T
+    d = {k: torch.from_numpy(v).to(device) for k, v in synth.layer_inputs(T, n, seed=5).items()}
+    ids = torch.empty((T, 2, 2048), dtype=torch.int32, device=device)
+    out = torch.empty((T, HEADS, D), dtype=torch.float16, device=device)
+    sws = torch.empty(max(16, qsa.qsa_select_workspace_bytes(T, pos0, n)), dtype=torch.uint8, device=device)
+    pws = torch.empty(qsa.qsa_flash_prefill_workspace_bytes(T, pos0, n), dtype=torch.uint8, device=device)
+    cap = qsa.chunk_cap_for()
+    part = torch.empty((T, cap, HEADS, 258), device=device)
+    nch = torch.empty(T, dtype=torch.int32, device=device)
+    xp = torch.empty((T, HEADS, D), device=device)
+    if case == "gather":
+        qsa.qsa_select(d["q"], d["kq"], d["ksc"], n, T, pos0, ids, sws)
+
+    def once():
+        if case in ("select", "decode"):
+            qsa.qsa_select(d["q"], d["kq"], d["ksc"], n, T, pos0, ids, sws)
+        if case in ("dense", "gather"):
+            qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n, T, pos0,
+                                  None if case == "dense" else ids, out, pws)
+        if case == "decode":
+            qsa.qsa_decode_partial(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n, T, pos0, ids, part, nch, cap)
+            qsa.qsa_merge(part, nch, T, cap, xp)
+    for _ in range(args.warmup + args.steps):
+        once()
+    torch.cuda.synchronize(device)
+    qsa.qsa_check_device_status()
+    print(f"profile case {case}: {args.warmup + args.steps} runs done", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -562,6 +811,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration timings")
+    ap.add_argument("--profile", default=None, choices=PROFILE_CASES,
+                    help="only run one workload's calls (--warmup + --steps times) for a profiler capture")
     ap.add_argument("--eager", action="store_true", help="time eager API calls instead of CUDA graph replays")
     ap.add_argument("--clocks-csv", default=None,
                     help="also keep the nvidia-smi samples of the timed region in this CSV ({rank} is replaced)")
@@ -570,6 +822,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.profile:
+        run_profile_case(args)
+        return
 
     if args.impl == "reference":
         # the reference arm is the CPU oracle, timed on the host cores; rank 0 only

@@ -152,11 +152,12 @@ QSA_API int qsa_decode_partial(const uint16_t* q, const int8_t* kq, const int8_t
 
 /*
  * qsa_merge - log-sum-exp merge of decode partials (the pages' qsa_merge / qsa_merge2,
- * "round 27 track b", decision: float2 (m,l) loads; correctness: L = sum l_k e_k over
- * ascending k):
+ * "round 27 track b", decision: float2 (m,l) loads; correctness: the merge formula):
  *   M = max_k m_k,  L = sum_k l_k exp(m_k - M),  xp = sum_k exp(m_k - M) o_k / L
  * over k < n_chunks[t] (1 <= n_chunks[t] <= chunk_cap; other values are flagged in the
- * status word and produce NaN rows).  chunk_cap <= 1024.
+ * status word and produce NaN rows).  chunk_cap <= 1024.  The sums are fp32 reductions in
+ * a tree order (not a serial chain over ascending k), so the last bits may differ from a
+ * serial sum; results are within the library's float tolerance of the exact merge.
  */
 QSA_API int qsa_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp, void* stream);
 

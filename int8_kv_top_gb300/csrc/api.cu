@@ -307,7 +307,9 @@ extern "C" int qsa_select_noalloc(const uint16_t* q, const int8_t* kq, const uin
   if ((rc = check_layer(q, kq, ksc, n_cells, T, pos0))) return rc;
   if (qsa::first_selected_token(pos0, p.identity_max) >= T) return ok();  // nothing to select
   const size_t need = qsa::select_workspace_bytes(T, pos0, n_cells, p);
-  if (need == 0 || need > kNoAllocScratchBytes)
+  if (need == 0)
+    return fail(QSA_ERR_UNSUPPORTED, "selection over n_kv up to %lld cells is not supported", (long long)pos0 + T);
+  if (need > kNoAllocScratchBytes)
     return fail(QSA_ERR_UNSUPPORTED,
                 "qsa_select_noalloc: this call needs %zu bytes of scratch but the built-in scratch holds %zu "
                 "(about 16 selected tokens over 16384 cells); use qsa_select with a caller workspace",

@@ -47,8 +47,8 @@ def test_single_process_is_identity():
 
 
 def test_whole_job_rate_scales_with_replicas():
-    one = bench.whole_job_rate(20.0, 1)
-    assert one == pytest.approx(2 * 1984 / 20e-3)
+    one = bench.whole_job_rate(20.0, 1)              # 12 layers in 20 ms: 1984 tokens per 20/12 ms
+    assert one == pytest.approx(1984 / (20e-3 / 12))
     assert bench.whole_job_rate(20.0, 4) == pytest.approx(4 * one)
 
 

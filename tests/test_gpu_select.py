@@ -60,18 +60,26 @@ def test_config3_reduced_all_tokens():
     assert_close(out, ref_out, "T=48 pos0=30000")
 
 
-def test_config3_full_size_sampled():
+def test_config3_full_size_every_row():
+    # the selected prefill at the benchmark's size (T=1984 at pos0=30000 over 31,984 cells,
+    # seed 5): all 3,968 (token, group) id rows bit-exact against the oracle's exact ranking,
+    # and every token's output within tolerance
     T, pos0 = 1984, 30000
     inp = synth.layer_inputs(T, pos0 + T, seed=5)
     ids, out = gpu_select_prefill(inp, T, pos0)
-    toks = np.array([0, 1, 2, 127, 128, 511, 1000, 1500, 1982, 1983], dtype=np.int32)
-    ref_out, ref_ids, _, _ = oracle.prefill(inp, T, pos0, toks=toks)
-    np.testing.assert_array_equal(ids[toks], ref_ids)
-    assert_close(out[toks], ref_out, "config 3 sampled")
-    # properties at every row: ascending, unique, causal
-    assert (np.diff(ids, axis=-1) > 0).all()
-    assert (ids[..., 0] >= 0).all() and (ids[..., -1] <= pos0 + np.arange(T)[:, None]).all()
-    assert np.isfinite(out).all()
+    ref_out, ref_ids, n_set, _ = oracle.prefill(inp, T, pos0)
+    assert (n_set == 2048).all()
+    bad = np.nonzero((ids != ref_ids).any(axis=-1))
+    assert len(bad[0]) == 0, f"{len(bad[0])} of {T * 2} id rows differ, first (token, group): {bad[0][0]}, {bad[1][0]}"
+    assert_close(out, ref_out, "config 3 all tokens")
+    for t in (0, 1, 127, 128, 1000, 1983):
+        assert_close(out[t], ref_out[t], f"config 3 token {t}")
+    # how often a float64 ranking of the same scores would pick a different set: those rows
+    # are the ones only the exact re-ranking gets right (diagnostic, on a sample of tokens)
+    toks = np.arange(0, T, 31, dtype=np.int32)
+    _, ids64, _, differs = oracle.prefill(inp, T, pos0, toks=toks, f64_check=True)
+    np.testing.assert_array_equal(ids[toks], ids64)
+    print(f"config 3: {int(differs.sum())} of {differs.size} sampled rows rank differently in float64")
 
 
 def test_exact_ties_resolve_to_lower_index():

@@ -273,3 +273,41 @@ def test_quantize_roundtrip_bounds():
     # the scale is the fp16 rounding of absmax / 127
     a = np.abs(xs).max(axis=-1)
     np.testing.assert_array_equal(xsc.reshape(200, 2, 4), (a.astype(np.float32) / np.float32(127)).astype(np.float16))
+
+
+def test_quantize_rounds_exact_halves_away_from_zero():
+    # absmax 127 * 2^-8 makes the scale exactly 2^-8 (a / 127 and its fp16 rounding are exact),
+    # so x = (k + 1/2) * 2^-8 gives x / scale = k + 1/2 exactly: a true tie for even and odd k.
+    # Round-half-away-from-zero sends k + 1/2 to k + 1 and -(k + 1/2) to -(k + 1); a
+    # ties-to-even rule would send the even k down instead.
+    ks = np.array([0, 1, 2, 3, 10, 11, 62, 63, 124, 125], dtype=np.float64)
+    vals = np.concatenate([[127.0], ks + 0.5, -(ks + 0.5)])          # in units of the scale
+    x = np.zeros((1, 256), np.float16)
+    x[0, :len(vals)] = (vals * 2.0 ** -8).astype(np.float16)
+    assert np.array_equal(x[0, :len(vals)].astype(np.float64), vals * 2.0 ** -8)  # every value exact in fp16
+    xq, xsc = oracle.quantize(x)
+    assert xsc.view(np.uint16)[0, 0] == np.float16(2.0 ** -8).view(np.uint16)
+    expect = (np.sign(vals) * np.floor(np.abs(vals) + 0.5)).astype(np.int64)
+    np.testing.assert_array_equal(xq[0, :len(vals)].astype(np.int64), expect)
+    assert list(expect[1:5]) == [1, 2, 3, 4] and list(expect[11:15]) == [-1, -2, -3, -4]
+
+
+def test_decode_part_layout_is_per_group_partials_in_head_order():
+    # oracle.decode's part [N][cap][24][258] must hold, for token t, chunk k and query head
+    # 12 g + h, the partial of group g's head h over chunk k of the token's ascending set
+    # ("round 27 track b - qsa prep and merge", correctness: head stride 258, chunk stride
+    # 24 * 258); slots past the chunk count are left untouched.
+    P, N, topk, idmax = 150, 3, 40, 151
+    inp = tiny_inputs(N, P + N, seed=15)
+    part, n_chunks, merged, _, ids = oracle.decode(inp, N, P, topk=topk, identity_max=idmax)
+    cap = part.shape[1]
+    for t in range(N):
+        n_kv = P + t + 1
+        for g in range(NG):
+            cells, _ = oracle.cell_set(inp["q"][t], inp["kq"], inp["ksc"], n_kv, g, topk=topk, identity_max=idmax)
+            gp = oracle.partials(inp["q"][t], inp["kq"], inp["vq"], inp["ksc"], inp["vsc"], g, cells)
+            nc = gp.shape[0]
+            assert n_chunks[t] == nc
+            np.testing.assert_array_equal(part[t, :nc, g * HPG:(g + 1) * HPG, :], gp)
+            assert np.isnan(part[t, nc:cap, g * HPG:(g + 1) * HPG, :]).all()
+    assert list(n_chunks) == [3, 1, 1]    # 151 identity cells (3 chunks), then top-40 (1 chunk)
