@@ -378,7 +378,7 @@ def run_ours(args, rank, world, local_rank):
     configs = None
     if not args.no_configs:
         configs = measure_configs(torch, qsa, synth, device, stream, (hbm_gbs, bf16_tf), A, B)
-        for k in ("select_prefill", "decode_select", "decode_partial", "merge"):
+        for k in ("select_prefill", "decode_select", "decode_partial", "merge", "decode_layer", "decode_layer_batched"):
             if k in configs.get("hbm_calls", {}):
                 per_launch[k] = configs["hbm_calls"][k]
 
@@ -576,12 +576,52 @@ def measure_configs(torch, qsa, synth, device, stream, peaks, A, B, reps=10):
                           "bytes": tot_bytes, "bytes_note": "each needed input row read once, the merged output "
                           "and the ids written once (partials between the calls not counted)",
                           "hbm": _roof(tot_bytes / (med / LAYERS * 1e-6) / 1e9, hbm_gbs, "GB/s", "hbm")}
+            # the same step in one launch (qsa_decode_layer): select, attend and merge fused
+            xpf = [torch.empty((N, HEADS, D), device=device) for _ in range(LAYERS)]
+            idf = [torch.empty((N, 2, 2048), dtype=torch.int32, device=device) for _ in range(LAYERS)]
+
+            def ffused():
+                for l, d in enumerate(bufs):
+                    qsa.qsa_decode_layer(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n, N, P, idf[l], xpf[l])
+            med, _ = gt(ffused)
+            e["fused"] = {"us_per_call": med / LAYERS, "us_per_token_per_layer": med / LAYERS / N,
+                          "bytes": tot_bytes, "launches": 1,
+                          "hbm": _roof(tot_bytes / (med / LAYERS * 1e-6) / 1e9, hbm_gbs, "GB/s", "hbm")}
             dec[f"N{N}_P{P}"] = e
             if N == 1 and P == 8192:
-                for k, name in (("decode_select", "select"), ("decode_partial", "partial"), ("merge", "merge")):
+                for k, name in (("decode_select", "select"), ("decode_partial", "partial"), ("merge", "merge"),
+                                ("decode_layer", "fused")):
                     hbm_calls[k] = dict(e[name]["hbm"], call=f"{name} N=1 P=8192", us_per_call=e[name]["us_per_call"])
-            del bufs, ids, part, nch, xp, ws
+            del bufs, ids, part, nch, xp, ws, xpf, idf
     res["config4_decode"] = dec
+    # continuous batching: 64 sequences of one decode token each at P=8192 in one launch
+    B_SEQ, P_B = 64, 8192
+    n1 = P_B + 1
+    pool = {}
+    parts = [synth.layer_inputs(1, n1, seed=3000 + b) for b in range(B_SEQ)]
+    for k in ("q", "kq", "vq", "ksc", "vsc"):
+        pool[k] = torch.from_numpy(np.concatenate([pc[k] for pc in parts], axis=0)).to(device)
+    del parts
+    seqs = torch.tensor([[b * n1, n1, P_B, b] for b in range(B_SEQ)], dtype=torch.int32, device=device)
+    ids_b = torch.empty((B_SEQ, 2, 2048), dtype=torch.int32, device=device)
+    xp_b = torch.empty((B_SEQ, HEADS, D), device=device)
+
+    def fbatch():
+        qsa.qsa_decode_layer_batched(pool["q"], pool["kq"], pool["vq"], pool["ksc"], pool["vsc"], B_SEQ * n1, seqs,
+                                     B_SEQ, B_SEQ, n1, ids_b, xp_b)
+    med, mn = gt(fbatch)
+    fbatch()
+    torch.cuda.synchronize(device)
+    qsa.qsa_check_device_status()
+    idn = ids_b.cpu().numpy()
+    rows = sum(len(np.unique(idn[b, g])) for b in range(B_SEQ) for g in range(2))
+    by = B_SEQ * n1 * 2 * 264 + rows * 264 + B_SEQ * HEADS * D * (2 + 4) + B_SEQ * 2 * 2048 * 4
+    res["decode_batched"] = {"sequences": B_SEQ, "tokens_per_sequence": 1, "P": P_B, "us_per_launch": med,
+                             "us_per_launch_min": mn, "tokens_per_s": B_SEQ / (med * 1e-6), "bytes": by,
+                             "hbm": _roof(by / (med * 1e-6) / 1e9, hbm_gbs, "GB/s", "hbm"),
+                             "call": "qsa_decode_layer_batched, one launch"}
+    hbm_calls["decode_layer_batched"] = dict(res["decode_batched"]["hbm"], call="qsa_decode_layer_batched 64 x P=8192")
+    del pool
     res["hbm_calls"] = hbm_calls
     return res
 

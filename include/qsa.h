@@ -162,6 +162,46 @@ QSA_API int qsa_decode_partial(const uint16_t* q, const int8_t* kq, const int8_t
 QSA_API int qsa_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp, void* stream);
 
 /*
+ * qsa_decode_layer - one whole decode step of the layer in a single launch: the selection of
+ * qsa_select, the split attention of qsa_decode_partial and the merge of qsa_merge ("round 27
+ * track b - qsa prep and merge", decision: the production decode chain qsa_score, qsa_topk,
+ * qsa_attn2, qsa_merge2; "round 6 track b - qsa flash", experiment contract: the 2051/2052
+ * budget boundary).  For decode token t (position pos0 + t, n_kv = pos0 + t + 1) and head h:
+ *   xp[t,h,:] = sum_{c in set(t,g)} softmax_c(sm_scale * q[t,h,:] . k^[c,g,:]) * v^[c,g,:]
+ * with set(t,g) the identity range or the exact top-k of qsa_select, k^ = kq * ksc and
+ * v^ = fp16(vq * vsc).  fp32 output; the split into partials is internal (the cluster of CTAs
+ * that takes a (token, group) splits its cells, and the merge runs inside the launch), so the
+ * result equals the merge of the 64-cell partials up to fp32 rounding.
+ *   xp  [N][24][256] fp32 (written)
+ *   ids [N][2][topk] int32, or NULL: the selected ids of tokens above the threshold, ascending,
+ *       exactly as qsa_select writes them (rows of identity tokens are not written)
+ * Needs no workspace and allocates nothing.  n_kv of every token must not exceed 65536 cells
+ * (32768 on a GPU that cannot co-schedule clusters of 16 CTAs; QSA_ERR_UNSUPPORTED otherwise).
+ */
+QSA_API int qsa_decode_layer(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
+                             const uint16_t* vsc, int n_cells, int N, int pos0, int32_t* ids, float* xp,
+                             const qsa_params* params, void* stream);
+
+/*
+ * qsa_decode_layer_batched - qsa_decode_layer for many sequences in one launch (continuous
+ * batching: every sequence brings its own tokens and its own cache).  The caches live in one
+ * pool of n_pool cells with the layouts above (kq [n_pool][2][256] ...); sequence s owns the
+ * pool cells seqs[s][0] .. seqs[s][0] + seqs[s][1] - 1 and its tokens are the consecutive rows
+ * seqs[s][3] .. seqs[s+1][3] - 1 of q / xp / ids (the last sequence runs to n_tok), at
+ * positions seqs[s][2] + 0, 1, ... within the sequence (ids are cell indices within the
+ * sequence).  Every sequence obeys the cache contract: pos0 + its token count <= its cell count.
+ *   seqs  DEVICE array [n_seq][4] int32 {first pool cell, n_cells, pos0, first token row},
+ *         first token rows increasing from 0; 16-byte aligned
+ *   max_n_kv  an upper bound on every token's n_kv (the largest pos0 + token count), at most
+ *         65536; it picks the cluster shape
+ * A sequence whose entry breaks these rules is skipped (its rows are not written) and flagged
+ * in the status word (QSA_ERR_DEVICE); so is a token above max_n_kv's cluster capacity.
+ */
+QSA_API int qsa_decode_layer_batched(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
+                                     const uint16_t* vsc, int64_t n_pool, const int32_t* seqs, int n_seq, int n_tok,
+                                     int max_n_kv, int32_t* ids, float* xp, const qsa_params* params, void* stream);
+
+/*
  * qsa_select_noalloc - qsa_select without a caller workspace.  The paper has no
  * counterpart: this entry point exists for callers that cannot allocate device memory
  * when they call the layer, for example a runtime whose device memory is all reserved up

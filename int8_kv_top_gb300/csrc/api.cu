@@ -236,6 +236,75 @@ int qsa_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, 
   return ok();
 }
 
+// Largest n_kv the fused decode takes on this device (cells per CTA x the largest cluster).
+static int decode_layer_limit(int* rc) {
+  int c = 0;
+  cudaError_t e = qsa::decode_layer_max_cluster(&c);
+  if (e != cudaSuccess) {
+    *rc = cuda_fail(e, "qsa_decode_layer set-up");
+    return 0;
+  }
+  return c * qsa::decode_layer_cells_per_cta();
+}
+
+int qsa_decode_layer(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc, const uint16_t* vsc,
+                     int n_cells, int N, int pos0, int32_t* ids, float* xp, const qsa_params* params, void* stream) {
+  qsa::Params p;
+  int rc = resolve_params(params, &p);
+  if (rc) return rc;
+  if ((rc = check_layer(q, kq, ksc, n_cells, N, pos0))) return rc;
+  CHECK_PTR(vq, "vq");
+  CHECK_PTR(vsc, "vsc");
+  CHECK_PTR(xp, "xp");
+  if (ids && !aligned16(ids)) return fail(QSA_ERR_INVALID_ARG, "ids is not 16-byte aligned");
+  if (N > 65535) return fail(QSA_ERR_UNSUPPORTED, "N must be at most 65535 (got %d)", N);
+  const int limit = decode_layer_limit(&rc);
+  if (!limit) return rc;
+  if ((long long)pos0 + N > limit)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_decode_layer takes n_kv up to %d cells (got %lld)", limit,
+                (long long)pos0 + N);
+  int* st = status_ptr(&rc);
+  if (!st) return rc;
+  cudaError_t e = qsa::launch_decode_layer(
+      reinterpret_cast<const __half*>(q), kq, vq, reinterpret_cast<const __half*>(ksc),
+      reinterpret_cast<const __half*>(vsc), nullptr, 1, (long long)n_cells, n_cells, pos0, N, pos0 + N, ids, xp, p, st,
+      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_decode_layer launch");
+  return ok();
+}
+
+int qsa_decode_layer_batched(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
+                             const uint16_t* vsc, int64_t n_pool, const int32_t* seqs, int n_seq, int n_tok,
+                             int max_n_kv, int32_t* ids, float* xp, const qsa_params* params, void* stream) {
+  qsa::Params p;
+  int rc = resolve_params(params, &p);
+  if (rc) return rc;
+  CHECK_PTR(q, "q");
+  CHECK_PTR(kq, "kq");
+  CHECK_PTR(vq, "vq");
+  CHECK_PTR(ksc, "ksc");
+  CHECK_PTR(vsc, "vsc");
+  CHECK_PTR(seqs, "seqs");
+  CHECK_PTR(xp, "xp");
+  if (ids && !aligned16(ids)) return fail(QSA_ERR_INVALID_ARG, "ids is not 16-byte aligned");
+  if (n_pool <= 0) return fail(QSA_ERR_INVALID_ARG, "n_pool must be positive");
+  if (n_seq < 1 || n_tok < n_seq)
+    return fail(QSA_ERR_INVALID_ARG, "need 1 <= n_seq <= n_tok (got n_seq %d, n_tok %d)", n_seq, n_tok);
+  if (n_tok > 65535) return fail(QSA_ERR_UNSUPPORTED, "n_tok must be at most 65535 (got %d)", n_tok);
+  const int limit = decode_layer_limit(&rc);
+  if (!limit) return rc;
+  if (max_n_kv < 1 || max_n_kv > limit)
+    return fail(QSA_ERR_UNSUPPORTED, "max_n_kv must be in [1, %d] (got %d)", limit, max_n_kv);
+  int* st = status_ptr(&rc);
+  if (!st) return rc;
+  cudaError_t e = qsa::launch_decode_layer(
+      reinterpret_cast<const __half*>(q), kq, vq, reinterpret_cast<const __half*>(ksc),
+      reinterpret_cast<const __half*>(vsc), reinterpret_cast<const int4*>(seqs), n_seq, (long long)n_pool, 0, 0, n_tok,
+      max_n_kv, ids, xp, p, st, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_decode_layer_batched launch");
+  return ok();
+}
+
 int qsa_check_device_status(void* stream) {
   int rc = 0;
   int* st = status_ptr(&rc);

@@ -105,6 +105,16 @@ cudaError_t launch_decode_partial(const __half* q, const int8_t* kq, const int8_
                                   int chunk_cap, int n_cells, int N, int pos0, Params p, int* status,
                                   cudaStream_t stream);
 
+// Fused decode layer (decode_fused.cu): selection, attention and merge in one launch, one
+// cluster per (token, group).  seqs (device, may be null) lists {first pool cell, n_cells, pos0,
+// first token} per sequence; with null the call is one sequence of n_cells cells at pos0.
+int decode_layer_cells_per_cta();
+cudaError_t decode_layer_max_cluster(int* c);
+cudaError_t launch_decode_layer(const __half* q, const int8_t* kq, const int8_t* vq, const __half* ksc,
+                                const __half* vsc, const int4* seqs, int n_seq, long long n_pool, int n_cells, int pos0,
+                                int n_tok, int max_n_kv, int32_t* ids, float* xp, Params p, int* status,
+                                cudaStream_t stream);
+
 cudaError_t launch_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp,
                          int* status, cudaStream_t stream);
 

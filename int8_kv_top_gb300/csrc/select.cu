@@ -32,6 +32,7 @@
 //              desc, index asc); a band beyond shared-memory capacity takes an exact radix
 //              select over recomputed keys.  Ids are emitted in ascending order.
 #include "common.cuh"
+#include "select_math.cuh"
 
 namespace qsa {
 namespace {
@@ -89,69 +90,10 @@ WsLayout ws_layout(int T, int pos0, Params p) {
   return L;
 }
 
-// fp16 value times 2^24 as an exact integer (finite values).
-__device__ __forceinline__ long long half_int24(uint16_t h) {
-  const int e = (h >> 10) & 31, m = h & 1023;
-  const long long v = (e == 0) ? (long long)m : ((long long)(1024 + m) << (e - 1));
-  return (h & 0x8000) ? -v : v;
-}
-
 // ----------------------------------------------------------------- 1. prep
-// Round an exact integer multiple of 2^-24 (a = |value| * 2^24) to fp16, nearest-even.
-// Returns the fp16 magnitude bits and sets *r to the rounded magnitude in the same units.
-// Magnitudes below 2048 units are fp16 values already (subnormal below 1024, e = 1 above)
-// and their bit pattern is the integer itself; above, 11 significant bits are kept.
-__device__ __forceinline__ uint32_t units_to_half_mag(unsigned long long a, unsigned long long* r) {
-  if (a < 2048ull) {
-    *r = a;
-    return (uint32_t)a;
-  }
-  int s = 53 - __clzll((long long)a);  // bit length - 11 (>= 1)
-  unsigned long long mant = a >> s;
-  const unsigned long long rem = a & ((1ull << s) - 1), half = 1ull << (s - 1);
-  if (rem > half || (rem == half && (mant & 1ull))) ++mant;
-  if (mant == 2048ull) {
-    mant = 1024ull;
-    ++s;
-  }
-  const int e = s + 1;  // value = mant * 2^(e - 25), biased exponent e
-  if (e > 30) {         // beyond the fp16 range: infinity, like a rounding conversion
-    *r = a;
-    return 0x7C00u;
-  }
-  *r = mant << s;
-  return ((uint32_t)e << 10) | (uint32_t)(mant - 1024ull);
-}
-
-__device__ __forceinline__ __half signed_half(uint32_t mag_bits, bool neg) {
-  return __ushort_as_half((unsigned short)(mag_bits | (neg ? 0x8000u : 0u)));
-}
-
-// grid (T_pad, 2), 256 threads: thread = dim.  Row layout of qhl: for each 64-dim block b,
-// [hi_b (64) | lo_b (64)] at columns 128 b .. 128 b + 127, with Qsum = hi + lo + residual.
-// All arithmetic is exact in 64-bit integers (units of 2^-24): Qsum of 12 fp16 values is
-// below 2^44 units, and the block sums of |residual| and |hi| + |lo| stay below 2^51.
-// Qsum_d = sum of the group's 12 query heads at dim d for token t (exact, units of 2^-24), split
-// into hi = fp16(Qsum) and lo = fp16(Qsum - hi); e = |Qsum - hi - lo| and h = |hi| + |lo|.
-__device__ __forceinline__ void qsum_split(const __half* __restrict__ q, int t, int g, int d, __half& hi, __half& lo,
-                                           long long& e, long long& h_abs) {
-  const uint16_t* qt = reinterpret_cast<const uint16_t*>(q) + ((size_t)t * kHeads + g * kHPG) * kD;
-  long long sum = 0;
-#pragma unroll
-  for (int h = 0; h < kHPG; ++h) sum += half_int24(__ldg(qt + h * kD + d));
-  unsigned long long rh, rl;
-  const bool neg = sum < 0;
-  const uint32_t hb = units_to_half_mag((unsigned long long)(neg ? -sum : sum), &rh);
-  hi = signed_half(hb, neg);
-  const long long rest = sum - (neg ? -(long long)rh : (long long)rh);  // exact
-  const bool neg2 = rest < 0;
-  const uint32_t lb = units_to_half_mag((unsigned long long)(neg2 ? -rest : rest), &rl);
-  lo = signed_half(lb, neg2);
-  e = rest - (neg2 ? -(long long)rl : (long long)rl);  // exact residual
-  if (e < 0) e = -e;
-  h_abs = (long long)rh + (long long)rl;
-}
-
+// prep_q: grid (T_pad, 2), 256 threads: thread = dim.  Row layout of qhl: for each 64-dim block
+// b, [hi_b (64) | lo_b (64)] at columns 128 b .. 128 b + 127, with Qsum = hi + lo + residual.
+//
 // E_b = sum |residual| and H_b = sum (|hi| + |lo|) over each 64-dim block (two warps), one
 // row, 256 threads (thread = dim); threads 0-3 write eh[0..3] = E_b and eh[4..7] = H_b.
 __device__ __forceinline__ void write_eh(long long e, long long h_abs, float* __restrict__ eh_row,

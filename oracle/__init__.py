@@ -182,3 +182,26 @@ def decode(inp: dict, N: int, P: int, topk=2048, identity_max=2051, sm_scale=1 /
                         _p(_bits(inp["ksc"])), _p(_bits(inp["vsc"])), int(N), int(P), int(topk), int(identity_max),
                         float(sm_scale), cap, _p(part), _p(n_chunks), _p(out), _p(direct), _p(ids))
     return part, n_chunks, out, direct, ids
+
+
+def decode_batch(pool: dict, seqs, topk=2048, identity_max=2051, sm_scale=1 / 16):
+    """Decode oracle for many sequences sharing one cell pool (the batched decode contract).
+
+    pool: {"q": [n_tok][24][256], "kq"/"vq": [n_pool][2][256], "ksc"/"vsc": [n_pool][2][4]};
+    seqs: rows (first pool cell, n_cells, pos0, first token row), first rows increasing from 0.
+    Sequence s is decode() over its own cells and token rows.  Returns (merged [n_tok][24][256],
+    ids [n_tok][2][topk], with -1 in the rows of identity tokens)."""
+    seqs = np.asarray(seqs, dtype=np.int64).reshape(-1, 4)
+    n_tok = pool["q"].shape[0]
+    out = np.zeros((n_tok, NH, HD), dtype=np.float64)
+    ids = np.full((n_tok, NG, topk), -1, dtype=np.int32)
+    for s, (c0, n, pos0, t0) in enumerate(seqs):
+        t1 = int(seqs[s + 1][3]) if s + 1 < len(seqs) else n_tok
+        sub = {"q": np.ascontiguousarray(pool["q"][t0:t1])}
+        for k in ("kq", "vq", "ksc", "vsc"):
+            sub[k] = np.ascontiguousarray(pool[k][c0:c0 + n])
+        _, _, merged, _, sid = decode(sub, int(t1 - t0), int(pos0), topk=topk, identity_max=identity_max,
+                                      sm_scale=sm_scale)
+        out[t0:t1] = merged
+        ids[t0:t1] = sid
+    return out, ids

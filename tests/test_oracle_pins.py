@@ -311,3 +311,26 @@ def test_decode_part_layout_is_per_group_partials_in_head_order():
             np.testing.assert_array_equal(part[t, :nc, g * HPG:(g + 1) * HPG, :], gp)
             assert np.isnan(part[t, nc:cap, g * HPG:(g + 1) * HPG, :]).all()
     assert list(n_chunks) == [3, 1, 1]    # 151 identity cells (3 chunks), then top-40 (1 chunk)
+
+
+def test_batched_decode_oracle_is_per_sequence_decode_on_its_slice():
+    # three sequences in one pool: the batch oracle must give each sequence exactly what a
+    # decode of that sequence's own cache and tokens gives (no cell or token of another leaks in)
+    rng = np.random.default_rng(4)
+    lens = [(90, 85, 2), (40, 37, 3), (130, 120, 1)]          # (n_cells, pos0, tokens)
+    pieces = [tiny_inputs(nt, n, seed=30 + i) for i, (n, p0, nt) in enumerate(lens)]
+    pool = {k: np.concatenate([pc[k] for pc in pieces], axis=0) for k in ("q", "kq", "vq", "ksc", "vsc")}
+    seqs, c0, t0 = [], 0, 0
+    for n, p0, nt in lens:
+        seqs.append((c0, n, p0, t0))
+        c0 += n
+        t0 += nt
+    out, ids = oracle.decode_batch(pool, seqs, topk=40, identity_max=71)
+    t0 = 0
+    for (n, p0, nt), pc in zip(lens, pieces):
+        _, _, merged, direct, sid = oracle.decode(pc, nt, p0, topk=40, identity_max=71)
+        np.testing.assert_array_equal(out[t0:t0 + nt], merged)
+        np.testing.assert_array_equal(ids[t0:t0 + nt], sid)
+        np.testing.assert_allclose(merged, direct, rtol=1e-12, atol=1e-13)   # merge identity per sequence
+        t0 += nt
+    del rng
