@@ -69,3 +69,10 @@ def merge_partials(n_chunks, chunk_cap: int, seed: int = 5) -> np.ndarray:
         part[t, :c, :, HEAD_DIM] = m
         part[t, :c, :, HEAD_DIM + 1] = l
     return part
+
+
+def gate_input(T: int, seed: int = 5, spread: float = 2.0) -> np.ndarray:
+    """Output-gate values [T][24][256] fp16, normal with standard deviation `spread` (a mix of
+    nearly closed, half open and nearly open gates)."""
+    rng = _rng(seed)
+    return (rng.standard_normal((T, N_HEADS, HEAD_DIM)) * spread).astype(np.float16)

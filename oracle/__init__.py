@@ -60,6 +60,7 @@ def lib():
         _lib.oracle_merge_group.argtypes = [P, I, P]
         _lib.oracle_prefill.argtypes = [P, P, P, P, P, I, I, P, I, I, I, D64, P, P, P, P]
         _lib.oracle_decode.argtypes = [P, P, P, P, P, I, I, I, I, D64, I, P, P, P, P, P]
+        _lib.oracle_apply_gate.argtypes = [P, P, ctypes.c_int64]
     return _lib
 
 
@@ -205,3 +206,12 @@ def decode_batch(pool: dict, seqs, topk=2048, identity_max=2051, sm_scale=1 / 16
         out[t0:t1] = merged
         ids[t0:t1] = sid
     return out, ids
+
+
+def apply_gate(out: np.ndarray, gate: np.ndarray) -> np.ndarray:
+    """Output gate: out * sigmoid(gate), elementwise in float64 (a new array; gate fp16, out's shape)."""
+    res = np.ascontiguousarray(out, dtype=np.float64).copy()
+    g = _bits(np.ascontiguousarray(gate, dtype=np.float16))
+    assert g.size == res.size
+    lib().oracle_apply_gate(_p(res), _p(g), res.size)
+    return res

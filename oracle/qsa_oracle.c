@@ -339,6 +339,19 @@ void oracle_merge_group(const double* part, int n_chunks, double* out) {
   for (int h = 0; h < HPG; ++h) merge_head(part + (size_t)h * PSTRIDE, (size_t)HPG * PSTRIDE, n_chunks, out + h * HD);
 }
 
+/* ------------------------------------------------------------ output gate */
+
+/*
+ * The gate input the pages' evaluator feeds the layer ("round 6 track b - qsa flash",
+ * experiment contract: deterministic random int8, scales, query and gate inputs).  The pages
+ * give no formula; this oracle takes the plainest reading, an elementwise sigmoid gate on the
+ * attention output of every (token, head, dim):  out *= 1 / (1 + exp(-gate)), in float64.
+ * out and gate share a layout ([T][24][256]); gate holds fp16 bits.
+ */
+void oracle_apply_gate(double* out, const uint16_t* gate, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] *= 1.0 / (1.0 + exp(-oracle_half_to_double(gate[i])));
+}
+
 /* ------------------------------------------------------------ call-level drivers */
 
 /*

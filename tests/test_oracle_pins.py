@@ -334,3 +334,27 @@ def test_batched_decode_oracle_is_per_sequence_decode_on_its_slice():
         np.testing.assert_allclose(merged, direct, rtol=1e-12, atol=1e-13)   # merge identity per sequence
         t0 += nt
     del rng
+
+
+
+# ------------------------------------------------------------------ output gate
+def test_gate_zero_halves_and_symmetric_gates_sum_to_the_output():
+    rng = np.random.default_rng(8)
+    out = rng.standard_normal((3, 24, 256))
+    zero = np.zeros((3, 24, 256), np.float16)
+    np.testing.assert_array_equal(oracle.apply_gate(out, zero), out / 2)        # sigmoid(0) = 1/2 exactly
+    g = synth.gate_input(3, seed=9)
+    both = oracle.apply_gate(out, g) + oracle.apply_gate(out, -g)              # sigmoid(x) + sigmoid(-x) = 1
+    np.testing.assert_allclose(both, out, rtol=1e-14, atol=1e-15)
+
+
+def test_gate_matches_the_library_logistic_function():
+    from scipy.special import expit
+    rng = np.random.default_rng(10)
+    out = rng.standard_normal((2, 24, 256))
+    g = synth.gate_input(2, seed=11, spread=6.0)
+    ref = out * expit(g.astype(np.float64))
+    np.testing.assert_allclose(oracle.apply_gate(out, g), ref, rtol=1e-13, atol=0)
+    big = np.full((1, 24, 256), 30.0, np.float16)                              # a fully open gate
+    np.testing.assert_allclose(oracle.apply_gate(out[:1], big), out[:1], rtol=1e-12)
+    np.testing.assert_allclose(oracle.apply_gate(out[:1], -big), 0.0, atol=1e-12)
