@@ -478,7 +478,17 @@ def measure_configs(torch, qsa, synth, device, stream, peaks, A, B, reps=10):
     b1 = [up(synth.layer_inputs(512, 512, seed=5 + l)) for l in range(LAYERS)]
     res["config1"] = prefill_entry(512, 0, LAYERS, *gt(prefill_set(512, 0, b1)))
     res["config2"] = prefill_entry(T_PREFILL, 0, LAYERS, *gt(prefill_set(T_PREFILL, 0, A)))
-    del b0, b1
+    # the same layers with the output gate applied in the epilogue (qsa_flash_prefill_gated)
+    gates = [torch.from_numpy(synth.gate_input(T_PREFILL, seed=500 + l)).to(device) for l in range(LAYERS)]
+    outg = [torch.empty((T_PREFILL, HEADS, D), dtype=torch.float16, device=device) for _ in range(LAYERS)]
+    wsg = torch.empty(qsa.qsa_flash_prefill_workspace_bytes(T_PREFILL, 0, T_PREFILL), dtype=torch.uint8, device=device)
+
+    def gated2():
+        for l, d in enumerate(A):
+            qsa.qsa_flash_prefill_gated(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], T_PREFILL, T_PREFILL, 0, None,
+                                        gates[l], outg[l], wsg)
+    res["config2_gated"] = prefill_entry(T_PREFILL, 0, LAYERS, *gt(gated2))
+    del b0, b1, gates, outg, wsg
 
     # config 3: select, then the gathered prefill, and both
     nB = POS0_B + T_PREFILL

@@ -137,6 +137,19 @@ QSA_API int qsa_flash_prefill(const uint16_t* q, const int8_t* kq, const int8_t*
                               void* ws, size_t ws_bytes, const qsa_params* params, void* stream);
 
 /*
+ * qsa_flash_prefill_gated - qsa_flash_prefill with an output gate: every output element is
+ * multiplied by the logistic function of the gate input before its fp16 rounding,
+ *   out[t,h,d] = fp16( attention[t,h,d] * 1 / (1 + exp(-gate[t,h,d])) ).
+ * The pages' evaluator feeds the layer a gate input ("round 6 track b - qsa flash", experiment
+ * contract) without stating its formula; this elementwise sigmoid gate is the library's reading.
+ *   gate [T][24][256] fp16 (DEVICE, 16-byte aligned); NULL gives qsa_flash_prefill.
+ */
+QSA_API int qsa_flash_prefill_gated(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
+                                    const uint16_t* vsc, int n_cells, int T, int pos0, const int32_t* ids,
+                                    const uint16_t* gate, uint16_t* out, void* ws, size_t ws_bytes,
+                                    const qsa_params* params, void* stream);
+
+/*
  * qsa_decode_partial - split-KV partial attention for N decode tokens at positions
  * pos0 .. pos0+N-1 (the pages' qsa_attn / qsa_attn2, "round 27 track b", decision and
  * correctness).  Token t's cell set (identity or ids, ascending) is cut into consecutive
@@ -162,6 +175,14 @@ QSA_API int qsa_decode_partial(const uint16_t* q, const int8_t* kq, const int8_t
 QSA_API int qsa_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp, void* stream);
 
 /*
+ * qsa_merge_gated - qsa_merge with the output gate of qsa_flash_prefill_gated applied to the
+ * merged output: xp[t,h,d] *= 1 / (1 + exp(-gate[t,h,d])).  gate [N][24][256] fp16 (DEVICE,
+ * 16-byte aligned); NULL gives qsa_merge.
+ */
+QSA_API int qsa_merge_gated(const float* part, const int32_t* n_chunks, int N, int chunk_cap, const uint16_t* gate,
+                            float* xp, void* stream);
+
+/*
  * qsa_decode_layer - one whole decode step of the layer in a single launch: the selection of
  * qsa_select, the split attention of qsa_decode_partial and the merge of qsa_merge ("round 27
  * track b - qsa prep and merge", decision: the production decode chain qsa_score, qsa_topk,
@@ -175,12 +196,13 @@ QSA_API int qsa_merge(const float* part, const int32_t* n_chunks, int N, int chu
  *   xp  [N][24][256] fp32 (written)
  *   ids [N][2][topk] int32, or NULL: the selected ids of tokens above the threshold, ascending,
  *       exactly as qsa_select writes them (rows of identity tokens are not written)
+ *   gate [N][24][256] fp16, or NULL: the output gate of qsa_flash_prefill_gated, applied to xp
  * Needs no workspace and allocates nothing.  n_kv of every token must not exceed 65536 cells
  * (32768 on a GPU that cannot co-schedule clusters of 16 CTAs; QSA_ERR_UNSUPPORTED otherwise).
  */
 QSA_API int qsa_decode_layer(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
-                             const uint16_t* vsc, int n_cells, int N, int pos0, int32_t* ids, float* xp,
-                             const qsa_params* params, void* stream);
+                             const uint16_t* vsc, int n_cells, int N, int pos0, int32_t* ids, const uint16_t* gate,
+                             float* xp, const qsa_params* params, void* stream);
 
 /*
  * qsa_decode_layer_batched - qsa_decode_layer for many sequences in one launch (continuous
@@ -194,12 +216,14 @@ QSA_API int qsa_decode_layer(const uint16_t* q, const int8_t* kq, const int8_t* 
  *         first token rows increasing from 0; 16-byte aligned
  *   max_n_kv  an upper bound on every token's n_kv (the largest pos0 + token count), at most
  *         65536; it picks the cluster shape
+ *   gate  [n_tok][24][256] fp16 output gate, or NULL (as in qsa_decode_layer)
  * A sequence whose entry breaks these rules is skipped (its rows are not written) and flagged
  * in the status word (QSA_ERR_DEVICE); so is a token above max_n_kv's cluster capacity.
  */
 QSA_API int qsa_decode_layer_batched(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
                                      const uint16_t* vsc, int64_t n_pool, const int32_t* seqs, int n_seq, int n_tok,
-                                     int max_n_kv, int32_t* ids, float* xp, const qsa_params* params, void* stream);
+                                     int max_n_kv, int32_t* ids, const uint16_t* gate, float* xp,
+                                     const qsa_params* params, void* stream);
 
 /*
  * qsa_select_noalloc - qsa_select without a caller workspace.  The paper has no

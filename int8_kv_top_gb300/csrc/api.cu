@@ -164,6 +164,13 @@ size_t qsa_flash_prefill_workspace_bytes(int T, int pos0, int n_cells, const qsa
 int qsa_flash_prefill(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc, const uint16_t* vsc,
                       int n_cells, int T, int pos0, const int32_t* ids, uint16_t* out, void* ws, size_t ws_bytes,
                       const qsa_params* params, void* stream) {
+  return qsa_flash_prefill_gated(q, kq, vq, ksc, vsc, n_cells, T, pos0, ids, nullptr, out, ws, ws_bytes, params,
+                                 stream);
+}
+
+int qsa_flash_prefill_gated(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
+                            const uint16_t* vsc, int n_cells, int T, int pos0, const int32_t* ids, const uint16_t* gate,
+                            uint16_t* out, void* ws, size_t ws_bytes, const qsa_params* params, void* stream) {
   qsa::Params p;
   int rc = resolve_params(params, &p);
   if (rc) return rc;
@@ -173,6 +180,7 @@ int qsa_flash_prefill(const uint16_t* q, const int8_t* kq, const int8_t* vq, con
   CHECK_PTR(out, "out");
   const int t_sel = qsa::first_selected_token(pos0, p.identity_max);
   if (t_sel < T) CHECK_PTR(ids, "ids (needed: some tokens are above the identity threshold)");
+  if (gate && !aligned16(gate)) return fail(QSA_ERR_INVALID_ARG, "gate is not 16-byte aligned");
   const size_t need = qsa::prefill_workspace_bytes(T, pos0);
   if (!ws || ws_bytes < need)
     return fail(QSA_ERR_WORKSPACE, "prefill workspace of %zu bytes given, %zu needed", ws ? ws_bytes : (size_t)0,
@@ -181,7 +189,8 @@ int qsa_flash_prefill(const uint16_t* q, const int8_t* kq, const int8_t* vq, con
   int* st = status_ptr(&rc);
   if (!st) return rc;
   qsa::FlashArgs a{reinterpret_cast<const __half*>(q), kq, vq, reinterpret_cast<const __half*>(ksc),
-                   reinterpret_cast<const __half*>(vsc), ids, reinterpret_cast<__half*>(out), n_cells, T, pos0, p, st};
+                   reinterpret_cast<const __half*>(vsc), ids, reinterpret_cast<const __half*>(gate),
+                   reinterpret_cast<__half*>(out), n_cells, T, pos0, p, st};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int n = pos0 + T;
   __half* khat = static_cast<__half*>(ws);
@@ -223,6 +232,12 @@ int qsa_decode_partial(const uint16_t* q, const int8_t* kq, const int8_t* vq, co
 }
 
 int qsa_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp, void* stream) {
+  return qsa_merge_gated(part, n_chunks, N, chunk_cap, nullptr, xp, stream);
+}
+
+int qsa_merge_gated(const float* part, const int32_t* n_chunks, int N, int chunk_cap, const uint16_t* gate, float* xp,
+                    void* stream) {
+  if (gate && !aligned16(gate)) return fail(QSA_ERR_INVALID_ARG, "gate is not 16-byte aligned");
   CHECK_PTR(part, "part");
   CHECK_PTR(n_chunks, "n_chunks");
   CHECK_PTR(xp, "xp");
@@ -231,7 +246,8 @@ int qsa_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, 
   int rc = 0;
   int* st = status_ptr(&rc);
   if (!st) return rc;
-  cudaError_t e = qsa::launch_merge(part, n_chunks, N, chunk_cap, xp, st, static_cast<cudaStream_t>(stream));
+  cudaError_t e = qsa::launch_merge(part, n_chunks, N, chunk_cap, reinterpret_cast<const __half*>(gate), xp, st,
+                                    static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qsa_merge launch");
   return ok();
 }
@@ -248,7 +264,8 @@ static int decode_layer_limit(int* rc) {
 }
 
 int qsa_decode_layer(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc, const uint16_t* vsc,
-                     int n_cells, int N, int pos0, int32_t* ids, float* xp, const qsa_params* params, void* stream) {
+                     int n_cells, int N, int pos0, int32_t* ids, const uint16_t* gate, float* xp,
+                     const qsa_params* params, void* stream) {
   qsa::Params p;
   int rc = resolve_params(params, &p);
   if (rc) return rc;
@@ -257,6 +274,7 @@ int qsa_decode_layer(const uint16_t* q, const int8_t* kq, const int8_t* vq, cons
   CHECK_PTR(vsc, "vsc");
   CHECK_PTR(xp, "xp");
   if (ids && !aligned16(ids)) return fail(QSA_ERR_INVALID_ARG, "ids is not 16-byte aligned");
+  if (gate && !aligned16(gate)) return fail(QSA_ERR_INVALID_ARG, "gate is not 16-byte aligned");
   if (N > 65535) return fail(QSA_ERR_UNSUPPORTED, "N must be at most 65535 (got %d)", N);
   const int limit = decode_layer_limit(&rc);
   if (!limit) return rc;
@@ -267,15 +285,16 @@ int qsa_decode_layer(const uint16_t* q, const int8_t* kq, const int8_t* vq, cons
   if (!st) return rc;
   cudaError_t e = qsa::launch_decode_layer(
       reinterpret_cast<const __half*>(q), kq, vq, reinterpret_cast<const __half*>(ksc),
-      reinterpret_cast<const __half*>(vsc), nullptr, 1, (long long)n_cells, n_cells, pos0, N, pos0 + N, ids, xp, p, st,
-      static_cast<cudaStream_t>(stream));
+      reinterpret_cast<const __half*>(vsc), nullptr, 1, (long long)n_cells, n_cells, pos0, N, pos0 + N, ids,
+      reinterpret_cast<const __half*>(gate), xp, p, st, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qsa_decode_layer launch");
   return ok();
 }
 
 int qsa_decode_layer_batched(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
                              const uint16_t* vsc, int64_t n_pool, const int32_t* seqs, int n_seq, int n_tok,
-                             int max_n_kv, int32_t* ids, float* xp, const qsa_params* params, void* stream) {
+                             int max_n_kv, int32_t* ids, const uint16_t* gate, float* xp, const qsa_params* params,
+                             void* stream) {
   qsa::Params p;
   int rc = resolve_params(params, &p);
   if (rc) return rc;
@@ -287,6 +306,7 @@ int qsa_decode_layer_batched(const uint16_t* q, const int8_t* kq, const int8_t* 
   CHECK_PTR(seqs, "seqs");
   CHECK_PTR(xp, "xp");
   if (ids && !aligned16(ids)) return fail(QSA_ERR_INVALID_ARG, "ids is not 16-byte aligned");
+  if (gate && !aligned16(gate)) return fail(QSA_ERR_INVALID_ARG, "gate is not 16-byte aligned");
   if (n_pool <= 0) return fail(QSA_ERR_INVALID_ARG, "n_pool must be positive");
   if (n_seq < 1 || n_tok < n_seq)
     return fail(QSA_ERR_INVALID_ARG, "need 1 <= n_seq <= n_tok (got n_seq %d, n_tok %d)", n_seq, n_tok);
@@ -300,7 +320,7 @@ int qsa_decode_layer_batched(const uint16_t* q, const int8_t* kq, const int8_t* 
   cudaError_t e = qsa::launch_decode_layer(
       reinterpret_cast<const __half*>(q), kq, vq, reinterpret_cast<const __half*>(ksc),
       reinterpret_cast<const __half*>(vsc), reinterpret_cast<const int4*>(seqs), n_seq, (long long)n_pool, 0, 0, n_tok,
-      max_n_kv, ids, xp, p, st, static_cast<cudaStream_t>(stream));
+      max_n_kv, ids, reinterpret_cast<const __half*>(gate), xp, p, st, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qsa_decode_layer_batched launch");
   return ok();
 }

@@ -85,6 +85,7 @@ struct FlashArgs {
   const __half* ksc;
   const __half* vsc;
   const int32_t* ids;
+  const __half* gate;  // output gate [T][24][256], or null
   __half* out;
   int n_cells, T, pos0;
   Params p;
@@ -112,11 +113,14 @@ int decode_layer_cells_per_cta();
 cudaError_t decode_layer_max_cluster(int* c);
 cudaError_t launch_decode_layer(const __half* q, const int8_t* kq, const int8_t* vq, const __half* ksc,
                                 const __half* vsc, const int4* seqs, int n_seq, long long n_pool, int n_cells, int pos0,
-                                int n_tok, int max_n_kv, int32_t* ids, float* xp, Params p, int* status,
-                                cudaStream_t stream);
+                                int n_tok, int max_n_kv, int32_t* ids, const __half* gate, float* xp, Params p,
+                                int* status, cudaStream_t stream);
 
-cudaError_t launch_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp,
-                         int* status, cudaStream_t stream);
+// Output gate: the elementwise logistic function of the gate input, in fp32.
+__device__ __forceinline__ float gate_sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+
+cudaError_t launch_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, const __half* gate,
+                         float* xp, int* status, cudaStream_t stream);
 
 cudaError_t launch_quantize(const __half* x, int64_t n_rows, int8_t* xq, __half* xsc, cudaStream_t stream);
 

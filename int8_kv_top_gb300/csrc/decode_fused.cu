@@ -43,7 +43,8 @@
 //  5. merge   each CTA pushes its (m, l) and, to CTA r, the r-th 1/C of its 12 x 256 partial
 //             outputs; barrier; CTA r merges its share (M = max m, L = sum l 2^(m - M),
 //             xp = sum o 2^(m - M) / L) from its own shared memory.  The ids of selected tokens are
-//             written in ascending order from per-CTA offsets.
+//             written in ascending order from per-CTA offsets.  With a gate input the output is
+//             multiplied by sigmoid(gate) before it is stored.
 //
 // No global scratch and no spin on global memory: the waits are cluster barriers and bounded
 // mbarrier waits on the bulk copies.
@@ -109,6 +110,7 @@ struct FusedArgs {
   long long n_pool;  // cells in the pool (bounds of every sequence)
   int n_cells, pos0; // the one sequence when seqs is null
   int32_t* ids;      // [n_tok][2][topk] or null
+  const __half* gate;  // [n_tok][24][256] output gate, or null
   float* xp;         // [n_tok][24][256]
   Params p;
   int* status;
@@ -912,7 +914,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
       L = fmaf(r_l[qq * 12 + h], w, L);
       O = fmaf(r_o[qq * kPerCta + e], w, O);
     }
-    a.xp[((size_t)t * kHeads + g * kHPG + h) * kD + d] = O / L;
+    float v = O / L;
+    if (a.gate) v *= gate_sigmoid(__half2float(a.gate[((size_t)t * kHeads + g * kHPG + h) * kD + d]));
+    a.xp[((size_t)t * kHeads + g * kHPG + h) * kD + d] = v;
   }
   // ids of a selected token: this CTA's kept cells at the offset of the CTAs before it
   if (selected && a.ids != nullptr) {
@@ -1028,9 +1032,9 @@ cudaError_t decode_layer_max_cluster(int* c) {
 
 cudaError_t launch_decode_layer(const __half* q, const int8_t* kq, const int8_t* vq, const __half* ksc,
                                 const __half* vsc, const int4* seqs, int n_seq, long long n_pool, int n_cells, int pos0,
-                                int n_tok, int max_n_kv, int32_t* ids, float* xp, Params p, int* status,
-                                cudaStream_t stream) {
-  FusedArgs a{q, kq, vq, ksc, vsc, seqs, n_seq, n_pool, n_cells, pos0, ids, xp, p, status};
+                                int n_tok, int max_n_kv, int32_t* ids, const __half* gate, float* xp, Params p,
+                                int* status, cudaStream_t stream) {
+  FusedArgs a{q, kq, vq, ksc, vsc, seqs, n_seq, n_pool, n_cells, pos0, ids, gate, xp, p, status};
   int state = 0;
   cudaError_t e = device_setup(&state);
   if (e != cudaSuccess) return e;

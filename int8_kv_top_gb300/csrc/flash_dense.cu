@@ -113,8 +113,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     flash_dense_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                       const __grid_constant__ CUtensorMap map_q, __half* __restrict__ out, int pos0, int t_begin,
-                       int t_end, float scale_log2, int* status) {
+                       const __grid_constant__ CUtensorMap map_q, const __half* __restrict__ gate,
+                       __half* __restrict__ out, int pos0, int t_begin, int t_end, float scale_log2, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Bars bars;
@@ -457,6 +457,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int tok = t0 + quarter * 8 + (lane >> 2);
         const bool tok_valid = tok <= t_last;
         __half* gdst = out + ((size_t)(tok_valid ? tok : 0) * kHeads + it.g * kHPG + it.hq * kHQ) * kD + 16 * gq;
+        // this lane's own row (head it.hq * kHQ + gq of token tok) in the gate input
+        const __half* grow =
+            gate ? gate + ((size_t)(tok_valid ? tok : 0) * kHeads + it.g * kHPG + it.hq * kHQ + gq) * kD : nullptr;
 #pragma unroll 1
         for (int c0 = wg * 128; c0 < wg * 128 + 128; c0 += 64) {
           uint32_t oa[32], ob[32];
@@ -464,10 +467,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_ld32(lane_base + kColO + c0 + 32, ob);
           tmem_wait_ld();
           uint32_t B[32];  // block b (dims c0 + 16 b ..) = words 8 b .. 8 b + 7
+          if (grow) {  // output gate: o / l * sigmoid(gate), rounded to fp16 once
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            B[i] = pack_half2(__uint_as_float(oa[2 * i]) * inv_l, __uint_as_float(oa[2 * i + 1]) * inv_l);
-            B[16 + i] = pack_half2(__uint_as_float(ob[2 * i]) * inv_l, __uint_as_float(ob[2 * i + 1]) * inv_l);
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint32_t* src = hh ? ob : oa;
+              uint4 gw[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) gw[u] = __ldg(reinterpret_cast<const uint4*>(grow + c0 + 32 * hh) + u);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const uint32_t w = i % 4 == 0 ? gw[i / 4].x : i % 4 == 1 ? gw[i / 4].y : i % 4 == 2 ? gw[i / 4].z : gw[i / 4].w;
+                const float2 gv = __half22float2(*reinterpret_cast<const __half2*>(&w));
+                B[16 * hh + i] = pack_half2(__uint_as_float(src[2 * i]) * inv_l * gate_sigmoid(gv.x),
+                                            __uint_as_float(src[2 * i + 1]) * inv_l * gate_sigmoid(gv.y));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              B[i] = pack_half2(__uint_as_float(oa[2 * i]) * inv_l, __uint_as_float(oa[2 * i + 1]) * inv_l);
+              B[16 + i] = pack_half2(__uint_as_float(ob[2 * i]) * inv_l, __uint_as_float(ob[2 * i + 1]) * inv_l);
+            }
           }
 #pragma unroll
           for (int b1 = 0; b1 < 2; ++b1)  // blocks (b1, 1 - g0) to and from lane ^ 1
@@ -581,8 +601,8 @@ cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const
   const float scale_log2 = a.p.sm_scale * kLog2e;
   const int n_items = (n_ttiles + 1) / 2 * 6;  // (pair of tiles, group, head quad)
   const int n_clusters = std::min(n_clusters_max, n_items);  // persistent: each takes items in snake order
-  return launch_pdl(flash_dense_kernel, dim3(n_clusters * 2), dim3(kThreads), kSmemAlloc, stream, mk, mv, mq, a.out,
-                    a.pos0, t_begin, t_end, scale_log2, a.status);
+  return launch_pdl(flash_dense_kernel, dim3(n_clusters * 2), dim3(kThreads), kSmemAlloc, stream, mk, mv, mq, a.gate,
+                    a.out, a.pos0, t_begin, t_end, scale_log2, a.status);
 }
 
 }  // namespace qsa

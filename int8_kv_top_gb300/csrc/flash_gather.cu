@@ -110,8 +110,9 @@ __device__ __forceinline__ void st6(uint32_t taddr, int wg, const uint32_t (&r)[
 
 __global__ void __launch_bounds__(kThreads, 1)
     flash_gather_kernel(const __grid_constant__ CUtensorMap map_q, const __half* __restrict__ khat,
-                        const __half* __restrict__ vhat, const int32_t* __restrict__ ids, __half* __restrict__ out,
-                        int pos0, int t_begin, int n_items, int K, float scale_log2, int* status) {
+                        const __half* __restrict__ vhat, const int32_t* __restrict__ ids,
+                        const __half* __restrict__ gate, __half* __restrict__ out, int pos0, int t_begin, int n_items,
+                        int K, float scale_log2, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ GBars bars;
@@ -467,14 +468,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // epilogue: thread = dim i (half 0) and 128 + i (half 1)
       __half* orow = out + ((size_t)t * kHeads + g * kHPG + h0) * kD;
+      const __half* grow = gate ? gate + ((size_t)t * kHeads + g * kHPG + h0) * kD : nullptr;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t o[kHPW];
         ld6(lane_base + kColO + (k & 1) * 32 + half * 16, wg, o);
+        float gs[kHPW];  // output gate: sigmoid(gate) per element, 1 without a gate
+#pragma unroll
+        for (int j = 0; j < kHPW; ++j) gs[j] = grow ? gate_sigmoid(__half2float(grow[j * kD + half * 128 + i])) : 1.f;
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < kHPW; ++j)
-          orow[j * kD + half * 128 + i] = __float2half_rn(__uint_as_float(o[j]) * inv_l[j]);
+          orow[j * kD + half * 128 + i] = __float2half_rn(__uint_as_float(o[j]) * inv_l[j] * gs[j]);
       }
       tc_fence_before();
       named_bar_any(bar_id, 128, false);  // s_l may be rewritten by the next item only after everyone read it
@@ -526,8 +531,8 @@ cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, cons
   const float scale_log2 = a.p.sm_scale * kLog2e;
   CUtensorMap mq;
   if (!make_q_map(&mq, a.q, a.T)) return cudaErrorInvalidValue;
-  return launch_pdl(flash_gather_kernel, dim3(grid), dim3(kThreads), kSmemAlloc, stream, mq, khat, vhat, a.ids, a.out,
-                    a.pos0, t_begin, n_items, a.p.topk, scale_log2, a.status);
+  return launch_pdl(flash_gather_kernel, dim3(grid), dim3(kThreads), kSmemAlloc, stream, mq, khat, vhat, a.ids, a.gate,
+                    a.out, a.pos0, t_begin, n_items, a.p.topk, scale_log2, a.status);
 }
 
 }  // namespace qsa

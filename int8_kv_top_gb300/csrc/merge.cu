@@ -10,7 +10,8 @@
 // chunk count is known (every chunk slot below the capacity is inside the buffer; slots past
 // the count are never used), so the CTA waits on one round of loads rather than a chain.
 // Every warp reduces M = max m and L = sum l * exp(m - M) itself with shuffles (lane = chunk),
-// and takes the chunk weights exp(m_k - M) / L from lane k.
+// and takes the chunk weights exp(m_k - M) / L from lane k.  With a gate input the merged
+// output is multiplied by sigmoid(gate) before it is stored.
 #include "common.cuh"
 
 namespace qsa {
@@ -22,7 +23,8 @@ constexpr int kMaxChunks = 1024;
 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __restrict__ part,
                                                               const int32_t* __restrict__ n_chunks, int chunk_cap,
-                                                              float* __restrict__ xp, int* status) {
+                                                              const __half* __restrict__ gate, float* __restrict__ xp,
+                                                              int* status) {
   pdl_begin();
   const int t = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -80,18 +82,23 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
     a4[k & 3].x = fmaf(w, ok.x, a4[k & 3].x);
     a4[k & 3].y = fmaf(w, ok.y, a4[k & 3].y);
   }
-  const float2 acc =
+  float2 acc =
       make_float2((a4[0].x + a4[1].x) + (a4[2].x + a4[3].x), (a4[0].y + a4[1].y) + (a4[2].y + a4[3].y));
+  if (gate) {  // output gate: xp *= sigmoid(gate)
+    const float2 gv = __half22float2(*reinterpret_cast<const __half2*>(gate + ((size_t)t * kHeads + h) * kD + d));
+    acc.x *= gate_sigmoid(gv.x);
+    acc.y *= gate_sigmoid(gv.y);
+  }
   *reinterpret_cast<float2*>(xp + ((size_t)t * kHeads + h) * kD + d) = acc;
 }
 
 }  // namespace
 
-cudaError_t launch_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, float* xp, int* status,
-                         cudaStream_t stream) {
+cudaError_t launch_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, const __half* gate,
+                         float* xp, int* status, cudaStream_t stream) {
   if (chunk_cap > kMaxChunks) return cudaErrorInvalidValue;
-  return launch_pdl(merge_kernel, dim3(N * kHeads), dim3(kMergeThreads), 0, stream, part, n_chunks, chunk_cap, xp,
-                    status);
+  return launch_pdl(merge_kernel, dim3(N * kHeads), dim3(kMergeThreads), 0, stream, part, n_chunks, chunk_cap, gate,
+                    xp, status);
 }
 
 }  // namespace qsa

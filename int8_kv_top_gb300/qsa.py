@@ -29,7 +29,8 @@ N_GROUPS, HEADS_PER_GROUP, N_HEADS, HEAD_DIM, CHUNK, PART_STRIDE = 2, 12, 24, 25
 # every symbol include/qsa.h declares
 EXPORTS = ("qsa_last_error", "qsa_prep_quantize", "qsa_select_workspace_bytes", "qsa_select",
            "qsa_flash_prefill_workspace_bytes", "qsa_flash_prefill",
-           "qsa_decode_partial", "qsa_merge", "qsa_decode_layer", "qsa_decode_layer_batched",
+           "qsa_flash_prefill_gated", "qsa_decode_partial", "qsa_merge", "qsa_merge_gated", "qsa_decode_layer",
+           "qsa_decode_layer_batched",
            "qsa_check_device_status", "qsa_select_noalloc")
 
 
@@ -67,8 +68,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_flash_prefill.argtypes = [P, P, P, P, P, I, I, I, P, P, P, SZ, PP, P]
     lib.qsa_decode_partial.argtypes = [P, P, P, P, P, I, I, I, P, P, P, I, PP, P]
     lib.qsa_merge.argtypes = [P, P, I, I, P, P]
-    lib.qsa_decode_layer.argtypes = [P, P, P, P, P, I, I, I, P, P, PP, P]
-    lib.qsa_decode_layer_batched.argtypes = [P, P, P, P, P, I64, P, I, I, I, P, P, PP, P]
+    lib.qsa_flash_prefill_gated.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P, SZ, PP, P]
+    lib.qsa_merge_gated.argtypes = [P, P, I, I, P, P, P]
+    lib.qsa_decode_layer.argtypes = [P, P, P, P, P, I, I, I, P, P, P, PP, P]
+    lib.qsa_decode_layer_batched.argtypes = [P, P, P, P, P, I64, P, I, I, I, P, P, P, PP, P]
     lib.qsa_check_device_status.argtypes = [P]
     lib.qsa_select_noalloc.argtypes = [P, P, P, I, I, I, P, PP, P]
     for name in EXPORTS:
@@ -152,17 +155,30 @@ def qsa_merge(part, n_chunks, N: int, chunk_cap: int, xp, stream=None):
     _check(load().qsa_merge(_ptr(part), _ptr(n_chunks), N, chunk_cap, _ptr(xp), _stream(stream)))
 
 
-def qsa_decode_layer(q, kq, vq, ksc, vsc, n_cells: int, N: int, pos0: int, ids, xp, params=None, stream=None):
-    """One decode step (select, attend, merge) in one launch; ids may be None."""
+def qsa_flash_prefill_gated(q, kq, vq, ksc, vsc, n_cells: int, T: int, pos0: int, ids, gate, out, ws=None,
+                            params=None, stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().qsa_flash_prefill_gated(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), n_cells, T, pos0,
+                                          _ptr(ids), _ptr(gate), _ptr(out), _ptr(ws), ws_bytes, _params(params),
+                                          _stream(stream)))
+
+
+def qsa_merge_gated(part, n_chunks, N: int, chunk_cap: int, gate, xp, stream=None):
+    _check(load().qsa_merge_gated(_ptr(part), _ptr(n_chunks), N, chunk_cap, _ptr(gate), _ptr(xp), _stream(stream)))
+
+
+def qsa_decode_layer(q, kq, vq, ksc, vsc, n_cells: int, N: int, pos0: int, ids, xp, params=None, stream=None,
+                     gate=None):
+    """One decode step (select, attend, merge) in one launch; ids and gate may be None."""
     _check(load().qsa_decode_layer(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), n_cells, N, pos0, _ptr(ids),
-                                   _ptr(xp), _params(params), _stream(stream)))
+                                   _ptr(gate), _ptr(xp), _params(params), _stream(stream)))
 
 
 def qsa_decode_layer_batched(q, kq, vq, ksc, vsc, n_pool: int, seqs, n_seq: int, n_tok: int, max_n_kv: int, ids, xp,
-                             params=None, stream=None):
+                             params=None, stream=None, gate=None):
     """Decode steps of many sequences in one launch; seqs is a device int32 tensor [n_seq][4]."""
     _check(load().qsa_decode_layer_batched(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), n_pool, _ptr(seqs),
-                                           n_seq, n_tok, max_n_kv, _ptr(ids), _ptr(xp), _params(params),
+                                           n_seq, n_tok, max_n_kv, _ptr(ids), _ptr(gate), _ptr(xp), _params(params),
                                            _stream(stream)))
 
 

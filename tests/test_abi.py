@@ -111,3 +111,26 @@ def test_select_workspace_covers_the_score_rows(lib):
                 assert need >= prev[pos0], (T, pos0)
             prev[pos0] = need
     assert lib.qsa_select_workspace_bytes(512, 30000, 30512, None) >= lib.qsa_select_workspace_bytes(512, 8192, 8704, None)
+
+
+def test_decode_layer_and_gated_calls_validate_on_the_host(lib):
+    P = ctypes.c_void_p
+    args = (P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE))
+    # qsa_decode_layer(q, kq, vq, ksc, vsc, n_cells, N, pos0, ids, gate, xp, params, stream)
+    assert lib.qsa_decode_layer(*args, 100, 0, 0, None, None, P(FAKE), None, None) == qsa.QSA_ERR_INVALID_ARG  # N = 0
+    assert lib.qsa_decode_layer(*args, 100, 4, 97, None, None, P(FAKE), None, None) == qsa.QSA_ERR_INVALID_ARG
+    assert b"cache too small" in lib.qsa_last_error()
+    assert lib.qsa_decode_layer(*args, 100, 4, 0, None, None, None, None, None) == qsa.QSA_ERR_INVALID_ARG  # xp
+    assert lib.qsa_decode_layer(*args, 100, 4, 0, None, P(FAKE + 2), P(FAKE), None, None) == qsa.QSA_ERR_INVALID_ARG
+    assert b"gate" in lib.qsa_last_error()
+    # qsa_decode_layer_batched(q, kq, vq, ksc, vsc, n_pool, seqs, n_seq, n_tok, max_n_kv, ids, gate, xp, params, stream)
+    assert lib.qsa_decode_layer_batched(*args, 100, None, 1, 1, 100, None, None, P(FAKE), None, None) == \
+        qsa.QSA_ERR_INVALID_ARG                                                     # seqs NULL
+    assert lib.qsa_decode_layer_batched(*args, 100, P(FAKE), 3, 2, 100, None, None, P(FAKE), None, None) == \
+        qsa.QSA_ERR_INVALID_ARG                                                     # more sequences than tokens
+    assert lib.qsa_decode_layer_batched(*args, 0, P(FAKE), 1, 1, 100, None, None, P(FAKE), None, None) == \
+        qsa.QSA_ERR_INVALID_ARG                                                     # empty pool
+    # gated prefill and merge: a misaligned gate is refused before anything else runs
+    assert lib.qsa_flash_prefill_gated(*args, 100, 4, 0, None, P(FAKE + 2), P(FAKE), P(FAKE), 1 << 20, None,
+                                       None) == qsa.QSA_ERR_INVALID_ARG
+    assert lib.qsa_merge_gated(P(FAKE), P(FAKE), 1, 33, P(FAKE + 2), P(FAKE), None) == qsa.QSA_ERR_INVALID_ARG
