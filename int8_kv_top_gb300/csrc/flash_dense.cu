@@ -347,6 +347,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int t = t0 + tl;
     const bool row_valid = t <= t_last;
     const int n_kv_row = row_valid ? pos0 + t + 1 : 0;
+    if (gate != nullptr && row_valid) {
+      // the row's gate values (this warpgroup's 128 dims) go to L2 now; the epilogue reads them
+      const char* grow = reinterpret_cast<const char*>(
+          gate + ((size_t)t * kHeads + it.g * kHPG + it.hq * kHQ + (lane & 3)) * kD + wg * 128);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(grow));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(grow + 128));
+    }
 
     float m_run = -INFINITY, l_run = 0.f;  // m_run in log2 units; l_run: this half of the row
     for (int j = 0; j < J; ++j) {

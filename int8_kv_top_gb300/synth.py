@@ -76,3 +76,17 @@ def gate_input(T: int, seed: int = 5, spread: float = 2.0) -> np.ndarray:
     nearly closed, half open and nearly open gates)."""
     rng = _rng(seed)
     return (rng.standard_normal((T, N_HEADS, HEAD_DIM)) * spread).astype(np.float16)
+
+
+def prep_inputs(T: int, seed: int = 5) -> dict:
+    """Raw projections of T new tokens for the fused prep: q_raw [T][24][256], k_raw and v_raw
+    [T][2][256] fp16 (normal with a random gain per row), and the RMS-norm gains q_gamma,
+    k_gamma [256] fp32 (1 + 0.1 N(0,1))."""
+    rng = _rng(seed)
+    def rows(shape):
+        gain = np.exp(rng.uniform(-1.0, 1.0, size=shape[:-1] + (1,)))
+        return (rng.standard_normal(shape) * gain).astype(np.float16)
+    return {"q_raw": rows((T, N_HEADS, HEAD_DIM)), "k_raw": rows((T, N_GROUPS, HEAD_DIM)),
+            "v_raw": rows((T, N_GROUPS, HEAD_DIM)),
+            "q_gamma": (1.0 + 0.1 * rng.standard_normal(HEAD_DIM)).astype(np.float32),
+            "k_gamma": (1.0 + 0.1 * rng.standard_normal(HEAD_DIM)).astype(np.float32)}

@@ -61,6 +61,7 @@ def lib():
         _lib.oracle_prefill.argtypes = [P, P, P, P, P, I, I, P, I, I, I, D64, P, P, P, P]
         _lib.oracle_decode.argtypes = [P, P, P, P, P, I, I, I, I, D64, I, P, P, P, P, P]
         _lib.oracle_apply_gate.argtypes = [P, P, ctypes.c_int64]
+        _lib.oracle_prep.argtypes = [P, P, P, P, P, I, I, D64, I, D64, P, P, P]
     return _lib
 
 
@@ -215,3 +216,18 @@ def apply_gate(out: np.ndarray, gate: np.ndarray) -> np.ndarray:
     assert g.size == res.size
     lib().oracle_apply_gate(_p(res), _p(g), res.size)
     return res
+
+
+def prep(q_raw, k_raw, q_gamma, k_gamma, T: int, pos0: int, pos3=None, base=10000.0, rotary_dim=256, eps=1e-6,
+         sections=(32, 48, 48)):
+    """Fused prep oracle: (qcur [T][24][256], kcur [T][2][256]) float64 (RMS norm with gain, then
+    rotary embedding at positions pos0 + t, or the mrope positions pos3 [T][3])."""
+    qc = np.zeros((T, NH, HD), dtype=np.float64)
+    kc = np.zeros((T, NG, HD), dtype=np.float64)
+    qg = np.ascontiguousarray(q_gamma, dtype=np.float64)
+    kg = np.ascontiguousarray(k_gamma, dtype=np.float64)
+    sec = np.ascontiguousarray(sections, dtype=np.int32)
+    p3 = None if pos3 is None else np.ascontiguousarray(pos3, dtype=np.int32)
+    lib().oracle_prep(_p(_bits(q_raw)), _p(_bits(k_raw)), _p(qg), _p(kg), None if p3 is None else _p(p3), int(T),
+                      int(pos0), float(base), int(rotary_dim), float(eps), _p(sec), _p(qc), _p(kc))
+    return qc, kc

@@ -352,6 +352,62 @@ void oracle_apply_gate(double* out, const uint16_t* gate, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] *= 1.0 / (1.0 + exp(-oracle_half_to_double(gate[i])));
 }
 
+/* ------------------------------------------------------------ fused prep */
+
+/*
+ * The pages' fused prep (qsa_prep: "round 27 track b - qsa prep and merge", decision and
+ * rejected prep fusion: raw rows, their gamma, a norm_rope step, mrope variants; correctness:
+ * it writes qcur and the int8 cache kq vq ksc vsc).  The pages name the parts but not their
+ * formulas; this oracle takes the plainest readings:
+ *  - RMS norm per head row of 256 values with a learned gain:
+ *      y_d = x_d / sqrt(mean_d(x^2) + eps) * gamma_d            (q rows use q_gamma, k rows k_gamma)
+ *  - rotary position embedding on the normed q and k rows, halves paired (i, i + rd/2) for
+ *    i < rd/2 (rd = rotary_dim; dims >= rd untouched), angle theta_i = p * base^(-2 i / rd):
+ *      (y_i, y_{i+rd/2}) -> (y_i cos - y_{i+rd/2} sin,  y_{i+rd/2} cos + y_i sin)
+ *    with p = pos0 + t; for mrope, pair i takes component c of the token's three positions
+ *    pos3[t][c], c = 0, 1, 2 over consecutive frequency sections of sizes sections[0..2];
+ *  - v rows are not normed or rotated.
+ * Outputs (float64): qcur [T][24][256], kcur [T][2][256].  The cache rows of cell pos0 + t are
+ * the quantiser (step 8) applied to fp16(kcur) and to v.
+ */
+static void prep_row(const uint16_t* x, const double* gamma, double p_or_nan, const int32_t* p3, int rotary_dim,
+                     double base, double eps, const int* sections, double* y) {
+  double ms = 0.0;
+  for (int d = 0; d < HD; ++d) {
+    const double v = oracle_half_to_double(x[d]);
+    ms += v * v;
+  }
+  ms /= HD;
+  const double r = 1.0 / sqrt(ms + eps);
+  for (int d = 0; d < HD; ++d) y[d] = oracle_half_to_double(x[d]) * r * gamma[d];
+  const int h = rotary_dim / 2;
+  for (int i = 0; i < h; ++i) {
+    double p = p_or_nan;
+    if (p3) p = (double)p3[i < sections[0] ? 0 : (i < sections[0] + sections[1] ? 1 : 2)];
+    const double theta = p * pow(base, -2.0 * i / rotary_dim);
+    const double c = cos(theta), sn = sin(theta);
+    const double a = y[i], b = y[i + h];
+    y[i] = a * c - b * sn;
+    y[i + h] = b * c + a * sn;
+  }
+}
+
+void oracle_prep(const uint16_t* q_raw, const uint16_t* k_raw, const double* q_gamma, const double* k_gamma,
+                 const int32_t* pos3, int T, int pos0, double base, int rotary_dim, double eps, const int* sections,
+                 double* qcur, double* kcur) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const double p = (double)pos0 + t;
+    const int32_t* p3 = pos3 ? pos3 + 3 * t : NULL;
+    for (int h = 0; h < NH; ++h)
+      prep_row(q_raw + ((size_t)t * NH + h) * HD, q_gamma, p, p3, rotary_dim, base, eps, sections,
+               qcur + ((size_t)t * NH + h) * HD);
+    for (int g = 0; g < NG; ++g)
+      prep_row(k_raw + ((size_t)t * NG + g) * HD, k_gamma, p, p3, rotary_dim, base, eps, sections,
+               kcur + ((size_t)t * NG + g) * HD);
+  }
+}
+
 /* ------------------------------------------------------------ call-level drivers */
 
 /*

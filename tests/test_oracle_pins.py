@@ -358,3 +358,76 @@ def test_gate_matches_the_library_logistic_function():
     big = np.full((1, 24, 256), 30.0, np.float16)                              # a fully open gate
     np.testing.assert_allclose(oracle.apply_gate(out[:1], big), out[:1], rtol=1e-12)
     np.testing.assert_allclose(oracle.apply_gate(out[:1], -big), 0.0, atol=1e-12)
+
+
+
+# ------------------------------------------------------------------ fused prep (norm, rope)
+def prep_case(T=3, seed=12):
+    return synth.prep_inputs(T, seed=seed)
+
+
+def test_prep_at_position_zero_is_the_library_rms_norm():
+    # theta = 0 at position 0: the rotation is the identity, leaving torch's rms_norm with weight
+    inp = prep_case()
+    qc, kc = oracle.prep(inp["q_raw"], inp["k_raw"], inp["q_gamma"], inp["k_gamma"], 1, 0)
+    x = torch.from_numpy(inp["q_raw"][:1].astype(np.float64))
+    ref = torch.nn.functional.rms_norm(x, (256,), torch.from_numpy(inp["q_gamma"].astype(np.float64)), eps=1e-6)
+    np.testing.assert_allclose(qc, ref.numpy(), rtol=1e-12, atol=1e-12)
+    xk = torch.from_numpy(inp["k_raw"][:1].astype(np.float64))
+    refk = torch.nn.functional.rms_norm(xk, (256,), torch.from_numpy(inp["k_gamma"].astype(np.float64)), eps=1e-6)
+    np.testing.assert_allclose(kc, refk.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_prep_rotation_is_multiplication_by_exp_i_theta():
+    # RoFormer's definition: the pair (y_i, y_{i+128}) read as y_i + i y_{i+128} is multiplied by
+    # e^{i p theta_i}, theta_i = base^(-2i/256); the rotated rows against the normed rows at p = 0
+    inp = prep_case(T=4)
+    T, pos0 = 4, 1000
+    qc, kc = oracle.prep(inp["q_raw"], inp["k_raw"], inp["q_gamma"], inp["k_gamma"], T, pos0)
+    for t in range(T):
+        one = {k: v[t:t + 1] for k, v in inp.items() if k.endswith("raw")}
+        q0, k0 = oracle.prep(one["q_raw"], one["k_raw"], inp["q_gamma"], inp["k_gamma"], 1, 0)
+        theta = (pos0 + t) * 10000.0 ** (-2.0 * np.arange(128) / 256)
+        z = (q0[0, :, :128] + 1j * q0[0, :, 128:]) * np.exp(1j * theta)
+        np.testing.assert_allclose(qc[t, :, :128], z.real, rtol=0, atol=1e-11)
+        np.testing.assert_allclose(qc[t, :, 128:], z.imag, rtol=0, atol=1e-11)
+
+
+def test_prep_rotation_keeps_pair_norms_and_depends_only_on_relative_position():
+    inp = prep_case(T=1, seed=13)
+    dots = []
+    for m, n in [(5, 2), (1005, 1002), (60005, 60002)]:
+        qa, _ = oracle.prep(inp["q_raw"], inp["k_raw"], inp["q_gamma"], inp["k_gamma"], 1, m)
+        _, kb = oracle.prep(inp["q_raw"], inp["k_raw"], inp["q_gamma"], inp["k_gamma"], 1, n)
+        dots.append(np.einsum("hd,d->h", qa[0], kb[0, 0]))
+        q0, _ = oracle.prep(inp["q_raw"], inp["k_raw"], inp["q_gamma"], inp["k_gamma"], 1, 0)
+        np.testing.assert_allclose(qa[0, :, :128] ** 2 + qa[0, :, 128:] ** 2, q0[0, :, :128] ** 2 + q0[0, :, 128:] ** 2,
+                                   rtol=1e-12)
+    np.testing.assert_allclose(dots[1], dots[0], rtol=1e-9, atol=1e-9)
+    np.testing.assert_allclose(dots[2], dots[0], rtol=1e-7, atol=1e-7)
+
+
+def test_prep_mrope_with_equal_positions_is_rope_and_sections_pick_components():
+    inp = prep_case(T=2, seed=14)
+    pos3 = np.array([[70, 70, 70], [71, 71, 71]], np.int32)
+    a = oracle.prep(inp["q_raw"], inp["k_raw"], inp["q_gamma"], inp["k_gamma"], 2, 70)
+    b = oracle.prep(inp["q_raw"], inp["k_raw"], inp["q_gamma"], inp["k_gamma"], 2, 0, pos3=pos3)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+    # pairs of section 0 follow component 0 only: changing components 1 and 2 leaves them alone
+    c = oracle.prep(inp["q_raw"], inp["k_raw"], inp["q_gamma"], inp["k_gamma"], 2, 0,
+                    pos3=np.array([[70, 3, 9], [71, 4, 8]], np.int32))
+    np.testing.assert_array_equal(c[0][..., :32], a[0][..., :32])
+    np.testing.assert_array_equal(c[0][..., 128:160], a[0][..., 128:160])
+    assert not np.allclose(c[0][..., 32:128], a[0][..., 32:128])
+
+
+def test_prep_partial_rotary_leaves_the_tail_unrotated():
+    inp = prep_case(T=1, seed=15)
+    q64, _ = oracle.prep(inp["q_raw"], inp["k_raw"], inp["q_gamma"], inp["k_gamma"], 1, 500, rotary_dim=64)
+    q0, _ = oracle.prep(inp["q_raw"], inp["k_raw"], inp["q_gamma"], inp["k_gamma"], 1, 0)
+    np.testing.assert_array_equal(q64[..., 64:], q0[..., 64:])
+    theta = 500 * 10000.0 ** (-2.0 * np.arange(32) / 64)
+    z = (q0[0, :, :32] + 1j * q0[0, :, 32:64]) * np.exp(1j * theta)
+    np.testing.assert_allclose(q64[0, :, :32], z.real, atol=1e-12)
+    np.testing.assert_allclose(q64[0, :, 32:64], z.imag, atol=1e-12)
