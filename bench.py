@@ -378,7 +378,8 @@ def run_ours(args, rank, world, local_rank):
     configs = None
     if not args.no_configs:
         configs = measure_configs(torch, qsa, synth, device, stream, (hbm_gbs, bf16_tf), A, B)
-        for k in ("select_prefill", "decode_select", "decode_partial", "merge", "decode_layer", "decode_layer_batched"):
+        for k in ("select_prefill", "decode_select", "decode_partial", "merge", "decode_layer", "decode_layer_batched",
+                  "prep"):
             if k in configs.get("hbm_calls", {}):
                 per_launch[k] = configs["hbm_calls"][k]
 
@@ -490,6 +491,24 @@ def measure_configs(torch, qsa, synth, device, stream, peaks, A, B, reps=10):
     res["config2_gated"] = prefill_entry(T_PREFILL, 0, LAYERS, *gt(gated2))
     del b0, b1, gates, outg, wsg
 
+    # the fused prep of the same windows (T=1984 new tokens; norm + rotary + quantise into the cache)
+    preps = [{k: torch.from_numpy(v).to(device) for k, v in synth.prep_inputs(T_PREFILL, seed=700 + l).items()}
+             for l in range(LAYERS)]
+    qcur = [torch.empty((T_PREFILL, HEADS, D), dtype=torch.float16, device=device) for _ in range(LAYERS)]
+
+    def prep_all():
+        for l, d in enumerate(A):
+            pi = preps[l]
+            qsa.qsa_prep(pi["q_raw"], pi["k_raw"], pi["v_raw"], pi["q_gamma"], pi["k_gamma"], T_PREFILL, 0, T_PREFILL,
+                         qcur[l], None, d["kq"], d["ksc"], d["vq"], d["vsc"])
+    med, mn = gt(prep_all)
+    per_layer = med / LAYERS
+    by = T_PREFILL * ((HEADS + 4) * D * 2 + HEADS * D * 2 + 2 * 2 * (D + 8))
+    res["prep"] = {"T": T_PREFILL, "us_per_layer": per_layer, "tokens_per_s_per_layer": T_PREFILL / (per_layer * 1e-6),
+                   "bytes": by, "bytes_note": "raw q, k, v rows read; qcur, the int8 K/V rows and scales written",
+                   "hbm": _roof(by / (per_layer * 1e-6) / 1e9, hbm_gbs, "GB/s", "hbm"), "call": "qsa_prep"}
+    del preps, qcur
+
     # config 3: select, then the gathered prefill, and both
     nB = POS0_B + T_PREFILL
     idsB = [torch.empty((T_PREFILL, 2, 2048), dtype=torch.int32, device=device) for _ in range(LAYERS)]
@@ -517,7 +536,8 @@ def measure_configs(torch, qsa, synth, device, stream, peaks, A, B, reps=10):
     e3["flash_tensor"] = _roof(flops_prefill(T_PREFILL, POS0_B) / (f_med / LAYERS * 1e-6) / 1e12, tf_burst,
                                "TFLOP/s", "tensor")
     res["config3"] = e3
-    hbm_calls = {"select_prefill": dict(e3["select_hbm"], call="qsa_select T=1984 pos0=30000")}
+    hbm_calls = {"select_prefill": dict(e3["select_hbm"], call="qsa_select T=1984 pos0=30000"),
+                 "prep": dict(res["prep"]["hbm"], call="qsa_prep T=1984")}
 
     # config 4: decode
     cap = qsa.chunk_cap_for()

@@ -92,6 +92,37 @@ QSA_API const char* qsa_last_error(void);
  */
 QSA_API int qsa_prep_quantize(const uint16_t* x, int64_t n_rows, int8_t* xq, uint16_t* xsc, void* stream);
 
+/* Position-encoding parameters of qsa_prep; a NULL pointer means {10000, 256, 1e-6, {32, 48, 48}}. */
+typedef struct qsa_rope {
+  float base;       /* rotary base: theta_i = p * base^(-2 i / rotary_dim)                           */
+  int rotary_dim;   /* rotated dims per row, a power of two in [16, 256]; dims >= rotary_dim unrotated */
+  float eps;        /* RMS-norm epsilon                                                              */
+  int sections[3];  /* mrope: rotation pairs taken by position components 0, 1, 2 (sum rotary_dim/2) */
+} qsa_rope;
+
+/*
+ * qsa_prep - the fused prep of T new tokens at positions pos0 .. pos0+T-1 (the pages' qsa_prep,
+ * "round 27 track b - qsa prep and merge": decision and rejected prep fusion name its raw rows,
+ * gains, norm_rope step and mrope variants; correctness lists its outputs qcur kq vq ksc vsc).
+ * The pages do not give the formulas; the library's readings:
+ *   q and k rows: y = x / sqrt(mean(x^2) + eps) * gamma (per head row of 256), then the rotary
+ *     embedding with halves paired: for i < rd/2 (rd = rotary_dim),
+ *     (y_i, y_{i+rd/2}) -> (y_i cos th - y_{i+rd/2} sin th, y_{i+rd/2} cos th + y_i sin th),
+ *     th = p * base^(-2 i / rd), p = pos0 + t, or for mrope p = pos3[t][c] with c the position
+ *     component whose section holds pair i (sections[0], [1], [2] consecutive pairs);
+ *   v rows are used as given.
+ * Writes qcur [T][24][256] fp16; kcur [T][2][256] fp16 (the k rows before quantisation; may be
+ * NULL); and cache cell pos0 + t of kq/ksc and vq/vsc ([n_cells][2][256] int8, [n_cells][2][4]
+ * fp16): the qsa_prep_quantize rule applied to kcur's rows and to v_raw's rows.  Other cells are
+ * not touched.
+ *   q_raw [T][24][256], k_raw, v_raw [T][2][256] fp16; q_gamma, k_gamma [256] fp32;
+ *   pos3 [T][3] int32 (DEVICE) or NULL for plain positions.
+ */
+QSA_API int qsa_prep(const uint16_t* q_raw, const uint16_t* k_raw, const uint16_t* v_raw, const float* q_gamma,
+                     const float* k_gamma, const int32_t* pos3, const qsa_rope* rope, int T, int pos0, int n_cells,
+                     uint16_t* qcur, uint16_t* kcur, int8_t* kq, uint16_t* ksc, int8_t* vq, uint16_t* vsc,
+                     void* stream);
+
 /*
  * Bytes of device workspace qsa_select needs for a call with T tokens at pos0 over a
  * cache of n_cells cells (0 when no token of the call is above the identity threshold).

@@ -126,6 +126,44 @@ int qsa_prep_quantize(const uint16_t* x, int64_t n_rows, int8_t* xq, uint16_t* x
   return ok();
 }
 
+int qsa_prep(const uint16_t* q_raw, const uint16_t* k_raw, const uint16_t* v_raw, const float* q_gamma,
+             const float* k_gamma, const int32_t* pos3, const qsa_rope* rope, int T, int pos0, int n_cells,
+             uint16_t* qcur, uint16_t* kcur, int8_t* kq, uint16_t* ksc, int8_t* vq, uint16_t* vsc, void* stream) {
+  qsa_rope r{10000.f, 256, 1e-6f, {32, 48, 48}};
+  if (rope) r = *rope;
+  CHECK_PTR(q_raw, "q_raw");
+  CHECK_PTR(k_raw, "k_raw");
+  CHECK_PTR(v_raw, "v_raw");
+  CHECK_PTR(q_gamma, "q_gamma");
+  CHECK_PTR(k_gamma, "k_gamma");
+  CHECK_PTR(qcur, "qcur");
+  CHECK_PTR(kq, "kq");
+  CHECK_PTR(ksc, "ksc");
+  CHECK_PTR(vq, "vq");
+  CHECK_PTR(vsc, "vsc");
+  if (kcur && !aligned16(kcur)) return fail(QSA_ERR_INVALID_ARG, "kcur is not 16-byte aligned");
+  if (pos3 && (reinterpret_cast<uintptr_t>(pos3) & 3u)) return fail(QSA_ERR_INVALID_ARG, "pos3 is not 4-byte aligned");
+  if (T <= 0) return fail(QSA_ERR_INVALID_ARG, "T must be positive (got %d)", T);
+  if (pos0 < 0) return fail(QSA_ERR_INVALID_ARG, "pos0 must be >= 0 (got %d)", pos0);
+  if ((long long)pos0 + T > (long long)n_cells)
+    return fail(QSA_ERR_INVALID_ARG, "cache too small: pos0 + T = %lld > n_cells = %d", (long long)pos0 + T, n_cells);
+  const int rd = r.rotary_dim;
+  if (rd < 16 || rd > 256 || (rd & (rd - 1)))
+    return fail(QSA_ERR_UNSUPPORTED, "rotary_dim must be a power of two in [16, 256] (got %d)", rd);
+  if (!(r.base > 1.f) || !(r.base < 3.0e38f)) return fail(QSA_ERR_INVALID_ARG, "rope base must be > 1 and finite");
+  if (!(r.eps > 0.f) || !(r.eps < 1.f)) return fail(QSA_ERR_INVALID_ARG, "eps must be in (0, 1)");
+  if (pos3 && (r.sections[0] < 0 || r.sections[1] < 0 || r.sections[2] < 0 ||
+               r.sections[0] + r.sections[1] + r.sections[2] != rd / 2))
+    return fail(QSA_ERR_INVALID_ARG, "mrope sections must be >= 0 and sum to rotary_dim / 2 = %d", rd / 2);
+  cudaError_t e = qsa::launch_prep(
+      reinterpret_cast<const __half*>(q_raw), reinterpret_cast<const __half*>(k_raw),
+      reinterpret_cast<const __half*>(v_raw), q_gamma, k_gamma, pos3, T, pos0, (double)r.base, rd, r.eps, r.sections,
+      reinterpret_cast<__half*>(qcur), reinterpret_cast<__half*>(kcur), kq, reinterpret_cast<__half*>(ksc), vq,
+      reinterpret_cast<__half*>(vsc), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_prep launch");
+  return ok();
+}
+
 size_t qsa_select_workspace_bytes(int T, int pos0, int n_cells, const qsa_params* params) {
   qsa::Params p;
   if (T <= 0 || pos0 < 0 || n_cells <= 0 || resolve_params(params, &p) != QSA_OK) return 0;

@@ -124,6 +124,13 @@ cudaError_t launch_merge(const float* part, const int32_t* n_chunks, int N, int 
 
 cudaError_t launch_quantize(const __half* x, int64_t n_rows, int8_t* xq, __half* xsc, cudaStream_t stream);
 
+// Fused prep (prep.cu): RMS norm + rotary embedding of q and k, qcur / kcur, and the int8 cache
+// rows of cells pos0 .. pos0 + T - 1.
+cudaError_t launch_prep(const __half* q_raw, const __half* k_raw, const __half* v_raw, const float* q_gamma,
+                        const float* k_gamma, const int32_t* pos3, int T, int pos0, double base, int rotary_dim,
+                        float eps, const int* sections, __half* qcur, __half* kcur, int8_t* kq, __half* ksc,
+                        int8_t* vq, __half* vsc, cudaStream_t stream);
+
 size_t select_workspace_bytes(int T, int pos0, int n_cells, Params p);
 cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, int n_cells, int T, int pos0,
                           int32_t* ids, void* ws, Params p, int* status, cudaStream_t stream);

@@ -27,7 +27,7 @@ QSA_ERR_DEVICE = -6
 N_GROUPS, HEADS_PER_GROUP, N_HEADS, HEAD_DIM, CHUNK, PART_STRIDE = 2, 12, 24, 256, 64, 258
 
 # every symbol include/qsa.h declares
-EXPORTS = ("qsa_last_error", "qsa_prep_quantize", "qsa_select_workspace_bytes", "qsa_select",
+EXPORTS = ("qsa_last_error", "qsa_prep_quantize", "qsa_prep", "qsa_select_workspace_bytes", "qsa_select",
            "qsa_flash_prefill_workspace_bytes", "qsa_flash_prefill",
            "qsa_flash_prefill_gated", "qsa_decode_partial", "qsa_merge", "qsa_merge_gated", "qsa_decode_layer",
            "qsa_decode_layer_batched",
@@ -42,6 +42,11 @@ class QSAError(RuntimeError):
 
 class qsa_params(ctypes.Structure):
     _fields_ = [("topk", ctypes.c_int), ("identity_max", ctypes.c_int), ("sm_scale", ctypes.c_float)]
+
+
+class qsa_rope(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_float), ("rotary_dim", ctypes.c_int), ("eps", ctypes.c_float),
+                ("sections", ctypes.c_int * 3)]
 
 
 _lib = None
@@ -60,6 +65,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_last_error.argtypes = []
     lib.qsa_last_error.restype = ctypes.c_char_p
     lib.qsa_prep_quantize.argtypes = [P, I64, P, P, P]
+    lib.qsa_prep.argtypes = [P, P, P, P, P, P, ctypes.POINTER(qsa_rope), I, I, I, P, P, P, P, P, P, P]
     lib.qsa_select_workspace_bytes.argtypes = [I, I, I, PP]
     lib.qsa_select_workspace_bytes.restype = SZ
     lib.qsa_select.argtypes = [P, P, P, I, I, I, P, P, SZ, PP, P]
@@ -116,6 +122,19 @@ def qsa_last_error() -> str:
 def qsa_prep_quantize(x, xq, xsc, stream=None):
     n_rows = x.numel() // HEAD_DIM
     _check(load().qsa_prep_quantize(_ptr(x), n_rows, _ptr(xq), _ptr(xsc), _stream(stream)))
+
+
+def qsa_prep(q_raw, k_raw, v_raw, q_gamma, k_gamma, T: int, pos0: int, n_cells: int, qcur, kcur, kq, ksc, vq, vsc,
+             pos3=None, rope=None, stream=None):
+    """Fused prep: norm + rotary of q and k, qcur / kcur and the new tokens' int8 cache rows.
+    rope: None or (base, rotary_dim, eps, (s0, s1, s2))."""
+    r = None
+    if rope is not None:
+        base, rd, eps, sec = rope
+        r = ctypes.byref(qsa_rope(float(base), int(rd), float(eps), (ctypes.c_int * 3)(*sec)))
+    _check(load().qsa_prep(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(q_gamma), _ptr(k_gamma), _ptr(pos3), r, T,
+                           pos0, n_cells, _ptr(qcur), _ptr(kcur), _ptr(kq), _ptr(ksc), _ptr(vq), _ptr(vsc),
+                           _stream(stream)))
 
 
 def qsa_select_workspace_bytes(T: int, pos0: int, n_cells: int, params=None) -> int:
