@@ -823,7 +823,7 @@ def oracle_sample(seconds_budget=20.0):
     return value, desc, cores, spent
 
 
-PROFILE_CASES = ("dense", "gather", "select", "decode")
+PROFILE_CASES = ("dense", "gather", "select", "decode", "decode_layer", "prep")
 
 
 def run_profile_case(args):
@@ -838,6 +838,21 @@ def run_profile_case(args):
     torch.cuda.set_device(device)
     qsa.load()
     case = args.profile
+    if case == "prep":
+        pi = {k: torch.from_numpy(v).to(device) for k, v in synth.prep_inputs(T_PREFILL, seed=5).items()}
+        n = T_PREFILL
+        kq = torch.empty((n, 2, D), dtype=torch.int8, device=device)
+        vq = torch.empty((n, 2, D), dtype=torch.int8, device=device)
+        ksc = torch.empty((n, 2, 4), dtype=torch.float16, device=device)
+        vsc = torch.empty((n, 2, 4), dtype=torch.float16, device=device)
+        qcur = torch.empty((T_PREFILL, HEADS, D), dtype=torch.float16, device=device)
+        for _ in range(args.warmup + args.steps):
+            qsa.qsa_prep(pi["q_raw"], pi["k_raw"], pi["v_raw"], pi["q_gamma"], pi["k_gamma"], T_PREFILL, 0, n, qcur,
+                         None, kq, ksc, vq, vsc)
+        torch.cuda.synchronize(device)
+        qsa.qsa_check_device_status()
+        print(f"profile case prep: {args.warmup + args.steps} runs done", flush=True)
+        return
     if case == "dense":
         T, pos0 = T_PREFILL, 0
     elif case in ("select", "gather"):
@@ -858,6 +873,9 @@ def run_profile_case(args):
         qsa.qsa_select(d["q"], d["kq"], d["ksc"], n, T, pos0, ids, sws)
 
     def once():
+        if case == "decode_layer":
+            qsa.qsa_decode_layer(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n, T, pos0, ids, xp)
+            return
         if case in ("select", "decode"):
             qsa.qsa_select(d["q"], d["kq"], d["ksc"], n, T, pos0, ids, sws)
         if case in ("dense", "gather"):

@@ -8,12 +8,12 @@
 //   outputs:   qcur = fp16(q rows); kcur = fp16(k rows) (optional); the cache cell pos0 + t gets
 //              quantise(kcur) and quantise(v rows), the absmax rule of qsa_prep_quantize.
 //
-// One CTA (256 threads) per token.  The token's rd/2 rotation angles are formed once: the
-// angle p * inv_freq_i in fp64 (inv_freq from a host-built fp64 table), reduced modulo 2 pi in
-// fp64, then sincosf in fp32 (positions up to 65,536 keep the angle to about 1e-7 rad).  Then a
-// warp per row: lane = 8 consecutive dims (one 16-byte load), the sum of squares by shuffles,
-// the rotation partner (dim +- rd/2) on lane ^ (rd/16), and the quantiser's 64-element blocks
-// on lanes 8b .. 8b+7.
+// One CTA (256 threads) per token; each warp issues the loads of all its rows (and the gains)
+// before it uses any, so a CTA waits on one memory round trip.  The token's rd/2 rotation
+// angles are formed once, in fp32 with the product's error recovered and a three-part 2 pi
+// (rope_angle), then sincosf.  Then a warp per row: lane = 8 consecutive dims (one 16-byte load),
+// the sum of squares by shuffles, the rotation partner (dim +- rd/2) on lane ^ (rd/16), and the
+// quantiser's 64-element blocks on lanes 8b .. 8b+7.
 #include "common.cuh"
 
 namespace qsa {
@@ -22,10 +22,25 @@ namespace {
 constexpr int kPrepRows = kHeads + 2 * kGroups;  // 24 q rows, 2 k rows, 2 v rows per token
 
 struct PrepCfg {
-  double inv_freq[kD / 2];  // base^(-2i / rd), i < rd / 2
+  float inv_hi[kD / 2], inv_lo[kD / 2];  // base^(-2i / rd) as a float pair hi + lo, i < rd / 2
   int rotary_dim, sec0, sec1;
   float eps;
 };
+
+// theta = p * (hi + lo) reduced to about [-pi, pi], all in fp32 (GB300's fp64 rate is low): the
+// product's rounding error is recovered exactly with an fma, and 2 pi is split Cody-Waite style
+// into C1 (8 significant bits, so k * C1 is exact for k < 2^16) + C2 + C3.  For positions up to
+// 2^17 the result is within about 3e-7 of the exact angle modulo 2 pi.
+__device__ __forceinline__ float rope_angle(int p, float hi, float lo) {
+  const float P = (float)p;
+  const float prod = P * hi;
+  const float err = fmaf(P, hi, -prod) + P * lo;  // p * (hi + lo) - prod
+  const float k = rintf(prod * 0.15915494309189535f);
+  float r = fmaf(-k, 6.28125f, prod);  // exact: k * C1 has at most 22 significant bits
+  r = fmaf(-k, 1.9353071795864769e-3f, r);
+  r = fmaf(-k, 1.0253131677018246e-11f, r);
+  return r + err;
+}
 
 // The quantiser of qsa_prep_quantize, on a lane's 8 values of a 64-element block held by the
 // 8 lanes 8b .. 8b+7: IEEE fp32 a / 127 rounded to fp16, codes round-half-away(x / s) clamped.
@@ -59,27 +74,42 @@ __global__ void __launch_bounds__(256) prep_kernel(const __half* __restrict__ q_
   pdl_begin();
   const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rd = cfg.rotary_dim, h2 = rd / 2;
+  // this warp's rows r = warp + 8 j (j < 4, r < 28) and the gains: every load issued before any use
+  constexpr int kRowsPerWarp = (kPrepRows + 7) / 8;
+  uint4 raw[kRowsPerWarp];
+#pragma unroll
+  for (int j = 0; j < kRowsPerWarp; ++j) {
+    const int r = warp + 8 * j;
+    raw[j] = make_uint4(0u, 0u, 0u, 0u);
+    if (r < kPrepRows) {
+      const __half* src = r >= kHeads + kGroups ? v_raw + ((size_t)t * kGroups + (r - kHeads - kGroups)) * kD
+                          : r >= kHeads ? k_raw + ((size_t)t * kGroups + (r - kHeads)) * kD
+                                        : q_raw + ((size_t)t * kHeads + r) * kD;
+      raw[j] = __ldg(reinterpret_cast<const uint4*>(src) + lane);
+    }
+  }
+  const float4 qg0 = __ldg(reinterpret_cast<const float4*>(q_gamma) + 2 * lane);
+  const float4 qg1 = __ldg(reinterpret_cast<const float4*>(q_gamma) + 2 * lane + 1);
+  const float4 kg0 = __ldg(reinterpret_cast<const float4*>(k_gamma) + 2 * lane);
+  const float4 kg1 = __ldg(reinterpret_cast<const float4*>(k_gamma) + 2 * lane + 1);
   if (tid < h2) {
     int p = pos0 + t;
     if (pos3) p = __ldg(pos3 + 3 * t + (tid < cfg.sec0 ? 0 : (tid < cfg.sec0 + cfg.sec1 ? 1 : 2)));
-    const double ang = (double)p * cfg.inv_freq[tid];
-    const double k = rint(ang * 0.15915494309189535);                         // 1 / (2 pi)
-    const double red = fma(-k, 2.4492935982947064e-16, fma(-k, 6.283185307179586, ang));  // ang - 2 pi k
     float sn, cs;
-    sincosf((float)red, &sn, &cs);
+    sincosf(rope_angle(p, cfg.inv_hi[tid], cfg.inv_lo[tid]), &sn, &cs);
     s_cs[tid] = make_float2(cs, sn);
   }
   __syncthreads();
   const int cell = pos0 + t;
-  for (int r = warp; r < kPrepRows; r += 8) {
+#pragma unroll
+  for (int j = 0; j < kRowsPerWarp; ++j) {
+    const int r = warp + 8 * j;
+    if (r >= kPrepRows) break;  // warp-uniform
     const bool is_v = r >= kHeads + kGroups, is_k = !is_v && r >= kHeads;
     const int g = is_v ? r - kHeads - kGroups : r - kHeads;  // group of a k or v row
-    const __half* src = is_v ? v_raw + ((size_t)t * kGroups + g) * kD
-                             : (is_k ? k_raw + ((size_t)t * kGroups + g) * kD : q_raw + ((size_t)t * kHeads + r) * kD);
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src) + lane);
     float x[8];
     {
-      const __half2* h = reinterpret_cast<const __half2*>(&raw);
+      const __half2* h = reinterpret_cast<const __half2*>(&raw[j]);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const float2 f = __half22float2(h[u]);
@@ -94,10 +124,8 @@ __global__ void __launch_bounds__(256) prep_kernel(const __half* __restrict__ q_
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       const float rs = 1.f / sqrtf(ss * (1.f / kD) + cfg.eps);
-      const float* gam = is_k ? k_gamma : q_gamma;
-      const float4 g0 = __ldg(reinterpret_cast<const float4*>(gam) + 2 * lane);
-      const float4 g1 = __ldg(reinterpret_cast<const float4*>(gam) + 2 * lane + 1);
-      const float gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const float gw[8] = {is_k ? kg0.x : qg0.x, is_k ? kg0.y : qg0.y, is_k ? kg0.z : qg0.z, is_k ? kg0.w : qg0.w,
+                           is_k ? kg1.x : qg1.x, is_k ? kg1.y : qg1.y, is_k ? kg1.z : qg1.z, is_k ? kg1.w : qg1.w};
 #pragma unroll
       for (int u = 0; u < 8; ++u) x[u] = x[u] * rs * gw[u];
       // rotation: dims 8 lane + u < rd pair with dim +- h2 on lane ^ (rd / 16)
@@ -147,7 +175,11 @@ cudaError_t launch_prep(const __half* q_raw, const __half* k_raw, const __half* 
                         float eps, const int* sections, __half* qcur, __half* kcur, int8_t* kq, __half* ksc,
                         int8_t* vq, __half* vsc, cudaStream_t stream) {
   PrepCfg cfg{};
-  for (int i = 0; i < rotary_dim / 2; ++i) cfg.inv_freq[i] = pow(base, -2.0 * i / rotary_dim);
+  for (int i = 0; i < rotary_dim / 2; ++i) {
+    const double inv = pow(base, -2.0 * i / rotary_dim);
+    cfg.inv_hi[i] = (float)inv;
+    cfg.inv_lo[i] = (float)(inv - (double)cfg.inv_hi[i]);
+  }
   cfg.rotary_dim = rotary_dim;
   cfg.sec0 = sections[0];
   cfg.sec1 = sections[1];
