@@ -3,7 +3,8 @@
 One step = 12 QSA layers (distinct, seeded synthetic buffers per layer) of each of:
   A  prefill  T=1984 at pos0=0      (identity: every causal cell)       qsa_flash_prefill
   B  prefill  T=1984 at pos0=30000  (31,984-cell cache, top-2048)       qsa_select + qsa_flash_prefill
-  C  decode   N=1 at P=8192         (top-2048, 64-cell split)           qsa_select + qsa_decode_partial + qsa_merge
+  C  decode   N=1 at P=8192         (top-2048)                          qsa_decode_layer (select, attend, merge:
+                                                                          one launch)
 value = identity-prefill tokens per second per layer (T=1984, the pages' own convention: tokens of
 the window / time of one layer), from the A part of the timed steps, times the number of replicas.
 The timed steps replay one CUDA graph per workload (captured from the same API calls); --eager
@@ -193,7 +194,7 @@ def run_ours(args, rank, world, local_rank):
     # our kernel launches per step (the select workspace memset is not counted):
     # A mirror 1 + dense 1; B select 4 (prep_q, prep_k, score, top-k) + mirror 1 + gather 1;
     # C select 2 (score_small, top-k) + partial 1 + merge 1
-    launches_per_step = LAYERS * (2 + 6 + 4)
+    launches_per_step = LAYERS * (2 + 6 + 1)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
@@ -229,12 +230,7 @@ def run_ours(args, rank, world, local_rank):
         for l in range(LAYERS):
             d = C[l]
             mark("Cs")
-            qsa.qsa_select(d["q"], d["kq"], d["ksc"], nC, N_DEC, P_DEC, idsC[l], wsC)
-            mark("Cp")
-            qsa.qsa_decode_partial(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nC, N_DEC, P_DEC, idsC[l], partC,
-                                   nchC, cap)
-            mark("Cm")
-            qsa.qsa_merge(partC, nchC, N_DEC, cap, xpC[l])
+            qsa.qsa_decode_layer(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nC, N_DEC, P_DEC, idsC[l], xpC[l])
         mark("C1")
 
     def step(marks=None):
@@ -316,8 +312,7 @@ def run_ours(args, rank, world, local_rank):
         qsa.qsa_check_device_status()
 
     # ---- per-kernel-family times from the marks (averaged over steps)
-    fam = {"dense_prefill": 0.0, "select_B": 0.0, "gather_prefill": 0.0, "select_C": 0.0, "decode_partial": 0.0,
-           "merge": 0.0}
+    fam = {"dense_prefill": 0.0, "select_B": 0.0, "gather_prefill": 0.0, "decode_layer": 0.0}
     for marks in all_marks:
         names = [m[0] for m in marks]
         evs = [m[1] for m in marks]
@@ -331,11 +326,7 @@ def run_ours(args, rank, world, local_rank):
             elif n == "Bf":
                 fam["gather_prefill"] += dt
             elif n == "Cs":
-                fam["select_C"] += dt
-            elif n == "Cp":
-                fam["decode_partial"] += dt
-            elif n == "Cm":
-                fam["merge"] += dt
+                fam["decode_layer"] += dt
             del nxt
     fam = {k: v / max(1, len(all_marks)) for k, v in fam.items()}  # ms per step (12 launches each)
     # per-workload times of the timed steps: graph replays when available, else the eager marks
@@ -343,7 +334,7 @@ def run_ours(args, rank, world, local_rank):
         sec = {"A": sec_ms[0], "B": sec_ms[1], "C": sec_ms[2]}
     else:
         sec = {"A": fam["dense_prefill"], "B": fam["select_B"] + fam["gather_prefill"],
-               "C": fam["select_C"] + fam["decode_partial"] + fam["merge"]}
+               "C": fam["decode_layer"]}
 
     # ---- e2e: same step through the public API from pinned host buffers
     e2e = None
@@ -391,7 +382,7 @@ def run_ours(args, rank, world, local_rank):
         "[-127,127], fp16 scales U[0.005,0.02])",
         "config": {"workload": "prefill T=1984 pos0=0, 12 QSA layers (identity ids; the value); each timed step "
                                "also runs 12 layers of prefill T=1984 pos0=30000 (31984-cell cache, top-2048) and "
-                               "12 layers of decode N=1 P=8192", "layers": LAYERS,
+                               "12 layers of decode N=1 P=8192 (qsa_decode_layer)", "layers": LAYERS,
                    "heads": "2 KV x 12 q, dim 256", "l2": "inputs larger than L2 (12 distinct layer buffer sets)",
                    "parallelism": f"replicas x{world}"},
         "value_definition": "T / (time of one identity-prefill layer), T = 1984, times replicas",
@@ -672,7 +663,7 @@ def run_e2e(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, p
             "whole_step": {"ms_per_step": full["ms"], "h2d_bytes_per_step": full["h2d"],
                            "d2h_bytes_per_step": full["d2h"],
                            "workload": "12 layers each of prefill T=1984 pos0=0, prefill T=1984 pos0=30000 and "
-                                       "decode N=1 P=8192, with host copies"}}
+                                       "decode N=1 P=8192 (single launch), with host copies"}}
 
 
 def _e2e_leg(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, partC, nchC, xpC, wsB, wsC, pwsA,
@@ -700,10 +691,7 @@ def _e2e_leg(args, torch, qsa, device, stream, A, B, C, outA, outB, idsB, idsC, 
         jobs.append((B[l], hostB[l], run_b, outB[l], hOutB[l]))
     for l in range(LAYERS if "C" in which else 0):
         def run_c(d, l=l):
-            qsa.qsa_select(d["q"], d["kq"], d["ksc"], nC, N_DEC, P_DEC, idsC[l], wsC)
-            qsa.qsa_decode_partial(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nC, N_DEC, P_DEC, idsC[l], partC,
-                                   nchC, cap)
-            qsa.qsa_merge(partC, nchC, N_DEC, cap, xpC[l])
+            qsa.qsa_decode_layer(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], nC, N_DEC, P_DEC, idsC[l], xpC[l])
         jobs.append((C[l], hostC[l], run_c, xpC[l], hXp[l]))
 
     # Copies run on their own streams so that they overlap the kernels of other layers: job j's

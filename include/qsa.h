@@ -278,6 +278,16 @@ QSA_API int qsa_select_noalloc(const uint16_t* q, const int8_t* kq, const uint16
                                int pos0, int32_t* ids, const qsa_params* params, void* stream);
 
 /*
+ * qsa_debug_wait_probe - a test hook for the failure path of the bounded device waits; the
+ * pages have no counterpart.  Launches one CTA whose bounded mbarrier wait (the wait every
+ * pipeline of this library uses) is given budget_ns (1 us .. 2 s) on a barrier that nothing
+ * arrives on, so the wait gives up and sets the device status word: the next
+ * qsa_check_device_status returns QSA_ERR_TIMEOUT and clears it.  Nothing is left in flight,
+ * and the context stays usable.
+ */
+QSA_API int qsa_debug_wait_probe(uint64_t budget_ns, void* stream);
+
+/*
  * qsa_check_device_status - synchronize `stream`, read and clear this device's status
  * word.  Returns QSA_OK, QSA_ERR_TIMEOUT (a bounded wait inside a kernel gave up) or
  * QSA_ERR_DEVICE (an id out of range, a capacity overflow, a bad chunk count).

@@ -363,6 +363,37 @@ int qsa_decode_layer_batched(const uint16_t* q, const int8_t* kq, const int8_t* 
   return ok();
 }
 
+}  // extern "C"
+
+namespace {
+// One warp waits, with the library's bounded mbarrier wait and the given budget, for the first
+// phase of a barrier that nothing arrives on; the wait can only give up, which sets the status
+// word.  Nothing asynchronous is in flight, so the CTA leaves cleanly.
+__global__ void wait_probe_kernel(unsigned long long budget_ns, int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    qsa::mbar_init(&bar, 1);
+    qsa::fence_mbar_init();
+  }
+  __syncthreads();
+  qsa::mbar_wait(&bar, 0u, status, nullptr, budget_ns);
+}
+}  // namespace
+
+extern "C" {
+
+int qsa_debug_wait_probe(uint64_t budget_ns, void* stream) {
+  if (budget_ns < 1000ull || budget_ns > qsa::kWaitBudgetNs)
+    return fail(QSA_ERR_INVALID_ARG, "budget_ns must be in [1000, %llu]", (unsigned long long)qsa::kWaitBudgetNs);
+  int rc = 0;
+  int* st = status_ptr(&rc);
+  if (!st) return rc;
+  wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((unsigned long long)budget_ns, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_debug_wait_probe launch");
+  return ok();
+}
+
 int qsa_check_device_status(void* stream) {
   int rc = 0;
   int* st = status_ptr(&rc);

@@ -54,22 +54,26 @@
 namespace qsa {
 namespace {
 
-constexpr int kFThreads = 256;
+constexpr int kFThreads = 512;
 constexpr int kFWarps = kFThreads / 32;
 constexpr int kMaxW = 4096;          // cells per CTA
 constexpr int kHistBins = 4096;      // top 12 bits of the fp32 order key
-constexpr int kTile = 128;           // cells per scoring tile: 16 per warp
-constexpr int kBoxB = kTile * 128;   // one TMA box: 128 cells x 128 code bytes, 128B-swizzled
-constexpr int kStages = 4;           // scoring ring depth
+constexpr int kTile = 256;           // cells per scoring tile: 16 per warp
+constexpr int kBoxB = kTile * 128;   // one TMA box: 256 cells x 128 code bytes, 128B-swizzled
+constexpr int kStages = 2;           // scoring ring depth
 constexpr int kTileBytes = 2 * kBoxB + kTile * 16;  // codes (two boxes), then both groups' 4 K scales per cell
 constexpr int kRingBytes = kStages * kTileBytes;
 constexpr int kRowB = 272;           // attention: staged code row stride (256 + 16: conflict-free 32-bit reads)
 constexpr int kBatch = 64;           // attention batch (cells)
+constexpr int kQKWarps = kBatch / 8; // warps that form logits: 8 cells each
+constexpr int kDimsPerWarp = kD / kFWarps;  // P.V output dims per warp
+static_assert(kDimsPerWarp == 16, "one ldmatrix.x4.trans (two 8-dim tiles) per 16-cell step");
 constexpr int kBatchBytes = kBatch * kRowB * 2 + kBatch * 32;  // K rows, V rows, K scales, V scales
 constexpr int kVhStride = 264;       // halves per V^ row (528 B: conflict-free ldmatrix)
 constexpr int kQStride = 264;        // halves per staged q row
 constexpr int kPStride = 72;         // halves per P row
-constexpr int kCandPush = 2048;      // candidates a CTA receives by push: kCandPush / C per source
+constexpr int kCandPush = 1792;      // candidates a CTA receives by push: kCandPush / C per source
+constexpr int kDenseOff = 256;       // fast path: own candidates use entries [0, kDenseOff) of their arrays
 constexpr int kCandStage = 768;      // remote candidates staged per round (pull fallback)
 
 // shared-memory map (bytes from a 1024-byte aligned base)
@@ -327,21 +331,23 @@ __global__ void __launch_bounds__(kFThreads, 1)
     for (int i = 0; i < kStages; ++i) issue(i);
     // Qsum (exact), its hi/lo split and the error terms while the first tiles land; thread = dim
     {
-      __half hi, lo;
-      long long e, habs, ex;
-      qsum_split_exact(a.q, t, g, tid, hi, lo, e, habs, ex);
-      s_qsum[tid] = ex;
-      s_hl[tid] = hi;
-      s_hl[256 + tid] = lo;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        e += __shfl_xor_sync(0xffffffffu, e, o);
-        habs += __shfl_xor_sync(0xffffffffu, habs, o);
-      }
       __shared__ long long s_e2[16];
-      if (lane == 0) {
-        s_e2[warp] = e;
-        s_e2[8 + warp] = habs;
+      if (tid < kD) {  // thread = dim
+        __half hi, lo;
+        long long e, habs, ex;
+        qsum_split_exact(a.q, t, g, tid, hi, lo, e, habs, ex);
+        s_qsum[tid] = ex;
+        s_hl[tid] = hi;
+        s_hl[256 + tid] = lo;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          e += __shfl_xor_sync(0xffffffffu, e, o);
+          habs += __shfl_xor_sync(0xffffffffu, habs, o);
+        }
+        if (lane == 0) {
+          s_e2[warp] = e;
+          s_e2[8 + warp] = habs;
+        }
       }
       __syncthreads();
       if (tid < 4) {
@@ -447,17 +453,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     cluster_arrive();
     cluster_wait();  // #2: every CTA holds the cluster's histogram
-    // the bin holding the K-th largest score: thread tid sums the 16 bins 4095-16tid .. 4080-16tid
+    // the bin holding the K-th largest score: thread tid sums the kPerB bins from 4095 - kPerB tid down
     {
-      unsigned cnt = 0;
-      const uint4* hp = reinterpret_cast<const uint4*>(s_hist + kHistBins - 16 * (tid + 1));
-      const uint4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
-      cnt = h0.x + h0.y + h0.z + h0.w + h1.x + h1.y + h1.z + h1.w + h2.x + h2.y + h2.z + h2.w + h3.x + h3.y + h3.z + h3.w;
+      constexpr int kPerB = kHistBins / kFThreads;
+      static_assert(kPerB == 8, "two 16-byte reads per thread");
+      const uint4* hp = reinterpret_cast<const uint4*>(s_hist + kHistBins - kPerB * (tid + 1));
+      const uint4 h0 = hp[0], h1 = hp[1];
+      const unsigned cnt = h0.x + h0.y + h0.z + h0.w + h1.x + h1.y + h1.z + h1.w;
       int tot;
       const int before = block_scan((int)cnt, s_red, &tot);  // counts in higher bins
       if (before < K && before + (int)cnt >= K) {
-        int run = before, bin = kHistBins - 16 * tid - 1;
-        for (; bin >= kHistBins - 16 * (tid + 1); --bin) {
+        int run = before, bin = kHistBins - kPerB * tid - 1;
+        for (; bin >= kHistBins - kPerB * (tid + 1); --bin) {
           run += (int)s_hist[bin];
           if (run >= K) break;
         }
@@ -577,41 +584,51 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     cluster_arrive();
     cluster_wait();  // #3: counts and candidates delivered
-    if (tid == 0) {
-      int in = 0, slow = 0;
-      for (int qq = 0; qq < C; ++qq) {
-        in += s_ccnt[qq][0];
-        slow |= s_ccnt[qq][1] > kSlot;
+    __shared__ int s_coff[17];  // exclusive prefix of the sources' candidate counts
+    if (warp == 0) {  // lane q: source CTA q's counts; sums and prefix by shuffles
+      const int in_q = lane < C ? s_ccnt[lane][0] : 0, nq = lane < C ? s_ccnt[lane][1] : 0;
+      int in = in_q, pre = nq;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, pre, o);
+        if (lane >= o) pre += y;
       }
-      int need = K - in;
-      if (need < 0) {  // cannot happen: surely-in cells lie strictly above the k-th score
-        set_dev_status(a.status, QSA_DEV_BAND_OVERFLOW);
-        need = 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) in += __shfl_xor_sync(0xffffffffu, in, o);
+      const bool over = __any_sync(0xffffffffu, nq > kSlot);
+      if (lane < C) s_coff[lane] = pre - nq;
+      if (lane == C - 1) s_coff[C] = pre;
+      if (lane == 0) {
+        int need = K - in;
+        if (need < 0) {  // cannot happen: surely-in cells lie strictly above the k-th score
+          set_dev_status(a.status, QSA_DEV_BAND_OVERFLOW);
+          need = 0;
+        }
+        s_need = need;
+        s_slow = over;
       }
-      s_need = need;
-      s_slow = slow;
     }
     __syncthreads();
     const bool slow = s_slow != 0;  // uniform over the cluster: every CTA sees the same counts
     const int need = s_need;
     if (!slow) {
-      // the received candidates compacted into dense arrays (source-major), then a warp per own
-      // candidate with its lanes over consecutive entries.  The dense arrays use the tails of the
-      // own-candidate arrays: here nc <= kSlot <= kDenseOff and kDenseOff + kCandPush <= kMaxW
-      constexpr int kDenseOff = kCandPush / 8;
-      static_assert(kDenseOff + kCandPush <= kMaxW, "dense arrays fit");
-      long long* d_hi = c_hi_key + kDenseOff;
-      unsigned long long* d_lo = c_lo_key + kDenseOff;
+      // the received candidates compacted into dense arrays (source-major) in one pass, then a
+      // warp per own candidate with its lanes over consecutive entries.  The dense arrays use the
+      // tails of the own-candidate arrays (here nc <= kSlot <= kDenseOff); a key is one 16-byte
+      // word (lo, hi).
+      static_assert(kCandPush / 8 <= kDenseOff, "own candidates (at most kSlot) stay below the dense arrays");
+      static_assert((kDenseOff + kCandPush) * 16 <= kMaxW * 8, "dense 16-byte keys fit the own hi-key array");
+      static_assert(kDenseOff + kCandPush <= kMaxW, "dense indices fit the own index array");
+      ulonglong2* d_key = reinterpret_cast<ulonglong2*>(c_hi_key) + kDenseOff;  // bytes 16 kDenseOff ..
       int* d_idx = c_idx + kDenseOff;
-      int total = 0;
-      for (int qq = 0; qq < C; ++qq) {
-        const int nq = s_ccnt[qq][1];
-        for (int e = tid; e < nq; e += kFThreads) {
-          d_hi[total + e] = r_hi[qq * kSlot + e];
-          d_lo[total + e] = r_lo[qq * kSlot + e];
-          d_idx[total + e] = r_idx[qq * kSlot + e];
+      const int total = s_coff[C];
+      for (int slot = tid; slot < C * kSlot; slot += kFThreads) {
+        const int qq = slot / kSlot, e = slot - qq * kSlot;
+        if (e < s_ccnt[qq][1]) {
+          const int at = s_coff[qq] + e;
+          d_key[at] = make_ulonglong2(r_lo[slot], (unsigned long long)r_hi[slot]);
+          d_idx[at] = r_idx[slot];
         }
-        total += nq;
       }
       __syncthreads();
       for (int i = warp; i < nc; i += kFWarps) {
@@ -620,7 +637,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
         const int mi = c_idx[i];
         int rank = 0;
 #pragma unroll 4
-        for (int e = lane; e < total; e += 32) rank += ranks_ahead(d_hi[e], d_lo[e], d_idx[e], mh, ml, mi);
+        for (int e = lane; e < total; e += 32) {
+          const ulonglong2 kk = d_key[e];
+          rank += ranks_ahead((long long)kk.y, kk.x, d_idx[e], mh, ml, mi);
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
         if (lane == 0 && rank < need) s_stat[mi - c_lo] = 1;
@@ -664,13 +684,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
     __syncthreads();
     // ---- ascending list of the kept owned cells
     {
-      constexpr int kPerT = kMaxW / kFThreads;  // 16 consecutive cells per thread
-      static_assert(kPerT == 16, "one 16-byte status read per thread");
+      constexpr int kPerT = kMaxW / kFThreads;  // 8 consecutive cells per thread
+      static_assert(kPerT == 8, "one 8-byte status read per thread");
       const int i0 = tid * kPerT;
       uint32_t keep = 0;  // bit u: cell i0 + u is kept
       if (i0 < nloc) {
-        const uint4 w = *reinterpret_cast<const uint4*>(s_stat + i0);
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+        const uint2 w = *reinterpret_cast<const uint2*>(s_stat + i0);
+        const uint32_t ww[2] = {w.x, w.y};
 #pragma unroll
         for (int u = 0; u < kPerT; ++u)
           if (i0 + u < nloc && ((ww[u >> 2] >> (8 * (u & 3))) & 0xFFu) == 1u) keep |= 1u << u;
@@ -692,9 +712,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
   }
 
   // ---- 4. attention over the kept owned cells, batches of 64 (bulk copies, two stages)
-  float o_acc[4][4];
+  float o_acc[2][4];  // O rows r8, r8 + 8 x this warp's 16 dims
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
+  for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
     for (int u = 0; u < 4; ++u) o_acc[nt][u] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};  // heads r8 and r8 + 8 (log2 units)
@@ -750,10 +770,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
         *reinterpret_cast<uint4*>(s_vh + cell * kVhStride + c8 * 8) = outw;
       }
-      // logits of this warp's 8 cells for the 12 heads (rows 12-15 of A are zero)
-      float sc[4];  // (r8, 2j), (r8, 2j+1), (r8+8, 2j), (r8+8, 2j+1)
+      // logits of this warp's 8 cells for the 12 heads (rows 12-15 of A are zero); warps
+      // kQKWarps and above have no cells and only take part in V^ and P.V
+      float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // (r8, 2j), (r8, 2j+1), (r8+8, 2j), (r8+8, 2j+1)
       const bool row1 = r8 + 8 < 12;
-      {
+      const bool qk = warp < kQKWarps;
+      if (qk) {
         float acc[4][4];
 #pragma unroll
         for (int b = 0; b < 4; ++b)
@@ -796,7 +818,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
       }
-      if (j == 0) {
+      if (j == 0 && qk) {
         s_wred[warp][r8] = mx0;
         s_wred[warp][r8 + 8] = mx1;
       }
@@ -806,7 +828,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       for (int hr = 0; hr < 2; ++hr) {
         float m = m_run[hr];
 #pragma unroll
-        for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, s_wred[w][r8 + 8 * hr]);
+        for (int w = 0; w < kQKWarps; ++w) m = fmaxf(m, s_wred[w][r8 + 8 * hr]);
         Mn[hr] = m;
         alpha[hr] = (m == -INFINITY) ? 1.f : fast_exp2(m_run[hr] - m);
       }
@@ -814,7 +836,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       float pr[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) pr[u] = (sc[u] == -INFINITY) ? 0.f : fast_exp2(sc[u] - Mn[u >> 1]);
-      {
+      if (qk) {
         const int cA = 8 * warp + 2 * j;
         *reinterpret_cast<uint32_t*>(s_p + r8 * kPStride + cA) = pack_half2(pr[0], pr[1]);
         *reinterpret_cast<uint32_t*>(s_p + (r8 + 8) * kPStride + cA) = pack_half2(pr[2], pr[3]);
@@ -826,7 +848,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         rs1 += __shfl_xor_sync(0xffffffffu, rs1, o);
       }
       __syncthreads();  // maxima read by all; P and V^ complete; this batch's stage is free
-      if (j == 0) {
+      if (j == 0 && qk) {
         s_wred[warp][r8] = rs0;
         s_wred[warp][r8 + 8] = rs1;
       }
@@ -836,18 +858,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
       for (int hr = 0; hr < 2; ++hr) {
         float rs = 0.f;
 #pragma unroll
-        for (int w = 0; w < kFWarps; ++w) rs += s_wred[w][r8 + 8 * hr];
+        for (int w = 0; w < kQKWarps; ++w) rs += s_wred[w][r8 + 8 * hr];
         l_run[hr] = l_run[hr] * alpha[hr] + rs;
         m_run[hr] = Mn[hr];
       }
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
+      for (int nt = 0; nt < 2; ++nt) {
         o_acc[nt][0] *= alpha[0];
         o_acc[nt][1] *= alpha[0];
         o_acc[nt][2] *= alpha[1];
         o_acc[nt][3] *= alpha[1];
       }
-      // O[16 heads][32 dims of this warp] += P[16][64] x V^[64][32]
+      // O[16 heads][16 dims of this warp] += P[16][64] x V^[64][16]
 #pragma unroll
       for (int kk = 0; kk < kBatch / 16; ++kk) {
         uint32_t pa0, pa1, pa2, pa3;
@@ -855,15 +877,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
           const int row = (lane & 7) + ((lane >> 3) & 1) * 8, col = 16 * kk + (lane >> 4) * 8;
           ldsm_x4(smem_u32(s_p + row * kPStride + col), pa0, pa1, pa2, pa3);
         }
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          uint32_t v0, v1, v2, v3;
-          const int krow = 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int ncol = 32 * warp + 16 * np + (lane >> 4) * 8;
-          ldsm_x4_t(smem_u32(s_vh + krow * kVhStride + ncol), v0, v1, v2, v3);
-          mma16816(o_acc[2 * np], pa0, pa1, pa2, pa3, v0, v1);
-          mma16816(o_acc[2 * np + 1], pa0, pa1, pa2, pa3, v2, v3);
-        }
+        uint32_t v0, v1, v2, v3;
+        const int krow = 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int ncol = kDimsPerWarp * warp + (lane >> 4) * 8;
+        ldsm_x4_t(smem_u32(s_vh + krow * kVhStride + ncol), v0, v1, v2, v3);
+        mma16816(o_acc[0], pa0, pa1, pa2, pa3, v0, v1);
+        mma16816(o_acc[1], pa0, pa1, pa2, pa3, v2, v3);
       }
     }
     cp_async_wait<0>();
@@ -875,8 +894,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
   float* r_l = r_m + 16 * 12;              // [C][12]
   if (!selected) cluster_wait();           // #0 (the selected path waited before its first push)
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-    const int d = 32 * warp + 8 * nt + 2 * j;
+  for (int nt = 0; nt < 2; ++nt) {
+    const int d = kDimsPerWarp * warp + 8 * nt + 2 * j;
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int h = r8 + 8 * hr;

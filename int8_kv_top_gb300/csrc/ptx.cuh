@@ -84,7 +84,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // memory, may be null) lets one failing role release the others early.
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
-                                          volatile int* abort = nullptr) {
+                                          volatile int* abort = nullptr,
+                                          unsigned long long budget_ns = kWaitBudgetNs) {
   if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -92,7 +93,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     if (it > 4) __nanosleep(it < 64 ? 32 : 128);  // back off so waiting warps free the issue slots
     if ((it & 7u) == 0u) {
       if (abort && *abort) return false;
-      if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+      if (globaltimer_ns() - t0 > budget_ns) {
         set_dev_status(status, QSA_DEV_WAIT_TIMEOUT);
         if (abort) *abort = 1;
         return false;

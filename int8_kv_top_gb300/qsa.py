@@ -31,7 +31,7 @@ EXPORTS = ("qsa_last_error", "qsa_prep_quantize", "qsa_prep", "qsa_select_worksp
            "qsa_flash_prefill_workspace_bytes", "qsa_flash_prefill",
            "qsa_flash_prefill_gated", "qsa_decode_partial", "qsa_merge", "qsa_merge_gated", "qsa_decode_layer",
            "qsa_decode_layer_batched",
-           "qsa_check_device_status", "qsa_select_noalloc")
+           "qsa_check_device_status", "qsa_select_noalloc", "qsa_debug_wait_probe")
 
 
 class QSAError(RuntimeError):
@@ -79,6 +79,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_decode_layer.argtypes = [P, P, P, P, P, I, I, I, P, P, P, PP, P]
     lib.qsa_decode_layer_batched.argtypes = [P, P, P, P, P, I64, P, I, I, I, P, P, P, PP, P]
     lib.qsa_check_device_status.argtypes = [P]
+    lib.qsa_debug_wait_probe.argtypes = [ctypes.c_uint64, P]
     lib.qsa_select_noalloc.argtypes = [P, P, P, I, I, I, P, PP, P]
     for name in EXPORTS:
         if name not in ("qsa_last_error", "qsa_select_workspace_bytes", "qsa_flash_prefill_workspace_bytes"):
@@ -199,6 +200,11 @@ def qsa_decode_layer_batched(q, kq, vq, ksc, vsc, n_pool: int, seqs, n_seq: int,
     _check(load().qsa_decode_layer_batched(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), n_pool, _ptr(seqs),
                                            n_seq, n_tok, max_n_kv, _ptr(ids), _ptr(gate), _ptr(xp), _params(params),
                                            _stream(stream)))
+
+
+def qsa_debug_wait_probe(budget_ns: int, stream=None):
+    """Test hook: a bounded device wait that can only give up after budget_ns (sets the status word)."""
+    _check(load().qsa_debug_wait_probe(int(budget_ns), _stream(stream)))
 
 
 def qsa_check_device_status(stream=None):

@@ -134,3 +134,8 @@ def test_decode_layer_and_gated_calls_validate_on_the_host(lib):
     assert lib.qsa_flash_prefill_gated(*args, 100, 4, 0, None, P(FAKE + 2), P(FAKE), P(FAKE), 1 << 20, None,
                                        None) == qsa.QSA_ERR_INVALID_ARG
     assert lib.qsa_merge_gated(P(FAKE), P(FAKE), 1, 33, P(FAKE + 2), P(FAKE), None) == qsa.QSA_ERR_INVALID_ARG
+
+
+def test_wait_probe_rejects_budgets_outside_its_range(lib):
+    assert lib.qsa_debug_wait_probe(10, None) == qsa.QSA_ERR_INVALID_ARG
+    assert lib.qsa_debug_wait_probe(10_000_000_000, None) == qsa.QSA_ERR_INVALID_ARG
