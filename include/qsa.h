@@ -228,8 +228,11 @@ QSA_API int qsa_merge_gated(const float* part, const int32_t* n_chunks, int N, i
  *   ids [N][2][topk] int32, or NULL: the selected ids of tokens above the threshold, ascending,
  *       exactly as qsa_select writes them (rows of identity tokens are not written)
  *   gate [N][24][256] fp16, or NULL: the output gate of qsa_flash_prefill_gated, applied to xp
- * Needs no workspace and allocates nothing.  n_kv of every token must not exceed 65536 cells
- * (32768 on a GPU that cannot co-schedule clusters of 16 CTAs; QSA_ERR_UNSUPPORTED otherwise).
+ * Needs no workspace and allocates nothing.  n_kv of every token must not exceed 131072 cells
+ * (65536 on a GPU that cannot co-schedule clusters of 16 CTAs; QSA_ERR_UNSUPPORTED otherwise).
+ * A (token, group) whose cells hold more than 4096 exactly tied candidates within one of its
+ * 16 slices (massive exact ties, only possible above 65536 cells) is flagged in the status
+ * word (QSA_ERR_DEVICE) instead of ranked.
  */
 QSA_API int qsa_decode_layer(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
                              const uint16_t* vsc, int n_cells, int N, int pos0, int32_t* ids, const uint16_t* gate,
@@ -246,7 +249,7 @@ QSA_API int qsa_decode_layer(const uint16_t* q, const int8_t* kq, const int8_t* 
  *   seqs  DEVICE array [n_seq][4] int32 {first pool cell, n_cells, pos0, first token row},
  *         first token rows increasing from 0; 16-byte aligned
  *   max_n_kv  an upper bound on every token's n_kv (the largest pos0 + token count), at most
- *         65536; it picks the cluster shape
+ *         131072; it picks the cluster shape
  *   gate  [n_tok][24][256] fp16 output gate, or NULL (as in qsa_decode_layer)
  * A sequence whose entry breaks these rules is skipped (its rows are not written) and flagged
  * in the status word (QSA_ERR_DEVICE); so is a token above max_n_kv's cluster capacity.

@@ -10,7 +10,7 @@
 // The pages split this over five dependent dispatches; on GB300 a decode token's work is a
 // few megabytes, so the dispatch chain, not the bytes, set the time.  Here one thread-block
 // cluster of C CTAs (C = 16, or 8) takes one (token, group); CTA r owns the cells
-// [r W, (r + 1) W) of the token's n_kv cells, W = ceil(n_kv / C).  The CTAs exchange data by
+// [r W, (r + 1) W) of the token's n_kv cells, W = ceil(n_kv / C) <= 8192.  The CTAs exchange data by
 // PUSHING it into each other's shared memory (remote stores and adds need no round trip; a
 // remote load costs hundreds of cycles) and a cluster barrier makes it visible:
 //
@@ -56,7 +56,8 @@ namespace {
 
 constexpr int kFThreads = 512;
 constexpr int kFWarps = kFThreads / 32;
-constexpr int kMaxW = 4096;          // cells per CTA
+constexpr int kMaxW = 8192;          // cells per CTA
+constexpr int kOwnCap = 4096;        // a CTA's candidates with exact keys (more: flagged, see below)
 constexpr int kHistBins = 4096;      // top 12 bits of the fp32 order key
 constexpr int kTile = 256;           // cells per scoring tile: 16 per warp
 constexpr int kBoxB = kTile * 128;   // one TMA box: 256 cells x 128 code bytes, 128B-swizzled
@@ -88,10 +89,10 @@ constexpr int kOffSlice = kOffHist + kHistBins * 4;          // u32 [512] the ow
 constexpr int kOffP = kOffSlice + 512 * 4;                   // fp16 [16][kPStride]
 constexpr int kOffBar = kOffP + 16 * kPStride * 2;           // mbarriers of the scoring ring
 constexpr int kSmemBytes = kOffBar + 8 * 8 + 1024;           // + the alignment slack
-// candidates inside the ring region: own keys hi [kMaxW] | lo [kMaxW] | index [kMaxW] |
+// candidates inside the ring region: own keys hi [kOwnCap] | lo [kOwnCap] | index [kOwnCap] |
 // received (pushed) hi [kCandPush] | lo | index | staged copy (pull fallback) hi | lo | index
-constexpr int kCandHi = kOffRing, kCandLo = kCandHi + kMaxW * 8, kCandIdx = kCandLo + kMaxW * 8;
-constexpr int kRcvHi = kCandIdx + kMaxW * 4, kRcvLo = kRcvHi + kCandPush * 8, kRcvIdx = kRcvLo + kCandPush * 8;
+constexpr int kCandHi = kOffRing, kCandLo = kCandHi + kOwnCap * 8, kCandIdx = kCandLo + kOwnCap * 8;
+constexpr int kRcvHi = kCandIdx + kOwnCap * 4, kRcvLo = kRcvHi + kCandPush * 8, kRcvIdx = kRcvLo + kCandPush * 8;
 constexpr int kStgHi = kRcvIdx + kCandPush * 4, kStgLo = kStgHi + kCandStage * 8, kStgIdx = kStgLo + kCandStage * 8;
 static_assert(kStgIdx + kCandStage * 4 <= kOffRing + kRingBytes, "candidates fit the ring region");
 // attention inside the ring region: two batch stages, then V^
@@ -519,7 +520,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
         int slot0 = 0;
         if (lane == 0 && m) slot0 = atomicAdd(&s_cnt_cand, __popc(m));
         slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-        if (st == 2) c_idx[slot0 + __popc(m & ((1u << lane) - 1u))] = c_lo + i;
+        const int slot = slot0 + __popc(m & ((1u << lane) - 1u));
+        if (st == 2 && slot < kOwnCap) c_idx[slot] = c_lo + i;
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) n_in += __shfl_xor_sync(0xffffffffu, n_in, o);
@@ -531,18 +533,19 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     // exact key of each candidate: a warp per candidate, lane = 8 dims; a warp loads the rows
     // of up to four candidates before it uses any
-    const int nc = s_cnt_cand;
-    for (int c4 = 4 * warp; c4 < nc; c4 += 4 * kFWarps) {
+    const int nc = s_cnt_cand;               // may exceed kOwnCap (then the cluster flags and stops ranking)
+    const int nc_st = min(nc, kOwnCap);      // candidates stored with their keys
+    for (int c4 = 4 * warp; c4 < nc_st; c4 += 4 * kFWarps) {
       uint2 w[4], sw[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int c = c4 + u < nc ? c_idx[c4 + u] : c_lo;
+        const int c = c4 + u < nc_st ? c_idx[c4 + u] : c_lo;
         w[u] = __ldg(reinterpret_cast<const uint2*>(kq + ((size_t)c * kGroups + g) * kD + lane * 8));
         sw[u] = __ldg(reinterpret_cast<const uint2*>(ksc + ((size_t)c * kGroups + g) * kNB));
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        if (c4 + u >= nc) break;  // warp-uniform
+        if (c4 + u >= nc_st) break;  // warp-uniform
         long long part = 0;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -596,6 +599,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) in += __shfl_xor_sync(0xffffffffu, in, o);
       const bool over = __any_sync(0xffffffffu, nq > kSlot);
+      // more candidates in one CTA than it keeps keys for (kOwnCap: only massive exact ties among
+      // more than 65,536 cells do that): the ranking would be incomplete, so the token is flagged
+      // and not ranked
+      const bool beyond = __any_sync(0xffffffffu, nq > kOwnCap);
       if (lane < C) s_coff[lane] = pre - nq;
       if (lane == C - 1) s_coff[C] = pre;
       if (lane == 0) {
@@ -605,20 +612,23 @@ __global__ void __launch_bounds__(kFThreads, 1)
           need = 0;
         }
         s_need = need;
-        s_slow = over;
+        s_slow = beyond ? 2 : over;
+        if (beyond && r == 0) set_dev_status(a.status, QSA_DEV_BAND_OVERFLOW);
       }
     }
     __syncthreads();
-    const bool slow = s_slow != 0;  // uniform over the cluster: every CTA sees the same counts
+    const bool slow = s_slow == 1;  // uniform over the cluster: every CTA sees the same counts
     const int need = s_need;
-    if (!slow) {
+    if (s_slow == 2) {
+      // flagged above; the kept set is left at the surely-in cells
+    } else if (!slow) {
       // the received candidates compacted into dense arrays (source-major) in one pass, then a
       // warp per own candidate with its lanes over consecutive entries.  The dense arrays use the
       // tails of the own-candidate arrays (here nc <= kSlot <= kDenseOff); a key is one 16-byte
       // word (lo, hi).
       static_assert(kCandPush / 8 <= kDenseOff, "own candidates (at most kSlot) stay below the dense arrays");
-      static_assert((kDenseOff + kCandPush) * 16 <= kMaxW * 8, "dense 16-byte keys fit the own hi-key array");
-      static_assert(kDenseOff + kCandPush <= kMaxW, "dense indices fit the own index array");
+      static_assert((kDenseOff + kCandPush) * 16 <= kOwnCap * 8, "dense 16-byte keys fit the own hi-key array");
+      static_assert(kDenseOff + kCandPush <= kOwnCap, "dense indices fit the own index array");
       ulonglong2* d_key = reinterpret_cast<ulonglong2*>(c_hi_key) + kDenseOff;  // bytes 16 kDenseOff ..
       int* d_idx = c_idx + kDenseOff;
       const int total = s_coff[C];
@@ -684,13 +694,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
     __syncthreads();
     // ---- ascending list of the kept owned cells
     {
-      constexpr int kPerT = kMaxW / kFThreads;  // 8 consecutive cells per thread
-      static_assert(kPerT == 8, "one 8-byte status read per thread");
+      constexpr int kPerT = kMaxW / kFThreads;  // 16 consecutive cells per thread
+      static_assert(kPerT == 16, "one 16-byte status read per thread");
       const int i0 = tid * kPerT;
       uint32_t keep = 0;  // bit u: cell i0 + u is kept
       if (i0 < nloc) {
-        const uint2 w = *reinterpret_cast<const uint2*>(s_stat + i0);
-        const uint32_t ww[2] = {w.x, w.y};
+        const uint4 w = *reinterpret_cast<const uint4*>(s_stat + i0);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int u = 0; u < kPerT; ++u)
           if (i0 + u < nloc && ((ww[u >> 2] >> (8 * (u & 3))) & 0xFFu) == 1u) keep |= 1u << u;

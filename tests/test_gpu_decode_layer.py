@@ -51,10 +51,10 @@ def test_decode_layer_small_budgets(N, P, params):
     check(inp, N, P, params)
 
 
-def test_decode_layer_longest_context():
-    # n_kv up to 65,536 cells: 4,096 cells per CTA of a 16-CTA cluster
-    N, P = 2, 65534
-    inp = synth.layer_inputs(N, P + N, seed=77)
+@pytest.mark.parametrize("N,P", [(2, 65534), (2, 100000), (1, 131071)])
+def test_decode_layer_long_context(N, P):
+    # long caches: up to 8,192 cells per CTA of a 16-CTA cluster, 131,072 cells in all
+    inp = synth.layer_inputs(N, P + N, seed=77 + P)
     check(inp, N, P)
 
 
