@@ -260,6 +260,52 @@ QSA_API int qsa_decode_layer_batched(const uint16_t* q, const int8_t* kq, const 
                                      const qsa_params* params, void* stream);
 
 /*
+ * Bytes of device workspace qsa_flash_prefill_batched needs: a work list of the identity
+ * tokens' tiles (16 bytes per 64 tokens and per sequence, plus 16) rounded up to 256 bytes,
+ * then the fp16 dequantised K and V rows of every sequence's identity cells, a fixed
+ * R = round_up(min(identity_max, max_n_kv), 128) rows per sequence:
+ * 2 * n_seq * R * 2 * 256 * 2 bytes.  0 for invalid arguments.
+ */
+QSA_API size_t qsa_flash_prefill_batched_workspace_bytes(int n_seq, int n_tok, int max_n_kv,
+                                                         const qsa_params* params);
+
+/*
+ * qsa_flash_prefill_batched - qsa_flash_prefill_gated for many sequences in one call
+ * (continuous batching of prompts: every sequence brings its own new tokens and its own cache),
+ * with the selection of qsa_select done inside the call.  Same pool and seqs table as
+ * qsa_decode_layer_batched: sequence s owns pool cells seqs[s][0] .. seqs[s][0] + seqs[s][1] - 1,
+ * its tokens are rows seqs[s][3] .. seqs[s+1][3] - 1 of q / out / ids (the last runs to n_tok) at
+ * positions seqs[s][2] + 0, 1, ..., and its new tokens' K/V are already in its cells.  Token t of
+ * sequence s attends to the sequence's cells 0 .. n_kv(t) - 1 (n_kv = pos0 + t + 1), all of them
+ * when n_kv <= identity_max ("round 6 track b - qsa flash", delivered change: identity ids under
+ * the budget), else the exact top-k of the select score (as qsa_select ranks it):
+ *   out[t,h,:] = fp16( sum_{c in set(t,g)} softmax_c(sm_scale * q[t,h,:] . k^[c,g,:]) * v^[c,g,:]
+ *                      * (gate ? 1 / (1 + exp(-gate[t,h,:])) : 1) )
+ * The pages run one window per call ("round 27 track b - qsa prep and merge", correctness); this
+ * batched form is the library's.
+ *   seqs  DEVICE [n_seq][4] int32 {first pool cell, n_cells, pos0, first token row}, first token
+ *         rows non-decreasing from 0; 16-byte aligned
+ *   max_n_kv  an upper bound on every token's n_kv (every sequence's pos0 + token count): at most
+ *         131072, and at most qsa_decode_layer's limit when it exceeds identity_max
+ *   ids   [n_tok][2][topk] int32, or NULL: the selected ids of tokens above the threshold,
+ *         ascending (rows of identity tokens are not written)
+ *   gate  [n_tok][24][256] fp16, or NULL
+ *   out   [n_tok][24][256] fp16 (written)
+ *   ws    qsa_flash_prefill_batched_workspace_bytes(n_seq, n_tok, max_n_kv, params) bytes, 16-byte
+ *         aligned, clobbered
+ * Identity tokens run on the tensor cores over per-sequence fp16 mirrors (one work list of
+ * 64-token tiles, heaviest first); selected tokens take the single-launch decode layer's cluster
+ * kernel, whose cost grows with the token count: a sequence with many selected tokens is served
+ * better by qsa_select + qsa_flash_prefill.  A sequence whose entry breaks the cache contract or
+ * exceeds max_n_kv is skipped (its rows are not written) and flagged in the status word
+ * (QSA_ERR_DEVICE).  n_tok and n_seq at most 65535.
+ */
+QSA_API int qsa_flash_prefill_batched(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
+                                      const uint16_t* vsc, int64_t n_pool, const int32_t* seqs, int n_seq, int n_tok,
+                                      int max_n_kv, int32_t* ids, const uint16_t* gate, uint16_t* out, void* ws,
+                                      size_t ws_bytes, const qsa_params* params, void* stream);
+
+/*
  * qsa_select_noalloc - qsa_select without a caller workspace.  The paper has no
  * counterpart: this entry point exists for callers that cannot allocate device memory
  * when they call the layer, for example a runtime whose device memory is all reserved up

@@ -363,6 +363,74 @@ int qsa_decode_layer_batched(const uint16_t* q, const int8_t* kq, const int8_t* 
   return ok();
 }
 
+size_t qsa_flash_prefill_batched_workspace_bytes(int n_seq, int n_tok, int max_n_kv, const qsa_params* params) {
+  qsa::Params p;
+  if (n_seq < 1 || n_tok < 1 || max_n_kv < 1 || resolve_params(params, &p) != QSA_OK) return 0;
+  return qsa::batched_prefill_layout(n_seq, n_tok, max_n_kv, p.identity_max).bytes;
+}
+
+int qsa_flash_prefill_batched(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc,
+                              const uint16_t* vsc, int64_t n_pool, const int32_t* seqs, int n_seq, int n_tok,
+                              int max_n_kv, int32_t* ids, const uint16_t* gate, uint16_t* out, void* ws,
+                              size_t ws_bytes, const qsa_params* params, void* stream) {
+  qsa::Params p;
+  int rc = resolve_params(params, &p);
+  if (rc) return rc;
+  CHECK_PTR(q, "q");
+  CHECK_PTR(kq, "kq");
+  CHECK_PTR(vq, "vq");
+  CHECK_PTR(ksc, "ksc");
+  CHECK_PTR(vsc, "vsc");
+  CHECK_PTR(seqs, "seqs");
+  CHECK_PTR(out, "out");
+  if (ids && !aligned16(ids)) return fail(QSA_ERR_INVALID_ARG, "ids is not 16-byte aligned");
+  if (gate && !aligned16(gate)) return fail(QSA_ERR_INVALID_ARG, "gate is not 16-byte aligned");
+  if (n_pool <= 0) return fail(QSA_ERR_INVALID_ARG, "n_pool must be positive");
+  if (n_seq < 1 || n_tok < 1) return fail(QSA_ERR_INVALID_ARG, "need n_seq >= 1 and n_tok >= 1 (got %d, %d)", n_seq, n_tok);
+  if (n_tok > 65535 || n_seq > 65535)
+    return fail(QSA_ERR_UNSUPPORTED, "n_tok and n_seq must be at most 65535 (got %d, %d)", n_tok, n_seq);
+  const bool any_selected = max_n_kv > p.identity_max;
+  int limit = 131072;  // the dense work list counts up to 1024 super-chunks of 128 cells
+  if (any_selected) {
+    const int l2 = decode_layer_limit(&rc);
+    if (!l2) return rc;
+    limit = l2 < limit ? l2 : limit;
+  }
+  if (max_n_kv < 1 || max_n_kv > limit)
+    return fail(QSA_ERR_UNSUPPORTED, "max_n_kv must be in [1, %d] (got %d)", limit, max_n_kv);
+  const qsa::BatchedPrefillLayout L = qsa::batched_prefill_layout(n_seq, n_tok, max_n_kv, p.identity_max);
+  if (L.mirror_rows > 0x7fffffffLL) return fail(QSA_ERR_UNSUPPORTED, "n_seq x mirror rows per sequence exceeds 2^31");
+  if (!ws || ws_bytes < L.bytes)
+    return fail(QSA_ERR_WORKSPACE, "batched prefill workspace of %zu bytes given, %zu needed", ws ? ws_bytes : (size_t)0,
+                L.bytes);
+  if (!aligned16(ws)) return fail(QSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  int* st = status_ptr(&rc);
+  if (!st) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int4* sq = reinterpret_cast<const int4*>(seqs);
+  const __half* hksc = reinterpret_cast<const __half*>(ksc);
+  const __half* hvsc = reinterpret_cast<const __half*>(vsc);
+  cudaError_t e = qsa::launch_batched_prefill_prep(kq, vq, hksc, hvsc, sq, n_seq, n_tok, (long long)n_pool, max_n_kv,
+                                                   p.identity_max, L, ws, st, s);
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_flash_prefill_batched (work list and mirror) launch");
+  if (L.rows_per_seq > 0) {
+    const int4* plan = static_cast<const int4*>(ws);
+    const __half* khat = reinterpret_cast<const __half*>(static_cast<const uint8_t*>(ws) + L.plan_bytes);
+    const __half* vhat = khat + (size_t)L.mirror_rows * QSA_N_GROUPS * QSA_HEAD_DIM;
+    e = qsa::launch_flash_dense_batched(reinterpret_cast<const __half*>(q), n_tok, reinterpret_cast<const __half*>(gate),
+                                        reinterpret_cast<__half*>(out), plan, L.max_pairs, khat, vhat,
+                                        (int)L.mirror_rows, p.sm_scale, st, s);
+    if (e != cudaSuccess) return cuda_fail(e, "qsa_flash_prefill_batched (identity tokens) launch");
+  }
+  if (any_selected) {
+    e = qsa::launch_decode_layer(reinterpret_cast<const __half*>(q), kq, vq, hksc, hvsc, sq, n_seq, (long long)n_pool, 0,
+                                 0, n_tok, max_n_kv, ids, reinterpret_cast<const __half*>(gate), nullptr, p, st, s,
+                                 reinterpret_cast<__half*>(out), true);
+    if (e != cudaSuccess) return cuda_fail(e, "qsa_flash_prefill_batched (selected tokens) launch");
+  }
+  return ok();
+}
+
 }  // extern "C"
 
 namespace {

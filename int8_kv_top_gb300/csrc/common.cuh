@@ -101,6 +101,24 @@ cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const
 cudaError_t launch_flash_gather(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
                                 cudaStream_t stream);
 
+// Batched prefill (many sequences, the seqs table of the batched decode): a work list of the
+// identity tokens' tiles and one fp16 mirror of rows_per_seq rows per sequence, built on the
+// device (mirror.cu), then the dense kernel over that list.  Workspace: the list (plan_bytes),
+// then K^ and V^ of mirror_rows rows each.
+struct BatchedPrefillLayout {
+  int rows_per_seq, max_pairs;
+  long long mirror_rows;
+  size_t plan_bytes, bytes;
+};
+BatchedPrefillLayout batched_prefill_layout(int n_seq, int n_tok, int max_n_kv, int identity_max);
+cudaError_t launch_batched_prefill_prep(const int8_t* kq, const int8_t* vq, const __half* ksc, const __half* vsc,
+                                        const int4* seqs, int n_seq, int n_tok, long long n_pool, int max_n_kv,
+                                        int identity_max, const BatchedPrefillLayout& L, void* ws, int* status,
+                                        cudaStream_t stream);
+cudaError_t launch_flash_dense_batched(const __half* q, int n_tok, const __half* gate, __half* out, const int4* plan,
+                                       int max_pairs, const __half* khat, const __half* vhat, int mirror_rows,
+                                       float sm_scale, int* status, cudaStream_t stream);
+
 cudaError_t launch_decode_partial(const __half* q, const int8_t* kq, const int8_t* vq, const __half* ksc,
                                   const __half* vsc, const int32_t* ids, float* part, int32_t* n_chunks,
                                   int chunk_cap, int n_cells, int N, int pos0, Params p, int* status,
@@ -114,7 +132,7 @@ cudaError_t decode_layer_max_cluster(int* c);
 cudaError_t launch_decode_layer(const __half* q, const int8_t* kq, const int8_t* vq, const __half* ksc,
                                 const __half* vsc, const int4* seqs, int n_seq, long long n_pool, int n_cells, int pos0,
                                 int n_tok, int max_n_kv, int32_t* ids, const __half* gate, float* xp, Params p,
-                                int* status, cudaStream_t stream);
+                                int* status, cudaStream_t stream, __half* out16 = nullptr, bool selected_only = false);
 
 // Output gate: the elementwise logistic function of the gate input, in fp32.
 __device__ __forceinline__ float gate_sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }

@@ -119,6 +119,8 @@ struct FusedArgs {
   float* xp;         // [n_tok][24][256]
   Params p;
   int* status;
+  __half* out16;     // [n_tok][24][256] fp16 output instead of xp (a prefill), or null
+  int selected_only; // tokens at or under the identity threshold are left to another kernel
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -275,6 +277,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     return;
   }
   const bool selected = n_kv > p.identity_max;
+  if (!selected && a.selected_only) return;  // uniform over the cluster, before any cluster barrier
   const int K = p.topk;
   const int W = (n_kv + C - 1) / C;
   const int c_lo = r * W, c_hi = min(n_kv, c_lo + W), nloc = max(0, c_hi - c_lo);
@@ -945,7 +948,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     float v = O / L;
     if (a.gate) v *= gate_sigmoid(__half2float(a.gate[((size_t)t * kHeads + g * kHPG + h) * kD + d]));
-    a.xp[((size_t)t * kHeads + g * kHPG + h) * kD + d] = v;
+    const size_t o = ((size_t)t * kHeads + g * kHPG + h) * kD + d;
+    if (a.out16) a.out16[o] = __float2half_rn(v);
+    else a.xp[o] = v;
   }
   // ids of a selected token: this CTA's kept cells at the offset of the CTAs before it
   if (selected && a.ids != nullptr) {
@@ -1062,8 +1067,9 @@ cudaError_t decode_layer_max_cluster(int* c) {
 cudaError_t launch_decode_layer(const __half* q, const int8_t* kq, const int8_t* vq, const __half* ksc,
                                 const __half* vsc, const int4* seqs, int n_seq, long long n_pool, int n_cells, int pos0,
                                 int n_tok, int max_n_kv, int32_t* ids, const __half* gate, float* xp, Params p,
-                                int* status, cudaStream_t stream) {
-  FusedArgs a{q, kq, vq, ksc, vsc, seqs, n_seq, n_pool, n_cells, pos0, ids, gate, xp, p, status};
+                                int* status, cudaStream_t stream, __half* out16, bool selected_only) {
+  FusedArgs a{q, kq, vq, ksc, vsc, seqs, n_seq, n_pool, n_cells, pos0, ids, gate, xp, p, status, out16,
+              selected_only ? 1 : 0};
   int state = 0;
   cudaError_t e = device_setup(&state);
   if (e != cudaSuccess) return e;

@@ -81,18 +81,32 @@ struct __align__(8) Bars {
 };
 
 // Items (pair of 32-token tiles, group, head quad), heaviest (latest tokens) first; a
-// cluster takes every nC-th item in snake order so that the clusters' loads even out.
+// cluster takes every nC-th item in snake order so that the clusters' loads even out.  A
+// batched call (many sequences) reads its pairs from a work list built on the device, already
+// sorted heaviest first: {first token row, end of the sequence's identity rows, pos0 - first
+// row of the sequence, first row of the sequence's mirror}.
 struct Item {
   int g, hq, t0p, J;  // t0p: first token of the pair; J: super-chunks
+  int t_end, p0, cbase;  // rows >= t_end are not this item's; n_kv(t) = p0 + t + 1; first mirror row
 };
-__device__ __forceinline__ Item item_at(int q, int n_pairs, int t_begin, int t_end, int pos0) {
+__device__ __forceinline__ Item item_at(int q, const int4* plan, int n_pairs, int t_begin, int t_end, int pos0) {
   Item it;
-  const int pair = n_pairs - 1 - q / 6;
   it.g = (q % 6) / 3;
   it.hq = q % 3;
-  it.t0p = t_begin + pair * 2 * kTok;
-  const int t_last_pair = min(it.t0p + 2 * kTok, t_end) - 1;
-  it.J = (pos0 + t_last_pair + 1 + kKV - 1) / kKV;
+  if (plan != nullptr) {
+    const int4 e = __ldg(&plan[1 + q / 6]);
+    it.t0p = e.x;
+    it.t_end = e.y;
+    it.p0 = e.z;
+    it.cbase = e.w;
+  } else {
+    it.t0p = t_begin + (n_pairs - 1 - q / 6) * 2 * kTok;
+    it.t_end = t_end;
+    it.p0 = pos0;
+    it.cbase = 0;
+  }
+  const int t_last_pair = min(it.t0p + 2 * kTok, it.t_end) - 1;
+  it.J = (it.p0 + t_last_pair + 1 + kKV - 1) / kKV;
   return it;
 }
 __device__ __forceinline__ int item_of(int c, int nC, int n, int n_items) {
@@ -114,7 +128,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     flash_dense_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                        const __grid_constant__ CUtensorMap map_q, const __half* __restrict__ gate,
-                       __half* __restrict__ out, int pos0, int t_begin, int t_end, float scale_log2, int* status) {
+                       __half* __restrict__ out, const int4* __restrict__ plan, int pos0, int t_begin, int t_end,
+                       float scale_log2, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Bars bars;
@@ -125,7 +140,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const int n_ttiles = (t_end - t_begin + kTok - 1) / kTok;
   const int n_pairs = (n_ttiles + 1) / 2;
-  const int n_items = n_pairs * 6;
   const int c = blockIdx.x >> 1, nC = gridDim.x >> 1;
 
   if (tid == 0) {
@@ -159,6 +173,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   pdl_begin();
+  const int n_items = (plan != nullptr ? __ldg(&plan[0].x) : n_pairs) * 6;  // a work list comes from the previous launch
 
   // Global super-chunk index gj (over this cluster's items) drives every ring's stage and phase.
   if (warp == 0 || warp == 2) {
@@ -178,7 +193,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (; ok; ++n) {
         const int q = item_of(c, nC, n, n_items);
         if (q < 0) break;
-        const Item it = item_at(q, n_pairs, t_begin, t_end, pos0);
+        const Item it = item_at(q, plan, n_pairs, t_begin, t_end, pos0);
         if (!is_v) {  // Q tile (rows = 32 tokens x 4 heads, token-major), once the last QK of the previous item is done
           if (n > 0 && !mbar_wait(&bars.q_empty, (n - 1) & 1, status, &s_abort)) break;
           mbar_arrive_expect_tx(&bars.q_full, kQBytes);
@@ -198,11 +213,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (is_v) {  // dims 128 rank .. 128 rank + 127 of the super-chunk's cells
 #pragma unroll
             for (int blk = 0; blk < 2; ++blk)
-              tma_load_3d(dst + blk * (kKV * 128), map, &full[s], (int)rank * 128 + blk * 64, it.g, j * kKV);
+              tma_load_3d(dst + blk * (kKV * 128), map, &full[s], (int)rank * 128 + blk * 64, it.g,
+                          it.cbase + j * kKV);
           } else {     // cells 128 j + 64 rank .. + 63, all dims
 #pragma unroll
             for (int blk = 0; blk < kNB; ++blk)
-              tma_load_3d(dst + blk * ((kKV / 2) * 128), map, &full[s], blk * 64, it.g, j * kKV + (int)rank * (kKV / 2));
+              tma_load_3d(dst + blk * ((kKV / 2) * 128), map, &full[s], blk * 64, it.g,
+                          it.cbase + j * kKV + (int)rank * (kKV / 2));
           }
         }
       }
@@ -220,7 +237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int n = 0; ok; ++n) {
         const int q = item_of(c, nC, n, n_items);
         if (q < 0) break;
-        const Item it = item_at(q, n_pairs, t_begin, t_end, pos0);
+        const Item it = item_at(q, plan, n_pairs, t_begin, t_end, pos0);
         if (!mbar_wait(&bars.q_full, n & 1, status, &s_abort)) break;
         mbar_arrive_cluster(q_rem);
         for (int j = 0; j < it.J; ++j, ++gj) {
@@ -243,7 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int n = 0; ok; ++n) {
         const int q = item_of(c, nC, n, n_items);
         if (q < 0) break;
-        const Item it = item_at(q, n_pairs, t_begin, t_end, pos0);
+        const Item it = item_at(q, plan, n_pairs, t_begin, t_end, pos0);
         for (int j = 0; j < it.J; ++j, ++gj) {
           const int s = gj % kVStages;
           if (!mbar_wait(&bars.v_full[s], (gj / kVStages) & 1, status, &s_abort)) {
@@ -304,7 +321,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int n = 0; ok; ++n) {
         const int q = item_of(c, nC, n, n_items);
         if (q < 0) break;
-        const int J = item_at(q, n_pairs, t_begin, t_end, pos0).J;
+        const int J = item_at(q, plan, n_pairs, t_begin, t_end, pos0).J;
         ok = mbar_wait(&bars.q_full, n & 1, status, &s_abort) && issue_qk(base);
         if (ok && J == 1) umma2_commit(&bars.q_empty, kBothCtas);  // Q no longer read
         for (int j = 0; ok && j < J; ++j) {
@@ -340,13 +357,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int n = 0; ok; ++n) {
     const int q = item_of(c, nC, n, n_items);
     if (q < 0) break;
-    const Item it = item_at(q, n_pairs, t_begin, t_end, pos0);
+    const Item it = item_at(q, plan, n_pairs, t_begin, t_end, pos0);
     const int J = it.J;
     const int t0 = it.t0p + (int)rank * kTok;         // this CTA's first token
-    const int t_last = min(t0 + kTok, t_end) - 1;      // < t0 for an empty tile
+    const int t_last = min(t0 + kTok, it.t_end) - 1;   // < t0 for an empty tile
     const int t = t0 + tl;
     const bool row_valid = t <= t_last;
-    const int n_kv_row = row_valid ? pos0 + t + 1 : 0;
+    const int n_kv_row = row_valid ? it.p0 + t + 1 : 0;
     if (gate != nullptr && row_valid) {
       // the row's gate values (this warpgroup's 128 dims) go to L2 now; the epilogue reads them
       const char* grow = reinterpret_cast<const char*>(
@@ -576,30 +593,40 @@ bool make_q_map(CUtensorMap* map, const __half* q, int T) {
 
 }  // namespace
 
-cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
-                               cudaStream_t stream) {
-  if (t_end <= t_begin) return cudaSuccess;
-  // per device, set once (0 = not yet): the shared-memory attribute and how many CTA pairs fit on
-  // the GPU at once; threads that race here both set the same attribute and store the same count
+namespace {
+
+// Per device, set once (0 = not yet): the shared-memory attribute and how many CTA pairs fit on the
+// GPU at once; threads that race here both set the same attribute and store the same count.
+cudaError_t dense_clusters(int* n_clusters_max) {
   static std::atomic<int> max_clusters[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64) return cudaErrorInvalidDevice;
-  int n_clusters_max = max_clusters[dev].load(std::memory_order_acquire);
-  if (n_clusters_max == 0) {
+  int nc = max_clusters[dev].load(std::memory_order_acquire);
+  if (nc == 0) {
     cudaError_t e = cudaFuncSetAttribute(flash_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemAlloc;
-    int nc = 0;
     e = cudaOccupancyMaxActiveClusters(&nc, flash_dense_kernel, &cfg);
     if (e != cudaSuccess) return e;
     if (nc < 1) return cudaErrorInvalidConfiguration;
     max_clusters[dev].store(nc, std::memory_order_release);
-    n_clusters_max = nc;
   }
+  *n_clusters_max = nc;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
+                               cudaStream_t stream) {
+  if (t_end <= t_begin) return cudaSuccess;
+  int n_clusters_max = 0;
+  cudaError_t e = dense_clusters(&n_clusters_max);
+  if (e != cudaSuccess) return e;
   const int n = a.pos0 + a.T;  // cells in the mirror
   CUtensorMap mk, mv, mq;
   if (!make_mirror_map(&mk, khat, n, kKV / 2) || !make_mirror_map(&mv, vhat, n, kKV) || !make_q_map(&mq, a.q, a.T))
@@ -609,7 +636,23 @@ cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const
   const int n_items = (n_ttiles + 1) / 2 * 6;  // (pair of tiles, group, head quad)
   const int n_clusters = std::min(n_clusters_max, n_items);  // persistent: each takes items in snake order
   return launch_pdl(flash_dense_kernel, dim3(n_clusters * 2), dim3(kThreads), kSmemAlloc, stream, mk, mv, mq, a.gate,
-                    a.out, a.pos0, t_begin, t_end, scale_log2, a.status);
+                    a.out, static_cast<const int4*>(nullptr), a.pos0, t_begin, t_end, scale_log2, a.status);
+}
+
+cudaError_t launch_flash_dense_batched(const __half* q, int n_tok, const __half* gate, __half* out, const int4* plan,
+                                       int max_pairs, const __half* khat, const __half* vhat, int mirror_rows,
+                                       float sm_scale, int* status, cudaStream_t stream) {
+  if (max_pairs <= 0) return cudaSuccess;
+  int n_clusters_max = 0;
+  cudaError_t e = dense_clusters(&n_clusters_max);
+  if (e != cudaSuccess) return e;
+  CUtensorMap mk, mv, mq;
+  if (!make_mirror_map(&mk, khat, mirror_rows, kKV / 2) || !make_mirror_map(&mv, vhat, mirror_rows, kKV) ||
+      !make_q_map(&mq, q, n_tok))
+    return cudaErrorInvalidValue;
+  const int n_clusters = (int)std::min<long long>(n_clusters_max, 6LL * max_pairs);
+  return launch_pdl(flash_dense_kernel, dim3(n_clusters * 2), dim3(kThreads), kSmemAlloc, stream, mk, mv, mq, gate,
+                    out, plan, 0, 0, 0, sm_scale * kLog2e, status);
 }
 
 }  // namespace qsa

@@ -30,7 +30,7 @@ N_GROUPS, HEADS_PER_GROUP, N_HEADS, HEAD_DIM, CHUNK, PART_STRIDE = 2, 12, 24, 25
 EXPORTS = ("qsa_last_error", "qsa_prep_quantize", "qsa_prep", "qsa_select_workspace_bytes", "qsa_select",
            "qsa_flash_prefill_workspace_bytes", "qsa_flash_prefill",
            "qsa_flash_prefill_gated", "qsa_decode_partial", "qsa_merge", "qsa_merge_gated", "qsa_decode_layer",
-           "qsa_decode_layer_batched",
+           "qsa_decode_layer_batched", "qsa_flash_prefill_batched_workspace_bytes", "qsa_flash_prefill_batched",
            "qsa_check_device_status", "qsa_select_noalloc", "qsa_debug_wait_probe")
 
 
@@ -78,11 +78,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_merge_gated.argtypes = [P, P, I, I, P, P, P]
     lib.qsa_decode_layer.argtypes = [P, P, P, P, P, I, I, I, P, P, P, PP, P]
     lib.qsa_decode_layer_batched.argtypes = [P, P, P, P, P, I64, P, I, I, I, P, P, P, PP, P]
+    lib.qsa_flash_prefill_batched_workspace_bytes.argtypes = [I, I, I, PP]
+    lib.qsa_flash_prefill_batched_workspace_bytes.restype = SZ
+    lib.qsa_flash_prefill_batched.argtypes = [P, P, P, P, P, I64, P, I, I, I, P, P, P, P, SZ, PP, P]
     lib.qsa_check_device_status.argtypes = [P]
     lib.qsa_debug_wait_probe.argtypes = [ctypes.c_uint64, P]
     lib.qsa_select_noalloc.argtypes = [P, P, P, I, I, I, P, PP, P]
     for name in EXPORTS:
-        if name not in ("qsa_last_error", "qsa_select_workspace_bytes", "qsa_flash_prefill_workspace_bytes"):
+        if name not in ("qsa_last_error", "qsa_select_workspace_bytes", "qsa_flash_prefill_workspace_bytes",
+                        "qsa_flash_prefill_batched_workspace_bytes"):
             getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -200,6 +204,19 @@ def qsa_decode_layer_batched(q, kq, vq, ksc, vsc, n_pool: int, seqs, n_seq: int,
     _check(load().qsa_decode_layer_batched(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), n_pool, _ptr(seqs),
                                            n_seq, n_tok, max_n_kv, _ptr(ids), _ptr(gate), _ptr(xp), _params(params),
                                            _stream(stream)))
+
+
+def qsa_flash_prefill_batched_workspace_bytes(n_seq: int, n_tok: int, max_n_kv: int, params=None) -> int:
+    return int(load().qsa_flash_prefill_batched_workspace_bytes(n_seq, n_tok, max_n_kv, _params(params)))
+
+
+def qsa_flash_prefill_batched(q, kq, vq, ksc, vsc, n_pool: int, seqs, n_seq: int, n_tok: int, max_n_kv: int, ids,
+                              out, ws, params=None, stream=None, gate=None):
+    """Prefill of many sequences in one call (selection included); seqs is a device int32 tensor [n_seq][4]."""
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().qsa_flash_prefill_batched(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), n_pool, _ptr(seqs),
+                                            n_seq, n_tok, max_n_kv, _ptr(ids), _ptr(gate), _ptr(out), _ptr(ws),
+                                            ws_bytes, _params(params), _stream(stream)))
 
 
 def qsa_debug_wait_probe(budget_ns: int, stream=None):

@@ -209,6 +209,29 @@ def decode_batch(pool: dict, seqs, topk=2048, identity_max=2051, sm_scale=1 / 16
     return out, ids
 
 
+def prefill_batch(pool: dict, seqs, topk=2048, identity_max=2051, sm_scale=1 / 16):
+    """Prefill oracle for many sequences sharing one cell pool (the batched prefill contract, the
+    same seqs table as decode_batch): sequence s is prefill() over its own cells and token rows.
+    Returns (out [n_tok][24][256] float64, ids [n_tok][2][topk], with -1 in the rows of identity
+    tokens)."""
+    seqs = np.asarray(seqs, dtype=np.int64).reshape(-1, 4)
+    n_tok = pool["q"].shape[0]
+    out = np.zeros((n_tok, NH, HD), dtype=np.float64)
+    ids = np.full((n_tok, NG, topk), -1, dtype=np.int32)
+    for s, (c0, n, pos0, t0) in enumerate(seqs):
+        t1 = int(seqs[s + 1][3]) if s + 1 < len(seqs) else n_tok
+        if t1 <= t0:
+            continue
+        sub = {"q": np.ascontiguousarray(pool["q"][t0:t1])}
+        for k in ("kq", "vq", "ksc", "vsc"):
+            sub[k] = np.ascontiguousarray(pool[k][c0:c0 + n])
+        o, sid, _, _ = prefill(sub, int(t1 - t0), int(pos0), topk=topk, identity_max=identity_max, sm_scale=sm_scale)
+        out[t0:t1] = o
+        sel = (pos0 + np.arange(t1 - t0) + 1) > identity_max
+        ids[t0:t1][sel] = sid[sel]
+    return out, ids
+
+
 def apply_gate(out: np.ndarray, gate: np.ndarray) -> np.ndarray:
     """Output gate: out * sigmoid(gate), elementwise in float64 (a new array; gate fp16, out's shape)."""
     res = np.ascontiguousarray(out, dtype=np.float64).copy()

@@ -136,6 +136,33 @@ def test_decode_layer_and_gated_calls_validate_on_the_host(lib):
     assert lib.qsa_merge_gated(P(FAKE), P(FAKE), 1, 33, P(FAKE + 2), P(FAKE), None) == qsa.QSA_ERR_INVALID_ARG
 
 
+def test_batched_prefill_validates_on_the_host(lib):
+    P = ctypes.c_void_p
+    args = (P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE))
+    # workspace: a 256-byte-rounded work list, then K^ and V^ of round_up(min(2051, max_n_kv), 128)
+    # rows per sequence, 2 groups x 256 fp16 each
+    assert lib.qsa_flash_prefill_batched_workspace_bytes(3, 10, 100, None) == 256 + 2 * 3 * 128 * 2 * 256 * 2
+    assert lib.qsa_flash_prefill_batched_workspace_bytes(2, 1000, 9000, None) == \
+        (1 + 1000 // 64 + 2) * 16 // 256 * 256 + 256 + 2 * 2 * 2176 * 2 * 256 * 2
+    assert lib.qsa_flash_prefill_batched_workspace_bytes(0, 10, 100, None) == 0
+    ws = 1 << 24
+    # qsa_flash_prefill_batched(q, kq, vq, ksc, vsc, n_pool, seqs, n_seq, n_tok, max_n_kv, ids, gate, out, ws,
+    #                           ws_bytes, params, stream)
+    call = lib.qsa_flash_prefill_batched
+    assert call(*args, 100, None, 1, 1, 100, None, None, P(FAKE), P(FAKE), ws, None, None) == qsa.QSA_ERR_INVALID_ARG
+    assert call(*args, 100, P(FAKE), 1, 1, 100, None, None, None, P(FAKE), ws, None, None) == qsa.QSA_ERR_INVALID_ARG
+    assert call(*args, 100, P(FAKE), 0, 1, 100, None, None, P(FAKE), P(FAKE), ws, None, None) == qsa.QSA_ERR_INVALID_ARG
+    assert call(*args, 100, P(FAKE), 1, 1, 100, None, P(FAKE + 2), P(FAKE), P(FAKE), ws, None, None) == \
+        qsa.QSA_ERR_INVALID_ARG                                                      # misaligned gate
+    assert call(*args, 100, P(FAKE), 1, 70000, 100, None, None, P(FAKE), P(FAKE), ws, None, None) == \
+        qsa.QSA_ERR_UNSUPPORTED                                                      # n_tok > 65535
+    assert call(*args, 100, P(FAKE), 1, 1, 0, None, None, P(FAKE), P(FAKE), ws, None, None) == qsa.QSA_ERR_UNSUPPORTED
+    assert call(*args, 100, P(FAKE), 1, 1, 100, None, None, P(FAKE), P(FAKE), 1000, None, None) == \
+        qsa.QSA_ERR_WORKSPACE                                                        # too small
+    assert call(*args, 100, P(FAKE), 1, 1, 100, None, None, P(FAKE), P(FAKE + 8), ws, None, None) == \
+        qsa.QSA_ERR_INVALID_ARG                                                      # misaligned ws
+
+
 def test_wait_probe_rejects_budgets_outside_its_range(lib):
     assert lib.qsa_debug_wait_probe(10, None) == qsa.QSA_ERR_INVALID_ARG
     assert lib.qsa_debug_wait_probe(10_000_000_000, None) == qsa.QSA_ERR_INVALID_ARG

@@ -337,6 +337,54 @@ def test_batched_decode_oracle_is_per_sequence_decode_on_its_slice():
 
 
 
+def test_batched_prefill_oracle_matches_brute_force_over_the_pool():
+    # three sequences at different pool offsets (one with an unused gap of cells before it, one
+    # with no tokens): every token's set is found from the pool rows by brute force (identity
+    # range, or the exact rational top-k with ties to the lower index), then plain float64 softmax
+    # attention of its 12 heads; the batch oracle must agree to rounding
+    topk, idmax = 4, 7
+    lens = [(9, 3, 4), (12, 10, 2), (5, 5, 0), (20, 6, 3)]         # (n_cells, pos0, tokens)
+    gap = 6
+    pieces = [tiny_inputs(max(nt, 1), n, seed=40 + i) for i, (n, p0, nt) in enumerate(lens)]
+    q = np.concatenate([pc["q"][:nt] for pc, (n, p0, nt) in zip(pieces, lens)], axis=0)
+    pool, seqs, c0, t0 = {k: [] for k in ("kq", "vq", "ksc", "vsc")}, [], 0, 0
+    for i, ((n, p0, nt), pc) in enumerate(zip(lens, pieces)):
+        if i == 1:   # unused pool cells before sequence 1
+            filler = tiny_inputs(1, gap, seed=99)
+            for k in pool:
+                pool[k].append(filler[k])
+            c0 += gap
+        for k in pool:
+            pool[k].append(pc[k])
+        seqs.append((c0, n, p0, t0))
+        c0 += n
+        t0 += nt
+    pool = {k: np.concatenate(v, axis=0) for k, v in pool.items()}
+    pool["q"] = q
+    out, ids = oracle.prefill_batch(pool, seqs, topk=topk, identity_max=idmax)
+    k_all, v_all = dequant(pool["kq"], pool["ksc"]), dequant(pool["vq"], pool["vsc"])
+    n_tok = q.shape[0]
+    for r in range(n_tok):
+        s = max(i for i, e in enumerate(seqs) if e[3] <= r and (i + 1 == len(seqs) or seqs[i + 1][3] > r))
+        cfirst, _, p0, tfirst = seqs[s]
+        n_kv = p0 + (r - tfirst) + 1
+        for g in range(NG):
+            if n_kv <= idmax:
+                cells = np.arange(n_kv)
+                assert (ids[r, g] == -1).all()
+            else:
+                sub_kq = pool["kq"][cfirst:cfirst + n_kv]
+                sub_ksc = pool["ksc"][cfirst:cfirst + n_kv]
+                sc = exact_scores(q[r], sub_kq, sub_ksc, g, n_kv)
+                cells = np.sort(sorted(range(n_kv), key=lambda c: (-sc[c], c))[:topk])
+                np.testing.assert_array_equal(ids[r, g], cells)
+            kk, vv = k_all[cfirst + cells, g], v_all[cfirst + cells, g]
+            for h in range(HPG):
+                logit = (kk @ q[r, g * HPG + h].astype(np.float64)) / 16
+                w = np.exp(logit - logit.max())
+                np.testing.assert_allclose(out[r, g * HPG + h], (w / w.sum()) @ vv, rtol=1e-12, atol=1e-13)
+
+
 # ------------------------------------------------------------------ output gate
 def test_gate_zero_halves_and_symmetric_gates_sum_to_the_output():
     rng = np.random.default_rng(8)
