@@ -373,6 +373,9 @@ def run_ours(args, rank, world, local_rank):
                   "prep"):
             if k in configs.get("hbm_calls", {}):
                 per_launch[k] = configs["hbm_calls"][k]
+        if "prefill_batched" in configs:
+            per_launch["prefill_batched"] = dict(configs["prefill_batched"]["hbm"],
+                                                 call="qsa_flash_prefill_batched 64 x T=128")
 
     value = whole_job_rate(max_over_ranks(sec["A"], dist, device), world)
     line = {
@@ -643,6 +646,43 @@ def measure_configs(torch, qsa, synth, device, stream, peaks, A, B, reps=10):
                              "call": "qsa_decode_layer_batched, one launch"}
     hbm_calls["decode_layer_batched"] = dict(res["decode_batched"]["hbm"], call="qsa_decode_layer_batched 64 x P=8192")
     del pool
+    # continuous batching of prompts: 64 sequences of 128 new tokens each (no cached prefix) in one
+    # batched prefill call, against the same 64 prompts as 64 single-sequence calls
+    P_SEQ, P_T = 64, 128
+    parts = [synth.layer_inputs(P_T, P_T, seed=3500 + b) for b in range(P_SEQ)]
+    pool = {k: torch.from_numpy(np.concatenate([pc[k] for pc in parts], axis=0)).to(device)
+            for k in ("q", "kq", "vq", "ksc", "vsc")}
+    singles = [up(pc) for pc in parts]
+    del parts
+    seqs = torch.tensor([[b * P_T, P_T, 0, b * P_T] for b in range(P_SEQ)], dtype=torch.int32, device=device)
+    n_tok = P_SEQ * P_T
+    out_p = torch.empty((n_tok, HEADS, D), dtype=torch.float16, device=device)
+    ws_p = torch.empty(qsa.qsa_flash_prefill_batched_workspace_bytes(P_SEQ, n_tok, P_T), dtype=torch.uint8,
+                       device=device)
+
+    def fpb():
+        qsa.qsa_flash_prefill_batched(pool["q"], pool["kq"], pool["vq"], pool["ksc"], pool["vsc"], n_tok, seqs, P_SEQ,
+                                      n_tok, P_T, None, out_p, ws_p)
+    med, mn = gt(fpb)
+    outs1 = [torch.empty((P_T, HEADS, D), dtype=torch.float16, device=device) for _ in range(P_SEQ)]
+    ws1 = torch.empty(qsa.qsa_flash_prefill_workspace_bytes(P_T, 0, P_T), dtype=torch.uint8, device=device)
+
+    def floop():
+        for b, d in enumerate(singles):
+            qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], P_T, P_T, 0, None, outs1[b], ws1)
+    med1, _ = gt(floop)
+    fl = P_SEQ * flops_prefill(P_T, 0)
+    # short prompts move more bytes than they compute: q in, out back (fp16), every cell's int8
+    # K/V codes and fp16 scales once
+    by = 2 * n_tok * HEADS * D * 2 + n_tok * 2 * 2 * (D + 8)
+    res["prefill_batched"] = {"sequences": P_SEQ, "tokens_per_sequence": P_T, "pos0": 0, "us_per_call": med,
+                              "us_per_call_min": mn, "tokens_per_s": n_tok / (med * 1e-6),
+                              "us_for_single_calls": med1, "gflop": fl / 1e9, "bytes": by,
+                              "hbm": _roof(by / (med * 1e-6) / 1e9, hbm_gbs, "GB/s", "hbm"),
+                              "tensor": _roof(fl / (med * 1e-6) / 1e12, tf_burst, "TFLOP/s", "tensor"),
+                              "call": "qsa_flash_prefill_batched (work list + mirror + dense: 3 launches), against "
+                                      "64 qsa_flash_prefill calls in one graph"}
+    del pool, singles, outs1
     res["hbm_calls"] = hbm_calls
     return res
 
@@ -812,7 +852,7 @@ def oracle_sample(seconds_budget=20.0):
     return value, desc, cores, spent
 
 
-PROFILE_CASES = ("dense", "gather", "select", "decode", "decode_layer", "prep")
+PROFILE_CASES = ("dense", "gather", "select", "decode", "decode_layer", "prep", "batched")
 
 
 def run_profile_case(args):
@@ -841,6 +881,23 @@ def run_profile_case(args):
         torch.cuda.synchronize(device)
         qsa.qsa_check_device_status()
         print(f"profile case prep: {args.warmup + args.steps} runs done", flush=True)
+        return
+    if case == "batched":  # 64 prompts of 128 tokens in one qsa_flash_prefill_batched call
+        n_seq, tp = 64, 128
+        parts = [synth.layer_inputs(tp, tp, seed=3500 + b) for b in range(n_seq)]
+        pool = {k: torch.from_numpy(np.concatenate([pc[k] for pc in parts], axis=0)).to(device)
+                for k in ("q", "kq", "vq", "ksc", "vsc")}
+        seqs = torch.tensor([[b * tp, tp, 0, b * tp] for b in range(n_seq)], dtype=torch.int32, device=device)
+        n_tok = n_seq * tp
+        out = torch.empty((n_tok, HEADS, D), dtype=torch.float16, device=device)
+        ws = torch.empty(qsa.qsa_flash_prefill_batched_workspace_bytes(n_seq, n_tok, tp), dtype=torch.uint8,
+                         device=device)
+        for _ in range(args.warmup + args.steps):
+            qsa.qsa_flash_prefill_batched(pool["q"], pool["kq"], pool["vq"], pool["ksc"], pool["vsc"], n_tok, seqs,
+                                          n_seq, n_tok, tp, None, out, ws)
+        torch.cuda.synchronize(device)
+        qsa.qsa_check_device_status()
+        print(f"profile case batched: {args.warmup + args.steps} runs done", flush=True)
         return
     if case == "dense":
         T, pos0 = T_PREFILL, 0

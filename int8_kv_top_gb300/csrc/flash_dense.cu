@@ -276,7 +276,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ rank 0: MMA issue
     // One thread issues QK(j + 1) before PV(j), so the in-order tensor pipe never holds the
     // S of the next super-chunk behind a PV: QK(j + 1) needs its buffer back from PV(j - 1)
-    // (the two share no accumulator, so that completion is awaited), PV(j) needs P(j).
+    // (the two share no accumulator, so that completion is awaited), PV(j) needs P(j).  The
+    // thread polls (no suspend, no sleep): the tensor pipe's instruction queue is short, and a
+    // late wake-up after a completion leaves it idle.
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_f16_f32(2 * kRows, kKV, 0, 0);
       const uint32_t idesc_pv = idesc_f16_f32(2 * kRows, kD, 0, 1);
@@ -286,8 +288,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // overwrites O, so the previous item's O must have been read out (o_free)
       auto issue_qk = [&](int gj) -> bool {
         const int b = gj % kNS, s = gj % kKStages;
-        if (gj >= kNS && !mbar_wait(&bars.pv_done[b], ((gj / kNS) - 1) & 1, status, &s_abort)) return false;
-        if (!mbar_wait(&bars.k_full[s], (gj / kKStages) & 1, status, &s_abort)) return false;
+        if (gj >= kNS && !mbar_wait_poll(&bars.pv_done[b], ((gj / kNS) - 1) & 1, status, &s_abort)) return false;
+        if (!mbar_wait_poll(&bars.k_full[s], (gj / kKStages) & 1, status, &s_abort)) return false;
         tc_fence_after();
         const uint64_t kdesc = sdesc_sw128(k0 + s * kHalfK, 16, 1024);
         const uint32_t scol = tmem + kColS + b * kKV;
@@ -302,8 +304,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int gj, bool restart) -> bool {
         const int b = gj % kNS, s = gj % kVStages;
-        if (!mbar_wait(&bars.p_full[b], (gj / kNS) & 1, status, &s_abort)) return false;
-        if (!mbar_wait(&bars.v_full[s], (gj / kVStages) & 1, status, &s_abort)) return false;
+        if (!mbar_wait_poll(&bars.p_full[b], (gj / kNS) & 1, status, &s_abort)) return false;
+        if (!mbar_wait_poll(&bars.v_full[s], (gj / kVStages) & 1, status, &s_abort)) return false;
         tc_fence_after();
         // descriptor built once; the start-address field (bytes >> 4, low bits) advances per K step
         const uint64_t vdesc = sdesc_sw128(v0 + s * kHalfV, kKV * 128, 1024);
@@ -322,14 +324,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int q = item_of(c, nC, n, n_items);
         if (q < 0) break;
         const int J = item_at(q, plan, n_pairs, t_begin, t_end, pos0).J;
-        ok = mbar_wait(&bars.q_full, n & 1, status, &s_abort) && issue_qk(base);
+        ok = mbar_wait_poll(&bars.q_full, n & 1, status, &s_abort) && issue_qk(base);
         if (ok && J == 1) umma2_commit(&bars.q_empty, kBothCtas);  // Q no longer read
         for (int j = 0; ok && j < J; ++j) {
           if (j + 1 < J) {
             ok = issue_qk(base + j + 1);
             if (ok && j + 2 == J) umma2_commit(&bars.q_empty, kBothCtas);
           }
-          if (ok && j == 0 && n > 0) ok = mbar_wait(&bars.o_free, (n - 1) & 1, status, &s_abort);
+          if (ok && j == 0 && n > 0) ok = mbar_wait_poll(&bars.o_free, (n - 1) & 1, status, &s_abort);
           ok = ok && issue_pv(base + j, j == 0);
         }
         base += J;

@@ -102,6 +102,47 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// Bounded wait that polls without suspending or sleeping (mbarrier.test_wait), for a thread
+// whose latency after the phase completes is on the critical path (a tensor-core issue thread
+// feeding a short instruction queue).  The timer is read only once the first poll has failed.
+template <bool kCluster = true>
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, int* status,
+                                               volatile int* abort = nullptr) {
+  auto test = [&]() -> bool {
+    uint32_t ok;
+    if (kCluster)
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(smem_u32(bar)), "r"(parity)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(smem_u32(bar)), "r"(parity)
+          : "memory");
+    return ok != 0;
+  };
+  if (test()) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (test()) return true;
+    if ((it & 63u) == 0u) {
+      if (abort && *abort) return false;
+      if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+        set_dev_status(status, QSA_DEV_WAIT_TIMEOUT);
+        if (abort) *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Warp-uniform bounded wait: every lane waits, and the warp proceeds only if all lanes
 // saw the phase complete (so warp-collective tcgen05 operations never diverge).
 template <bool kCluster = false>
