@@ -126,3 +126,48 @@ def test_decode_end_to_end_with_select(N, P):
     check_ids(ids.cpu().numpy(), ref_ids, N, P, 2051)
     np.testing.assert_array_equal(nch.cpu().numpy(), ref_nc)
     assert_close(xp.cpu().numpy(), ref_out, f"decode N={N} P={P}")
+
+
+# ---- the score-GEMM path (more than 8 selected rows) on tied and structured caches
+
+def test_gemm_path_exact_ties_resolve_to_lower_index():
+    # every cell identical: all scores tie exactly, the band holds every cell (the top-k's
+    # large-band exact radix select)
+    T, pos0 = 16, 5000
+    inp = synth.layer_inputs(T, pos0 + T, seed=4)
+    inp["kq"][:] = inp["kq"][0]
+    inp["ksc"][:] = inp["ksc"][0]
+    ids, out = gpu_select_prefill(inp, T, pos0)
+    np.testing.assert_array_equal(ids, np.broadcast_to(np.arange(2048, dtype=np.int32), ids.shape))
+
+
+def test_gemm_path_near_ties_from_duplicates():
+    T, pos0 = 24, 3000
+    inp = synth.layer_inputs(T, pos0 + T, seed=22)
+    src = np.arange(0, 3000, 7)
+    inp["kq"][src + 3] = inp["kq"][src]
+    inp["ksc"][src + 3] = inp["ksc"][src]
+    ids, out = gpu_select_prefill(inp, T, pos0)
+    ref_out, ref_ids, _, _ = oracle.prefill(inp, T, pos0)
+    np.testing.assert_array_equal(ids, ref_ids)
+    assert_close(out, ref_out, "duplicates, GEMM path")
+
+
+def test_gemm_path_periodic_cache():
+    # every 8th cell points along the first 8 tokens' query sum and outscores everything else
+    # (a periodic structure that a sampled bracket sees in full); the other 8 tokens have their
+    # own queries.  Both must give the exact ranking.
+    T, pos0 = 16, 6000
+    n = pos0 + T
+    inp = synth.layer_inputs(T, n, seed=31)
+    inp["q"][1:8] = inp["q"][0]
+    qsum = inp["q"][0].astype(np.float64).reshape(2, 12, 256).sum(axis=1)  # [group][dim]
+    hot = np.arange(0, n, 8)
+    for g in range(2):
+        inp["kq"][hot, g, :] = np.where(qsum[g] >= 0, 100, -100).astype(np.int8)
+        inp["ksc"][hot, g, :] = np.float16(0.02)
+    ids, out = gpu_select_prefill(inp, T, pos0)
+    ref_out, ref_ids, _, _ = oracle.prefill(inp, T, pos0)
+    np.testing.assert_array_equal(ids, ref_ids)
+    assert_close(out, ref_out, "periodic cache")
+    assert np.isin(hot[hot < pos0 + 1], ids[0, 0]).all()  # the hot cells are all kept
