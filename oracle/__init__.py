@@ -156,6 +156,8 @@ def prefill(inp: dict, T: int, pos0: int, toks=None, topk=2048, identity_max=205
             f64_check=False):
     """Prefill oracle over tokens `toks` (default all): (out [n][24][256], ids [n][2][topk], n_set [n][2], differs)."""
     toks = np.arange(T, dtype=np.int32) if toks is None else np.ascontiguousarray(toks, dtype=np.int32)
+    # the cache contract: every token's causal cells exist (the C code reads cells 0 .. pos0 + t)
+    assert inp["kq"].shape[0] >= pos0 + T and inp["q"].shape[0] >= T, "cache or query rows too short"
     n = len(toks)
     out = np.zeros((n, NH, HD), dtype=np.float64)
     ids = np.zeros((n, NG, topk), dtype=np.int32)
@@ -174,6 +176,7 @@ def chunk_cap_for(topk=2048, identity_max=2051) -> int:
 
 def decode(inp: dict, N: int, P: int, topk=2048, identity_max=2051, sm_scale=1 / 16):
     """Decode oracle: (part [N][cap][24][258], n_chunks [N], merged [N][24][256], direct [N][24][256], ids [N][2][topk])."""
+    assert inp["kq"].shape[0] >= P + N and inp["q"].shape[0] >= N, "cache or query rows too short"
     cap = chunk_cap_for(topk, identity_max)
     part = np.full((N, cap, NH, PSTRIDE), np.nan, dtype=np.float64)
     n_chunks = np.zeros(N, dtype=np.int32)

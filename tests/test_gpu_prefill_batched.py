@@ -138,5 +138,14 @@ def test_batched_prefill_flags_a_bad_sequence_and_keeps_the_rest():
     assert e.value.code == qsa.QSA_ERR_DEVICE
     out = out.float().cpu().numpy()
     assert np.isnan(out[300:]).all()   # the bad sequence's rows are not written
-    ref_out, _ = oracle.prefill_batch({k: v for k, v in pool.items()}, seqs[:1], topk=2048)
-    assert_close(out[:300], ref_out[:300], "the good sequence")
+    good = dict(pool)
+    good["q"] = pool["q"][:300]        # the good sequence's own tokens only
+    ref_out, _ = oracle.prefill_batch(good, seqs[:1], topk=2048)
+    assert_close(out[:300], ref_out, "the good sequence")
+
+
+def test_batched_prefill_long_context_next_to_short_prompts():
+    # a 100,004-cell sequence (selection in 16-CTA clusters) beside short prompts and a boundary one
+    specs = [(100004, 100000, 4), (200, 0, 200), (2060, 2040, 20)]
+    pool, seqs = make_pool(specs, seed0=2700, gap=2)
+    check(pool, seqs, max_n_kv=100004)

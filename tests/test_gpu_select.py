@@ -171,3 +171,14 @@ def test_gemm_path_periodic_cache():
     np.testing.assert_array_equal(ids, ref_ids)
     assert_close(out, ref_out, "periodic cache")
     assert np.isin(hot[hot < pos0 + 1], ids[0, 0]).all()  # the hot cells are all kept
+
+
+@pytest.mark.parametrize("T,pos0", [(2, 50000), (12, 65524)])
+def test_select_at_the_largest_caches(T, pos0):
+    # past 32,768 cells the top-k holds 128 cells per thread (its largest form); (12, 65524) ends
+    # at the 65,536-cell limit on the score-GEMM path, (2, 50000) is a few-row call
+    inp = synth.layer_inputs(T, pos0 + T, seed=T + pos0)
+    ids, out = gpu_select_prefill(inp, T, pos0)
+    ref_out, ref_ids, _, _ = oracle.prefill(inp, T, pos0)
+    np.testing.assert_array_equal(ids, ref_ids)
+    assert_close(out, ref_out, f"T={T} pos0={pos0}")
