@@ -125,7 +125,8 @@ QSA_API int qsa_prep(const uint16_t* q_raw, const uint16_t* k_raw, const uint16_
 
 /*
  * Bytes of device workspace qsa_select needs for a call with T tokens at pos0 over a
- * cache of n_cells cells (0 when no token of the call is above the identity threshold).
+ * cache of n_cells cells (0 when no token of the call is above the identity threshold, and
+ * for caches beyond 65,536 visible cells, whose selection needs no workspace: see qsa_select).
  */
 QSA_API size_t qsa_select_workspace_bytes(int T, int pos0, int n_cells, const qsa_params* params);
 
@@ -139,7 +140,10 @@ QSA_API size_t qsa_select_workspace_bytes(int T, int pos0, int n_cells, const qs
  * cell index, written in ascending cell order.  The ranking is exact: candidates near the
  * cut are re-scored in exact integer arithmetic, so ids are bit-identical to a ranking by
  * the mathematically exact score.  Rows of tokens at or under the threshold are not
- * written.  ws must hold qsa_select_workspace_bytes(T, pos0, n_cells, params) bytes and
+ * written.  Calls whose largest n_kv (pos0 + T) exceeds 65,536 cells are selected by the
+ * cluster kernel of qsa_decode_layer (one 16-CTA cluster per (token, group), ids only, the same
+ * exact ranking), up to that call's limit of 131,072 cells; they need no workspace and take at
+ * most 65535 tokens.  ws must hold qsa_select_workspace_bytes(T, pos0, n_cells, params) bytes and
  * is clobbered.  A device-side capacity overflow sets the status word (QSA_ERR_DEVICE).
  */
 QSA_API int qsa_select(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_cells, int T, int pos0,

@@ -108,6 +108,38 @@ int check_layer(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_
   return QSA_OK;
 }
 
+// Largest n_kv the fused decode takes on this device (cells per CTA x the largest cluster).
+int decode_layer_limit(int* rc) {
+  int c = 0;
+  cudaError_t e = qsa::decode_layer_max_cluster(&c);
+  if (e != cudaSuccess) {
+    *rc = cuda_fail(e, "qsa_decode_layer set-up");
+    return 0;
+  }
+  return c * qsa::decode_layer_cells_per_cta();
+}
+
+// Selection over a cache longer than the score-GEMM path holds: the single-launch decode layer's
+// cluster kernel, ids only (its exact ranking; no attention, V not read, no workspace).
+int select_long(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_cells, int T, int pos0, int32_t* ids,
+                const qsa::Params& p, void* stream, const char* who) {
+  int rc = 0;
+  const int limit = decode_layer_limit(&rc);
+  if (!limit) return rc;
+  if ((long long)pos0 + T > limit)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: selection over n_kv up to %lld cells is not supported (at most %d)", who,
+                (long long)pos0 + T, limit);
+  if (T > 65535) return fail(QSA_ERR_UNSUPPORTED, "%s: at most 65535 tokens over %d cells", who, qsa::select_max_cells());
+  int* st = status_ptr(&rc);
+  if (!st) return rc;
+  cudaError_t e = qsa::launch_decode_layer(reinterpret_cast<const __half*>(q), kq, nullptr,
+                                           reinterpret_cast<const __half*>(ksc), nullptr, nullptr, 1, (long long)n_cells,
+                                           n_cells, pos0, T, pos0 + T, ids, nullptr, nullptr, p, st,
+                                           static_cast<cudaStream_t>(stream), nullptr, false, true);
+  if (e != cudaSuccess) return cuda_fail(e, who);
+  return ok();
+}
+
 }  // namespace
 
 extern "C" {
@@ -179,6 +211,8 @@ int qsa_select(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_c
   const int t_sel = qsa::first_selected_token(pos0, p.identity_max);
   if (t_sel >= T) return ok();  // every token at or under the threshold: nothing to select
   CHECK_PTR(ids, "ids");
+  if ((long long)pos0 + T > qsa::select_max_cells())
+    return select_long(q, kq, ksc, n_cells, T, pos0, ids, p, stream, "qsa_select");
   const size_t need = qsa::select_workspace_bytes(T, pos0, n_cells, p);
   if (need == 0) return fail(QSA_ERR_UNSUPPORTED, "selection over n_kv up to %lld cells is not supported",
                              (long long)pos0 + T);
@@ -288,17 +322,6 @@ int qsa_merge_gated(const float* part, const int32_t* n_chunks, int N, int chunk
                                     static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qsa_merge launch");
   return ok();
-}
-
-// Largest n_kv the fused decode takes on this device (cells per CTA x the largest cluster).
-static int decode_layer_limit(int* rc) {
-  int c = 0;
-  cudaError_t e = qsa::decode_layer_max_cluster(&c);
-  if (e != cudaSuccess) {
-    *rc = cuda_fail(e, "qsa_decode_layer set-up");
-    return 0;
-  }
-  return c * qsa::decode_layer_cells_per_cta();
 }
 
 int qsa_decode_layer(const uint16_t* q, const int8_t* kq, const int8_t* vq, const uint16_t* ksc, const uint16_t* vsc,
@@ -532,6 +555,10 @@ extern "C" int qsa_select_noalloc(const uint16_t* q, const int8_t* kq, const uin
   if (rc) return rc;
   if ((rc = check_layer(q, kq, ksc, n_cells, T, pos0))) return rc;
   if (qsa::first_selected_token(pos0, p.identity_max) >= T) return ok();  // nothing to select
+  if ((long long)pos0 + T > qsa::select_max_cells()) {  // needs no scratch at all
+    CHECK_PTR(ids, "ids");
+    return select_long(q, kq, ksc, n_cells, T, pos0, ids, p, stream, "qsa_select_noalloc");
+  }
   const size_t need = qsa::select_workspace_bytes(T, pos0, n_cells, p);
   if (need == 0)
     return fail(QSA_ERR_UNSUPPORTED, "selection over n_kv up to %lld cells is not supported", (long long)pos0 + T);

@@ -132,7 +132,8 @@ cudaError_t decode_layer_max_cluster(int* c);
 cudaError_t launch_decode_layer(const __half* q, const int8_t* kq, const int8_t* vq, const __half* ksc,
                                 const __half* vsc, const int4* seqs, int n_seq, long long n_pool, int n_cells, int pos0,
                                 int n_tok, int max_n_kv, int32_t* ids, const __half* gate, float* xp, Params p,
-                                int* status, cudaStream_t stream, __half* out16 = nullptr, bool selected_only = false);
+                                int* status, cudaStream_t stream, __half* out16 = nullptr, bool selected_only = false,
+                                bool ids_only = false);
 
 // Output gate: the elementwise logistic function of the gate input, in fp32.
 __device__ __forceinline__ float gate_sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
@@ -149,6 +150,9 @@ cudaError_t launch_prep(const __half* q_raw, const __half* k_raw, const __half* 
                         float eps, const int* sections, __half* qcur, __half* kcur, int8_t* kq, __half* ksc,
                         int8_t* vq, __half* vsc, cudaStream_t stream);
 
+// The score-GEMM and top-k selection holds caches of up to select_max_cells() cells; longer
+// caches are selected by the single-launch decode layer's cluster kernel (ids only).
+int select_max_cells();
 size_t select_workspace_bytes(int T, int pos0, int n_cells, Params p);
 cudaError_t launch_select(const __half* q, const int8_t* kq, const __half* ksc, int n_cells, int T, int pos0,
                           int32_t* ids, void* ws, Params p, int* status, cudaStream_t stream);

@@ -121,6 +121,7 @@ struct FusedArgs {
   int* status;
   __half* out16;     // [n_tok][24][256] fp16 output instead of xp (a prefill), or null
   int selected_only; // tokens at or under the identity threshold are left to another kernel
+  int ids_only;      // the selection alone: ids of selected tokens, no attention (V not read)
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     return;
   }
   const bool selected = n_kv > p.identity_max;
-  if (!selected && a.selected_only) return;  // uniform over the cluster, before any cluster barrier
+  if (!selected && (a.selected_only || a.ids_only)) return;  // uniform over the cluster, before any cluster barrier
   const int K = p.topk;
   const int W = (n_kv + C - 1) / C;
   const int c_lo = r * W, c_hi = min(n_kv, c_lo + W), nloc = max(0, c_hi - c_lo);
@@ -293,6 +294,30 @@ __global__ void __launch_bounds__(kFThreads, 1)
   uint16_t* s_list = reinterpret_cast<uint16_t*>(sm + kOffHist);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   bool ok_waits = true;
+  // ids of a selected token: this CTA's kept cells (ascending in s_list) at the offset of the
+  // CTAs before it, once every CTA's kept count is in s_nsel_all
+  auto write_ids = [&](int n_sel) {
+    if (a.ids == nullptr) return;
+    int off = 0, total = 0;
+#pragma unroll
+    for (int qq = 0; qq < C; ++qq) {
+      const int c = s_nsel_all[qq];
+      off += qq < r ? c : 0;
+      total += c;
+    }
+    if (total != p.topk && r == 0 && tid == 0) set_dev_status(a.status, QSA_DEV_BAND_OVERFLOW);
+    int32_t* row = a.ids + ((size_t)t * kGroups + g) * p.topk;
+    for (int i = tid; i < n_sel; i += kFThreads)
+      if (off + i < p.topk) row[off + i] = c_lo + (int)s_list[i];
+  };
+  // a copy wait that gave up: wait (bounded) for the last phase of every ring barrier used
+  auto drain = [&]() {
+    if (!ok_waits) {
+      const int ntiles = selected ? (nloc + kTile - 1) / kTile : 0;
+      for (int s = 0; s < kStages; ++s)
+        if (ntiles > s) mbar_wait(&bars[s], (uint32_t)(((ntiles - 1 - s) / kStages) & 1), nullptr);
+    }
+  };
 
   // receive buffers that others add into start at zero; then the first half of barrier #0,
   // whose second half (before the first remote access) also guarantees every CTA has started
@@ -517,7 +542,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
           s_stat[i] = (uint8_t)st;
           n_in += st == 1;
           // the V rows of the cells that may be kept go to L2 now, for the attention phase
-          if (st != 0) prefetch_l2_256(vq + ((size_t)(c_lo + i) * kGroups + g) * kD);
+          if (st != 0 && !a.ids_only) prefetch_l2_256(vq + ((size_t)(c_lo + i) * kGroups + g) * kD);
         }
         const unsigned m = __ballot_sync(0xffffffffu, st == 2);
         int slot0 = 0;
@@ -718,6 +743,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
       if (tid == 0) s_nlist = total;
       __syncthreads();
       n_sel = s_nlist;
+    }
+    if (a.ids_only) {  // uniform: the kept counts to every CTA, then the ids; no attention
+      if (tid < C) st_cluster_u32(mapa_shared(smem_u32(&s_nsel_all[r]), tid), (uint32_t)n_sel);
+      cluster_arrive();
+      cluster_wait();  // #4 of this form: every CTA's kept count delivered
+      write_ids(n_sel);
+      drain();
+      return;
     }
   } else {
     // identity: the V rows to L2 while the first batch is set up
@@ -952,25 +985,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
     if (a.out16) a.out16[o] = __float2half_rn(v);
     else a.xp[o] = v;
   }
-  // ids of a selected token: this CTA's kept cells at the offset of the CTAs before it
-  if (selected && a.ids != nullptr) {
-    int off = 0, total = 0;
-#pragma unroll
-    for (int qq = 0; qq < C; ++qq) {
-      const int c = s_nsel_all[qq];
-      off += qq < r ? c : 0;
-      total += c;
-    }
-    if (total != K && r == 0 && tid == 0) set_dev_status(a.status, QSA_DEV_BAND_OVERFLOW);
-    int32_t* row = a.ids + ((size_t)t * kGroups + g) * K;
-    for (int i = tid; i < n_sel; i += kFThreads)
-      if (off + i < K) row[off + i] = c_lo + (int)s_list[i];
-  }
-  if (!ok_waits) {  // a copy wait gave up: wait (bounded) for the last phase of every barrier used
-    const int ntiles = selected ? (nloc + kTile - 1) / kTile : 0;
-    for (int s = 0; s < kStages; ++s)
-      if (ntiles > s) mbar_wait(&bars[s], (uint32_t)(((ntiles - 1 - s) / kStages) & 1), nullptr);
-  }
+  if (selected) write_ids(n_sel);
+  drain();
 }
 
 cudaLaunchConfig_t launch_config(int C, int n_tok, cudaStream_t stream, cudaLaunchAttribute (&attr)[2]) {
@@ -1067,9 +1083,10 @@ cudaError_t decode_layer_max_cluster(int* c) {
 cudaError_t launch_decode_layer(const __half* q, const int8_t* kq, const int8_t* vq, const __half* ksc,
                                 const __half* vsc, const int4* seqs, int n_seq, long long n_pool, int n_cells, int pos0,
                                 int n_tok, int max_n_kv, int32_t* ids, const __half* gate, float* xp, Params p,
-                                int* status, cudaStream_t stream, __half* out16, bool selected_only) {
+                                int* status, cudaStream_t stream, __half* out16, bool selected_only,
+                                bool ids_only) {
   FusedArgs a{q, kq, vq, ksc, vsc, seqs, n_seq, n_pool, n_cells, pos0, ids, gate, xp, p, status, out16,
-              selected_only ? 1 : 0};
+              selected_only ? 1 : 0, ids_only ? 1 : 0};
   int state = 0;
   cudaError_t e = device_setup(&state);
   if (e != cudaSuccess) return e;

@@ -1194,6 +1194,8 @@ cudaError_t launch_score_gemm(const WsLayout& L, int pos0, __half* qhi, __half* 
 
 }  // namespace
 
+int select_max_cells() { return kMaxCells; }
+
 size_t select_workspace_bytes(int T, int pos0, int n_cells, Params p) {
   (void)n_cells;
   const WsLayout L = ws_layout(T, pos0, p);

@@ -182,3 +182,26 @@ def test_select_at_the_largest_caches(T, pos0):
     ref_out, ref_ids, _, _ = oracle.prefill(inp, T, pos0)
     np.testing.assert_array_equal(ids, ref_ids)
     assert_close(out, ref_out, f"T={T} pos0={pos0}")
+
+
+@pytest.mark.parametrize("T,pos0", [(3, 70000), (2, 100000)])
+def test_select_beyond_the_score_path_limit(T, pos0):
+    # n_kv above 65,536: qsa_select hands the call to the single-launch decode layer's cluster
+    # kernel in its ids-only form (no workspace); ids bit-exact, and the gathered prefill over them
+    inp = synth.layer_inputs(T, pos0 + T, seed=T + pos0)
+    n = pos0 + T
+    assert qsa.qsa_select_workspace_bytes(T, pos0, n) == 0
+    d = to_dev(inp)
+    ids = torch.full((T, 2, 2048), -7, dtype=torch.int32, device="cuda")
+    qsa.qsa_select(d["q"], d["kq"], d["ksc"], n, T, pos0, ids, None)
+    ids2 = torch.full((T, 2, 2048), -7, dtype=torch.int32, device="cuda")
+    qsa.qsa_select_noalloc(d["q"], d["kq"], d["ksc"], n, T, pos0, ids2)
+    qsa.qsa_check_device_status()
+    ref_out, ref_ids, _, _ = oracle.prefill(inp, T, pos0)
+    np.testing.assert_array_equal(ids.cpu().numpy(), ref_ids)
+    np.testing.assert_array_equal(ids2.cpu().numpy(), ref_ids)
+    out = torch.full((T, 24, 256), float("nan"), dtype=torch.float16, device="cuda")
+    pws = torch.empty(qsa.qsa_flash_prefill_workspace_bytes(T, pos0, n), dtype=torch.uint8, device="cuda")
+    qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n, T, pos0, ids, out, pws)
+    qsa.qsa_check_device_status()
+    assert_close(out.float().cpu().numpy(), ref_out, f"prefill over {n} cells")
