@@ -9,7 +9,7 @@
 //   xp[t, h] = sum_c softmax_c(sm_scale q[t,h] . k^[c]) v^[c],   k^ = kq * ksc, v^ = fp16(vq * vsc).
 // The pages split this over five dependent dispatches; on GB300 a decode token's work is a
 // few megabytes, so the dispatch chain, not the bytes, set the time.  Here one thread-block
-// cluster of C CTAs (C = 16, or 8) takes one (token, group); CTA r owns the cells
+// cluster of C CTAs (C = 2, 4, 8 or 16, chosen per launch) takes one (token, group); CTA r owns the cells
 // [r W, (r + 1) W) of the token's n_kv cells, W = ceil(n_kv / C) <= 8192.  The CTAs exchange data by
 // PUSHING it into each other's shared memory (remote stores and adds need no round trip; a
 // remote load costs hundreds of cycles) and a cluster barrier makes it visible:
@@ -73,7 +73,8 @@ constexpr int kBatchBytes = kBatch * kRowB * 2 + kBatch * 32;  // K rows, V rows
 constexpr int kVhStride = 264;       // halves per V^ row (528 B: conflict-free ldmatrix)
 constexpr int kQStride = 264;        // halves per staged q row
 constexpr int kPStride = 72;         // halves per P row
-constexpr int kCandPush = 1792;      // candidates a CTA receives by push: kCandPush / C per source
+constexpr int kMinC = 2;             // the smallest cluster (largest slice of the histogram per CTA)
+constexpr int kCandPush = 1792;      // candidates a CTA receives by push: kCandPush / max(C, 8) per source
 constexpr int kDenseOff = 256;       // fast path: own candidates use entries [0, kDenseOff) of their arrays
 constexpr int kCandStage = 768;      // remote candidates staged per round (pull fallback)
 
@@ -85,8 +86,8 @@ constexpr int kOffHL = kOffQsum + 256 * 8;                   // fp16 hi[256] | l
 constexpr int kOffScore = kOffHL + 512 * 2;                  // f32 [kMaxW]; later the received partials
 constexpr int kOffStat = kOffScore + kMaxW * 4;              // u8 [kMaxW]
 constexpr int kOffHist = kOffStat + kMaxW;                   // u32 [kHistBins] own, then the cluster's; later u16 kept list
-constexpr int kOffSlice = kOffHist + kHistBins * 4;          // u32 [512] the owned bin slice, summed by the others
-constexpr int kOffP = kOffSlice + 512 * 4;                   // fp16 [16][kPStride]
+constexpr int kOffSlice = kOffHist + kHistBins * 4;          // u32 [kHistBins / C] the owned bin slice, summed by the others
+constexpr int kOffP = kOffSlice + kHistBins / kMinC * 4;     // fp16 [16][kPStride]
 constexpr int kOffBar = kOffP + 16 * kPStride * 2;           // mbarriers of the scoring ring
 constexpr int kSmemBytes = kOffBar + 8 * 8 + 1024;           // + the alignment slack
 // candidates inside the ring region: own keys hi [kOwnCap] | lo [kOwnCap] | index [kOwnCap] |
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
   // receive buffers that others add into start at zero; then the first half of barrier #0,
   // whose second half (before the first remote access) also guarantees every CTA has started
-  for (int i = tid; i < 512; i += kFThreads) s_slice[i] = 0u;
+  for (int i = tid; i < kHistBins / C; i += kFThreads) s_slice[i] = 0u;
   for (int i = tid; i < kHistBins; i += kFThreads) s_hist[i] = 0u;
   if (tid < 4) s_kmax_all[tid] = 0.f;
   if (tid == 0) {
@@ -597,7 +598,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     __syncthreads();
     // push the counts, and the candidates when they fit this CTA's slot, to every CTA
-    constexpr int kSlot = kCandPush / C;
+    constexpr int kSlot = kCandPush / (C < 8 ? 8 : C);  // a source's slot in every receiver
     long long* r_hi = reinterpret_cast<long long*>(sm + kRcvHi);
     unsigned long long* r_lo = reinterpret_cast<unsigned long long*>(sm + kRcvLo);
     int* r_idx = reinterpret_cast<int*>(sm + kRcvIdx);
@@ -1006,8 +1007,15 @@ cudaLaunchConfig_t launch_config(int C, int n_tok, cudaStream_t stream, cudaLaun
   return cfg;
 }
 
-// Per device: 0 = not set up, 1 = attributes set and clusters of 16 fit, 2 = set, only 8 fit.
+// Per device: 0 = not set up, 1 = attributes set and clusters of 16 fit, 2 = set, only 8 fit;
+// and the device's SM count, read at set-up.
 std::atomic<int> g_setup[64];
+std::atomic<int> g_sms[64];
+int g_dev_of_setup() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev >= 0 && dev < 64 ? dev : 0;
+}
 
 template <int C>
 cudaError_t set_attrs() {
@@ -1024,6 +1032,8 @@ cudaError_t device_setup(int* state) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   int s = g_setup[dev].load(std::memory_order_acquire);
   if (s == 0) {
+    if ((e = set_attrs<2>()) != cudaSuccess) return e;
+    if ((e = set_attrs<4>()) != cudaSuccess) return e;
     if ((e = set_attrs<8>()) != cudaSuccess) return e;
     if ((e = set_attrs<16>()) != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];
@@ -1032,6 +1042,9 @@ cudaError_t device_setup(int* state) {
     e = cudaOccupancyMaxActiveClusters(&n16, decode_fused_kernel<16>, &cfg);
     if (e != cudaSuccess) return e;
     s = n16 > 0 ? 1 : 2;
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    g_sms[dev].store(sms > 0 ? sms : 1, std::memory_order_release);
     g_setup[dev].store(s, std::memory_order_release);
   }
   *state = s;
@@ -1094,8 +1107,30 @@ cudaError_t launch_decode_layer(const __half* q, const int8_t* kq, const int8_t*
   // need them; otherwise 8, which keeps twice as many clusters resident.
   CUtensorMap tmc, tms;
   if (!encode_maps(kq, ksc, n_pool, &tmc, &tms)) return cudaErrorInvalidValue;
-  if (state == 1 && (max_n_kv > 8 * kMaxW || 2 * n_tok <= 8)) return launch_c<16>(a, n_tok, tmc, tms, stream);
-  return launch_c<8>(a, n_tok, tmc, tms, stream);
+  // The cluster size: the kernel's phases are latency bound, so a launch takes about (waves of
+  // CTAs) x (a fixed part + a part growing with the cells per CTA); measured on GB300 the two parts
+  // match at about 2,048 cells.  Few tokens: more CTAs per token (one wave either way); many tokens:
+  // fewer, larger CTAs (fewer waves).  C must hold max_n_kv in C x kMaxW cells.
+  const int sms = g_sms[g_dev_of_setup()].load(std::memory_order_acquire);
+  int best_c = 0;
+  double best_t = 0.0;
+  for (int c : {16, 8, 4, 2}) {
+    if ((c == 16 && state != 1) || (long long)max_n_kv > (long long)c * kMaxW) continue;
+    const long long ctas = (long long)kGroups * n_tok * c;
+    const double waves = (double)((ctas + sms - 1) / sms);
+    const double cells = (double)max_n_kv / c;
+    const double t = waves * (1.0 + cells / 2048.0);
+    if (best_c == 0 || t < best_t) {
+      best_c = c;
+      best_t = t;
+    }
+  }
+  switch (best_c) {
+    case 16: return launch_c<16>(a, n_tok, tmc, tms, stream);
+    case 4: return launch_c<4>(a, n_tok, tmc, tms, stream);
+    case 2: return launch_c<2>(a, n_tok, tmc, tms, stream);
+    default: return launch_c<8>(a, n_tok, tmc, tms, stream);
+  }
 }
 
 }  // namespace qsa

@@ -168,3 +168,33 @@ def test_decode_layer_batched_flags_a_bad_sequence_and_keeps_the_rest():
     first.update({k: pool[k][:600] for k in ("kq", "vq", "ksc", "vsc")})
     _, _, ref_out, _, _ = oracle.decode(first, 2, 590)
     assert_close(xp[:2], ref_out, "the good sequence")
+
+
+def test_decode_layer_batched_four_cta_clusters():
+    # 16 single-token sequences over caches of at most 32,768 cells: the launch takes clusters of 4
+    # CTAs (8,192 cells each); one sequence sits exactly at that limit
+    rng = np.random.default_rng(11)
+    specs = [(32768, 32767, 1)] + [(int(p) + 1, int(p), 1) for p in rng.integers(2100, 20000, size=15)]
+    pool, seqs = make_batch(specs, seed0=1900)
+    ids, xp = run_batched(pool, seqs, max_n_kv=32768)
+    qsa.qsa_check_device_status()
+    ref_out, ref_ids = oracle.decode_batch(pool, seqs)
+    ids = ids.cpu().numpy()
+    sel = ref_ids[:, :, 0] >= 0
+    np.testing.assert_array_equal(ids[sel], ref_ids[sel])
+    assert_close(xp.cpu().numpy(), ref_out, "batched decode, clusters of 4")
+
+
+def test_decode_layer_batched_two_cta_clusters():
+    # 64 single-token sequences over caches of at most 16,384 cells: the launch takes clusters of 2
+    # CTAs (8,192 cells each); one sequence sits exactly at that limit
+    rng = np.random.default_rng(12)
+    specs = [(16384, 16383, 1)] + [(int(p) + 1, int(p), 1) for p in rng.integers(2100, 16000, size=63)]
+    pool, seqs = make_batch(specs, seed0=2100)
+    ids, xp = run_batched(pool, seqs, max_n_kv=16384)
+    qsa.qsa_check_device_status()
+    ref_out, ref_ids = oracle.decode_batch(pool, seqs)
+    ids = ids.cpu().numpy()
+    sel = ref_ids[:, :, 0] >= 0
+    np.testing.assert_array_equal(ids[sel], ref_ids[sel])
+    assert_close(xp.cpu().numpy(), ref_out, "batched decode, clusters of 2")
