@@ -11,9 +11,12 @@
 // One CTA (256 threads) per token; each warp issues the loads of all its rows (and the gains)
 // before it uses any, so a CTA waits on one memory round trip.  The token's rd/2 rotation
 // angles are formed once, in fp32 with the product's error recovered and a three-part 2 pi
-// (rope_angle), then sincosf.  Then a warp per row: lane = 8 consecutive dims (one 16-byte load),
-// the sum of squares by shuffles, the rotation partner (dim +- rd/2) on lane ^ (rd/16), and the
-// quantiser's 64-element blocks on lanes 8b .. 8b+7.
+// (rope_angle), then sincosf, into shared memory; each lane then keeps its own four (cos, sin)
+// pairs in registers for all the token's rows.  A warp takes a row at a time with the lanes laid
+// out around the rotation: lane l < R = rd / 8 holds the four rotation pairs (4l + u, 4l + u + rd/2),
+// lanes l >= R hold 8 consecutive unrotated dims rd + 8 (l - R) ..; so every lane holds 8 values in
+// two 4-dim runs at dims (a, b), the rotation needs no exchange between lanes, and the row's
+// sum of squares and the quantiser's four 64-element block maxima are warp reductions.
 #include "common.cuh"
 
 namespace qsa {
@@ -42,25 +45,69 @@ __device__ __forceinline__ float rope_angle(int p, float hi, float lo) {
   return r + err;
 }
 
-// The quantiser of qsa_prep_quantize, on a lane's 8 values of a 64-element block held by the
-// 8 lanes 8b .. 8b+7: IEEE fp32 a / 127 rounded to fp16, codes round-half-away(x / s) clamped.
-__device__ __forceinline__ void quantize8(const float (&x)[8], int8_t* dst_codes, __half* dst_scale, int lane) {
-  float a = 0.f;
+// Dims of this lane's two 4-dim runs (see above): (a, b) with values x[0..3] at a .. a + 3 and
+// x[4..7] at b .. b + 3.
+__device__ __forceinline__ void lane_dims(int lane, int rd, int& a, int& b) {
+  const int R = rd >> 3;
+  if (lane < R) {
+    a = 4 * lane;
+    b = a + (rd >> 1);
+  } else {
+    a = rd + 8 * (lane - R);
+    b = a + 4;
+  }
+}
+
+__device__ __forceinline__ void unpack4(uint2 w, float* x) {
+  const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+  const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+  x[0] = f0.x;
+  x[1] = f0.y;
+  x[2] = f1.x;
+  x[3] = f1.y;
+}
+
+// The quantiser of qsa_prep_quantize on one 256-element row held as above: per 64-element block
+// IEEE fp32 a / 127 rounded to fp16, codes round-half-away(x / s) clamped to +-127 (all zero and
+// a +0 scale for an all-zero block).  The block maxima are reduced over the whole warp.
+__device__ __forceinline__ void quantize_row(const float (&x)[8], int a, int b, int8_t* codes, __half* scales,
+                                             int lane) {
+  float m[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int u = 0; u < 8; ++u) a = fmaxf(a, fabsf(x[u]));
+  for (int u = 0; u < 8; ++u) {
+    const int blk = (u < 4 ? a : b) >> 6;  // a run never crosses a block (4-aligned, 64-element blocks)
+    const float v = fabsf(x[u]);
 #pragma unroll
-  for (int o = 1; o < 8; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  const __half sh = __float2half_rn(__fdiv_rn(a, 127.0f));
-  const float s = __half2float(sh);
+    for (int k = 0; k < 4; ++k) m[k] = (blk == k) ? fmaxf(m[k], v) : m[k];
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m[k] = fmaxf(m[k], __shfl_xor_sync(0xffffffffu, m[k], o));
+  __half sh[4];
+  float sv[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    sh[k] = __float2half_rn(__fdiv_rn(m[k], 127.0f));
+    sv[k] = __half2float(sh[k]);
+  }
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
+    const int blk = (u < 4 ? a : b) >> 6;
+    const float s = blk == 0 ? sv[0] : blk == 1 ? sv[1] : blk == 2 ? sv[2] : sv[3];
     int c = 0;
     if (s != 0.f) c = (int)fminf(fmaxf(roundf(__fdiv_rn(x[u], s)), -127.f), 127.f);
     w[u >> 2] |= (uint32_t)(uint8_t)(int8_t)c << (8 * (u & 3));
   }
-  *reinterpret_cast<uint2*>(dst_codes) = make_uint2(w[0], w[1]);
-  if ((lane & 7) == 0) *dst_scale = (s == 0.f) ? __ushort_as_half(0) : sh;
+  *reinterpret_cast<uint32_t*>(codes + a) = w[0];
+  *reinterpret_cast<uint32_t*>(codes + b) = w[1];
+  if (lane == 0) {
+    __half o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = sv[k] == 0.f ? __ushort_as_half(0) : sh[k];
+    *reinterpret_cast<uint2*>(scales) = *reinterpret_cast<const uint2*>(o);
+  }
 }
 
 __global__ void __launch_bounds__(256) prep_kernel(const __half* __restrict__ q_raw, const __half* __restrict__ k_raw,
@@ -74,24 +121,29 @@ __global__ void __launch_bounds__(256) prep_kernel(const __half* __restrict__ q_
   pdl_begin();
   const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rd = cfg.rotary_dim, h2 = rd / 2;
+  const bool rot_lane = lane < (rd >> 3);
+  int da, db;
+  lane_dims(lane, rd, da, db);
   // this warp's rows r = warp + 8 j (j < 4, r < 28) and the gains: every load issued before any use
   constexpr int kRowsPerWarp = (kPrepRows + 7) / 8;
-  uint4 raw[kRowsPerWarp];
+  uint2 ra[kRowsPerWarp], rb[kRowsPerWarp];
 #pragma unroll
   for (int j = 0; j < kRowsPerWarp; ++j) {
     const int r = warp + 8 * j;
-    raw[j] = make_uint4(0u, 0u, 0u, 0u);
+    ra[j] = make_uint2(0u, 0u);
+    rb[j] = make_uint2(0u, 0u);
     if (r < kPrepRows) {
       const __half* src = r >= kHeads + kGroups ? v_raw + ((size_t)t * kGroups + (r - kHeads - kGroups)) * kD
                           : r >= kHeads ? k_raw + ((size_t)t * kGroups + (r - kHeads)) * kD
                                         : q_raw + ((size_t)t * kHeads + r) * kD;
-      raw[j] = __ldg(reinterpret_cast<const uint4*>(src) + lane);
+      ra[j] = __ldg(reinterpret_cast<const uint2*>(src + da));
+      rb[j] = __ldg(reinterpret_cast<const uint2*>(src + db));
     }
   }
-  const float4 qg0 = __ldg(reinterpret_cast<const float4*>(q_gamma) + 2 * lane);
-  const float4 qg1 = __ldg(reinterpret_cast<const float4*>(q_gamma) + 2 * lane + 1);
-  const float4 kg0 = __ldg(reinterpret_cast<const float4*>(k_gamma) + 2 * lane);
-  const float4 kg1 = __ldg(reinterpret_cast<const float4*>(k_gamma) + 2 * lane + 1);
+  const float4 qga = __ldg(reinterpret_cast<const float4*>(q_gamma + da));
+  const float4 qgb = __ldg(reinterpret_cast<const float4*>(q_gamma + db));
+  const float4 kga = __ldg(reinterpret_cast<const float4*>(k_gamma + da));
+  const float4 kgb = __ldg(reinterpret_cast<const float4*>(k_gamma + db));
   if (tid < h2) {
     int p = pos0 + t;
     if (pos3) p = __ldg(pos3 + 3 * t + (tid < cfg.sec0 ? 0 : (tid < cfg.sec0 + cfg.sec1 ? 1 : 2)));
@@ -100,6 +152,10 @@ __global__ void __launch_bounds__(256) prep_kernel(const __half* __restrict__ q_
     s_cs[tid] = make_float2(cs, sn);
   }
   __syncthreads();
+  // this lane's four rotation pairs 4 lane + u (rotated lanes only)
+  float2 cs4[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) cs4[u] = rot_lane ? s_cs[da + u] : make_float2(1.f, 0.f);
   const int cell = pos0 + t;
 #pragma unroll
   for (int j = 0; j < kRowsPerWarp; ++j) {
@@ -108,15 +164,8 @@ __global__ void __launch_bounds__(256) prep_kernel(const __half* __restrict__ q_
     const bool is_v = r >= kHeads + kGroups, is_k = !is_v && r >= kHeads;
     const int g = is_v ? r - kHeads - kGroups : r - kHeads;  // group of a k or v row
     float x[8];
-    {
-      const __half2* h = reinterpret_cast<const __half2*>(&raw[j]);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float2 f = __half22float2(h[u]);
-        x[2 * u] = f.x;
-        x[2 * u + 1] = f.y;
-      }
-    }
+    unpack4(ra[j], x);
+    unpack4(rb[j], x + 4);
     if (!is_v) {
       float ss = 0.f;
 #pragma unroll
@@ -124,35 +173,27 @@ __global__ void __launch_bounds__(256) prep_kernel(const __half* __restrict__ q_
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       const float rs = 1.f / sqrtf(ss * (1.f / kD) + cfg.eps);
-      const float gw[8] = {is_k ? kg0.x : qg0.x, is_k ? kg0.y : qg0.y, is_k ? kg0.z : qg0.z, is_k ? kg0.w : qg0.w,
-                           is_k ? kg1.x : qg1.x, is_k ? kg1.y : qg1.y, is_k ? kg1.z : qg1.z, is_k ? kg1.w : qg1.w};
+      const float gw[8] = {is_k ? kga.x : qga.x, is_k ? kga.y : qga.y, is_k ? kga.z : qga.z, is_k ? kga.w : qga.w,
+                           is_k ? kgb.x : qgb.x, is_k ? kgb.y : qgb.y, is_k ? kgb.z : qgb.z, is_k ? kgb.w : qgb.w};
 #pragma unroll
       for (int u = 0; u < 8; ++u) x[u] = x[u] * rs * gw[u];
-      // rotation: dims 8 lane + u < rd pair with dim +- h2 on lane ^ (rd / 16)
-      const int d0 = 8 * lane;
-      float other[8];
+      if (rot_lane) {  // pairs (x[u], x[4 + u]) = dims (a + u, a + u + rd / 2)
 #pragma unroll
-      for (int u = 0; u < 8; ++u) other[u] = __shfl_xor_sync(0xffffffffu, x[u], rd >> 4);
-      if (d0 < rd) {
-        const bool first = d0 < h2;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float2 c = s_cs[(d0 + u) & (h2 - 1)];
-          x[u] = first ? x[u] * c.x - other[u] * c.y : x[u] * c.x + other[u] * c.y;
+        for (int u = 0; u < 4; ++u) {
+          const float lo = x[u], hi = x[4 + u];
+          x[u] = lo * cs4[u].x - hi * cs4[u].y;
+          x[4 + u] = hi * cs4[u].x + lo * cs4[u].y;
         }
       }
     }
     if (!is_k && !is_v) {  // qcur
-      uint4 o;
-      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) ow[u] = pack_half2(x[2 * u], x[2 * u + 1]);
-      *reinterpret_cast<uint4*>(qcur + ((size_t)t * kHeads + r) * kD + 8 * lane) = o;
+      __half* dst = qcur + ((size_t)t * kHeads + r) * kD;
+      *reinterpret_cast<uint2*>(dst + da) = make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
+      *reinterpret_cast<uint2*>(dst + db) = make_uint2(pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
       continue;
     }
     if (is_k) {  // the cache holds the fp16 rounding of the k row, quantised
-      uint4 o;
-      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+      uint32_t ow[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         ow[u] = pack_half2(x[2 * u], x[2 * u + 1]);
@@ -160,11 +201,15 @@ __global__ void __launch_bounds__(256) prep_kernel(const __half* __restrict__ q_
         x[2 * u] = f.x;
         x[2 * u + 1] = f.y;
       }
-      if (kcur) *reinterpret_cast<uint4*>(kcur + ((size_t)t * kGroups + g) * kD + 8 * lane) = o;
+      if (kcur) {
+        __half* dst = kcur + ((size_t)t * kGroups + g) * kD;
+        *reinterpret_cast<uint2*>(dst + da) = make_uint2(ow[0], ow[1]);
+        *reinterpret_cast<uint2*>(dst + db) = make_uint2(ow[2], ow[3]);
+      }
     }
-    int8_t* codes = (is_k ? kq : vq) + ((size_t)cell * kGroups + g) * kD + 8 * lane;
-    __half* scale = (is_k ? ksc : vsc) + ((size_t)cell * kGroups + g) * kNB + (lane >> 3);
-    quantize8(x, codes, scale, lane);
+    int8_t* codes = (is_k ? kq : vq) + ((size_t)cell * kGroups + g) * kD;
+    __half* scale = (is_k ? ksc : vsc) + ((size_t)cell * kGroups + g) * kNB;
+    quantize_row(x, da, db, codes, scale, lane);
   }
 }
 
