@@ -135,8 +135,22 @@ cudaError_t launch_decode_layer(const __half* q, const int8_t* kq, const int8_t*
                                 int* status, cudaStream_t stream, __half* out16 = nullptr, bool selected_only = false,
                                 bool ids_only = false);
 
-// Output gate: the elementwise logistic function of the gate input, in fp32.
-__device__ __forceinline__ float gate_sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+// Output gate: the elementwise logistic function of the gate input, in fp32, 1 / (1 + e^-x).  The
+// exponential takes the special-function unit; the reciprocal of d = 1 + e^-x (d >= 1, and finite
+// for |x| <= 80, past which the result is 0 or 1 in every output format) is formed on the FMA
+// pipe, which the epilogues leave idle, so that the gate costs one special-function operation per
+// element instead of two: an estimate whose float bits are 0x7EF00000 - bits(d) (the exponent
+// negated and the mantissa mirrored; within 6.25% of 1/d), then three Newton-Raphson steps
+// r <- r (2 - d r), each of which squares the relative error (below 1e-9 before the last
+// rounding; sigmoid(0) is exactly 1/2).
+__device__ __forceinline__ float gate_sigmoid(float x) {
+  const float d = 1.f + __expf(-fminf(fmaxf(x, -80.f), 80.f));
+  float r = __int_as_float(0x7EF00000 - __float_as_int(d));
+  r = r * fmaf(-d, r, 2.f);
+  r = r * fmaf(-d, r, 2.f);
+  r = r * fmaf(-d, r, 2.f);
+  return r;
+}
 
 cudaError_t launch_merge(const float* part, const int32_t* n_chunks, int N, int chunk_cap, const __half* gate,
                          float* xp, int* status, cudaStream_t stream);
