@@ -143,7 +143,10 @@ QSA_API size_t qsa_select_workspace_bytes(int T, int pos0, int n_cells, const qs
  * written.  Calls whose largest n_kv (pos0 + T) exceeds 65,536 cells are selected by the
  * cluster kernel of qsa_decode_layer (one 16-CTA cluster per (token, group), ids only, the same
  * exact ranking), up to that call's limit of 131,072 cells; they need no workspace and take at
- * most 65535 tokens.  ws must hold qsa_select_workspace_bytes(T, pos0, n_cells, params) bytes and
+ * most 65535 tokens.  ws should hold qsa_select_workspace_bytes(T, pos0, n_cells, params) bytes;
+ * a smaller workspace, down to qsa_select_workspace_bytes(1, pos0 + T - 1, n_cells, params), is
+ * taken by selecting the tokens in consecutive chunks, the largest that fit (the same ids, the
+ * selection kernels once per chunk), so the memory a caller sets aside need not grow with T.  It
  * is clobbered.  A device-side capacity overflow sets the status word (QSA_ERR_DEVICE).
  */
 QSA_API int qsa_select(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_cells, int T, int pos0,

@@ -216,14 +216,36 @@ int qsa_select(const uint16_t* q, const int8_t* kq, const uint16_t* ksc, int n_c
   const size_t need = qsa::select_workspace_bytes(T, pos0, n_cells, p);
   if (need == 0) return fail(QSA_ERR_UNSUPPORTED, "selection over n_kv up to %lld cells is not supported",
                              (long long)pos0 + T);
-  if (!ws || ws_bytes < need)
-    return fail(QSA_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", ws ? ws_bytes : (size_t)0, need);
+  // A smaller workspace takes the selected tokens in consecutive chunks of Tc tokens, each the same
+  // call over its own token range (rows are independent; the ids are the same): the largest Tc whose
+  // last chunk (the one with the most cells) fits.
+  int Tc = T - t_sel;
+  if (ws && ws_bytes < need) {
+    const int T_sel = T - t_sel;
+    auto fits = [&](int c) {
+      const size_t nb = qsa::select_workspace_bytes(c, pos0 + T - c, n_cells, p);
+      return nb != 0 && nb <= ws_bytes;
+    };
+    Tc = 0;
+    for (int c = T_sel / 128 * 128; c >= 128 && !Tc; c -= 128)
+      if (fits(c)) Tc = c;
+    for (int c = 64; c >= 1 && !Tc; c >>= 1)
+      if (c < T_sel && fits(c)) Tc = c;
+  }
+  if (!ws || Tc == 0)
+    return fail(QSA_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed (at least %zu in chunks of one token)",
+                ws ? ws_bytes : (size_t)0, need, qsa::select_workspace_bytes(1, pos0 + T - 1, n_cells, p));
   if (!aligned16(ws)) return fail(QSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
   int* st = status_ptr(&rc);
   if (!st) return rc;
-  cudaError_t e = qsa::launch_select(reinterpret_cast<const __half*>(q), kq, reinterpret_cast<const __half*>(ksc),
-                                     n_cells, T, pos0, ids, ws, p, st, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "qsa_select launch");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int a = t_sel; a < T; a += Tc) {
+    const int b = a + Tc < T ? a + Tc : T;
+    cudaError_t e = qsa::launch_select(reinterpret_cast<const __half*>(q) + (size_t)a * QSA_N_HEADS * QSA_HEAD_DIM, kq,
+                                       reinterpret_cast<const __half*>(ksc), n_cells, b - a, pos0 + a,
+                                       ids + (size_t)a * QSA_N_GROUPS * p.topk, ws, p, st, s);
+    if (e != cudaSuccess) return cuda_fail(e, "qsa_select launch");
+  }
   return ok();
 }
 

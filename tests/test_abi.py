@@ -86,9 +86,13 @@ def test_select_rejects_missing_workspace(lib):
     need = lib.qsa_select_workspace_bytes(64, 2040, 2104, None)
     rc = lib.qsa_select(P(FAKE), P(FAKE), P(FAKE), 2104, 64, 2040, P(FAKE), None, 0, None, None)
     assert rc in (qsa.QSA_ERR_WORKSPACE, qsa.QSA_ERR_UNSUPPORTED)
-    if need:
-        rc = lib.qsa_select(P(FAKE), P(FAKE), P(FAKE), 2104, 64, 2040, P(FAKE), P(FAKE), need - 16, None, None)
-        assert rc == qsa.QSA_ERR_WORKSPACE
+    # a smaller workspace is taken in chunks of tokens, down to one token per chunk: below what the
+    # last single-token chunk needs, the call is refused
+    need1 = lib.qsa_select_workspace_bytes(1, 2040 + 63, 2104, None)
+    assert 0 < need1 < need
+    rc = lib.qsa_select(P(FAKE), P(FAKE), P(FAKE), 2104, 64, 2040, P(FAKE), P(FAKE), need1 - 16, None, None)
+    assert rc == qsa.QSA_ERR_WORKSPACE
+    assert b"in chunks of one token" in lib.qsa_last_error()
     # under the threshold nothing is needed or launched
     assert lib.qsa_select(P(FAKE), P(FAKE), P(FAKE), 100, 4, 0, None, None, 0, None, None) == qsa.QSA_OK
 

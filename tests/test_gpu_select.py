@@ -205,3 +205,26 @@ def test_select_beyond_the_score_path_limit(T, pos0):
     qsa.qsa_flash_prefill(d["q"], d["kq"], d["vq"], d["ksc"], d["vsc"], n, T, pos0, ids, out, pws)
     qsa.qsa_check_device_status()
     assert_close(out.float().cpu().numpy(), ref_out, f"prefill over {n} cells")
+
+
+@pytest.mark.parametrize("T,pos0,chunk", [(300, 30000, 64), (12, 3000, 1)])
+def test_select_in_chunks_with_a_small_workspace(T, pos0, chunk):
+    # a workspace sized for chunks of `chunk` tokens: the same ids as with the full workspace, and
+    # the oracle's on a sample of tokens
+    n = pos0 + T
+    inp = synth.layer_inputs(T, n, seed=T + pos0 + chunk)
+    full = qsa.qsa_select_workspace_bytes(T, pos0, n)
+    small = qsa.qsa_select_workspace_bytes(chunk, pos0 + T - chunk, n)
+    assert small < full
+    d = to_dev(inp)
+    ids_full = torch.full((T, 2, 2048), -7, dtype=torch.int32, device="cuda")
+    ids_small = torch.full((T, 2, 2048), -7, dtype=torch.int32, device="cuda")
+    qsa.qsa_select(d["q"], d["kq"], d["ksc"], n, T, pos0, ids_full, torch.empty(full, dtype=torch.uint8, device="cuda"))
+    qsa.qsa_select(d["q"], d["kq"], d["ksc"], n, T, pos0, ids_small,
+                   torch.empty(small, dtype=torch.uint8, device="cuda"))
+    qsa.qsa_check_device_status()
+    a, b = ids_full.cpu().numpy(), ids_small.cpu().numpy()
+    np.testing.assert_array_equal(a, b)
+    toks = np.arange(0, T, max(1, T // 10), dtype=np.int32)
+    _, ref_ids, _, _ = oracle.prefill(inp, T, pos0, toks=toks)
+    np.testing.assert_array_equal(b[toks], ref_ids)
