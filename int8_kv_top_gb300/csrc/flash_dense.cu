@@ -33,14 +33,20 @@
 //   warps 4-11  (both CTAs) two warpgroups, one (token, head) row per thread in each, half
 //               of the columns each: online softmax on S in base-2 units (max exchanged
 //               through shared memory, exp2, row sums), fp16 P -> TMEM over S, lazy O rescale
-//               (only when the running max grows by more than 2^8), final 1/l and fp16 out;
+//               (only when the running max grows by more than 2^8), 1/l at the item's end;
 //               P ready is signalled on rank 0's barrier.
+//   warps 12-15 (both CTAs, plain launches) epilogue: O / l to fp16 and out, one row per thread,
+//               while the softmax warpgroups and the tensor pipe start the next item; O is
+//               released to the next item's first PV once it has been read from TMEM.  A gated
+//               launch has no such warpgroup: the softmax warpgroups write O / l * sigmoid(gate)
+//               out themselves, half the dims each, after the item's last PV.
 // Two S/P buffers let QK(j + 1) run while super-chunk j is in the softmax.
 //
 // TMEM columns (each CTA): O [0,256)  S/P buffers [256 + 128 b, 384 + 128 b), b = 0, 1.
 // Every mbarrier wait is bounded; a timeout sets the status word and both CTAs drain to the
 // closing cluster barrier.
 #include <algorithm>
+#include <climits>
 #include <cstring>
 
 #include "common.cuh"
@@ -52,7 +58,6 @@ constexpr int kTok = 32;               // tokens per CTA tile
 constexpr int kHQ = 4;                 // heads per tile
 constexpr int kRows = kTok * kHQ;      // 128 rows per CTA, 256 per pair (UMMA M)
 constexpr int kKV = 128;               // cells per super-chunk (UMMA N of QK^T)
-constexpr int kThreads = 384;
 constexpr int kKStages = 3, kVStages = 2;  // K^ freed by QK(j), V^ by PV(j): separate rings
 constexpr int kNS = 2;                     // S/P buffers
 constexpr int kHalfK = (kKV / 2) * kD * 2;   // this CTA's K^ half: 64 cells x 256 dims fp16, 32 KB
@@ -78,6 +83,9 @@ struct __align__(8) Bars {
   // only after QK(j) (hence PV(j - kNS)) is done.
   uint64_t s_full[kNS], p_full[kNS], pv_done[kNS];
   uint64_t q_full, q_empty, o_free, drain;  // q_empty: last QK of an item done; o_free (rank 0): O read out
+  // o_full: the item's last PV is complete (O final); l_full / l_empty: the per-row 1/l slot handed
+  // from the softmax warpgroups to the epilogue warpgroup and back
+  uint64_t o_full, l_full, l_empty;
 };
 
 // Items (pair of 32-token tiles, group, head quad), heaviest (latest tokens) first; a
@@ -125,7 +133,81 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   tmem_st16(taddr + 16, b);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// One (token, head) row per thread: O columns [c_begin, c_end) of the thread's TMEM lane, times
+// 1/l (and the gate's sigmoid), rounded to fp16 once and stored.  The 4 lanes of a group hold the
+// 4 heads of one token, whose output rows are adjacent.  Per 64 dims each lane packs its row into
+// 4 blocks of 16 dims (32 B); a two-step butterfly gives lane g block g of all 4 rows, and each
+// 32-byte store of a warp then writes 8 whole 128-byte row segments instead of 32 scattered
+// pieces.  `loaded()` runs once the last piece is in registers: O may be overwritten after it.
+template <typename F>
+__device__ __forceinline__ void store_o_rows(uint32_t lane_base, int c_begin, int c_end, float inv_l, __half* gdst,
+                                             const __half* grow, bool tok_valid, int lane, F&& loaded) {
+  const int g0 = lane & 1, g1 = (lane >> 1) & 1;
+#pragma unroll 1
+  for (int c0 = c_begin; c0 < c_end; c0 += 64) {
+    uint32_t oa[32], ob[32];
+    tmem_ld32(lane_base + kColO + c0, oa);
+    tmem_ld32(lane_base + kColO + c0 + 32, ob);
+    tmem_wait_ld();
+    if (c0 + 64 == c_end) loaded();
+    uint32_t B[32];  // block b (dims c0 + 16 b ..) = words 8 b .. 8 b + 7
+    if (grow) {  // output gate: o / l * sigmoid(gate), rounded to fp16 once
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t* src = hh ? ob : oa;
+        uint4 gw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) gw[u] = __ldg(reinterpret_cast<const uint4*>(grow + c0 + 32 * hh) + u);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t w = i % 4 == 0 ? gw[i / 4].x : i % 4 == 1 ? gw[i / 4].y : i % 4 == 2 ? gw[i / 4].z : gw[i / 4].w;
+          const float2 gv = __half22float2(*reinterpret_cast<const __half2*>(&w));
+          B[16 * hh + i] = pack_half2(__uint_as_float(src[2 * i]) * inv_l * gate_sigmoid(gv.x),
+                                      __uint_as_float(src[2 * i + 1]) * inv_l * gate_sigmoid(gv.y));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        B[i] = pack_half2(__uint_as_float(oa[2 * i]) * inv_l, __uint_as_float(oa[2 * i + 1]) * inv_l);
+        B[16 + i] = pack_half2(__uint_as_float(ob[2 * i]) * inv_l, __uint_as_float(ob[2 * i + 1]) * inv_l);
+      }
+    }
+#pragma unroll
+    for (int b1 = 0; b1 < 2; ++b1)  // blocks (b1, 1 - g0) to and from lane ^ 1
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t x0 = B[(2 * b1) * 8 + i], x1 = B[(2 * b1 + 1) * 8 + i];
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, g0 ? x0 : x1, 1);
+        B[(2 * b1) * 8 + i] = g0 ? got : x0;
+        B[(2 * b1 + 1) * 8 + i] = g0 ? x1 : got;
+      }
+#pragma unroll
+    for (int e0 = 0; e0 < 2; ++e0)  // blocks (1 - g1, e0) to and from lane ^ 2
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t x0 = B[e0 * 8 + i], x1 = B[(2 + e0) * 8 + i];
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, g1 ? x0 : x1, 2);
+        B[e0 * 8 + i] = g1 ? got : x0;
+        B[(2 + e0) * 8 + i] = g1 ? x1 : got;
+      }
+    if (tok_valid) {  // block e = dims c0 + 16 gq .. of head e's row
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(gdst + e * kD + c0),
+                     "r"(B[8 * e]), "r"(B[8 * e + 1]), "r"(B[8 * e + 2]), "r"(B[8 * e + 3]), "r"(B[8 * e + 4]),
+                     "r"(B[8 * e + 5]), "r"(B[8 * e + 6]), "r"(B[8 * e + 7])
+                     : "memory");
+    }
+  }
+}
+
+// kEpiWG: a fourth warpgroup writes O out while the softmax warpgroups and the tensor pipe go on
+// with the next item (512 threads).  Without it (384 threads) the softmax warpgroups write O
+// themselves, half the dims each: the gated launch, whose sigmoid work would otherwise compete
+// with the next item's softmax for issue slots while O is still held in TMEM.
+template <bool kEpiWG>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kEpiWG ? 512 : 384, 1)
     flash_dense_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                        const __grid_constant__ CUtensorMap map_q, const __half* __restrict__ gate,
                        __half* __restrict__ out, const int4* __restrict__ plan, int pos0, int t_begin, int t_end,
@@ -133,6 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Bars bars;
+  __shared__ float s_invl[kRows];  // 1/l per row of the item being written out
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -160,7 +243,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars.q_full, n_in);
     mbar_init(&bars.q_empty, 1);
-    mbar_init(&bars.o_free, 16);
+    mbar_init(&bars.o_free, kEpiWG ? 8 : 16);  // the warps that read O out, in both CTAs
+    mbar_init(&bars.o_full, 1);
+    mbar_init(&bars.l_full, 4);  // the first softmax warpgroup's 4 warps
+    mbar_init(&bars.l_empty, 4); // the epilogue's 4 warps
     mbar_init(&bars.drain, 1);
     fence_mbar_init();
   }
@@ -333,6 +419,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (ok && j == 0 && n > 0) ok = mbar_wait_poll(&bars.o_free, (n - 1) & 1, status, &s_abort);
           ok = ok && issue_pv(base + j, j == 0);
+          if (kEpiWG && ok && j + 1 == J) umma2_commit(&bars.o_full, kBothCtas);  // O final: the epilogue may read it
         }
         base += J;
       }
@@ -341,11 +428,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_wait(&bars.drain, 0, status);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax rows
     // Two warpgroups share every row: warps 4-7 take S columns 0-63 of each super-chunk and O
-    // dims 0-127, warps 8-11 columns 64-127 and dims 128-255; they exchange half-row maxima
-    // (when needed) and sums through shared memory.
+    // dims 0-127 (for the lazy rescale), warps 8-11 columns 64-127 and dims 128-255; they exchange
+    // half-row maxima (when needed) and sums through shared memory.  At the end of an item they
+    // hand 1/l to the epilogue warpgroup and go straight on to the next item's first super-chunk.
     __shared__ float s_xm[2][kRows];  // half-row maxima, then half-row sums
     const int wg = warp >= 8 ? 1 : 0;
     const int quarter = warp & 3;
@@ -353,7 +441,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int tl = r >> 2;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t p_full0 = mapa_shared(smem_u32(&bars.p_full[0]), 0);  // rank 0's p_full[0]
-    const uint32_t o_free0 = mapa_shared(smem_u32(&bars.o_free), 0);     // rank 0's o_free
     bool ok = true;
     int base = 0;  // global index of the item's first super-chunk
     for (int n = 0; ok; ++n) {
@@ -366,14 +453,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int t = t0 + tl;
     const bool row_valid = t <= t_last;
     const int n_kv_row = row_valid ? it.p0 + t + 1 : 0;
-    if (gate != nullptr && row_valid) {
-      // the row's gate values (this warpgroup's 128 dims) go to L2 now; the epilogue reads them
+    if (!kEpiWG && gate != nullptr && row_valid) {
+      // the row's gate values (this warpgroup's 128 dims) go to L2 now; the write-out reads them
       const char* grow = reinterpret_cast<const char*>(
           gate + ((size_t)t * kHeads + it.g * kHPG + it.hq * kHQ + (lane & 3)) * kD + wg * 128);
       asm volatile("prefetch.global.L2 [%0];" ::"l"(grow));
       asm volatile("prefetch.global.L2 [%0];" ::"l"(grow + 128));
     }
-
     float m_run = -INFINITY, l_run = 0.f;  // m_run in log2 units; l_run: this half of the row
     for (int j = 0; j < J; ++j) {
       const int gj = base + j, b = gj % kNS;
@@ -469,93 +555,93 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
       s_xm[wg][r] = l_run;
       named_bar_any(1, 256, false);
-      const float l_tot = l_run + s_xm[wg ^ 1][r];
-      const int gl = base + J - 1;
-      const bool e_ok = mbar_wait_warp(&bars.pv_done[gl % kNS], (gl / kNS) & 1, status, &s_abort);
-      if (e_ok) {
-        tc_fence_after();
-        const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
-        // The 4 lanes of a group hold the 4 heads of one token, whose output rows are adjacent.
-        // Per 64 dims each lane packs its row into 4 blocks of 16 dims (32 B); a two-step
-        // butterfly gives lane g block g of all 4 rows, and each 32-byte store of a warp then
-        // writes 8 whole 128-byte row segments instead of 32 scattered pieces.
-        const int g0 = lane & 1, g1 = (lane >> 1) & 1, gq = lane & 3;
-        const int tok = t0 + quarter * 8 + (lane >> 2);
-        const bool tok_valid = tok <= t_last;
-        __half* gdst = out + ((size_t)(tok_valid ? tok : 0) * kHeads + it.g * kHPG + it.hq * kHQ) * kD + 16 * gq;
-        // this lane's own row (head it.hq * kHQ + gq of token tok) in the gate input
-        const __half* grow =
-            gate ? gate + ((size_t)(tok_valid ? tok : 0) * kHeads + it.g * kHPG + it.hq * kHQ + gq) * kD : nullptr;
-#pragma unroll 1
-        for (int c0 = wg * 128; c0 < wg * 128 + 128; c0 += 64) {
-          uint32_t oa[32], ob[32];
-          tmem_ld32(lane_base + kColO + c0, oa);
-          tmem_ld32(lane_base + kColO + c0 + 32, ob);
-          tmem_wait_ld();
-          uint32_t B[32];  // block b (dims c0 + 16 b ..) = words 8 b .. 8 b + 7
-          if (grow) {  // output gate: o / l * sigmoid(gate), rounded to fp16 once
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const uint32_t* src = hh ? ob : oa;
-              uint4 gw[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) gw[u] = __ldg(reinterpret_cast<const uint4*>(grow + c0 + 32 * hh) + u);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const uint32_t w = i % 4 == 0 ? gw[i / 4].x : i % 4 == 1 ? gw[i / 4].y : i % 4 == 2 ? gw[i / 4].z : gw[i / 4].w;
-                const float2 gv = __half22float2(*reinterpret_cast<const __half2*>(&w));
-                B[16 * hh + i] = pack_half2(__uint_as_float(src[2 * i]) * inv_l * gate_sigmoid(gv.x),
-                                            __uint_as_float(src[2 * i + 1]) * inv_l * gate_sigmoid(gv.y));
-              }
-            }
+      if constexpr (kEpiWG) {
+        if (wg == 0) {  // 1/l of the row to the epilogue warpgroup, once it has taken the previous item's
+          const float l_tot = l_run + s_xm[1][r];
+          if (n == 0 || mbar_wait_warp(&bars.l_empty, (n - 1) & 1, status, &s_abort)) {
+            s_invl[r] = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.l_full);
           } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              B[i] = pack_half2(__uint_as_float(oa[2 * i]) * inv_l, __uint_as_float(oa[2 * i + 1]) * inv_l);
-              B[16 + i] = pack_half2(__uint_as_float(ob[2 * i]) * inv_l, __uint_as_float(ob[2 * i + 1]) * inv_l);
-            }
-          }
-#pragma unroll
-          for (int b1 = 0; b1 < 2; ++b1)  // blocks (b1, 1 - g0) to and from lane ^ 1
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t x0 = B[(2 * b1) * 8 + i], x1 = B[(2 * b1 + 1) * 8 + i];
-              const uint32_t got = __shfl_xor_sync(0xffffffffu, g0 ? x0 : x1, 1);
-              B[(2 * b1) * 8 + i] = g0 ? got : x0;
-              B[(2 * b1 + 1) * 8 + i] = g0 ? x1 : got;
-            }
-#pragma unroll
-          for (int e0 = 0; e0 < 2; ++e0)  // blocks (1 - g1, e0) to and from lane ^ 2
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t x0 = B[e0 * 8 + i], x1 = B[(2 + e0) * 8 + i];
-              const uint32_t got = __shfl_xor_sync(0xffffffffu, g1 ? x0 : x1, 2);
-              B[e0 * 8 + i] = g1 ? got : x0;
-              B[(2 + e0) * 8 + i] = g1 ? x1 : got;
-            }
-          if (tok_valid) {  // block e = dims c0 + 16 gq .. of head e's row
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(gdst + e * kD + c0),
-                           "r"(B[8 * e]), "r"(B[8 * e + 1]), "r"(B[8 * e + 2]), "r"(B[8 * e + 3]), "r"(B[8 * e + 4]),
-                           "r"(B[8 * e + 5]), "r"(B[8 * e + 6]), "r"(B[8 * e + 7])
-                           : "memory");
+            ok = false;
           }
         }
-        // O is read out: the next item's first PV may overwrite it
-        tc_fence_before();
+      } else {  // this warpgroup's half of the dims, once the item's last PV is complete
+        const float l_tot = l_run + s_xm[wg ^ 1][r];
+        const int gl = base + J - 1;
+        if (mbar_wait_warp(&bars.pv_done[gl % kNS], (gl / kNS) & 1, status, &s_abort)) {
+          tc_fence_after();
+          const int gq = lane & 3;
+          const int tok = t0 + quarter * 8 + (lane >> 2);
+          const bool tok_valid = tok <= t_last;
+          const size_t orow = (size_t)(tok_valid ? tok : 0) * kHeads + it.g * kHPG + it.hq * kHQ;
+          store_o_rows(lane_base, wg * 128, wg * 128 + 128, (l_tot > 0.f) ? 1.f / l_tot : 0.f,
+                       out + orow * kD + 16 * gq, gate ? gate + (orow + gq) * kD : nullptr, tok_valid, lane, [&] {
+                         tc_fence_before();  // O is in registers: the next item's first PV may overwrite it
+                         __syncwarp();
+                         if (lane == 0) {
+                           if (rank == 0) mbar_arrive(&bars.o_free);
+                           else mbar_arrive_cluster(mapa_shared(smem_u32(&bars.o_free), 0));
+                         }
+                       });
+        } else {
+          ok = false;
+        }
+      }
+    }
+    // all 256 threads agree before the next item's barriers
+    if (named_bar_any(1, 256, !ok)) ok = false;
+    base += J;
+    }
+  } else if (kEpiWG && warp >= 12) {
+    // ------------------------------------------------------------ epilogue rows
+    // One row per thread, all 256 dims: once the item's last PV is complete, O is read from TMEM
+    // in 64-dim pieces, scaled by 1/l (and the gate), rounded to fp16 and stored; O is released
+    // to the next item's first PV as soon as its last piece is in registers.  Meanwhile the
+    // softmax warpgroups already work on the next item, so the read-out is off the tensor pipe's
+    // critical path.
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // TMEM lane == tile row
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t o_free0 = mapa_shared(smem_u32(&bars.o_free), 0);  // rank 0's o_free
+    const int gq = lane & 3;
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int q = item_of(c, nC, n, n_items);
+      if (q < 0) break;
+      const Item it = item_at(q, plan, n_pairs, t_begin, t_end, pos0);
+      const int t0 = it.t0p + (int)rank * kTok;        // this CTA's first token
+      const int t_last = min(t0 + kTok, it.t_end) - 1;  // < t0 for an empty tile
+      const int tok = t0 + quarter * 8 + (lane >> 2);
+      const bool tok_valid = tok <= t_last;
+      const size_t orow = (size_t)(tok_valid ? tok : 0) * kHeads + it.g * kHPG + it.hq * kHQ;
+      __half* gdst = out + orow * kD + 16 * gq;
+      // this lane's own row (head it.hq * kHQ + gq of token tok) in the gate input, sent to L2 now
+      const __half* grow = gate ? gate + (orow + gq) * kD : nullptr;
+      if (grow && tok_valid) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) asm volatile("prefetch.global.L2 [%0];" ::"l"(grow + 64 * u));
+      }
+      if (!mbar_wait_warp(&bars.l_full, n & 1, status, &s_abort)) {
+        ok = false;
+        break;
+      }
+      const float inv_l = s_invl[r];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.l_empty);
+      if (!mbar_wait_warp(&bars.o_full, n & 1, status, &s_abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      store_o_rows(lane_base, 0, kD, inv_l, gdst, grow, tok_valid, lane, [&] {
+        tc_fence_before();  // O is in registers: the next item's first PV may overwrite it
         __syncwarp();
         if (lane == 0) {
           if (rank == 0) mbar_arrive(&bars.o_free);
           else mbar_arrive_cluster(o_free0);
         }
-      } else {
-        ok = false;
-      }
-    }
-    // the epilogue wait is per warp: all 256 threads agree before the next item's barriers
-    if (named_bar_any(1, 256, !ok)) ok = false;
-    base += J;
+      });
     }
   }
 
@@ -599,6 +685,7 @@ namespace {
 
 // Per device, set once (0 = not yet): the shared-memory attribute and how many CTA pairs fit on the
 // GPU at once; threads that race here both set the same attribute and store the same count.
+template <bool kEpiWG>
 cudaError_t dense_clusters(int* n_clusters_max) {
   static std::atomic<int> max_clusters[64];
   int dev = 0;
@@ -606,13 +693,14 @@ cudaError_t dense_clusters(int* n_clusters_max) {
   if (dev >= 64) return cudaErrorInvalidDevice;
   int nc = max_clusters[dev].load(std::memory_order_acquire);
   if (nc == 0) {
-    cudaError_t e = cudaFuncSetAttribute(flash_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    cudaError_t e =
+        cudaFuncSetAttribute(flash_dense_kernel<kEpiWG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kEpiWG ? 512 : 384, 1, 1);
     cfg.dynamicSmemBytes = kSmemAlloc;
-    e = cudaOccupancyMaxActiveClusters(&nc, flash_dense_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&nc, flash_dense_kernel<kEpiWG>, &cfg);
     if (e != cudaSuccess) return e;
     if (nc < 1) return cudaErrorInvalidConfiguration;
     max_clusters[dev].store(nc, std::memory_order_release);
@@ -621,40 +709,44 @@ cudaError_t dense_clusters(int* n_clusters_max) {
   return cudaSuccess;
 }
 
+// The plain launch takes the epilogue warpgroup; the gated one does not (see flash_dense_kernel).
+template <typename... Args>
+cudaError_t launch_dense(const __half* gate, int n_items, cudaStream_t stream, Args&&... args) {
+  int n_clusters_max = 0;
+  const bool epi = gate == nullptr;
+  cudaError_t e = epi ? dense_clusters<true>(&n_clusters_max) : dense_clusters<false>(&n_clusters_max);
+  if (e != cudaSuccess) return e;
+  const int n_clusters = std::min(n_clusters_max, n_items);  // persistent: each takes items in snake order
+  if (epi)
+    return launch_pdl(flash_dense_kernel<true>, dim3(n_clusters * 2), dim3(512), kSmemAlloc, stream, args...);
+  return launch_pdl(flash_dense_kernel<false>, dim3(n_clusters * 2), dim3(384), kSmemAlloc, stream, args...);
+}
+
 }  // namespace
 
 cudaError_t launch_flash_dense(const FlashArgs& a, int t_begin, int t_end, const __half* khat, const __half* vhat,
                                cudaStream_t stream) {
   if (t_end <= t_begin) return cudaSuccess;
-  int n_clusters_max = 0;
-  cudaError_t e = dense_clusters(&n_clusters_max);
-  if (e != cudaSuccess) return e;
   const int n = a.pos0 + a.T;  // cells in the mirror
   CUtensorMap mk, mv, mq;
   if (!make_mirror_map(&mk, khat, n, kKV / 2) || !make_mirror_map(&mv, vhat, n, kKV) || !make_q_map(&mq, a.q, a.T))
     return cudaErrorInvalidValue;
   const int n_ttiles = (t_end - t_begin + kTok - 1) / kTok;
-  const float scale_log2 = a.p.sm_scale * kLog2e;
   const int n_items = (n_ttiles + 1) / 2 * 6;  // (pair of tiles, group, head quad)
-  const int n_clusters = std::min(n_clusters_max, n_items);  // persistent: each takes items in snake order
-  return launch_pdl(flash_dense_kernel, dim3(n_clusters * 2), dim3(kThreads), kSmemAlloc, stream, mk, mv, mq, a.gate,
-                    a.out, static_cast<const int4*>(nullptr), a.pos0, t_begin, t_end, scale_log2, a.status);
+  return launch_dense(a.gate, n_items, stream, mk, mv, mq, a.gate, a.out, static_cast<const int4*>(nullptr), a.pos0,
+                      t_begin, t_end, a.p.sm_scale * kLog2e, a.status);
 }
 
 cudaError_t launch_flash_dense_batched(const __half* q, int n_tok, const __half* gate, __half* out, const int4* plan,
                                        int max_pairs, const __half* khat, const __half* vhat, int mirror_rows,
                                        float sm_scale, int* status, cudaStream_t stream) {
   if (max_pairs <= 0) return cudaSuccess;
-  int n_clusters_max = 0;
-  cudaError_t e = dense_clusters(&n_clusters_max);
-  if (e != cudaSuccess) return e;
   CUtensorMap mk, mv, mq;
   if (!make_mirror_map(&mk, khat, mirror_rows, kKV / 2) || !make_mirror_map(&mv, vhat, mirror_rows, kKV) ||
       !make_q_map(&mq, q, n_tok))
     return cudaErrorInvalidValue;
-  const int n_clusters = (int)std::min<long long>(n_clusters_max, 6LL * max_pairs);
-  return launch_pdl(flash_dense_kernel, dim3(n_clusters * 2), dim3(kThreads), kSmemAlloc, stream, mk, mv, mq, gate,
-                    out, plan, 0, 0, 0, sm_scale * kLog2e, status);
+  const int n_items = (int)std::min<long long>(6LL * max_pairs, INT_MAX);
+  return launch_dense(gate, n_items, stream, mk, mv, mq, gate, out, plan, 0, 0, 0, sm_scale * kLog2e, status);
 }
 
 }  // namespace qsa
