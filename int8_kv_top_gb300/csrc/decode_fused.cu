@@ -1008,9 +1008,11 @@ cudaLaunchConfig_t launch_config(int C, int n_tok, cudaStream_t stream, cudaLaun
 }
 
 // Per device: 0 = not set up, 1 = attributes set and clusters of 16 fit, 2 = set, only 8 fit;
-// and the device's SM count, read at set-up.
+// and how many clusters of 2, 4, 8 and 16 CTAs the GPU holds at once, read at set-up (a cluster
+// lives inside one GPC, so large clusters fit fewer times than the SM count suggests).
 std::atomic<int> g_setup[64];
-std::atomic<int> g_sms[64];
+std::atomic<int> g_maxc[64][4];
+constexpr int kClusterSizes[4] = {2, 4, 8, 16};
 int g_dev_of_setup() {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1036,15 +1038,19 @@ cudaError_t device_setup(int* state) {
     if ((e = set_attrs<4>()) != cudaSuccess) return e;
     if ((e = set_attrs<8>()) != cudaSuccess) return e;
     if ((e = set_attrs<16>()) != cudaSuccess) return e;
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config(16, 1, nullptr, attr);
-    int n16 = 0;
-    e = cudaOccupancyMaxActiveClusters(&n16, decode_fused_kernel<16>, &cfg);
-    if (e != cudaSuccess) return e;
-    s = n16 > 0 ? 1 : 2;
-    int sms = 0;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    g_sms[dev].store(sms > 0 ? sms : 1, std::memory_order_release);
+    int nmax[4] = {0, 0, 0, 0};
+    for (int i = 0; i < 4; ++i) {
+      cudaLaunchAttribute attr[2];
+      cudaLaunchConfig_t cfg = launch_config(kClusterSizes[i], 1, nullptr, attr);
+      e = i == 0   ? cudaOccupancyMaxActiveClusters(&nmax[i], decode_fused_kernel<2>, &cfg)
+          : i == 1 ? cudaOccupancyMaxActiveClusters(&nmax[i], decode_fused_kernel<4>, &cfg)
+          : i == 2 ? cudaOccupancyMaxActiveClusters(&nmax[i], decode_fused_kernel<8>, &cfg)
+                   : cudaOccupancyMaxActiveClusters(&nmax[i], decode_fused_kernel<16>, &cfg);
+      if (e != cudaSuccess) return e;
+    }
+    if (nmax[2] <= 0) return cudaErrorInvalidConfiguration;  // clusters of 8 are portable
+    s = nmax[3] > 0 ? 1 : 2;
+    for (int i = 0; i < 4; ++i) g_maxc[dev][i].store(nmax[i], std::memory_order_release);
     g_setup[dev].store(s, std::memory_order_release);
   }
   *state = s;
@@ -1108,16 +1114,19 @@ cudaError_t launch_decode_layer(const __half* q, const int8_t* kq, const int8_t*
   CUtensorMap tmc, tms;
   if (!encode_maps(kq, ksc, n_pool, &tmc, &tms)) return cudaErrorInvalidValue;
   // The cluster size: the kernel's phases are latency bound, so a launch takes about (waves of
-  // CTAs) x (a fixed part + a part growing with the cells per CTA); measured on GB300 the two parts
-  // match at about 2,048 cells.  Few tokens: more CTAs per token (one wave either way); many tokens:
-  // fewer, larger CTAs (fewer waves).  C must hold max_n_kv in C x kMaxW cells.
-  const int sms = g_sms[g_dev_of_setup()].load(std::memory_order_acquire);
+  // clusters) x (a fixed part + a part growing with the cells per CTA); measured on GB300 the two
+  // parts match at about 2,048 cells.  Few tokens: more CTAs per token (one wave either way); many
+  // tokens: fewer, larger CTAs (fewer waves).  A wave is as many clusters of that size as the GPU
+  // holds at once.  C must hold max_n_kv in C x kMaxW cells.
+  const int dev = g_dev_of_setup();
+  const long long clusters = (long long)kGroups * n_tok;
   int best_c = 0;
   double best_t = 0.0;
-  for (int c : {16, 8, 4, 2}) {
-    if ((c == 16 && state != 1) || (long long)max_n_kv > (long long)c * kMaxW) continue;
-    const long long ctas = (long long)kGroups * n_tok * c;
-    const double waves = (double)((ctas + sms - 1) / sms);
+  for (int i = 3; i >= 0; --i) {
+    const int c = kClusterSizes[i];
+    const int maxc = g_maxc[dev][i].load(std::memory_order_acquire);
+    if (maxc <= 0 || (long long)max_n_kv > (long long)c * kMaxW) continue;
+    const double waves = (double)((clusters + maxc - 1) / maxc);
     const double cells = (double)max_n_kv / c;
     const double t = waves * (1.0 + cells / 2048.0);
     if (best_c == 0 || t < best_t) {

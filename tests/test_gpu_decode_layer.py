@@ -35,8 +35,9 @@ def check(inp, N, P, params=None):
         assert_close(xp[t], ref_out[t], f"decode layer N={N} P={P} token {t}")
 
 
-# single tokens and small batches at the pages' positions and the budget boundary; N = 1..4
-# takes clusters of 16 CTAs per (token, group), N = 8 clusters of 8
+# single tokens and small batches at the pages' positions and the budget boundary; one or two
+# tokens take clusters of 16 CTAs per (token, group), larger N clusters of 8 (as many as the GPU
+# holds at once in one wave)
 @pytest.mark.parametrize("N,P", [(1, 0), (3, 3), (1, 63), (2, 64), (1, 512), (4, 512), (1, 2048), (4, 2047),
                                  (4, 2048), (8, 2050), (1, 8192), (4, 8192), (8, 3000), (1, 30000)])
 def test_decode_layer_matches_oracle(N, P):
