@@ -38,7 +38,7 @@ namespace qsa {
 namespace {
 
 // ----------------------------------------------------------------- workspace layout
-constexpr int kGM = 128, kGN = 128, kGK = 64, kGStages = 5;
+constexpr int kGM = 128, kGN = 128, kGK = 64, kGStages = 4;
 constexpr int kMaxCells = 65536;
 constexpr int kTkThreads = 512;
 static_assert(kTkThreads >= 256, "top-k stages a 256-entry histogram and 256 Qsum dims one per thread");
@@ -175,7 +175,8 @@ __global__ void __launch_bounds__(256) prep_k_kernel(const int8_t* __restrict__ 
 constexpr int kNtPerCtaMax = 16;               // at most 2048 cells per CTA
 constexpr int kSmemA = kGM * kD * 2 * 2;       // 128 KB: 8 k-blocks (hi_b, lo_b) of [128 rows][64] SW128
 constexpr int kSmemBStage = kGN * kGK * 2;     // 16 KB: one 64-dim block of [128 cells][64] SW128
-constexpr int kScoreSmem = kSmemA + kGStages * kSmemBStage + 1024;
+constexpr int kSmemStg = kGM * kGN * 2;          // 32 KB: the tile's fp16 scores, 2 boxes of [128 rows][64] SW128
+constexpr int kScoreSmem = kSmemA + kGStages * kSmemBStage + kSmemStg + 1024;
 
 struct __align__(8) ScoreBars {
   uint64_t a_full, b_full[kGStages], b_empty[kGStages], acc_full[kNB], acc_empty[kNB], drain;
@@ -187,7 +188,7 @@ __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;"
 
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                 const __half* __restrict__ ksc, __half* __restrict__ scores, int T_sel, int T_pad, int n_pad,
+                 const __grid_constant__ CUtensorMap map_s, const __half* __restrict__ ksc, int T_sel, int T_pad, int n_pad,
                  int n_base, int m_tiles, int n_chunks, int nt_per_cta, float sm_scale, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -284,32 +285,35 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // epilogue: warps 4-7 take cells 0-63 of each 128-cell tile, warps 8-11 cells 64-127; thread
-    // = row.  The tile's K scales of group g are staged as fp32, block-major, one tile ahead, so
-    // that a block's 64 cells come in as sixteen 16-byte broadcast loads.
-    __shared__ __align__(16) float s_scale[2][kNB][kGN];
+    // = row.  The tile's K scales of group g are staged (fp16, block-major) before the tile, so that
+    // a block's 64 cells come in as eight 16-byte broadcast loads.  The scores go to a 128B-swizzled
+    // shared-memory tile that one thread stores with two TMA box stores: the warps do not wait on
+    // global stores, and cells past a row's causal end (inside its padded width, never read) and
+    // rows past T_sel (clipped by the tensor map) need no masking.
+    __shared__ __align__(16) __half s_scale[kNB][kGN];
     const int quarter = warp & 3, c0 = (warp >= 8) ? 64 : 0;
     const int et = tid - 128;  // 0..255
-    const int r = r0 + quarter * 32 + lane;
+    const int rl = quarter * 32 + lane;  // tile row
     const int n_lim = n_base + T_sel;  // cells that exist for this call
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    bool dead = false;  // after a failed wait keep meeting the epilogue barrier, skip the work
-    auto load_scales = [&](int i, float (&dst)[2]) {  // this thread stages two scales per tile
+    uint8_t* stg_row = smem + kSmemA + kGStages * kSmemBStage + (c0 >> 6) * (kGM * 128) + rl * 128;
+    bool dead = false;  // after a failed wait keep meeting the epilogue barriers, skip the work
+    auto load_scales = [&](int i, __half (&dst)[2]) {  // this thread stages two scales per tile
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
         const int e = et + 256 * x, cell = e >> 2, b = e & 3;
         const int c = (nt_begin + i) * kGN + cell;
-        dst[x] = (i < n_tiles && c < n_lim) ? __half2float(ksc[((size_t)c * kGroups + g) * kNB + b]) : 0.f;
+        dst[x] = (i < n_tiles && c < n_lim) ? ksc[((size_t)c * kGroups + g) * kNB + b] : __ushort_as_half(0);
       }
     };
-    float sc_next[2];
+    __half sc_next[2];
     load_scales(0, sc_next);
     for (int i = 0; i < n_tiles; ++i) {
-      const int a = i & 1;
       const int n0 = (nt_begin + i) * kGN;
 #pragma unroll
-      for (int x = 0; x < 2; ++x) {
+      for (int x = 0; x < 2; ++x) {  // s_scale is free: every thread passed the previous tile's barrier A
         const int e = et + 256 * x;
-        s_scale[a][e & 3][e >> 2] = sc_next[x];
+        s_scale[e & 3][e >> 2] = sc_next[x];
       }
       load_scales(i + 1, sc_next);  // one tile ahead: the loads overlap this tile's work
       epilogue_bar();
@@ -328,55 +332,52 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.acc_empty[b]);  // the next tile's block-b MMAs may start
-        const float4* sv = reinterpret_cast<const float4*>(&s_scale[a][b][c0]);
+        const uint4* sv = reinterpret_cast<const uint4*>(&s_scale[b][c0]);
 #pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4) {
-          const float4 s4 = sv[q4];
-          const int j = 4 * q4;
-          acc[j] = fmaf(s4.x, __uint_as_float(v[j >> 5][j & 31]), acc[j]);
-          acc[j + 1] = fmaf(s4.y, __uint_as_float(v[(j + 1) >> 5][(j + 1) & 31]), acc[j + 1]);
-          acc[j + 2] = fmaf(s4.z, __uint_as_float(v[(j + 2) >> 5][(j + 2) & 31]), acc[j + 2]);
-          acc[j + 3] = fmaf(s4.w, __uint_as_float(v[(j + 3) >> 5][(j + 3) & 31]), acc[j + 3]);
-        }
-      }
-      if (dead) continue;
-      // Per 32 cells, lanes 2j and 2j + 1 (adjacent rows) swap 32-byte halves so that each holds
-      // 16 cells of both rows, and each 32-byte store of the warp writes 16 row segments of 64
-      // bytes instead of 32 scattered 16-byte pieces.
-      const int g0 = lane & 1;
+        for (int q8 = 0; q8 < 8; ++q8) {
+          const uint4 s8 = sv[q8];
+          const uint32_t sw[4] = {s8.x, s8.y, s8.z, s8.w};
 #pragma unroll
-      for (int h32 = 0; h32 < 2; ++h32) {
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          w[j] = pack_half2(acc[32 * h32 + 2 * j] * sm_scale, acc[32 * h32 + 2 * j + 1] * sm_scale);
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          const uint32_t x0 = w[x], x1 = w[8 + x];
-          const uint32_t got = __shfl_xor_sync(0xffffffffu, g0 ? x0 : x1, 1);
-          w[x] = g0 ? got : x0;
-          w[8 + x] = g0 ? x1 : got;
-        }
-        const int cb = n0 + c0 + 32 * h32 + 16 * g0;  // w[8 e .. 8 e + 7]: cells cb .. cb + 15 of row (r & ~1) + e
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int rr = (r & ~1) + e;
-          const int nk = rr < T_sel ? n_base + rr + 1 : 0;  // that row's causal cells
-          if (cb < nk) {
-            __half* dp = scores + ((size_t)g * T_sel + rr) * n_pad + cb;
-            if (cb + 16 <= nk) {
-              asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dp), "r"(w[8 * e]),
-                           "r"(w[8 * e + 1]), "r"(w[8 * e + 2]), "r"(w[8 * e + 3]), "r"(w[8 * e + 4]),
-                           "r"(w[8 * e + 5]), "r"(w[8 * e + 6]), "r"(w[8 * e + 7])
-                           : "memory");
-            } else {
-              const __half* hw = reinterpret_cast<const __half*>(w + 8 * e);
-              for (int j = 0; j < nk - cb; ++j) dp[j] = hw[j];
-            }
+          for (int u = 0; u < 4; ++u) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&sw[u]));
+            const int j = 8 * q8 + 2 * u;
+            acc[j] = fmaf(f.x, __uint_as_float(v[j >> 5][j & 31]), acc[j]);
+            acc[j + 1] = fmaf(f.y, __uint_as_float(v[(j + 1) >> 5][(j + 1) & 31]), acc[j + 1]);
           }
         }
       }
+      // barrier A: every thread is done with s_scale, and the previous tile's store has read the
+      // staging tile
+      if (et == 0 && i > 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      epilogue_bar();
+      if (!dead) {
+        // this thread's 64 scores: 128 B of row rl in box c0 / 64, 16-byte chunks swizzled by rl mod 8
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const int j = 8 * ch;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(stg_row + ((ch ^ (rl & 7)) << 4))),
+                       "r"(pack_half2(acc[j] * sm_scale, acc[j + 1] * sm_scale)),
+                       "r"(pack_half2(acc[j + 2] * sm_scale, acc[j + 3] * sm_scale)),
+                       "r"(pack_half2(acc[j + 4] * sm_scale, acc[j + 5] * sm_scale)),
+                       "r"(pack_half2(acc[j + 6] * sm_scale, acc[j + 7] * sm_scale))
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();  // the staging writes are visible to the TMA engine
+      epilogue_bar();            // barrier B: the whole tile is staged
+      if (et == 0) {
+        const uint8_t* stg = smem + kSmemA + kGStages * kSmemBStage;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb)
+          asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                           reinterpret_cast<uint64_t>(&map_s)),
+                       "r"(n0 + 64 * hb), "r"(r0), "r"(g), "r"(smem_u32(stg + hb * (kGM * 128)))
+                       : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
     }
+    // every score store has completed before the CTA leaves
+    if (et == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
@@ -1136,6 +1137,20 @@ __global__ void __launch_bounds__(kTkThreads, (V <= 64 ? 2 : 1))
   }
 }
 
+// 3D map over the score matrix [2][T_sel][n_pad] fp16: box = 64 cells x 128 rows x 1 group, 128B
+// swizzle (the staged tile's layout); rows past T_sel are clipped on store.
+bool make_scores_map(CUtensorMap* map, void* base, int n_pad, int T_sel) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)n_pad, (cuuint64_t)T_sel, (cuuint64_t)kGroups};
+  const cuuint64_t strides[2] = {(cuuint64_t)n_pad * 2, (cuuint64_t)n_pad * 2 * (cuuint64_t)T_sel};
+  const cuuint32_t box[3] = {64u, (cuuint32_t)kGM, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 bool make_2d_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                  uint32_t box_outer) {
   EncodeTiledFn enc = encode_tiled_fn();
@@ -1170,9 +1185,9 @@ cudaError_t launch_score_gemm(const WsLayout& L, int pos0, __half* qhi, __half* 
     if (sms < 1) return cudaErrorInvalidConfiguration;
     n_sms[dev].store(sms, std::memory_order_release);
   }
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, ms;
   if (!make_2d_map(&ma, qhi, 2 * kD, (uint64_t)kGroups * L.T_pad, kGK, kGM) ||
-      !make_2d_map(&mb, kc, kD, (uint64_t)kGroups * L.n_pad, kGK, kGN))
+      !make_2d_map(&mb, kc, kD, (uint64_t)kGroups * L.n_pad, kGK, kGN) || !make_scores_map(&ms, sc, L.n_pad, L.T_sel))
     return cudaErrorInvalidValue;
   const int m_tiles = L.T_pad / kGM;
   const int n_tiles = L.n_pad / kGN;
@@ -1189,7 +1204,7 @@ cudaError_t launch_score_gemm(const WsLayout& L, int pos0, __half* qhi, __half* 
   const int n_chunks = (n_tiles + nt_per - 1) / nt_per;
   const int n_base = pos0 + L.t_sel;  // n_kv of selected row r is n_base + r + 1
   return launch_pdl(score_kernel, dim3(kGroups * m_tiles * n_chunks), dim3(kScoreThreads), kScoreSmem, stream, ma, mb,
-                    ksc, sc, L.T_sel, L.T_pad, L.n_pad, n_base, m_tiles, n_chunks, nt_per, sm_scale, status);
+                    ms, ksc, L.T_sel, L.T_pad, L.n_pad, n_base, m_tiles, n_chunks, nt_per, sm_scale, status);
 }
 
 }  // namespace
