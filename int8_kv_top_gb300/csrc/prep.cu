@@ -8,8 +8,10 @@
 //   outputs:   qcur = fp16(q rows); kcur = fp16(k rows) (optional); the cache cell pos0 + t gets
 //              quantise(kcur) and quantise(v rows), the absmax rule of qsa_prep_quantize.
 //
-// One CTA (256 threads) per token; each warp issues the loads of all its rows (and the gains)
-// before it uses any, so a CTA waits on one memory round trip.  The token's rd/2 rotation
+// One CTA (256 threads, at most 48 registers: five CTAs per SM) per token; each warp issues the
+// loads of all its rows before it uses any, so a CTA waits on one memory round trip, and the gains
+// are read per row from L1.  More CTAs per SM hide more of that round trip: a persistent form that
+// loads the next token's rows during the current one held fewer CTAs per SM and ran slower.  The token's rd/2 rotation
 // angles are formed once, in fp32 with the product's error recovered and a three-part 2 pi
 // (rope_angle), then sincosf, into shared memory; each lane then keeps its own four (cos, sin)
 // pairs in registers for all the token's rows.  A warp takes a row at a time with the lanes laid
@@ -110,7 +112,7 @@ __device__ __forceinline__ void quantize_row(const float (&x)[8], int a, int b, 
   }
 }
 
-__global__ void __launch_bounds__(256) prep_kernel(const __half* __restrict__ q_raw, const __half* __restrict__ k_raw,
+__global__ void __launch_bounds__(256, 5) prep_kernel(const __half* __restrict__ q_raw, const __half* __restrict__ k_raw,
                                                    const __half* __restrict__ v_raw, const float* __restrict__ q_gamma,
                                                    const float* __restrict__ k_gamma, const int32_t* __restrict__ pos3,
                                                    int pos0, const __grid_constant__ PrepCfg cfg,
@@ -140,10 +142,6 @@ __global__ void __launch_bounds__(256) prep_kernel(const __half* __restrict__ q_
       rb[j] = __ldg(reinterpret_cast<const uint2*>(src + db));
     }
   }
-  const float4 qga = __ldg(reinterpret_cast<const float4*>(q_gamma + da));
-  const float4 qgb = __ldg(reinterpret_cast<const float4*>(q_gamma + db));
-  const float4 kga = __ldg(reinterpret_cast<const float4*>(k_gamma + da));
-  const float4 kgb = __ldg(reinterpret_cast<const float4*>(k_gamma + db));
   if (tid < h2) {
     int p = pos0 + t;
     if (pos3) p = __ldg(pos3 + 3 * t + (tid < cfg.sec0 ? 0 : (tid < cfg.sec0 + cfg.sec1 ? 1 : 2)));
@@ -173,8 +171,10 @@ __global__ void __launch_bounds__(256) prep_kernel(const __half* __restrict__ q_
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       const float rs = 1.f / sqrtf(ss * (1.f / kD) + cfg.eps);
-      const float gw[8] = {is_k ? kga.x : qga.x, is_k ? kga.y : qga.y, is_k ? kga.z : qga.z, is_k ? kga.w : qga.w,
-                           is_k ? kgb.x : qgb.x, is_k ? kgb.y : qgb.y, is_k ? kgb.z : qgb.z, is_k ? kgb.w : qgb.w};
+      const float* gam = is_k ? k_gamma : q_gamma;  // this lane's gains (L1-resident after the first CTAs)
+      const float4 ga = __ldg(reinterpret_cast<const float4*>(gam + da));
+      const float4 gb = __ldg(reinterpret_cast<const float4*>(gam + db));
+      const float gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
 #pragma unroll
       for (int u = 0; u < 8; ++u) x[u] = x[u] * rs * gw[u];
       if (rot_lane) {  // pairs (x[u], x[4 + u]) = dims (a + u, a + u + rd / 2)
