@@ -84,6 +84,24 @@ __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, boo
                : "memory");
 }
 
+// Position in this CTA's walk over (item, tile): k-th own item, tile jl of it, and the item's
+// rotation (item mod tiles), advanced by compare-and-wrap instead of integer divisions.
+struct TileIter {
+  int k, jl, rot;
+  __device__ __forceinline__ void advance(int n_tiles, int rot_step) {
+    if (++jl == n_tiles) {
+      jl = 0;
+      ++k;
+      rot += rot_step;
+      if (rot >= n_tiles) rot -= n_tiles;
+    }
+  }
+  __device__ __forceinline__ int tile(int n_tiles) const {  // the tile taken at step jl (rotated order)
+    const int p = jl + rot;
+    return p >= n_tiles ? p - n_tiles : p;
+  }
+};
+
 __device__ __forceinline__ int pick4(const int (&v)[4], int x) {  // select chain: no local memory
   return x == 0 ? v[0] : x == 1 ? v[1] : x == 2 ? v[2] : v[3];
 }
@@ -125,6 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (K + kCells - 1) / kCells;
   const int my_items = (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   const int U = my_items * n_tiles;  // tiles this CTA processes
+  const int rot_step = (int)gridDim.x % n_tiles;     // item rotation step between this CTA's items
+  const TileIter it0{0, 0, (int)blockIdx.x % n_tiles};
 
   if (tid == 0) {
     s_abort = 0;
@@ -168,12 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Raw ids of tile u for a producer warp: lane l holds slots l, l+32, l+64, l+96 (kNoSlot past
   // the end of the id row).
   // Loaded a tile ahead and checked only when used, so the loads overlap the copies.
-  auto load_ids = [&](int u, int (&dst)[4], int& g_out, int& nkv_out) {
-    const int k = u / n_tiles, jl = u % n_tiles;
-    const int it = blockIdx.x + k * gridDim.x;
+  auto load_ids = [&](const TileIter& ti, int (&dst)[4], int& g_out, int& nkv_out) {
+    const int it = blockIdx.x + ti.k * gridDim.x;
     const int t = t_begin + (it >> 1), g = it & 1;
     const int32_t* idrow = ids + ((size_t)t * kGroups + g) * K;
-    const int pt = (jl + it) % n_tiles;  // tile order rotated per item (see above)
+    const int pt = ti.tile(n_tiles);  // tile order rotated per item (see above)
     g_out = g;
     nkv_out = pos0 + t + 1;
 #pragma unroll
@@ -201,8 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_s = idesc_f16_f32(kCells, kNQ, 0, 0);
       const uint32_t sK = smem_u32(smem + kOffK), sQ = smem_u32(smem + kOffQ);
       int f = 0;  // K fill counter
-      for (int s = 0; s < U; ++s) {  // S^T(s) = K^(s) . Q^T: two fills of two 64-dim blocks each
-        const int k = s / n_tiles, jl = s % n_tiles;
+      TileIter ti = it0;
+      for (int s = 0; s < U; ++s, ti.advance(n_tiles, rot_step)) {  // S^T(s) = K^(s) . Q^T: two fills of two 64-dim blocks each
+        const int k = ti.k, jl = ti.jl;
         if (jl == 0 && !mbar_wait(&bars.q_full[k & 1], (k >> 1) & 1, status, &s_abort)) break;
         if (s >= kNS && !mbar_wait(&bars.s_free[s % kNS], ((s / kNS) - 1) & 1, status, &s_abort)) break;
         const uint64_t bq0 = sdesc_sw128(sQ + (k & 1) * kQBytes, 16, 1024);
@@ -235,8 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = idesc_f16_f32(kCells, kNQ, 1, 0);
       const uint32_t sV = smem_u32(smem + kOffV), sP = smem_u32(smem + kOffP);
       int f = 0;  // V fill counter
-      for (int u = 0; u < U; ++u) {  // O^T += V^(u)^T . P^T(u): one fill per 128-dim half
-        const int k = u / n_tiles, jl = u % n_tiles, ob = k & 1;
+      TileIter ti = it0;
+      for (int u = 0; u < U; ++u, ti.advance(n_tiles, rot_step)) {  // O^T += V^(u)^T . P^T(u): one fill per 128-dim half
+        const int k = ti.k, jl = ti.jl, ob = k & 1;
         if (jl == 0 && k >= 2 && !mbar_wait(&bars.o_free[ob], ((k >> 1) & 1) ^ 1, status, &s_abort)) break;
         if (!mbar_wait(&bars.p_full[u % kNS], (u / kNS) & 1, status, &s_abort)) break;
         const uint64_t bp0 = sdesc_sw128(sP + (u % kNS) * kPBytes, 16, 1024);
@@ -277,7 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ch = lane & 15;
     int cur[4] = {-1, -1, -1, -1}, nxt[4] = {-1, -1, -1, -1};
     int g_cur = 0, g_nxt = 0, nkv_nxt = 0;
-    if (U > 0) load_ids(0, nxt, g_nxt, nkv_nxt);
+    TileIter ti = it0, ta = it0;  // tile s and tile s + 1 (ids loaded one tile ahead)
+    if (U > 0) load_ids(ta, nxt, g_nxt, nkv_nxt);
+    ta.advance(n_tiles, rot_step);
     if (warp == 2 && lane == 0) tma_prefetch_desc(&map_q);
     auto fill = [&](int f, int h) -> bool {
       if (f % kPoolPairs != pair) return true;  // fills go round-robin over the pool's pairs
@@ -306,13 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     int f = 0;
-    for (int s = 0; s < U; ++s) {
+    for (int s = 0; s < U; ++s, ti = ta, ta.advance(n_tiles, rot_step)) {
       check_ids(nxt, nkv_nxt, warp == 2);  // tile s: loaded during the previous step
 #pragma unroll
       for (int x = 0; x < 4; ++x) cur[x] = nxt[x];
       g_cur = g_nxt;
-      if (s + 1 < U) load_ids(s + 1, nxt, g_nxt, nkv_nxt);
-      const int k = s / n_tiles, jl = s % n_tiles;
+      if (s + 1 < U) load_ids(ta, nxt, g_nxt, nkv_nxt);
+      const int k = ti.k, jl = ti.jl;
       if (jl == 0 && warp == 2) {
         // Q^T tile for this item by TMA: per 64-dim block the group's 12 head rows land as
         // rows 0..11 of a 128B-swizzled [16][64] block (rows 12..15 stay zero)
@@ -354,7 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int last_v = -1;
       // the item's tiles are taken in rotated order, as the producers fill them
-      auto slot_of = [&](int jl) { return ((jl + it) % n_tiles) * kCells + i; };
+      const int rot = it % n_tiles;
+      auto slot_of = [&](int jl) {
+        const int p = jl + rot;
+        return (p >= n_tiles ? p - n_tiles : p) * kCells + i;
+      };
       int c_next = (slot_of(0) < K) ? idrow[slot_of(0)] : -1;  // this lane's id, one tile ahead
       for (int jl = 0; jl < n_tiles; ++jl, ++u) {
         const int c_cur = c_next;
