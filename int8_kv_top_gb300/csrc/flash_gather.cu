@@ -296,6 +296,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring_base = smem + (is_v ? kOffV : kOffK);
     const __half* base = is_v ? vhat : khat;
     const int ch = lane & 15;
+    // Byte offset of this lane's 16-byte chunk in row 2 (i0 + m) + lane / 16 of a fill, past
+    // 256 (i0 + m) bytes: i0 is a multiple of 8, so the row's swizzle phase is (2 m + lane / 16) mod 8.
+    uint32_t dsw[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      dsw[m] = (uint32_t)(128 * (lane >> 4) + (((ch & 7) ^ ((2 * m + (lane >> 4)) & 7)) << 4) + 256 * m);
     int cur[4] = {-1, -1, -1, -1}, nxt[4] = {-1, -1, -1, -1};
     int g_cur = 0, g_nxt = 0, nkv_nxt = 0;
     TileIter ti = it0, ta = it0;  // tile s and tile s + 1 (ids loaded one tile ahead)
@@ -318,12 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int cell[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) cell[m] = __shfl_sync(0xffffffffu, sel, (2 * (i0 + m) + (lane >> 4)) & 31);
+        uint8_t* dst_i0 = dst + 256 * i0;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const int r = 2 * (i0 + m) + (lane >> 4);
-          cp_async16_zfill(dst + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
-                           src_g + (size_t)(cell[m] >= 0 ? cell[m] : 0) * (kGroups * kD), cell[m] >= 0);
-        }
+        for (int m = 0; m < 8; ++m)
+          cp_async16_zfill(dst_i0 + dsw[m], src_g + (uint32_t)max(cell[m], 0) * (uint32_t)(kGroups * kD), cell[m] >= 0);
       }
       cp_async_arrive_noinc(&ring.full[slot]);
       return true;
