@@ -78,9 +78,9 @@ struct __align__(8) GBars {
 };
 
 // 16-byte copy that writes zeros (and reads nothing) when `valid` is false.
-__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 16 : 0)
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+               "r"(valid ? 16 : 0)
                : "memory");
 }
 
@@ -315,19 +315,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e = f - kRing;
         if (!mbar_wait_warp(&ring.empty[e % (2 * kRing)], (e / (2 * kRing)) & 1, status, &s_abort)) return false;
       }
-      uint8_t* dst = ring_base + slot * kSlotBytes + (ch >> 3) * kBlkBytes;
+      const uint32_t dst = smem_u32(ring_base + slot * kSlotBytes + (ch >> 3) * kBlkBytes);
       const __half* src_g = base + (size_t)g_cur * kD + h * 128 + ch * 8;
       // instruction i copies rows 2i, 2i+1; cells are resolved eight instructions at a time
 #pragma unroll 1
       for (int i0 = half_rows * (kCells / 4); i0 < (half_rows + 1) * (kCells / 4); i0 += 8) {
         const int sel = pick4(cur, (i0 >> 4) & 3);  // rows 2*i0 .. 2*i0 + 15 share one id register
+        const int sbase = ((2 * i0) & 31) + (lane >> 4);  // the lane holding row 2 i0's id, + 2 m for row 2 (i0 + m)
         int cell[8];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) cell[m] = __shfl_sync(0xffffffffu, sel, (2 * (i0 + m) + (lane >> 4)) & 31);
-        uint8_t* dst_i0 = dst + 256 * i0;
+        for (int m = 0; m < 8; ++m) cell[m] = __shfl_sync(0xffffffffu, sel, sbase + 2 * m);
+        const uint32_t d_i0 = dst + 256 * i0;
 #pragma unroll
         for (int m = 0; m < 8; ++m)
-          cp_async16_zfill(dst_i0 + dsw[m], src_g + (uint32_t)max(cell[m], 0) * (uint32_t)(kGroups * kD), cell[m] >= 0);
+          cp_async16_zfill(d_i0 + dsw[m], src_g + (uint32_t)max(cell[m], 0) * (uint32_t)(kGroups * kD), cell[m] >= 0);
       }
       cp_async_arrive_noinc(&ring.full[slot]);
       return true;
@@ -338,7 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int x = 0; x < 4; ++x) cur[x] = nxt[x];
       g_cur = g_nxt;
-      if (s + 1 < U) load_ids(ta, nxt, g_nxt, nkv_nxt);
+      // the next tile's ids, if this warp's pair fills in it (fills 2 (s + 1) and 2 (s + 1) + 1 go to pairs
+      // f mod 3); warp 2 always, for the item's Q tile and the bad-id report
+      const int f1 = 2 * (s + 1) % kPoolPairs;
+      if (s + 1 < U && (warp == 2 || f1 == pair || (f1 + 1) % kPoolPairs == pair)) load_ids(ta, nxt, g_nxt, nkv_nxt);
       const int k = ti.k, jl = ti.jl;
       if (jl == 0 && warp == 2) {
         // Q^T tile for this item by TMA: per 64-dim block the group's 12 head rows land as
