@@ -78,6 +78,9 @@ struct __align__(8) GBars {
 };
 
 // 16-byte copy that writes zeros (and reads nothing) when `valid` is false.
+__device__ __forceinline__ void cp_async16_sh(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)) : "memory");
+}
 __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
                "r"(valid ? 16 : 0)
@@ -303,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int m = 0; m < 8; ++m)
       dsw[m] = (uint32_t)(128 * (lane >> 4) + (((ch & 7) ^ ((2 * m + (lane >> 4)) & 7)) << 4) + 256 * m);
     int cur[4] = {-1, -1, -1, -1}, nxt[4] = {-1, -1, -1, -1};
+    bool cur_valid = false;  // every id of the current tile is in [0, n_kv) (warp-uniform)
     int g_cur = 0, g_nxt = 0, nkv_nxt = 0;
     TileIter ti = it0, ta = it0;  // tile s and tile s + 1 (ids loaded one tile ahead)
     if (U > 0) load_ids(ta, nxt, g_nxt, nkv_nxt);
@@ -326,9 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int m = 0; m < 8; ++m) cell[m] = __shfl_sync(0xffffffffu, sel, sbase + 2 * m);
         const uint32_t d_i0 = dst + 256 * i0;
+        if (cur_valid) {  // every slot of the tile holds a valid id: plain copies
 #pragma unroll
-        for (int m = 0; m < 8; ++m)
-          cp_async16_zfill(d_i0 + dsw[m], src_g + (uint32_t)max(cell[m], 0) * (uint32_t)(kGroups * kD), cell[m] >= 0);
+          for (int m = 0; m < 8; ++m) cp_async16_sh(d_i0 + dsw[m], src_g + (uint32_t)cell[m] * (uint32_t)(kGroups * kD));
+        } else {  // a ragged last tile or a bad id: those rows are zero-filled
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+            cp_async16_zfill(d_i0 + dsw[m], src_g + (uint32_t)max(cell[m], 0) * (uint32_t)(kGroups * kD), cell[m] >= 0);
+        }
       }
       cp_async_arrive_noinc(&ring.full[slot]);
       return true;
@@ -338,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       check_ids(nxt, nkv_nxt, warp == 2);  // tile s: loaded during the previous step
 #pragma unroll
       for (int x = 0; x < 4; ++x) cur[x] = nxt[x];
+      cur_valid = __all_sync(0xffffffffu, (cur[0] | cur[1] | cur[2] | cur[3]) >= 0);
       g_cur = g_nxt;
       // the next tile's ids, if this warp's pair fills in it (fills 2 (s + 1) and 2 (s + 1) + 1 go to pairs
       // f mod 3); warp 2 always, for the item's Q tile and the bad-id report
