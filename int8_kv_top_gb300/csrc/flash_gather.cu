@@ -380,7 +380,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h0 = wg * kHPW;           // this warpgroup's first head
     const uint32_t bar_id = 1 + wg;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    uint8_t* sP = smem + kOffP;
+    const uint32_t sP = smem_u32(smem + kOffP);
+    // this cell's byte offsets in a P^T buffer for the warpgroup's six heads (K-major SW128: 64-cell
+    // blocks of [16 rows][128 B]; head row h, chunk (cell mod 64) / 8 swizzled by h mod 8)
+    uint32_t poff[kHPW];
+#pragma unroll
+    for (int j = 0; j < kHPW; ++j) {
+      const int h = h0 + j;
+      poff[j] = (uint32_t)((i >> 6) * (kNQ * 128) + h * 128 + ((((i & 63) >> 3) ^ (h & 7)) << 4) + (i & 7) * 2);
+    }
     int u = 0;
     bool ok = true;
     for (int it = blockIdx.x, k = 0; ok && it < n_items; it += gridDim.x, ++k) {
@@ -476,15 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (named_bar_any(bar_id, 128, !f_ok)) { ok = false; break; }
         }
         // P^T[h][i] (K-major SW128: 64-cell blocks of [16 rows][128 B])
-        uint8_t* pb = sP + (u % kNS) * kPBytes + (i >> 6) * (kNQ * 128);
+        const uint32_t pb = sP + (u % kNS) * kPBytes;
 #pragma unroll
         for (int j = 0; j < kHPW; ++j) {
-          const int h = h0 + j;
-          const float mu = (m_run[j] == -INFINITY) ? 0.f : m_run[j];
-          const float p = fast_exp2(s[j] - mu);
+          const float p = fast_exp2(s[j] - ((m_run[j] == -INFINITY) ? 0.f : m_run[j]));
           l_part[j] += p;
-          *reinterpret_cast<__half*>(pb + h * 128 + ((((i & 63) >> 3) ^ (h & 7)) << 4) + (i & 7) * 2) =
-              __float2half_rn(p);
+          const __half hp = __float2half_rn(p);
+          asm volatile("st.shared.b16 [%0], %1;" ::"r"(pb + poff[j]), "h"(__half_as_ushort(hp)) : "memory");
         }
         fence_proxy_async_smem();
         tc_fence_before();
