@@ -409,7 +409,7 @@ int qsa_decode_layer_batched(const uint16_t* q, const int8_t* kq, const int8_t* 
 }
 
 size_t qsa_flash_prefill_batched_workspace_bytes(int n_seq, int n_tok, int max_n_kv, const qsa_params* params) {
-  qsa::Params p;
+  qsa::Params p{};
   if (n_seq < 1 || n_tok < 1 || max_n_kv < 1 || resolve_params(params, &p) != QSA_OK) return 0;
   return qsa::batched_prefill_layout(n_seq, n_tok, max_n_kv, p.identity_max).bytes;
 }
